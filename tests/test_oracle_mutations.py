@@ -1,0 +1,112 @@
+"""The pins bite: plant a plausible mistake in a copy of the oracle (on the CPU),
+rebuild it, and check that at least one pin fails.  Each mutation names the
+passage it breaks."""
+import ctypes as C
+import os
+import subprocess
+
+import pytest
+
+import oracle as ORC
+
+from . import test_oracle_ngram as TN
+from . import test_oracle_philox as TP
+from . import test_oracle_price as TPR
+from . import test_oracle_tree as TT
+from . import test_oracle_verify as TV
+
+SRC = os.path.join(os.path.dirname(ORC.__file__), "spec_oracle.c")
+
+MUTATIONS = [
+    # (name, original text, mutated text, pins expected to catch it)
+    ("philox multiplier", "#define PHILOX_M0 0xD2511F53u", "#define PHILOX_M0 0xD2511F55u",
+     [TP.test_philox_known_answers]),
+    ("philox key schedule", "k1 += PHILOX_W1;", "k1 += PHILOX_W0;", [TP.test_philox_known_answers]),
+    ("uniform conversion", "(double)(w >> 8) * (1.0 / 16777216.0)", "(double)(w >> 9) * (1.0 / 16777216.0)",
+     [TP.test_uniform_conversion_is_exact_24_bit]),
+    ("n-gram tie to the oldest occurrence", "(l == best_l && j > best_j)", "(l == best_l && j < best_j)",
+     [TN.test_runner_up_with_different_follower_disagrees]),
+    ("n-gram agreement compares the wrong tokens", "x[second_j + 1] == x[best_j + 1]",
+     "x[second_j] == x[best_j]", [TN.test_runner_up_with_different_follower_disagrees]),
+    ("n-gram continuation off by one", "x[best_j + 1 + i]", "x[best_j + i]",
+     [TN.test_exact_copy_gives_its_continuation]),
+    ("n-gram ignores the cap", "int32_t limit = copy_cap < j + 1 ? copy_cap : j + 1;",
+     "int32_t limit = j + 1;", [TN.test_match_length_capped_at_n_max_and_copy_length_at_cap]),
+    ("Eq. (1) drops the agreement term", "z = z + e->delta * (double)a;", "z = z;",
+     [TPR.test_full_match_indicator_and_agreement_terms]),
+    ("Eq. (1) swaps first / later copy weights", "(first ? e->kappa_first : e->kappa_rest)",
+     "(first ? e->kappa_rest : e->kappa_first)",
+     [TPR.test_copy_length_term_adds_5_7_logits_at_the_first_position]),
+    ("Eq. (1) drops the 1/15 in the log", "log((double)mm / (double)e->m_ref)", "log((double)mm)",
+     [TPR.test_full_match_indicator_and_agreement_terms]),
+    ("Eq. (1) sign of the match-length term", "z = z + (first ? e->w_first : e->w_rest) * (double)(n - e->n_ref);",
+     "z = z - (first ? e->w_first : e->w_rest) * (double)(n - e->n_ref);",
+     [TPR.test_full_match_indicator_and_agreement_terms]),
+    ("Eq. (3) sign of the price", "float t = S[k] - lambda;", "float t = S[k] + lambda;",
+     [TPR.test_table8_chain_values]),
+    ("contains rule takes the min", "Sr[k] = Sg[k] > Sd[k] ? Sg[k] : Sd[k];", "Sr[k] = Sg[k] < Sd[k] ? Sg[k] : Sd[k];",
+     [TPR.test_contains_rule_merges_survivals_and_continues_with_h]),
+    ("value rule ties to the model chain", "oracle_chain_value(Sg, gl, lambda) >=",
+     "oracle_chain_value(Sg, gl, lambda) >", [TPR.test_value_rule_ties_go_to_the_ngram_chain]),
+    ("allocation ties to the higher request", "if (a->r != b->r) return a->r < b->r ? -1 : 1;",
+     "if (a->r != b->r) return a->r > b->r ? -1 : 1;", [TPR.test_allocation_ties_go_to_lower_request_then_position]),
+    ("allocation keeps the lowest survivals", "if (a->s > b->s) return -1; /* survival descending */",
+     "if (a->s > b->s) return 1; /* survival descending */",
+     [TPR.test_allocation_is_the_best_prefix_closed_set_brute_force]),
+    ("row offsets forget the bonus row", "row_off[r + 1] = row_off[r] + verify_len[r] + 1;",
+     "row_off[r + 1] = row_off[r] + verify_len[r];", [TPR.test_allocation_is_the_best_prefix_closed_set_brute_force]),
+    ("accept ratio inverted", "ratio = p[yi] / q[yi];", "ratio = q[yi] / p[yi];",
+     [lambda o: TV.test_lossless_with_probabilistic_drafts(o, 3, 2, 0.7, 1)]),
+    ("residual max(0, q - p)", "v = p[x] - q[x] > 0.0 ? p[x] - q[x] : 0.0;", "v = q[x] - p[x] > 0.0 ? q[x] - p[x] : 0.0;",
+     [lambda o: TV.test_lossless_with_probabilistic_drafts(o, 3, 2, 0.7, 1)]),
+    ("point-mass residual keeps the rejected token", "v = (x == y) ? 0.0 : p[x];", "v = p[x];",
+     [lambda o: TV.test_lossless_with_point_mass_drafts(o, 3, 2, 1.0, 4)]),
+    ("bonus drawn from the last draft row", "row_softmax(target_logits, (int64_t)base + ell, vocab, dtype, temperature, p);",
+     "row_softmax(target_logits, (int64_t)base + ell - (ell > 0), vocab, dtype, temperature, p);",
+     [lambda o: TV.test_lossless_with_point_mass_drafts(o, 3, 2, 1.0, 4)]),
+    ("temperature ignored", "p[x] = exp((logit_at(base, row * vocab + x, dtype) - m) / T);",
+     "p[x] = exp((logit_at(base, row * vocab + x, dtype) - m));",
+     [lambda o: TV.test_lossless_with_point_mass_drafts(o, 4, 3, 0.7, 5)]),
+    ("inverse CDF one token late", "if (run > t) return x;", "if (run > t) return x + (x + 1 < vocab);",
+     [TV.test_bonus_draws_follow_p_chi_square]),
+    ("greedy ties to the highest index", "if (best < 0 || z > bv) {", "if (best < 0 || z >= bv) {",
+     [TV.test_greedy_ties_go_to_the_lowest_index]),
+    ("tree walk reads the child's own row", "a = row_argmax(logits, (int64_t)base + cur, vocab, dtype);",
+     "a = row_argmax(logits, (int64_t)base + (cur > 0 ? parent[base + cur] : 0), vocab, dtype);",
+     [TT.test_path_by_brute_force_over_root_to_node_paths]),
+    ("tree commits the last path token, not its argmax", "out_tokens[(int64_t)r * max_nodes + len - 1] = a;",
+     "out_tokens[(int64_t)r * max_nodes + len - 1] = tok[base + cur];",
+     [TT.test_path_by_brute_force_over_root_to_node_paths]),
+]
+
+
+@pytest.fixture(scope="module")
+def src_text():
+    return open(SRC).read()
+
+
+@pytest.mark.parametrize("name,orig,mut,pins", MUTATIONS, ids=[m[0] for m in MUTATIONS])
+def test_planted_mistake_is_caught(tmp_path, src_text, name, orig, mut, pins):
+    assert src_text.count(orig) == 1, f"mutation anchor not unique: {orig!r}"
+    src = tmp_path / "spec_oracle.c"
+    src.write_text(src_text.replace(orig, mut))
+    hdr = os.path.join(os.path.dirname(SRC), "spec_oracle.h")
+    (tmp_path / "spec_oracle.h").write_text(open(hdr).read())
+    so = tmp_path / "libmut.so"
+    subprocess.check_call(["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fPIC", "-shared",
+                           "-o", str(so), str(src), "-lm"])
+    ORC.lib()
+    saved = ORC._lib
+    mut_lib = C.CDLL(str(so))
+    ORC._declare(mut_lib)
+    ORC._lib = mut_lib
+    try:
+        caught = 0
+        for pin in pins:
+            try:
+                pin(ORC)
+            except AssertionError:
+                caught += 1
+        assert caught > 0, f"no pin caught the planted mistake: {name}"
+    finally:
+        ORC._lib = saved
