@@ -1,0 +1,373 @@
+"""Benchmark of one hybrid speculative-decoding round on GB300.
+
+A step is one whole round on the device: n-gram lookup over every history,
+pricing and batch-wide allocation, and chain verification over the
+full-vocabulary target rows of the allocated slots.  The workload is the
+batch-128 mixed editing / chat configuration (context 4096, budget 256,
+V = 151936 bf16 logits, T = 0); its logits are synthetic, laid out exactly as
+the allocation asks (the target forward itself is not part of the path).
+
+Timing: W warm-up steps, then K steps between a barrier and a device
+synchronisation, CUDA events on the launching stream; three input sets rotate
+so that every step reads logits that are not in L2 (3 x 117 MB > 129 MB).
+`value` = verified draft tokens per second (sum of verify_len per step);
+rows/s, per-kernel times, the verify kernel's HBM roofline fraction, an
+end-to-end figure through host buffers, the oracle's CPU time and the SM
+clocks seen during the timed region ride along on the same JSON line.
+
+--impl reference times the oracle (plain single-threaded C) on the host
+cores on bounded samples of the same workload and prints the same metric.
+Under torchrun each rank runs its own batch (weak scaling, no collective on
+the data path); rank 0 prints.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "verified draft tokens/sec and verify rows/sec at V=151936, BS 4/128; % HBM roofline"
+UNIT = "tokens/s"
+WORKLOAD = "mixed_bs128"
+NBUF = 3
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def build_workload(rank):
+    import workloads as W
+
+    return W.mixed_bs128(seed=1002 + rank)
+
+
+def config_json(cfg, extra=None):
+    d = {"workload": f"{WORKLOAD}: B={cfg['B']}, V={cfg['V']}, context 4096, budget {cfg['budget']}, "
+                     f"lambda {cfg['lam']}, T=0, bf16 logits",
+         "batch": cfg["B"], "vocab": cfg["V"], "context": 4096, "budget": cfg["budget"], "temperature": 0.0,
+         "l2": f"{NBUF} rotating input sets (logits {NBUF} x > L2/3); no flush"}
+    if extra:
+        d.update(extra)
+    return d
+
+
+# --------------------------------------------------------------------------- clocks
+class ClockSampler:
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.dev = device_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", str(self.dev)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- oracle baseline
+def oracle_round(cfg, lay, logits, reqs):
+    """The oracle's round over the requests `reqs` (lookup, batch pricing, their verification)."""
+    import oracle as O
+
+    sub = np.asarray(reqs)
+    ng = O.ngram_propose(cfg["hist"][sub], cfg["hist_len"][sub], cfg["n_min"], cfg["n_max"], cfg["L"],
+                         cfg["copy_cap"])
+    if len(sub) == cfg["B"]:
+        O.price_and_allocate(cfg["d"], cfg["c"], cfg["d_len"], ng.g, ng.g_len, ng.match_n, ng.agree,
+                             ng.copy_len, cfg["coef"], cfg["lam"], cfg["budget"], cfg["max_verify_len"],
+                             cfg["policy"], cfg["draft_greedy"])
+    rows = [np.arange(lay.row_off[r], lay.row_off[r + 1]) for r in sub]
+    ro = np.concatenate([[0], np.cumsum([len(x) for x in rows])]).astype(np.int32)
+    O.verify_chain(logits[np.concatenate(rows)], ro, lay.chain[sub], lay.verify_len[sub])
+    return int(lay.verify_len[sub].sum())
+
+
+def oracle_layout(cfg):
+    import oracle as O
+
+    ng = O.ngram_propose(cfg["hist"], cfg["hist_len"], cfg["n_min"], cfg["n_max"], cfg["L"], cfg["copy_cap"])
+    return O.price_and_allocate(cfg["d"], cfg["c"], cfg["d_len"], ng.g, ng.g_len, ng.match_n, ng.agree,
+                                ng.copy_len, cfg["coef"], cfg["lam"], cfg["budget"], cfg["max_verify_len"],
+                                cfg["policy"], cfg["draft_greedy"])
+
+
+def cpu_baseline(cfg, lay, logits, seconds=10.0):
+    tokens, t0, n = 0, time.perf_counter(), 0
+    while time.perf_counter() - t0 < seconds:
+        tokens += oracle_round(cfg, lay, logits, range(cfg["B"]))
+        n += 1
+    dt = time.perf_counter() - t0
+    return {"value": tokens / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{n} full oracle rounds of the {WORKLOAD} batch ({dt:.1f} s, single-threaded C)"}
+
+
+def run_reference(args):
+    import workloads as W
+
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    cfg = build_workload(0)
+    lay = oracle_layout(cfg)
+    logits = W.compact_logits(cfg, lay.row_off, lay.verify_len)
+    # size each step so that the whole run stays within ~2 minutes
+    t0 = time.perf_counter()
+    oracle_round(cfg, lay, logits, range(cfg["B"]))
+    t_full = time.perf_counter() - t0
+    per_step = 100.0 / max(1, args.steps + args.warmup)
+    s = int(max(1, min(cfg["B"], cfg["B"] * per_step / t_full)))
+    rng = np.random.default_rng(0)
+    for _ in range(args.warmup):
+        oracle_round(cfg, lay, logits, rng.choice(cfg["B"], s, replace=False))
+    tok, t0 = 0, time.perf_counter()
+    for _ in range(args.steps):
+        tok += oracle_round(cfg, lay, logits, np.sort(rng.choice(cfg["B"], s, replace=False)))
+    dt = time.perf_counter() - t0
+    v = tok / dt
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_json(cfg, {"sample_requests_per_step": s}),
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": f"{s} of {cfg['B']} requests per step (lookup + verify), batch pricing"},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------- GPU arm
+def run_gpu(args):
+    import torch
+
+    import speculative_decoding_draft_spec_gb300 as S
+    import workloads as W
+    from speculative_decoding_draft_spec_gb300.round import ChainRound
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    S.build()
+    cfg = build_workload(rank)
+    B, K, L, V = cfg["B"], cfg["K"], cfg["L"], cfg["V"]
+    max_rows = B * (L + 1)
+    rounds = []
+    for k in range(NBUF):
+        rnd = ChainRound(B, cfg["hist"].shape[1], K, L, V, torch.bfloat16, max_rows, cfg["coef"], cfg["n_min"],
+                         cfg["n_max"], cfg["copy_cap"])
+        rnd.load(cfg["hist"], cfg["hist_len"], cfg["d"], cfg["c"], cfg["d_len"])
+        rounds.append(rnd)
+    kw = dict(lam=cfg["lam"], budget=cfg["budget"], max_verify_len=cfg["max_verify_len"])
+    # the allocation (on the device) fixes the layout of the target rows
+    rounds[0].draft_and_price(**kw)
+    torch.cuda.synchronize()
+    row_off = rounds[0].row_off.cpu().numpy()
+    vlen = rounds[0].verify_len.cpu().numpy()
+    n_rows, n_tok = int(row_off[-1]), int(vlen.sum())
+    logits = W.compact_logits(cfg, row_off, vlen)
+    lt = torch.from_numpy(logits.view(np.int16)).view(torch.bfloat16)
+    for rnd in rounds:
+        rnd.logits[:n_rows].copy_(lt.to("cuda"))
+    torch.cuda.synchronize()
+
+    stream = torch.cuda.current_stream()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+
+    def step(i, rec=None):
+        rnd = rounds[i % NBUF]
+        if rec:
+            rec[0].record(stream)
+        S.spec_ngram_propose(rnd.hist, rnd.hist_len, rnd.n_min, rnd.n_max, L, rnd.copy_cap, rnd.g, rnd.g_len,
+                             rnd.match_n, rnd.agree, rnd.copy_len, rnd.ws)
+        if rec:
+            rec[1].record(stream)
+        S.spec_price_and_allocate(rnd.d, rnd.c, rnd.d_len, rnd.g, rnd.g_len, rnd.match_n, rnd.agree,
+                                  rnd.copy_len, rnd.est, cfg["lam"], cfg["budget"], cfg["max_verify_len"],
+                                  cfg["policy"], True, rnd.chain, rnd.S, rnd.chain_len, rnd.source,
+                                  rnd.verify_len, rnd.row_off, rnd.point_mass, rnd.ws)
+        if rec:
+            rec[2].record(stream)
+        S.spec_verify_chain(rnd.logits, rnd.row_off, max_rows, rnd.chain, rnd.verify_len, rnd.out_tokens,
+                            rnd.n_accepted, rnd.n_emitted, rnd.ws, point_mass=rnd.point_mass, temperature=0.0)
+        if rec:
+            rec[3].record(stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.barrier()
+
+    barrier()
+    torch.cuda.synchronize()
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        t_start.record(stream)
+        for i in range(args.steps):
+            step(i, ev[i])
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    ms = t_start.elapsed_time(t_end)
+    if world > 1:
+        import torch.distributed as dist
+
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    comp = {k: statistics.mean(e[a].elapsed_time(e[b]) for e in ev) * 1e3
+            for k, (a, b) in {"ngram": (0, 1), "price": (1, 2), "verify": (2, 3)}.items()}
+    ok = all(int(r.ws.status()) == 0 for r in rounds)
+
+    # graph-captured round time (one graph per input set)
+    graphs = []
+    for rnd in rounds:
+        graphs.append(rnd.capture(**kw))
+    torch.cuda.synchronize()
+    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for i in range(args.warmup):
+        graphs[i % NBUF].replay()
+    g0.record(stream)
+    for i in range(args.steps):
+        graphs[i % NBUF].replay()
+    g1.record(stream)
+    torch.cuda.synchronize()
+    graph_us = g0.elapsed_time(g1) * 1e3 / args.steps
+
+    # end to end through the public API with host buffers: H2D of the step's inputs
+    # (histories, drafter chain, confidences, logits) from pinned memory, the round,
+    # D2H of the emitted tokens and counts
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+    h_hist, h_len, h_d, h_c = pin(cfg["hist"]), pin(cfg["hist_len"]), pin(cfg["d"]), pin(cfg["c"])
+    h_logits = torch.from_numpy(logits.view(np.int16)).pin_memory()
+    h_out = torch.empty((B, L + 1), dtype=torch.int32).pin_memory()
+    h_na = torch.empty(B, dtype=torch.int32).pin_memory()
+    e_steps = max(3, min(args.steps, 50))
+    rnd = rounds[0]
+    h2d = sum(x.numel() * x.element_size() for x in (h_hist, h_len, h_d, h_c, h_logits))
+    d2h = h_out.numel() * 4 + h_na.numel() * 4
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for it in range(e_steps + 2):
+        if it == 2:
+            e0.record(stream)
+        rnd.hist.copy_(h_hist, non_blocking=True)
+        rnd.hist_len.copy_(h_len, non_blocking=True)
+        rnd.d.copy_(h_d, non_blocking=True)
+        rnd.c.copy_(h_c, non_blocking=True)
+        rnd.logits[:n_rows].view(torch.int16).copy_(h_logits, non_blocking=True)
+        rnd.run(**kw)
+        h_out.copy_(rnd.out_tokens, non_blocking=True)
+        h_na.copy_(rnd.n_accepted, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e_steps
+
+    if rank != 0:
+        return
+    hbm, peak_kind = peaks()
+    verify_us = comp["verify"]
+    alg_bytes = n_rows * V * 2
+    achieved = alg_bytes / (verify_us * 1e-6) / 1e9
+    cpu = cpu_baseline(cfg, oracle_layout(cfg), logits, seconds=args.cpu_seconds) if args.cpu_seconds > 0 else None
+    line = {
+        "metric": METRIC, "value": world * n_tok * args.steps / (ms * 1e-3), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": config_json(cfg),
+        "rows_per_s": world * n_rows * args.steps / (ms * 1e-3),
+        "verified_tokens_per_step": n_tok, "verify_rows_per_step": n_rows,
+        "components_us": {k: round(v, 3) for k, v in comp.items()},
+        "graph_round_us": round(graph_us, 3),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(achieved / hbm, 4), "traffic": None, "peak_kind": peak_kind,
+                     "kernel": "verify_rows_kernel<bf16, greedy>", "algorithmic_bytes": alg_bytes},
+        "cpu_baseline": cpu,
+        "e2e": {"value": world * n_tok / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clk.summary(),
+        "status_clean": ok,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()
