@@ -147,7 +147,7 @@ def _assert_price_equal(g, o):
 @pytest.mark.parametrize("name", ["tiny", "tiny_prob", "edit_bs4", "edit_bs4_prob", "mixed_bs128", "long_bs64"])
 def test_price_parity_on_workloads(S, name):
     c = {"tiny": lambda: W.tiny(), "tiny_prob": lambda: W.tiny(probabilistic=True),
-         "edit_bs4": lambda: W.edit_bs4(), "edit_bs4_prob": lambda: W.edit_bs4(1.0, True),
+         "edit_bs4": lambda: W.edit_bs4(), "edit_bs4_prob": lambda: W.edit_bs4(temperature=1.0, probabilistic=True),
          "mixed_bs128": W.mixed_bs128, "long_bs64": W.long_bs64}[name]()
     ng = _priced_inputs(c)
     g, o, ws = _price_both(S, c, ng)
