@@ -1,8 +1,9 @@
 """Benchmark of one hybrid speculative-decoding round on GB300.
 
 A step is one whole round on the device: n-gram lookup over every history,
-pricing and batch-wide allocation, and chain verification over the
-full-vocabulary target rows of the allocated slots.  The workload is the
+pricing and batch-wide allocation (one fused kernel, spec_draft_and_price), and
+chain verification over the full-vocabulary target rows of the allocated slots
+(spec_verify_chain).  The workload is the
 batch-128 mixed editing / chat configuration (context 4096, budget 256,
 V = 151936 bf16 logits, T = 0); its logits are synthetic, laid out exactly as
 the allocation asks (the target forward itself is not part of the path).
@@ -229,26 +230,22 @@ def run_gpu(args):
     torch.cuda.synchronize()
 
     stream = torch.cuda.current_stream()
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
 
     def step(i, rec=None):
         rnd = rounds[i % NBUF]
         if rec:
             rec[0].record(stream)
-        S.spec_ngram_propose(rnd.hist, rnd.hist_len, rnd.n_min, rnd.n_max, L, rnd.copy_cap, rnd.g, rnd.g_len,
-                             rnd.match_n, rnd.agree, rnd.copy_len, rnd.ws)
+        S.spec_draft_and_price(rnd.hist, rnd.hist_len, rnd.n_min, rnd.n_max, rnd.copy_cap, rnd.g, rnd.g_len,
+                               rnd.match_n, rnd.agree, rnd.copy_len, rnd.d, rnd.c, rnd.d_len, rnd.est, cfg["lam"],
+                               cfg["budget"], cfg["max_verify_len"], cfg["policy"], True, rnd.chain, rnd.S,
+                               rnd.chain_len, rnd.source, rnd.verify_len, rnd.row_off, rnd.point_mass, rnd.ws)
         if rec:
             rec[1].record(stream)
-        S.spec_price_and_allocate(rnd.d, rnd.c, rnd.d_len, rnd.g, rnd.g_len, rnd.match_n, rnd.agree,
-                                  rnd.copy_len, rnd.est, cfg["lam"], cfg["budget"], cfg["max_verify_len"],
-                                  cfg["policy"], True, rnd.chain, rnd.S, rnd.chain_len, rnd.source,
-                                  rnd.verify_len, rnd.row_off, rnd.point_mass, rnd.ws)
-        if rec:
-            rec[2].record(stream)
         S.spec_verify_chain(rnd.logits, rnd.row_off, max_rows, rnd.chain, rnd.verify_len, rnd.out_tokens,
                             rnd.n_accepted, rnd.n_emitted, rnd.ws, point_mass=rnd.point_mass, temperature=0.0)
         if rec:
-            rec[3].record(stream)
+            rec[2].record(stream)
 
     for i in range(args.warmup):
         step(i)
@@ -278,8 +275,13 @@ def run_gpu(args):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms = float(t.item())
     comp = {k: statistics.mean(e[a].elapsed_time(e[b]) for e in ev) * 1e3
-            for k, (a, b) in {"ngram": (0, 1), "price": (1, 2), "verify": (2, 3)}.items()}
+            for k, (a, b) in {"draft_price": (0, 1), "verify": (1, 2)}.items()}
     ok = all(int(r.ws.status()) == 0 for r in rounds)
+    if args.legs == "timed":
+        if rank == 0:
+            print(json.dumps({"legs": "timed", "ms_per_step": ms / args.steps, "components_us": comp,
+                              "status_clean": ok}), flush=True)
+        return
 
     # graph-captured round time (one graph per input set)
     graphs = []
@@ -346,7 +348,7 @@ def run_gpu(args):
         "cpu_baseline": cpu,
         "e2e": {"value": world * n_tok / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": 2 * args.steps,
         "clocks": clk.summary(),
         "status_clean": ok,
     }
@@ -360,6 +362,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--legs", default="all", choices=["all", "timed"],
+                    help="timed: only the warm-up and timed loop (for profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

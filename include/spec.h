@@ -237,6 +237,24 @@ spec_status spec_price_and_allocate(
     int32_t* row_off, uint8_t* point_mass, const spec_workspace* ws, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Steps 1 + 2 fused: spec_ngram_propose followed by spec_price_and_allocate
+ * in one launch, with identical outputs (every argument has the meaning it has
+ * in those two calls; max_propose = L).  Each request's n-gram CTA prices its
+ * own request from on-chip values ([HS] sec. 4.2: "the scan already computes
+ * n, a, and m, so the estimate adds only one fused elementwise step per
+ * request"), and the last request to finish allocates the budget for the
+ * batch.  Limits: those of both calls.
+ * ------------------------------------------------------------------------ */
+spec_status spec_draft_and_price(
+    const int32_t* hist, int64_t hist_stride, const int32_t* hist_len, int32_t batch, int32_t n_min,
+    int32_t n_max, int32_t copy_cap, int32_t* g, int32_t* g_len, int32_t* match_n, int32_t* agree,
+    int32_t* copy_len, int32_t K, int32_t L, const int32_t* d, const float* c, const int32_t* d_len,
+    const spec_estimator* est, const float* est_table, size_t est_table_bytes, float lambda,
+    int32_t budget, int32_t max_verify_len, spec_policy policy, int32_t draft_greedy, int32_t* chain,
+    float* S, int32_t* chain_len, int32_t* source, int32_t* verify_len, int32_t* row_off,
+    uint8_t* point_mass, const spec_workspace* ws, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
  * Step 3: chain verification ([HS] sec. 2 "accepts the longest prefix that
  * passes rejection sampling, plus one token of its own", App. H point masses;
  * [LS] sec. 2.1: accept y_i with probability min(1, p_i(y_i)/q_i(y_i)), at the

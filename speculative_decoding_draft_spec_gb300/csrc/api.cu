@@ -24,6 +24,13 @@ cudaError_t spec_launch_price(int32_t batch, int32_t K, int32_t L, const int32_t
                               int32_t* chain, float* S, int32_t* chain_len, int32_t* source,
                               int32_t* verify_len, int32_t* row_off, uint8_t* point_mass,
                               uint32_t* status, cudaStream_t stream);
+cudaError_t spec_launch_draft_price(
+    const int32_t* hist, int64_t stride, const int32_t* hist_len, int32_t batch, int32_t n_min, int32_t n_max,
+    int32_t cap, int32_t* g, int32_t* g_len, int32_t* match_n, int32_t* agree, int32_t* copy_len, int32_t K,
+    int32_t L, const int32_t* d, const float* c, const int32_t* d_len, const spec_estimator* est,
+    const float* table, float lambda, int32_t budget, int32_t mvl, int32_t policy, int32_t draft_greedy,
+    int32_t* chain, float* S, int32_t* chain_len, int32_t* source, int32_t* verify_len, int32_t* row_off,
+    uint8_t* point_mass, uint32_t* status, cudaStream_t stream, int* unsupported);
 cudaError_t spec_launch_verify_chain(int32_t batch, int32_t vocab, int32_t dtype, const void* logits,
                                      const int32_t* row_off, const void* draft, int32_t K,
                                      const int32_t* chain, int32_t L, const int32_t* verify_len,
@@ -41,7 +48,7 @@ cudaError_t spec_launch_verify_tree(int32_t batch, int32_t vocab, int32_t dtype,
 
 namespace {
 
-constexpr int32_t kMaxVerifyBatch = 4096;
+constexpr int32_t kMaxVerifyBatch = 2048;
 
 int device_sms() {
   int dev = 0;
@@ -196,6 +203,44 @@ spec_status spec_price_and_allocate(
                                      est, est_table, lambda, budget, max_verify_len, (int32_t)policy,
                                      draft_greedy ? 1 : 0, chain, S, chain_len, source, verify_len,
                                      row_off, point_mass, status_of(ws), stream));
+}
+
+spec_status spec_draft_and_price(
+    const int32_t* hist, int64_t hist_stride, const int32_t* hist_len, int32_t batch, int32_t n_min,
+    int32_t n_max, int32_t copy_cap, int32_t* g, int32_t* g_len, int32_t* match_n, int32_t* agree,
+    int32_t* copy_len, int32_t K, int32_t L, const int32_t* d, const float* c, const int32_t* d_len,
+    const spec_estimator* est, const float* est_table, size_t est_table_bytes, float lambda,
+    int32_t budget, int32_t max_verify_len, spec_policy policy, int32_t draft_greedy, int32_t* chain,
+    float* S, int32_t* chain_len, int32_t* source, int32_t* verify_len, int32_t* row_off,
+    uint8_t* point_mass, const spec_workspace* ws, cudaStream_t stream) {
+  // the checks of both steps
+  if (batch < 0 || hist_stride < 0 || K < 0 || L < 1 || K > L || budget < 0 || max_verify_len < 0 || !est ||
+      !(lambda == lambda) || (int)policy < 0 || (int)policy > 4)
+    return SPEC_ERR_INVALID_ARG;
+  if (n_min < 1 || n_max < n_min || copy_cap < n_max) return SPEC_ERR_INVALID_ARG;
+  if (n_max > SPEC_MAX_N || L > SPEC_MAX_L || copy_cap > SPEC_MAX_COPY_CAP || batch > SPEC_MAX_PRICE_BATCH)
+    return SPEC_ERR_UNSUPPORTED;
+  if (!est_table || !row_off) return SPEC_ERR_INVALID_ARG;
+  if (batch > 0 && (!hist_len || !g || !g_len || !match_n || !agree || !copy_len || !d_len || !chain || !S ||
+                    !chain_len || !source || !verify_len || !point_mass || (K > 0 && (!d || !c)) ||
+                    (hist_stride > 0 && !hist)))
+    return SPEC_ERR_INVALID_ARG;
+  if (!est->use_constant_h && (est->m_cap < 1 || est->m_cap > SPEC_MAX_COPY_CAP)) return SPEC_ERR_INVALID_ARG;
+  const size_t need = spec_estimator_table_bytes(est, L);
+  if (need == 0 || est_table_bytes < need) return SPEC_ERR_INVALID_ARG;
+  if (!ws_ok(ws)) return SPEC_ERR_WORKSPACE;
+  if (batch == 0) {
+    // nothing to draft or price: an empty layout
+    return from_cuda(cudaMemsetAsync(row_off, 0, sizeof(int32_t), stream));
+  }
+  int unsupported = 0;
+  const cudaError_t e = spec_launch_draft_price(
+      hist, hist_stride < 1 ? 1 : hist_stride, hist_len, batch, n_min, n_max, copy_cap, g, g_len, match_n, agree,
+      copy_len, K, L, d, c, d_len, est, est_table, lambda, budget, max_verify_len, (int32_t)policy,
+      draft_greedy ? 1 : 0, chain, S, chain_len, source, verify_len, row_off, point_mass, status_of(ws), stream,
+      &unsupported);
+  if (unsupported) return SPEC_ERR_UNSUPPORTED;
+  return from_cuda(e);
 }
 
 spec_status spec_verify_chain(int32_t batch, int32_t vocab, spec_dtype dtype, const void* target_logits,

@@ -18,7 +18,7 @@
 // through distributed shared memory and writes the proposal and features.
 #include <cooperative_groups.h>
 
-#include "common.cuh"
+#include "pricing.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -38,35 +38,14 @@ struct NgramParams {
   int32_t win_cap;  // tokens of the staged window per CTA (multiple of 4)
   int32_t suf_cap;  // tokens of the staged suffix (multiple of 4)
   int32_t use_bulk; // 1: history rows are 16-byte aligned (bulk copies allowed)
+  // fused pricing (draft-and-price kernel only)
+  const int32_t* d;
+  const float* c;
+  const int32_t* d_len;
+  PriceCtx cx;
+  SelectCtx sc;
+  uint32_t* arrive;  // request arrival counter (zero between calls)
 };
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-// bounded wait on phase `parity` of an mbarrier; false when the bound ran out
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint32_t max_iter) {
-  const uint32_t addr = smem_u32(bar);
-  for (uint32_t it = 0; it < max_iter; ++it) {
-    uint32_t done;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-        " selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(done)
-        : "r"(addr), "r"(parity)
-        : "memory");
-    if (done) return true;
-  }
-  return false;
-}
-
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
-          smem_u32(dst)),
-      "l"(src), "r"(bytes), "r"(smem_u32(bar))
-      : "memory");
-}
 
 // top-2 of a set of distinct keys held as (b1 >= b2) per lane, merged across the warp
 __device__ __forceinline__ void warp_top2(unsigned long long& b1, unsigned long long& b2) {
@@ -93,7 +72,8 @@ __device__ __forceinline__ void top2_insert(unsigned long long& b1, unsigned lon
   }
 }
 
-__global__ void __launch_bounds__(SPEC_CTA_THREADS) ngram_kernel(NgramParams p) {
+template <bool CLUSTER, bool PRICE>
+__global__ void __launch_bounds__(SPEC_CTA_THREADS, 1) ngram_kernel(NgramParams p) {
   extern __shared__ __align__(16) int32_t smem_tok[];
   __shared__ __align__(8) uint64_t bar;
   __shared__ unsigned long long warp_best[SPEC_WARPS_PER_CTA][2];
@@ -101,14 +81,25 @@ __global__ void __launch_bounds__(SPEC_CTA_THREADS) ngram_kernel(NgramParams p) 
   __shared__ int32_t s_flag;
 
   cg::cluster_group cluster = cg::this_cluster();
-  const int C = (int)cluster.num_blocks();
-  const int rank = (int)cluster.block_rank();
+  const int C = CLUSTER ? (int)cluster.num_blocks() : 1;
+  const int rank = CLUSTER ? (int)cluster.block_rank() : 0;
   const int r = blockIdx.x / C;
   const int tid = threadIdx.x;
   const int32_t* x = p.hist + (int64_t)r * p.stride;
 
   const int32_t T = p.hist_len[r];
   const bool valid = (T >= 0) && ((int64_t)T <= p.stride);
+  // fused pricing: warp 0 of rank 0 fetches the model drafter's chain now, while
+  // the history copy is in flight
+  __shared__ int32_t s_dv[SPEC_MAX_L], s_gv[SPEC_MAX_L], s_dl;
+  __shared__ float s_cv[SPEC_MAX_L];
+  if (PRICE && rank == 0 && tid < 32) {
+    if (tid == 0) s_dl = p.d_len[r];
+    if (tid < p.cx.K) {
+      s_dv[tid] = p.d[(int64_t)r * p.cx.K + tid];
+      s_cv[tid] = p.c[(int64_t)r * p.cx.K + tid];
+    }
+  }
   const int32_t nc = valid && T >= 2 ? T - 1 : 0;  // candidate end positions 0..T-2
   const int32_t per = (nc + C - 1) / C;
   const int32_t j0 = min(nc, rank * per);
@@ -127,15 +118,13 @@ __global__ void __launch_bounds__(SPEC_CTA_THREADS) ngram_kernel(NgramParams p) 
   if (work) {
     if (p.use_bulk) {
       if (tid == 0) {
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(smem_u32(&bar)) : "memory");
-        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+        mbar_init(&bar, 1);
+        fence_mbar_init();
       }
       __syncthreads();
       if (tid == 0) {
         const uint32_t wb = (uint32_t)(w1 - w0) * 4u, sb = (uint32_t)(s1 - s0) * 4u;
-        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(&bar)),
-                     "r"(wb + sb)
-                     : "memory");
+        mbar_arrive_expect_tx(&bar, wb + sb);
         bulk_g2s(win, x + w0, wb, &bar);
         bulk_g2s(suf, x + s0, sb, &bar);
       }
@@ -182,16 +171,24 @@ __global__ void __launch_bounds__(SPEC_CTA_THREADS) ngram_kernel(NgramParams p) 
     cta_best[0] = c1;
     cta_best[1] = c2;
   }
-  cluster.sync();
+  if (CLUSTER)
+    cluster.sync();
+  else
+    __syncthreads();
 
   if (rank == 0) {
     __shared__ unsigned long long fin[2];
     if (tid == 0) {
       unsigned long long c1 = 0ull, c2 = 0ull;
-      for (int q = 0; q < C; ++q) {
-        const unsigned long long* peer = cluster.map_shared_rank(cta_best, q);
-        top2_insert(c1, c2, peer[0]);
-        top2_insert(c1, c2, peer[1]);
+      if (CLUSTER) {
+        for (int q = 0; q < C; ++q) {
+          const unsigned long long* peer = cluster.map_shared_rank(cta_best, q);
+          top2_insert(c1, c2, peer[0]);
+          top2_insert(c1, c2, peer[1]);
+        }
+      } else {
+        c1 = cta_best[0];
+        c2 = cta_best[1];
       }
       fin[0] = c1;
       fin[1] = c2;
@@ -204,29 +201,53 @@ __global__ void __launch_bounds__(SPEC_CTA_THREADS) ngram_kernel(NgramParams p) 
       jb = (int32_t)(best & 0xFFFFFFFFull);
       len = min(p.L, T - 1 - jb);
     }
+    // x[t] for a proposal token: one CTA holds every position it can name in
+    // shared memory (window up to w1, suffix from s0); a cluster reads memory
+    auto tok_at = [&](int32_t t) -> int32_t {
+      if (!CLUSTER) return t < w1 ? win[t - w0] : suf[t - s0];
+      return x[t];
+    };
     for (int i = tid; i < p.L; i += blockDim.x)
-      p.g[(int64_t)r * p.L + i] = i < len ? x[jb + 1 + i] : -1;
-    if (tid == 0) {
-      if (best == 0ull) {
-        p.g_len[r] = 0;
-        p.match_n[r] = 0;
-        p.agree[r] = 0;
-        p.copy_len[r] = 0;
-      } else {
-        const int32_t lb = (int32_t)(best >> 32);
-        p.g_len[r] = len;
-        p.match_n[r] = min(lb, p.n_max);
-        p.copy_len[r] = lb;
-        int32_t a = 1;
-        if (second != 0ull) {
-          const int32_t j2 = (int32_t)(second & 0xFFFFFFFFull);
-          a = (x[j2 + 1] == x[jb + 1]) ? 1 : 0;
-        }
-        p.agree[r] = a;
+      p.g[(int64_t)r * p.L + i] = i < len ? tok_at(jb + 1 + i) : -1;
+    int32_t n_out = 0, a_out = 0, m_out = 0;
+    if (best != 0ull) {
+      const int32_t lb = (int32_t)(best >> 32);
+      n_out = min(lb, p.n_max);
+      m_out = lb;
+      a_out = 1;
+      if (second != 0ull) {
+        const int32_t j2 = (int32_t)(second & 0xFFFFFFFFull);
+        a_out = (tok_at(j2 + 1) == tok_at(jb + 1)) ? 1 : 0;
       }
     }
+    if (tid == 0) {
+      p.g_len[r] = len;
+      p.match_n[r] = n_out;
+      p.agree[r] = a_out;
+      p.copy_len[r] = m_out;
+    }
+    if (PRICE) {
+      // price this request from on-chip values (warp 0), then arrive; the CTA
+      // of the last request to arrive allocates the budget for the whole batch
+      __shared__ int32_t s_last;
+      if (tid < 32) {
+        uint32_t st = 0;
+        if (tid < p.L) s_gv[tid] = tid < len ? tok_at(jb + 1 + tid) : -1;
+        __syncwarp();
+        price_request_warp(p.cx, r, tid, s_gv, len, n_out, a_out, m_out, s_dv, s_cv, s_dl, st);
+        if (st) set_status(p.status, st);
+        __syncwarp();
+        if (tid == 0) {
+          const uint32_t old = atomic_add_acq_rel(p.arrive, 1u);
+          s_last = (old + 1u == (uint32_t)p.batch) ? 1 : 0;
+          if (s_last) *p.arrive = 0u;  // ready for the next call
+        }
+      }
+      __syncthreads();
+      if (s_last) select_budget_cta(p.sc, suf + p.suf_cap);
+    }
   }
-  cluster.sync();  // peers keep their shared memory until rank 0 has read it
+  if (CLUSTER) cluster.sync();  // peers keep their shared memory until rank 0 has read it
 }
 
 }  // namespace spec
@@ -234,50 +255,21 @@ __global__ void __launch_bounds__(SPEC_CTA_THREADS) ngram_kernel(NgramParams p) 
 // ---------------------------------------------------------------------------
 // host launcher (called from api.cu)
 // ---------------------------------------------------------------------------
-extern "C" cudaError_t spec_launch_ngram(const int32_t* hist, int64_t stride, const int32_t* hist_len,
-                                         int32_t batch, int32_t n_min, int32_t n_max, int32_t L,
-                                         int32_t cap, int32_t* g, int32_t* g_len, int32_t* match_n,
-                                         int32_t* agree, int32_t* copy_len, uint32_t* status,
-                                         int num_sms, cudaStream_t stream, int* unsupported) {
-  *unsupported = 0;
-  if (batch == 0) return cudaSuccess;
-  // cluster size: enough CTAs to cover the GPU, at least 256 positions each,
-  // at most 8 (the portable cluster limit)
-  int64_t c_len = (stride + 4095) / 4096;
-  int64_t c_occ = (2 * (int64_t)num_sms + batch - 1) / batch;
-  int64_t C = c_len > c_occ ? c_len : c_occ;
-  if (C > stride / 256) C = stride / 256;
-  if (C < 1) C = 1;
-  if (C > 8) C = 8;
-  const int64_t per = (stride + C - 1) / C;
-  const int64_t win_cap = ((per + cap + 8) + 3) & ~int64_t(3);
-  const int64_t suf_cap = ((int64_t)cap + 8 + 3) & ~int64_t(3);
-  const size_t smem = (size_t)(win_cap + suf_cap) * sizeof(int32_t);
-  if (smem > 200 * 1024) {
-    *unsupported = 1;
-    return cudaSuccess;
-  }
-  spec::NgramParams p;
-  p.hist = hist;
-  p.stride = stride;
-  p.hist_len = hist_len;
-  p.batch = batch;
-  p.n_min = n_min;
-  p.n_max = n_max;
-  p.L = L;
-  p.cap = cap;
-  p.g = g;
-  p.g_len = g_len;
-  p.match_n = match_n;
-  p.agree = agree;
-  p.copy_len = copy_len;
-  p.status = status;
-  p.win_cap = (int32_t)win_cap;
-  p.suf_cap = (int32_t)suf_cap;
-  p.use_bulk = ((reinterpret_cast<uintptr_t>(hist) & 15u) == 0 && (stride & 3) == 0) ? 1 : 0;
+namespace {
 
-  cudaError_t e = cudaFuncSetAttribute(spec::ngram_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem);
+template <bool PRICE>
+cudaError_t launch_ngram_kernel(const spec::NgramParams& p, int64_t C, size_t smem, int32_t batch,
+                                cudaStream_t stream) {
+  if (C == 1) {
+    // one CTA per request: a plain launch, no cluster barrier or DSMEM
+    cudaError_t e = cudaFuncSetAttribute(spec::ngram_kernel<false, PRICE>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    spec::ngram_kernel<false, PRICE><<<batch, SPEC_CTA_THREADS, smem, stream>>>(p);
+    return cudaGetLastError();
+  }
+  cudaError_t e = cudaFuncSetAttribute(spec::ngram_kernel<true, PRICE>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(batch * C), 1, 1);
@@ -291,5 +283,115 @@ extern "C" cudaError_t spec_launch_ngram(const int32_t* hist, int64_t stride, co
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, spec::ngram_kernel, p);
+  return cudaLaunchKernelEx(&cfg, spec::ngram_kernel<true, PRICE>, p);
+}
+
+// cluster size, staged-window sizes and shared memory of one launch; false if
+// the history rows are too long for shared memory
+bool ngram_geometry(int64_t stride, int32_t cap, int32_t extra_ints, int64_t* C_out, spec::NgramParams* p,
+                    size_t* smem_out) {
+  // one CTA per 8192 candidate positions (32 per thread), at most 8 (the
+  // portable cluster limit); a cluster of one needs no merge traffic
+  int64_t C = (stride + 8191) / 8192;
+  if (C < 1) C = 1;
+  if (C > 8) C = 8;
+  const int64_t per = (stride + C - 1) / C;
+  const int64_t win_cap = ((per + cap + 8) + 3) & ~int64_t(3);
+  const int64_t suf_cap = ((int64_t)cap + 8 + 3) & ~int64_t(3);
+  const size_t smem = (size_t)(win_cap + suf_cap + extra_ints) * sizeof(int32_t);
+  if (smem > 200 * 1024) return false;
+  p->win_cap = (int32_t)win_cap;
+  p->suf_cap = (int32_t)suf_cap;
+  *C_out = C;
+  *smem_out = smem;
+  return true;
+}
+
+void ngram_common(spec::NgramParams* p, const int32_t* hist, int64_t stride, const int32_t* hist_len,
+                  int32_t batch, int32_t n_min, int32_t n_max, int32_t L, int32_t cap, int32_t* g,
+                  int32_t* g_len, int32_t* match_n, int32_t* agree, int32_t* copy_len, uint32_t* status) {
+  *p = spec::NgramParams{};
+  p->hist = hist;
+  p->stride = stride;
+  p->hist_len = hist_len;
+  p->batch = batch;
+  p->n_min = n_min;
+  p->n_max = n_max;
+  p->L = L;
+  p->cap = cap;
+  p->g = g;
+  p->g_len = g_len;
+  p->match_n = match_n;
+  p->agree = agree;
+  p->copy_len = copy_len;
+  p->status = status;
+  p->use_bulk = ((reinterpret_cast<uintptr_t>(hist) & 15u) == 0 && (stride & 3) == 0) ? 1 : 0;
+}
+
+}  // namespace
+
+extern "C" cudaError_t spec_launch_ngram(const int32_t* hist, int64_t stride, const int32_t* hist_len,
+                                         int32_t batch, int32_t n_min, int32_t n_max, int32_t L,
+                                         int32_t cap, int32_t* g, int32_t* g_len, int32_t* match_n,
+                                         int32_t* agree, int32_t* copy_len, uint32_t* status,
+                                         int num_sms, cudaStream_t stream, int* unsupported) {
+  (void)num_sms;
+  *unsupported = 0;
+  if (batch == 0) return cudaSuccess;
+  spec::NgramParams p;
+  ngram_common(&p, hist, stride, hist_len, batch, n_min, n_max, L, cap, g, g_len, match_n, agree, copy_len,
+               status);
+  int64_t C;
+  size_t smem;
+  if (!ngram_geometry(stride, cap, 0, &C, &p, &smem)) {
+    *unsupported = 1;
+    return cudaSuccess;
+  }
+  return launch_ngram_kernel<false>(p, C, smem, batch, stream);
+}
+
+extern "C" cudaError_t spec_launch_draft_price(
+    const int32_t* hist, int64_t stride, const int32_t* hist_len, int32_t batch, int32_t n_min, int32_t n_max,
+    int32_t cap, int32_t* g, int32_t* g_len, int32_t* match_n, int32_t* agree, int32_t* copy_len, int32_t K,
+    int32_t L, const int32_t* d, const float* c, const int32_t* d_len, const spec_estimator* est,
+    const float* table, float lambda, int32_t budget, int32_t mvl, int32_t policy, int32_t draft_greedy,
+    int32_t* chain, float* S, int32_t* chain_len, int32_t* source, int32_t* verify_len, int32_t* row_off,
+    uint8_t* point_mass, uint32_t* status, cudaStream_t stream, int* unsupported) {
+  *unsupported = 0;
+  spec::NgramParams p;
+  ngram_common(&p, hist, stride, hist_len, batch, n_min, n_max, L, cap, g, g_len, match_n, agree, copy_len,
+               status);
+  p.d = d;
+  p.c = c;
+  p.d_len = d_len;
+  p.cx.K = K;
+  p.cx.L = L;
+  p.cx.table = table;
+  p.cx.tab_const = est->use_constant_h;
+  p.cx.n_full = est->n_full;
+  p.cx.m_cap = est->m_cap;
+  p.cx.lambda = lambda;
+  p.cx.policy = policy;
+  p.cx.draft_greedy = draft_greedy;
+  p.cx.chain = chain;
+  p.cx.S = S;
+  p.cx.chain_len = chain_len;
+  p.cx.source = source;
+  p.cx.point_mass = point_mass;
+  p.sc.batch = batch;
+  p.sc.L = L;
+  p.sc.budget = budget;
+  p.sc.mvl = mvl;
+  p.sc.S = S;
+  p.sc.chain_len = chain_len;
+  p.sc.verify_len = verify_len;
+  p.sc.row_off = row_off;
+  p.arrive = status + 2;  // the third word of the workspace header
+  int64_t C;
+  size_t smem;
+  if (!ngram_geometry(stride < 1 ? 1 : stride, cap, spec::select_scratch_ints(batch, L), &C, &p, &smem)) {
+    *unsupported = 1;
+    return cudaSuccess;
+  }
+  return launch_ngram_kernel<true>(p, C, smem, batch, stream);
 }

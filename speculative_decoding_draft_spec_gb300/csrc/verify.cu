@@ -32,6 +32,11 @@
 namespace spec {
 
 enum { MODE_CHAIN_GREEDY = 0, MODE_CHAIN_SAMPLE = 1, MODE_TREE = 2 };
+
+// streaming kernel: 12 warps per CTA, one CTA per SM, each warp with its own
+// ring of 2 x 8 KB stages (192 KB of shared memory in flight per SM)
+#define VR_WARPS 12
+#define VR_THREADS (32 * VR_WARPS)
 enum { KIND_POINT = 0, KIND_BONUS = 1, KIND_Q = 2 };
 
 struct VerifyParams {
@@ -200,106 +205,312 @@ __device__ __forceinline__ float load_one(const void* row, int64_t i) {
 }
 
 // ------------------------------------------------------------------ per unit
-// greedy: fold the unit's (max, lowest index) into the row key
+// A chunk is 8 KB of one row (4096 bf16 / 2048 fp32 entries).  Each lane holds
+// NV 16-byte vectors of it: vector vv = lane + 32 k covers chunk offsets
+// [8 vv, 8 vv + 8) (bf16) or [4 vv, 4 vv + 4) (fp32); vectors past the row's
+// end hold -inf.
 template <int DT>
-__device__ __forceinline__ void unit_argmax(const VerifyParams& p, const void* row, int u, int slot,
-                                            int lane) {
-  const int e0 = u * SPEC_UNIT;
-  const int n_el = min(SPEC_UNIT, p.vocab - e0);
-  const bool vec = p.vec_ok != 0;
-  int bad = 0;
-  float lane_max = -INFINITY;
-  int idx = 0x7FFFFFFF;
-  float wm;
-  if (DT == 1 && vec) {
-    // bf16 pairs: packed max on the tensor-free HMNMX2 path, NaN pairs ignored
-    const uint16_t* rp = static_cast<const uint16_t*>(row) + e0;
-    uint4 w[8];
+struct Vec {
+  static constexpr int NV = 16;                // vectors per lane per chunk
+  static constexpr int PER = DT == 1 ? 8 : 4;  // entries per vector
+  static constexpr int CH = 32 * NV * PER;     // entries per chunk: 4096 bf16 / 2048 fp32
+  static constexpr int BYTES = 8192;           // bytes per chunk (one pipeline stage)
+  static constexpr int STAGES = 2;
+  static constexpr int SUB = CH / SPEC_UNIT;   // 2048-entry units per chunk
+  static constexpr uint32_t NEG = DT == 1 ? 0xFF80FF80u : 0xFF800000u;
+};
+
+template <int DT>
+__device__ __forceinline__ void vec_load_global(const void* unit, int n_el, int lane, uint4 (&w)[Vec<DT>::NV]) {
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const int vv = lane + 32 * k;
-      w[k] = (8 * vv < n_el) ? ldg_stream(rp + 8 * vv)
-                             : make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);
-    }
-    __nv_bfloat162 m2 = __floats2bfloat162_rn(-INFINITY, -INFINITY);
-    uint32_t nan = 0;
+  for (int k = 0; k < Vec<DT>::NV; ++k) {
+    const int vv = lane + 32 * k;
+    w[k] = (Vec<DT>::PER * vv < n_el) ? ldg_stream(static_cast<const uint4*>(unit) + vv)
+                                      : make_uint4(Vec<DT>::NEG, Vec<DT>::NEG, Vec<DT>::NEG, Vec<DT>::NEG);
+  }
+}
+
+template <int DT>
+__device__ __forceinline__ void vec_load_smem(const void* unit, int n_el, int lane, uint4 (&w)[Vec<DT>::NV]) {
+  if (n_el == Vec<DT>::CH) {  // no bounds tests on a full chunk
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const uint32_t ws[4] = {w[k].x, w[k].y, w[k].z, w[k].w};
+    for (int k = 0; k < Vec<DT>::NV; ++k) w[k] = static_cast<const uint4*>(unit)[lane + 32 * k];
+    return;
+  }
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        uint32_t word = ws[q];
-        m2 = __hmax2(m2, *reinterpret_cast<const __nv_bfloat162*>(&word));
-        nan |= __vcmpgtu2(word & 0x7FFF7FFFu, 0x7F807F80u);
-      }
-    }
-    bad = nan != 0;
-    lane_max = fmaxf(__low2float(m2), __high2float(m2));
-    wm = warp_max(lane_max);
-    if (lane_max == wm) {
+  for (int k = 0; k < Vec<DT>::NV; ++k) {
+    const int vv = lane + 32 * k;
+    w[k] = (Vec<DT>::PER * vv < n_el) ? static_cast<const uint4*>(unit)[vv]
+                                      : make_uint4(Vec<DT>::NEG, Vec<DT>::NEG, Vec<DT>::NEG, Vec<DT>::NEG);
+  }
+}
+
+__device__ __forceinline__ float vec_elem_f32(const uint4& v, int e) {
+  const uint32_t x = e == 0 ? v.x : e == 1 ? v.y : e == 2 ? v.z : v.w;
+  return __uint_as_float(x);
+}
+
+// argmax of one unit: packed key of (max, lowest unit offset) or 0 when the unit
+// holds only NaN; `bad` collects NaN / +Inf (warp-uniform after the call).
+// Per-vector maxima first (independent, so the dependency chains stay short),
+// NaN-propagating so that one test per lane finds a NaN; the NaN-ignoring
+// maximum is recomputed only for a unit that holds one.
+__device__ __forceinline__ __nv_bfloat162 as_bf2(uint32_t x) { return *reinterpret_cast<__nv_bfloat162*>(&x); }
+__device__ __forceinline__ uint32_t bf2_bits(__nv_bfloat162 x) { return *reinterpret_cast<uint32_t*>(&x); }
+
+template <int DT>
+__device__ __forceinline__ unsigned long long unit_argmax_vec(const uint4 (&w)[Vec<DT>::NV], int n_el, int lane,
+                                                              int& bad) {
+  constexpr int NV = Vec<DT>::NV;
+  float vmax[NV];  // max of each vector (NaN-propagating)
+  if (DT == 1) {
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const int vv = lane + 32 * k;
-        const uint32_t ws[4] = {w[k].x, w[k].y, w[k].z, w[k].w};
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          if (idx == 0x7FFFFFFF && 8 * vv < n_el) {
-            if (bf16_lo(ws[q]) == wm)
-              idx = 8 * vv + 2 * q;
-            else if (bf16_hi(ws[q]) == wm)
-              idx = 8 * vv + 2 * q + 1;
-          }
-        }
-      }
+    for (int k = 0; k < NV; ++k) {
+      const __nv_bfloat162 a = __hmax2_nan(as_bf2(w[k].x), as_bf2(w[k].y));
+      const __nv_bfloat162 b = __hmax2_nan(as_bf2(w[k].z), as_bf2(w[k].w));
+      const __nv_bfloat162 c = __hmax2_nan(a, b);
+      vmax[k] = fmaxf(__low2float(c), __high2float(c));
+      if (__low2float(c) != __low2float(c) || __high2float(c) != __high2float(c)) vmax[k] = __int_as_float(0x7FC00000);
     }
   } else {
-    float v[64];
-    load_unit<DT>(row, e0, n_el, vec, lane, v);
 #pragma unroll
-    for (int j = 0; j < 64; ++j) {
-      lane_max = fmaxf(lane_max, v[j]);
-      bad |= (v[j] != v[j]);
+    for (int k = 0; k < NV; ++k) {
+      const float a = __uint_as_float(w[k].x), b = __uint_as_float(w[k].y);
+      const float c = __uint_as_float(w[k].z), d = __uint_as_float(w[k].w);
+      const float m = fmaxf(fmaxf(a, b), fmaxf(c, d));
+      vmax[k] = ((a != a) | (b != b) | (c != c) | (d != d)) ? __int_as_float(0x7FC00000) : m;
     }
-    wm = warp_max(lane_max);
-    if (lane_max == wm) {
+  }
+  // NaN-propagating tree over the vectors
+  float t[NV];
 #pragma unroll
-      for (int j = 0; j < 64; ++j) {
-        const int i = idx_strided<DT>(lane, j, vec);
-        if (i < n_el && v[j] == wm && i < idx) idx = i;
+  for (int k = 0; k < NV; ++k) t[k] = vmax[k];
+#pragma unroll
+  for (int h = NV / 2; h > 0; h >>= 1)
+#pragma unroll
+    for (int k = 0; k < h; ++k) t[k] = (t[k] != t[k] || t[k + h] != t[k + h]) ? __int_as_float(0x7FC00000)
+                                                                              : fmaxf(t[k], t[k + h]);
+  float lane_max = t[0];
+  const bool has_nan = lane_max != lane_max;
+  if (__any_sync(0xFFFFFFFFu, has_nan)) {
+    // rare: a unit with NaN.  Per-vector NaN-ignoring maxima.
+    bad = 1;
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      float m = -INFINITY;
+      if (DT == 1) {
+        const uint32_t ws[4] = {w[k].x, w[k].y, w[k].z, w[k].w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) m = fmaxf(m, fmaxf(bf16_lo(ws[q]), bf16_hi(ws[q])));
+      } else {
+        m = fmaxf(fmaxf(__uint_as_float(w[k].x), __uint_as_float(w[k].y)),
+                  fmaxf(__uint_as_float(w[k].z), __uint_as_float(w[k].w)));
+      }
+      vmax[k] = m;
+    }
+    lane_max = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < NV; ++k) lane_max = fmaxf(lane_max, vmax[k]);
+  }
+  const float wm = warp_max(lane_max);
+  int idx = 0x7FFFFFFF;
+  if (lane_max == wm) {
+    // the first vector whose maximum is wm, then the first entry in it
+    int kf = -1;
+#pragma unroll
+    for (int k = NV - 1; k >= 0; --k)
+      if (vmax[k] == wm && Vec<DT>::PER * (lane + 32 * k) < n_el) kf = k;
+    if (kf >= 0) {
+      uint4 v = w[0];
+#pragma unroll
+      for (int k = 1; k < NV; ++k)
+        if (k == kf) v = w[k];
+      const int base = Vec<DT>::PER * (lane + 32 * kf);
+      if (DT == 1) {
+        const uint32_t ws[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int q = 3; q >= 0; --q) {
+          if (bf16_hi(ws[q]) == wm) idx = base + 2 * q + 1;
+          if (bf16_lo(ws[q]) == wm) idx = base + 2 * q;
+        }
+      } else {
+#pragma unroll
+        for (int e = 3; e >= 0; --e)
+          if (vec_elem_f32(v, e) == wm) idx = base + e;
       }
     }
   }
-  if (wm == INFINITY) bad = 1;
-  // lowest index among the lanes holding the maximum
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) idx = min(idx, __shfl_xor_sync(0xFFFFFFFFu, idx, o));
-  if (__any_sync(0xFFFFFFFFu, bad) && lane == 0) set_status(p.ws.status, SPEC_DEV_NONFINITE);
-  if (lane == 0 && idx != 0x7FFFFFFF) atomicMax(&p.ws.rowkey[slot], argmax_key(wm, e0 + idx));
+  bad |= __any_sync(0xFFFFFFFFu, wm == INFINITY);
+  return idx == 0x7FFFFFFF ? 0ull : argmax_key(wm, idx);
 }
 
-// sampled: (max, sum 2^((z - max) c)) of the unit
+// the k-th vector of a register-held chunk, by a jump table rather than a chain
+// of selects (only the lane holding the maximum takes this path)
+template <int NV>
+__device__ __forceinline__ uint4 pick_vec(const uint4 (&w)[NV], int k) {
+  uint4 v = w[0];
+  switch (k) {
+#define SPEC_PICK(i) \
+  case i:            \
+    if (i < NV) v = w[i < NV ? i : 0]; \
+    break;
+    SPEC_PICK(0) SPEC_PICK(1) SPEC_PICK(2) SPEC_PICK(3) SPEC_PICK(4) SPEC_PICK(5) SPEC_PICK(6) SPEC_PICK(7)
+    SPEC_PICK(8) SPEC_PICK(9) SPEC_PICK(10) SPEC_PICK(11) SPEC_PICK(12) SPEC_PICK(13) SPEC_PICK(14) SPEC_PICK(15)
+#undef SPEC_PICK
+    default:
+      break;
+  }
+  return v;
+}
+
+// bf16 argmax of one register-held chunk.  Packed bf16x2 maxima, NaN-propagating
+// so that one test per lane finds a NaN; the lane holding the maximum locates
+// its vector from the per-vector maxima and then the entry inside it.
+__device__ __forceinline__ unsigned long long chunk_argmax_bf16(const uint4 (&w)[Vec<1>::NV], int n_el, int lane,
+                                                                int& bad) {
+  constexpr int NV = Vec<1>::NV;
+  __nv_bfloat162 vm[NV];
+#pragma unroll
+  for (int k = 0; k < NV; ++k)
+    vm[k] = __hmax2_nan(__hmax2_nan(as_bf2(w[k].x), as_bf2(w[k].y)), __hmax2_nan(as_bf2(w[k].z), as_bf2(w[k].w)));
+  __nv_bfloat162 t[NV];
+#pragma unroll
+  for (int k = 0; k < NV; ++k) t[k] = vm[k];
+#pragma unroll
+  for (int h = NV / 2; h > 0; h >>= 1)
+#pragma unroll
+    for (int k = 0; k < h; ++k) t[k] = __hmax2_nan(t[k], t[k + h]);
+  const float lo = __low2float(t[0]), hi = __high2float(t[0]);
+  float lane_max = fmaxf(lo, hi);
+  if (__any_sync(0xFFFFFFFFu, (lo != lo) || (hi != hi))) {
+    // rare: the chunk holds a NaN.  NaN-ignoring per-vector maxima instead.
+    bad = 1;
+#pragma unroll
+    for (int k = 0; k < NV; ++k)
+      vm[k] = __hmax2(__hmax2(as_bf2(w[k].x), as_bf2(w[k].y)), __hmax2(as_bf2(w[k].z), as_bf2(w[k].w)));
+    lane_max = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < NV; ++k) lane_max = fmaxf(lane_max, fmaxf(__low2float(vm[k]), __high2float(vm[k])));
+  }
+  const float wm = warp_max(lane_max);
+  int idx = 0x7FFFFFFF;
+  if (lane_max == wm) {
+    const __nv_bfloat162 wm2 = __float2bfloat162_rn(wm);  // exact: wm is a bf16 value
+    int kf = -1;
+#pragma unroll
+    for (int k = NV - 1; k >= 0; --k)
+      if (__heq2_mask(vm[k], wm2) != 0u && 8 * (lane + 32 * k) < n_el) kf = k;
+    if (kf >= 0) {
+      const uint4 x = pick_vec<NV>(w, kf);
+      const int base = 8 * (lane + 32 * kf);
+      const uint32_t ws[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+      for (int q = 3; q >= 0; --q) {
+        if (bf16_hi(ws[q]) == wm) idx = base + 2 * q + 1;
+        if (bf16_lo(ws[q]) == wm) idx = base + 2 * q;
+      }
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) idx = min(idx, __shfl_xor_sync(0xFFFFFFFFu, idx, o));
+  bad |= __any_sync(0xFFFFFFFFu, wm == INFINITY);
+  return idx == 0x7FFFFFFF ? 0ull : argmax_key(wm, idx);
+}
+
+// (max, sum 2^((z - max) c)) of one unit; an all -inf unit gives (-inf, 0).
+// Several independent partial maxima and sums keep the dependency chains short.
+template <int DT, int KB, int KN>
+__device__ __forceinline__ float2 unit_softmax_vec(const uint4 (&w)[Vec<DT>::NV], float c, int& bad) {
+  float vm[KN];
+#pragma unroll
+  for (int k = 0; k < KN; ++k) {
+    const uint4& x = w[KB + k];
+    if (DT == 1) {
+      const __nv_bfloat162 a = __hmax2(as_bf2(x.x), as_bf2(x.y));
+      const __nv_bfloat162 b = __hmax2(as_bf2(x.z), as_bf2(x.w));
+      const __nv_bfloat162 m2 = __hmax2(a, b);
+      vm[k] = fmaxf(__low2float(m2), __high2float(m2));
+    } else {
+      vm[k] = fmaxf(fmaxf(__uint_as_float(x.x), __uint_as_float(x.y)),
+                    fmaxf(__uint_as_float(x.z), __uint_as_float(x.w)));
+    }
+  }
+#pragma unroll
+  for (int h = KN / 2; h > 0; h >>= 1)
+#pragma unroll
+    for (int k = 0; k < h; ++k) vm[k] = fmaxf(vm[k], vm[k + h]);
+  const float m = warp_max(vm[0]);
+  float s = 0.0f;
+  if (m != -INFINITY) {
+    const float mc = m * c;
+    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+    for (int k = 0; k < KN; ++k) {
+      const uint4& x = w[KB + k];
+      const uint32_t ws[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        if (DT == 1) {
+          acc[q] += ex2(fmaf(bf16_lo(ws[q]), c, -mc)) + ex2(fmaf(bf16_hi(ws[q]), c, -mc));
+        } else {
+          acc[q] += ex2(fmaf(__uint_as_float(ws[q]), c, -mc));
+        }
+      }
+    }
+    s = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+  }
+  s = warp_sum(s);
+  bad |= (!(s == s) || m == INFINITY) ? 1 : 0;
+  return make_float2(m, s);
+}
+
+// the same two reductions for rows that are not 16-byte aligned (scalar loads,
+// element j of a lane at unit offset lane + 32 j)
 template <int DT>
-__device__ __forceinline__ void unit_softmax(const VerifyParams& p, const void* row, int u, int slot,
-                                             int lane) {
-  const int e0 = u * SPEC_UNIT;
-  const int n_el = min(SPEC_UNIT, p.vocab - e0);
+__device__ __forceinline__ unsigned long long unit_argmax_scalar(const void* unit, int n_el, int lane, int& bad) {
   float v[64];
-  load_unit<DT>(row, e0, n_el, p.vec_ok != 0, lane, v);
+  load_unit<DT>(unit, 0, n_el, false, lane, v);
+  float lm = -INFINITY;
+  int nan = 0;
+#pragma unroll
+  for (int j = 0; j < 64; ++j) {
+    lm = fmaxf(lm, v[j]);
+    nan |= (v[j] != v[j]);
+  }
+  const float wm = warp_max(lm);
+  int idx = 0x7FFFFFFF;
+  if (lm == wm) {
+#pragma unroll
+    for (int j = 0; j < 64; ++j) {
+      const int i = lane + 32 * j;
+      if (i < n_el && v[j] == wm && i < idx) idx = i;
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) idx = min(idx, __shfl_xor_sync(0xFFFFFFFFu, idx, o));
+  bad |= __any_sync(0xFFFFFFFFu, nan || wm == INFINITY);
+  return idx == 0x7FFFFFFF ? 0ull : argmax_key(wm, idx);
+}
+
+template <int DT>
+__device__ __forceinline__ float2 unit_softmax_scalar(const void* unit, int n_el, int lane, float c, int& bad) {
+  float v[64];
+  load_unit<DT>(unit, 0, n_el, false, lane, v);
   float lm = -INFINITY;
 #pragma unroll
   for (int j = 0; j < 64; ++j) lm = fmaxf(lm, v[j]);
   const float m = warp_max(lm);
   float s = 0.0f;
   if (m != -INFINITY) {
-    const float mc = m * p.c;
+    const float mc = m * c;
 #pragma unroll
-    for (int j = 0; j < 64; ++j) s += ex2(fmaf(v[j], p.c, -mc));
+    for (int j = 0; j < 64; ++j) s += ex2(fmaf(v[j], c, -mc));
   }
   s = warp_sum(s);
-  if (lane == 0) {
-    if (!(s == s) || m == INFINITY) set_status(p.ws.status, SPEC_DEV_NONFINITE);
-    __stcg(&p.ws.partial[(int64_t)slot * p.ws.units + u], make_float2(m, s));
-  }
+  bad |= (!(s == s) || m == INFINITY) ? 1 : 0;
+  return make_float2(m, s);
 }
 
 // ------------------------------------------------------------------ helpers
@@ -319,6 +530,27 @@ __device__ __forceinline__ float2 merge_row(const VerifyParams& p, int slot, int
   const float M = warp_max(m);
   const float sc = (m == -INFINITY) ? 0.0f : s * ex2((m - M) * p.c);
   return make_float2(M, warp_sum(sc));
+}
+
+// (max, sum) of a whole row from its unit partials, by one lane: a max pass and
+// a rescaled-sum pass, each over independent loads
+__device__ __forceinline__ float2 merge_row_lane(const VerifyParams& p, int slot) {
+  const float2* pr = &p.ws.partial[(int64_t)slot * p.ws.units];
+  float m = -INFINITY;
+#pragma unroll 8
+  for (int u = 0; u < p.units; ++u) m = fmaxf(m, __ldcg(&pr[u]).x);
+  if (m == -INFINITY) return make_float2(m, 0.0f);
+  float s0 = 0.0f, s1 = 0.0f;
+#pragma unroll 8
+  for (int u = 0; u < p.units; ++u) {
+    const float2 t = __ldcg(&pr[u]);
+    const float w = t.x == -INFINITY ? 0.0f : t.y * ex2((t.x - m) * p.c);
+    if (u & 1)
+      s1 += w;
+    else
+      s0 += w;
+  }
+  return make_float2(m, s0 + s1);
 }
 
 // Inverse CDF over unit weights w_u (unit order) held as 3+ consecutive units
@@ -463,14 +695,12 @@ __device__ __forceinline__ int q_slot_of(const VerifyParams& p, int r, int i /*1
 template <int DT>
 __device__ void finalize_chain_greedy(const VerifyParams& p, int r, int base, int ell, int lane) {
   const int32_t* y = p.chain + (int64_t)r * p.L;
-  int a = 0;
-  if (lane <= ell) {
-    unsigned long long* kp = &p.ws.rowkey[base + lane];
-    const unsigned long long key = __ldcg(kp);
-    a = key ? argmax_key_index(key) : 0;  // an all-NaN row: 0 (flagged already)
-    *kp = 0ull;
-  }
-  const int yi = lane < ell ? y[lane] : -1;
+  // both loads first, then use them
+  unsigned long long key = 0ull;
+  if (lane <= ell) key = __ldcg(&p.ws.rowkey[base + lane]);
+  const int yi = lane < ell ? __ldcg(y + lane) : -1;
+  const int a = key ? argmax_key_index(key) : 0;  // an all-NaN row: 0 (flagged already)
+  if (lane <= ell) p.ws.rowkey[base + lane] = 0ull;
   const bool tested = lane < ell;
   if (tested && (yi < 0 || yi >= p.vocab)) set_status(p.ws.status, SPEC_DEV_BAD_TOKEN);
   const bool ok = tested && yi == a;
@@ -500,25 +730,22 @@ template <int DT>
 __device__ void finalize_chain_sample(const VerifyParams& p, int r, int base, int ell, int lane) {
   const int32_t* y = p.chain + (int64_t)r * p.L;
   const uint8_t* pmr = p.pm ? p.pm + (int64_t)r * p.L : nullptr;
-  // (max, sum) of each p row (lane i keeps row i) and each q row (lane i-1)
+  // (max, sum) of each p row (lane i merges row i) and each q row (lane i-1
+  // merges the draft row of position i): every lane reads its own row's unit
+  // partials with independent loads
   float mrow = 0.0f, srow = 0.0f, mq = 0.0f, sq = 0.0f;
   int use_q_lane = 0;
-  for (int i = 0; i <= ell; ++i) {
-    const float2 ms = merge_row(p, base + i, lane);
-    if (lane == i) {
-      mrow = ms.x;
-      srow = ms.y;
-    }
+  if (lane <= ell) {
+    const float2 ms = merge_row_lane(p, base + lane);
+    mrow = ms.x;
+    srow = ms.y;
   }
-  for (int i = 1; i <= ell; ++i) {
-    const int uq = p.use_q && pmr && pmr[i - 1] == 0 && i <= p.K;
-    if (uq) {
-      const float2 ms = merge_row(p, q_slot_of(p, r, i), lane);
-      if (lane == i - 1) {
-        mq = ms.x;
-        sq = ms.y;
-        use_q_lane = 1;
-      }
+  if (lane < ell) {
+    use_q_lane = (p.use_q && pmr && pmr[lane] == 0 && lane + 1 <= p.K) ? 1 : 0;
+    if (use_q_lane) {
+      const float2 ms = merge_row_lane(p, q_slot_of(p, r, lane + 1));
+      mq = ms.x;
+      sq = ms.y;
     }
   }
   // accept tests: lane i-1 tests position i
@@ -727,18 +954,53 @@ __device__ void finalize_tree(const VerifyParams& p, int r, int base, int n, int
 }
 
 // ------------------------------------------------------------------ main kernel
-template <int DT, int MODE>
-__global__ void __launch_bounds__(SPEC_CTA_THREADS, 2) verify_rows_kernel(VerifyParams p) {
-  extern __shared__ __align__(16) int32_t sm[];
-  int32_t* s_pre = sm;                   // [batch + 1] exclusive prefix of work rows
-  int32_t* s_base = sm + p.batch + 1;    // [batch] first row
-  int32_t* s_len = s_base + p.batch;     // [batch] verify_len (chain) or nodes (tree)
-  __shared__ int32_t s_part[SPEC_CTA_THREADS];
+// A cursor walks work rows in increasing order and locates each row's data.
+struct Cursor {
+  int r, item, slot;
+  const char* row;
+};
 
+template <int MODE>
+__device__ __forceinline__ void locate(const VerifyParams& p, const int32_t* s_pre, const int32_t* s_base,
+                                       const int32_t* s_len, int item, size_t esz, Cursor& c) {
+  if (item == c.item) return;
+  while (s_pre[c.r + 1] <= item) ++c.r;
+  c.item = item;
+  const int li = item - s_pre[c.r];
+  const int len = s_len[c.r];
+  if (MODE == MODE_TREE || li <= len) {
+    c.slot = s_base[c.r] + li;
+    c.row = static_cast<const char*>(p.logits) + (int64_t)c.slot * p.vocab * esz;
+  } else {
+    // the (li - len)-th position (1-based) that carries a draft distribution
+    int want = li - len, pos = 1;
+    const uint8_t* pmr = p.pm + (int64_t)c.r * p.L;
+    for (int i = 1; i <= len && i <= p.K; ++i)
+      if (pmr[i - 1] == 0 && --want == 0) {
+        pos = i;
+        break;
+      }
+    c.slot = q_slot_of(p, c.r, pos);
+    c.row = static_cast<const char*>(p.draft) + ((int64_t)c.r * p.K + pos - 1) * p.vocab * esz;
+  }
+}
+
+template <int DT, int MODE>
+__global__ void __launch_bounds__(VR_THREADS, 1) verify_rows_kernel(VerifyParams p) {
+  constexpr int ST = Vec<DT>::STAGES, UB = Vec<DT>::BYTES;
+  constexpr size_t esz = DT == 1 ? 2 : 4;
+  extern __shared__ __align__(128) unsigned char smem[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  unsigned char* stage = smem + (size_t)warp * ST * UB;  // this warp's ring of unit buffers
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)VR_WARPS * ST * UB) + warp * ST;
+  int32_t* s_pre = reinterpret_cast<int32_t*>(smem + (size_t)VR_WARPS * ST * (UB + 8));
+  int32_t* s_base = s_pre + p.batch + 1;
+  int32_t* s_len = s_base + p.batch;
+  __shared__ int32_t s_part[VR_WARPS];
+
   const int B = p.batch;
-  // ---- per-request row counts (every CTA computes the same table)
-  const int per_t = (B + SPEC_CTA_THREADS - 1) / SPEC_CTA_THREADS;
+  // ---- per-request work rows (every CTA builds the same table)
+  const int per_t = (B + VR_THREADS - 1) / VR_THREADS;
   int32_t my_sum = 0;
   const int32_t tot_rows = p.row_off[B];
   for (int q = 0; q < per_t; ++q) {
@@ -770,20 +1032,27 @@ __global__ void __launch_bounds__(SPEC_CTA_THREADS, 2) verify_rows_kernel(Verify
     if (!valid && blockIdx.x == 0) set_status(p.ws.status, SPEC_DEV_BAD_LENGTH);
     s_base[r] = b0;
     s_len[r] = valid ? len : -1;
-    s_pre[r] = cnt;  // counts for now
+    s_pre[r] = cnt;
     my_sum += cnt;
   }
-  // block exclusive scan of the per-thread sums, then each thread's range
-  s_part[tid] = my_sum;
-  __syncthreads();
-  for (int o = 1; o < SPEC_CTA_THREADS; o <<= 1) {
-    const int32_t t = tid >= o ? s_part[tid - o] : 0;
-    __syncthreads();
-    s_part[tid] += t;
-    __syncthreads();
-  }
+  // block exclusive scan of the per-thread sums: warp shuffles, then the warp totals
   {
-    int32_t run = s_part[tid] - my_sum;
+    int32_t x = my_sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int32_t t = __shfl_up_sync(0xFFFFFFFFu, x, o);
+      if (lane >= o) x += t;
+    }
+    if (lane == 31) s_part[warp] = x;
+    __syncthreads();
+    int32_t before = 0, all = 0;
+#pragma unroll
+    for (int q = 0; q < VR_WARPS; ++q) {
+      const int32_t t = s_part[q];
+      if (q < warp) before += t;
+      all += t;
+    }
+    int32_t run = before + x - my_sum;
     for (int q = 0; q < per_t; ++q) {
       const int r = tid * per_t + q;
       if (r >= B) break;
@@ -791,13 +1060,13 @@ __global__ void __launch_bounds__(SPEC_CTA_THREADS, 2) verify_rows_kernel(Verify
       s_pre[r] = run;
       run += cnt;
     }
-    if (tid == SPEC_CTA_THREADS - 1) s_pre[B] = s_part[tid];
+    if (tid == 0) s_pre[B] = all;
   }
   __syncthreads();
 
   // ---- outputs of invalid requests (CTA 0 only)
   if (blockIdx.x == 0) {
-    for (int r = warp; r < B; r += SPEC_WARPS_PER_CTA) {
+    for (int r = warp; r < B; r += VR_WARPS) {
       if (s_len[r] >= 0) continue;
       if (MODE == MODE_TREE) {
         for (int j = lane; j < p.max_nodes; j += 32) {
@@ -811,68 +1080,196 @@ __global__ void __launch_bounds__(SPEC_CTA_THREADS, 2) verify_rows_kernel(Verify
     }
   }
 
-  // ---- stream the units
-  const int units = p.units;
+  // ---- this warp's contiguous range of chunks (8 KB of one row each)
+  constexpr int CH = Vec<DT>::CH;
+  const int units = (p.vocab + CH - 1) / CH;  // chunks per row
   const int64_t total = (int64_t)s_pre[B] * units;
-  const int64_t nwarps = (int64_t)gridDim.x * SPEC_WARPS_PER_CTA;
-  for (int64_t w = (int64_t)blockIdx.x * SPEC_WARPS_PER_CTA + warp; w < total; w += nwarps) {
-    const int32_t item = (int32_t)(w / units);
-    const int u = (int)(w - (int64_t)item * units);
-    // request owning this row: the last r with s_pre[r] <= item
-    int lo = 0, hi = B - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (s_pre[mid] <= item)
-        lo = mid;
-      else
-        hi = mid - 1;
-    }
-    const int r = lo;
-    const int li = item - s_pre[r];
-    const int len = s_len[r];
-    int slot;
-    const void* row;
-    const size_t esz = DT == 1 ? 2 : 4;
-    if (MODE == MODE_TREE || li <= len) {
-      slot = s_base[r] + li;
-      row = static_cast<const char*>(p.logits) + (int64_t)slot * p.vocab * esz;
-    } else {
-      // the (li - len)-th position (1-based) that carries a draft distribution
-      int want = li - len, pos = 0;
-      const uint8_t* pmr = p.pm + (int64_t)r * p.L;
-      for (int i = 1; i <= len && i <= p.K; ++i)
-        if (pmr[i - 1] == 0 && --want == 0) {
-          pos = i;
-          break;
-        }
-      slot = q_slot_of(p, r, pos);
-      row = static_cast<const char*>(p.draft) + ((int64_t)r * p.K + pos - 1) * p.vocab * esz;
-    }
-    if (MODE == MODE_CHAIN_SAMPLE)
-      unit_softmax<DT>(p, row, u, slot, lane);
-    else
-      unit_argmax<DT>(p, row, u, slot, lane);
+  const int64_t nw = (int64_t)gridDim.x * VR_WARPS;
+  const int64_t gw = (int64_t)blockIdx.x * VR_WARPS + warp;
+  const int64_t lo = gw * total / nw, hi = (gw + 1) * total / nw;
+  if (lo >= hi) return;
+  const bool vec = p.vec_ok != 0;
 
-    // arrival: the warp that completes the request finalizes it
+  Cursor ic, cc;  // issue and consume cursors
+  {
+    const int first = (int)(lo / units);
+    int a = 0, b = B - 1;  // last r with s_pre[r] <= first
+    while (a < b) {
+      const int mid = (a + b + 1) >> 1;
+      if (s_pre[mid] <= first)
+        a = mid;
+      else
+        b = mid - 1;
+    }
+    ic.r = cc.r = a;
+    ic.item = cc.item = -1;
+  }
+  // the issue cursor walks (item, chunk) incrementally from lo; it locates a
+  // row only when it enters it and then advances its source pointer
+  int is_item = (int)(lo / units), is_u = (int)(lo - (int64_t)is_item * units);
+  const char* is_src = nullptr;
+  auto issue = [&](int s) {
+    if (is_src == nullptr) {
+      locate<MODE>(p, s_pre, s_base, s_len, is_item, esz, ic);
+      is_src = ic.row + (size_t)is_u * CH * esz;
+    }
+    const uint32_t bytes = (is_u + 1 < units) ? (uint32_t)UB : (uint32_t)((p.vocab - is_u * CH) * esz);
+    mbar_arrive_expect_tx(&bars[s], bytes);
+    bulk_g2s(stage + (size_t)s * UB, is_src, bytes, &bars[s]);
+    is_src += UB;
+    if (++is_u == units) {
+      is_u = 0;
+      ++is_item;
+      is_src = nullptr;
+    }
+  };
+  if (vec) {
+    if (lane == 0) {
+      for (int s = 0; s < ST; ++s) mbar_init(&bars[s], 1);
+      fence_mbar_init();
+      for (int s = 0; s < ST && lo + s < hi; ++s) issue(s);
+    }
+    __syncwarp();
+  }
+
+  int run_r = -1, run_slot = -1;
+  uint32_t run_units = 0;
+  unsigned long long run_key = 0ull;
+  int bad = 0, aborted = 0;
+  int64_t w = lo;
+
+  auto flush_row = [&]() {
+    if (MODE != MODE_CHAIN_SAMPLE && run_slot >= 0 && run_key != 0ull && lane == 0)
+      atomicMax(&p.ws.rowkey[run_slot], run_key);
+  };
+  auto flush_request = [&]() {
+    if (run_r < 0) return;
     int last = 0;
     if (lane == 0) {
-      __threadfence();
-      const uint32_t need = (uint32_t)((s_pre[r + 1] - s_pre[r]) * units);
-      const uint32_t old = atomicAdd(&p.ws.counter[r], 1u);
-      last = (old + 1u == need);
+      // release this warp's partials / row keys, acquire everyone else's
+      const uint32_t need = (uint32_t)((s_pre[run_r + 1] - s_pre[run_r]) * units);
+      const uint32_t old = atomic_add_acq_rel(&p.ws.counter[run_r], run_units);
+      last = (old + run_units == need);
     }
     last = __shfl_sync(0xFFFFFFFFu, last, 0);
     if (last) {
-      __threadfence();
+      __syncwarp();  // orders every lane after lane 0's acquire
       if (MODE == MODE_TREE)
-        finalize_tree(p, r, s_base[r], len, lane);
+        finalize_tree(p, run_r, s_base[run_r], s_len[run_r], lane);
       else if (MODE == MODE_CHAIN_GREEDY)
-        finalize_chain_greedy<DT>(p, r, s_base[r], len, lane);
+        finalize_chain_greedy<DT>(p, run_r, s_base[run_r], s_len[run_r], lane);
       else
-        finalize_chain_sample<DT>(p, r, s_base[r], len, lane);
-      if (lane == 0) p.ws.counter[r] = 0u;
+        finalize_chain_sample<DT>(p, run_r, s_base[run_r], s_len[run_r], lane);
+      if (lane == 0) p.ws.counter[run_r] = 0u;
+    }
+  };
+
+  int item = (int)(lo / units), u = (int)(lo - (int64_t)item * units);
+  int s = 0;
+  uint32_t ph = 0;
+  for (; w < hi; ++w) {
+    locate<MODE>(p, s_pre, s_base, s_len, item, esz, cc);
+    if (cc.slot != run_slot) {
+      flush_row();
+      run_slot = cc.slot;
+      run_key = 0ull;
+    }
+    if (cc.r != run_r) {
+      flush_request();
+      run_r = cc.r;
+      run_units = 0;
+    }
+    const int e0 = u * CH;
+    const int n_el = min(CH, p.vocab - e0);
+    unsigned long long key = 0ull;
+    float2 ms[Vec<DT>::SUB];
+    if (vec) {
+      const bool landed = mbar_wait_bounded(&bars[s], ph, 1u << 22);
+      if (!__all_sync(0xFFFFFFFFu, landed)) {  // warp-uniform decision
+        aborted = 1;
+        break;
+      }
+      // copy the chunk to registers and refill the stage at once, so that two
+      // copies per warp stay in flight while it computes
+      uint4 v[Vec<DT>::NV];
+      vec_load_smem<DT>(stage + (size_t)s * UB, n_el, lane, v);
+      __syncwarp();
+      if (lane == 0 && w + ST < hi) issue(s);
+      if (MODE == MODE_CHAIN_SAMPLE) {
+        if (DT == 1) {
+          ms[0] = unit_softmax_vec<DT, 0, 8>(v, p.c, bad);
+          if (Vec<DT>::SUB > 1) ms[Vec<DT>::SUB - 1] = unit_softmax_vec<DT, 8, 8>(v, p.c, bad);
+        } else {
+          ms[0] = unit_softmax_vec<DT, 0, 16>(v, p.c, bad);
+        }
+      } else if (DT == 1) {
+        key = chunk_argmax_bf16(v, n_el, lane, bad);
+      } else {
+        key = unit_argmax_vec<DT>(v, n_el, lane, bad);
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < Vec<DT>::SUB; ++j) {
+        const int e1 = e0 + j * SPEC_UNIT;
+        const int n1 = min(SPEC_UNIT, p.vocab - e1);
+        if (n1 <= 0) {
+          ms[j] = make_float2(-INFINITY, 0.0f);
+          continue;
+        }
+        const void* unit = cc.row + (size_t)e1 * esz;
+        if (MODE == MODE_CHAIN_SAMPLE) {
+          ms[j] = unit_softmax_scalar<DT>(unit, n1, lane, p.c, bad);
+        } else {
+          unsigned long long k1 = unit_argmax_scalar<DT>(unit, n1, lane, bad);
+          if (k1 != 0ull) {  // rebase to the chunk offset
+            const int32_t i1 = argmax_key_index(k1) + j * SPEC_UNIT;
+            k1 = (k1 & 0xFFFFFFFF00000000ull) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)i1);
+            if (k1 > key) key = k1;
+          }
+        }
+      }
+    }
+    if (MODE == MODE_CHAIN_SAMPLE) {
+      if (lane == 0) {
+#pragma unroll
+        for (int j = 0; j < Vec<DT>::SUB; ++j) {
+          const int uu = u * Vec<DT>::SUB + j;
+          if (uu * SPEC_UNIT < p.vocab) __stcg(&p.ws.partial[(int64_t)cc.slot * p.ws.units + uu], ms[j]);
+        }
+      }
+    } else if (key != 0ull) {
+      // rebase the chunk offset to the row index; keys of one row fold by max
+      const int32_t idx = argmax_key_index(key) + e0;
+      const unsigned long long kk =
+          (key & 0xFFFFFFFF00000000ull) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)idx);
+      if (kk > run_key) run_key = kk;
+    }
+    ++run_units;
+    if (++u == units) {
+      u = 0;
+      ++item;
+    }
+    if (++s == ST) {
+      s = 0;
+      ph ^= 1u;
     }
   }
+  if (aborted) {
+    // a copy did not land in time: record it, wait (bounded) for every copy this
+    // warp still has in flight, and stop without finalizing
+    if (lane == 0) {
+      set_status(p.ws.status, SPEC_DEV_TIMEOUT);
+      for (int64_t x = w; x < hi && x < w + ST; ++x) {
+        const int s = (int)((x - lo) % ST);
+        mbar_wait_bounded(&bars[s], (uint32_t)(((x - lo) / ST) & 1), 1u << 22);
+      }
+    }
+    __syncwarp();
+    return;
+  }
+  flush_row();
+  flush_request();
+  if (bad && lane == 0) set_status(p.ws.status, SPEC_DEV_NONFINITE);
 }
 
 // ------------------------------------------------------------------ draw from max(0, p - q)
@@ -983,19 +1380,14 @@ int grid_for(Kern k, size_t smem, int num_sms) {
 
 template <int DT, int MODE>
 cudaError_t launch_rows(const spec::VerifyParams& p, int num_sms, cudaStream_t stream) {
-  const size_t smem = (size_t)(3 * p.batch + 1) * sizeof(int32_t);
+  using V = spec::Vec<DT>;
+  const size_t smem = (size_t)VR_WARPS * V::STAGES * (V::BYTES + 8) +
+                      (size_t)(3 * p.batch + 1) * sizeof(int32_t);
   auto k = spec::verify_rows_kernel<DT, MODE>;
-  if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-  }
-  static int cached_grid = 0;
-  static size_t cached_smem = 0;
-  if (cached_grid == 0 || cached_smem != smem) {
-    cached_grid = grid_for(k, smem, num_sms);
-    cached_smem = smem;
-  }
-  k<<<cached_grid, SPEC_CTA_THREADS, smem, stream>>>(p);
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  // one CTA per SM: the shared-memory rings hold the bytes in flight
+  k<<<num_sms, VR_THREADS, smem, stream>>>(p);
   return cudaGetLastError();
 }
 

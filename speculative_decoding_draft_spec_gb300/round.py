@@ -1,17 +1,18 @@
 """One hybrid speculative-decoding round on preallocated device buffers.
 
 ChainRound holds every buffer of steps 1-3 for one batch shape and launches
-spec_ngram_propose -> spec_price_and_allocate -> spec_verify_chain on one
-stream with no host synchronisation in between (Hybrid Spark sec. 4.4: the
-host only passes lambda and the budget as scalars).  The three launches can
-be captured once into a CUDA graph and replayed.
+spec_draft_and_price (steps 1 and 2 in one kernel; or spec_ngram_propose then
+spec_price_and_allocate) -> spec_verify_chain on one stream with no host
+synchronisation in between (Hybrid Spark sec. 4.4: the host only passes lambda
+and the budget as scalars).  The launches can be captured once into a CUDA
+graph and replayed.
 """
 from __future__ import annotations
 
 import torch
 
-from . import (EstimatorTable, Workspace, spec_ngram_propose, spec_price_and_allocate,
-               spec_verify_chain)
+from . import (EstimatorTable, Workspace, spec_draft_and_price, spec_ngram_propose,
+               spec_price_and_allocate, spec_verify_chain)
 
 
 class ChainRound:
@@ -47,7 +48,15 @@ class ChainRound:
         self.c.copy_(torch.as_tensor(c), non_blocking=True)
         self.d_len.copy_(torch.as_tensor(d_len), non_blocking=True)
 
-    def draft_and_price(self, lam, budget, max_verify_len, policy="proposed", draft_greedy=True, stream=None):
+    def draft_and_price(self, lam, budget, max_verify_len, policy="proposed", draft_greedy=True, stream=None,
+                        fused=True):
+        if fused:
+            spec_draft_and_price(self.hist, self.hist_len, self.n_min, self.n_max, self.copy_cap, self.g,
+                                 self.g_len, self.match_n, self.agree, self.copy_len, self.d, self.c, self.d_len,
+                                 self.est, lam, budget, max_verify_len, policy, draft_greedy, self.chain, self.S,
+                                 self.chain_len, self.source, self.verify_len, self.row_off, self.point_mass,
+                                 self.ws, stream)
+            return
         spec_ngram_propose(self.hist, self.hist_len, self.n_min, self.n_max, self.L, self.copy_cap, self.g,
                            self.g_len, self.match_n, self.agree, self.copy_len, self.ws, stream)
         spec_price_and_allocate(self.d, self.c, self.d_len, self.g, self.g_len, self.match_n, self.agree,

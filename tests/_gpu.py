@@ -137,3 +137,24 @@ def compare_sampled(g, o, logits, row_off, chain, verify_len, pm, draft, T, tol=
             stats["draw_band"] += 1
         stats["exact"] += 1
     return stats
+
+
+def gpu_draft_price(S, ws, est, hist, hist_len, n_min, n_max, cap, d, c, d_len, lam, budget, mvl, policy, greedy,
+                    L=15):
+    """the fused steps 1 + 2 through spec_draft_and_price"""
+    B, K = d.shape
+    i32 = dict(dtype=torch.int32, device=DEV)
+    g = torch.full((B, L), -7, **i32)
+    gl, n, a, m = (torch.full((B,), -7, **i32) for _ in range(4))
+    chain = torch.full((B, L), -7, **i32)
+    Sv = torch.full((B, L), -7.0, dtype=torch.float32, device=DEV)
+    chain_len, source, verify_len = (torch.full((B,), -7, **i32) for _ in range(3))
+    row_off = torch.full((B + 1,), -7, **i32)
+    pm = torch.full((B, L), 7, dtype=torch.uint8, device=DEV)
+    S.spec_draft_and_price(dev(hist, torch.int32), dev(hist_len, torch.int32), n_min, n_max, cap, g, gl, n, a, m,
+                           dev(d, torch.int32), dev(c, torch.float32), dev(d_len, torch.int32), est, lam, budget, mvl,
+                           policy, greedy, chain, Sv, chain_len, source, verify_len, row_off, pm, ws)
+    torch.cuda.synchronize()
+    return dict(g=host(g), g_len=host(gl), match_n=host(n), agree=host(a), copy_len=host(m), chain=host(chain),
+                S=host(Sv), chain_len=host(chain_len), source=host(source), verify_len=host(verify_len),
+                row_off=host(row_off), point_mass=host(pm))

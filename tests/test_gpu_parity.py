@@ -12,7 +12,8 @@ import torch
 import oracle as O
 import workloads as W
 
-from ._gpu import compare_sampled, gpu_chain, gpu_ngram, gpu_price, gpu_tree, host, logits_dev
+from ._gpu import (compare_sampled, gpu_chain, gpu_draft_price, gpu_ngram, gpu_price, gpu_tree, host,
+                   logits_dev)
 
 pytestmark = pytest.mark.gpu
 
@@ -53,13 +54,12 @@ def test_estimator_table_equals_oracle_on_every_key(S, name, coef):
             if n == nf:
                 continue
             for a in (0, 1):
-                got = tab[((k - 1) * 33 + n) * 2 + a]
+                got = tab[(n * 2 + a) * L + (k - 1)]
                 if got != O.estimate_h(coef, k, n, a, n):
                     mism.append((k, n, a))
         for a in (0, 1):
-            base = L * 66 + ((k - 1) * 2 + a) * (mcap + 1)
             for m in range(1, mcap + 1):
-                if tab[base + m] != O.estimate_h(coef, k, nf, a, m):
+                if tab[L * 66 + (a * (mcap + 1) + m) * L + (k - 1)] != O.estimate_h(coef, k, nf, a, m):
                     mism.append((k, nf, a, m))
     assert not mism, mism[:10]
 
@@ -191,6 +191,59 @@ def test_price_flags_out_of_range_confidences(S):
     g, o, ws = _price_both(S, cfg, ng, policy="model_only", greedy=True, budget=5, lam=0.1, mvl=15)
     _assert_price_equal(g, o)
     assert ws.status() & S.DEV_BITS["bad_value"]
+
+
+# ------------------------------------------------------------------ fused steps 1 + 2
+def _fused_vs_oracle(S, c, policy=None, greedy=None, budget=None, lam=None, mvl=None):
+    policy = c["policy"] if policy is None else policy
+    greedy = c["draft_greedy"] if greedy is None else greedy
+    budget = c["budget"] if budget is None else budget
+    lam = c["lam"] if lam is None else lam
+    mvl = c["max_verify_len"] if mvl is None else mvl
+    B, K = c["d"].shape
+    est = S.EstimatorTable(c["coef"], c["L"])
+    ws = _ws(S, B, 1, K, 1)
+    got = gpu_draft_price(S, ws, est, c["hist"], c["hist_len"], c["n_min"], c["n_max"], c["copy_cap"], c["d"],
+                          c["c"], c["d_len"], lam, budget, mvl, policy, greedy, L=c["L"])
+    ng = O.ngram_propose(c["hist"], c["hist_len"], c["n_min"], c["n_max"], c["L"], c["copy_cap"])
+    for k, want in (("g", ng.g), ("g_len", ng.g_len), ("match_n", ng.match_n), ("agree", ng.agree),
+                    ("copy_len", ng.copy_len)):
+        assert np.array_equal(got[k], want), k
+    o = O.price_and_allocate(c["d"], c["c"], c["d_len"], ng.g, ng.g_len, ng.match_n, ng.agree, ng.copy_len,
+                             c["coef"], lam, budget, mvl, policy, greedy)
+    _assert_price_equal(got, o)
+    return got, o, ws
+
+
+@pytest.mark.parametrize("name", ["tiny", "tiny_prob", "edit_bs4", "edit_bs4_prob", "mixed_bs128", "long_bs64"])
+def test_fused_draft_and_price_on_workloads(S, name):
+    c = {"tiny": lambda: W.tiny(), "tiny_prob": lambda: W.tiny(probabilistic=True),
+         "edit_bs4": lambda: W.edit_bs4(), "edit_bs4_prob": lambda: W.edit_bs4(temperature=1.0, probabilistic=True),
+         "mixed_bs128": W.mixed_bs128, "long_bs64": W.long_bs64}[name]()
+    got, o, ws = _fused_vs_oracle(S, c)
+    assert ws.status() == 0
+    # called twice in a row: the arrival counter is back at zero
+    got2, _, _ = _fused_vs_oracle(S, c)
+    assert np.array_equal(got2["row_off"], o.row_off)
+
+
+def test_fused_draft_and_price_random_stress(S):
+    rng = np.random.default_rng(41)
+    for trial in range(30):
+        B = int(rng.integers(1, 200))
+        stride = int(rng.choice([37, 64, 300, 2048]))
+        K, L = 7, 15
+        hist = rng.integers(0, int(rng.choice([2, 3, 5, 50])), (B, stride)).astype(np.int32)
+        hist_len = rng.integers(0, stride + 1, B).astype(np.int32)
+        d = np.where(rng.random((B, K)) < 0.5, hist[:, :K], rng.integers(0, 5, (B, K))).astype(np.int32)
+        c = {"hist": hist, "hist_len": hist_len, "n_min": int(rng.integers(1, 4)), "copy_cap": 256,
+             "d": d, "c": rng.choice([0.5, 0.9, 1.0, 0.3], (B, K)).astype(np.float32),
+             "d_len": rng.integers(0, K + 1, B).astype(np.int32), "L": L,
+             "coef": [W.table5_coef(n_full=6), W.table7_coef(3), W.constant_coef(0.9)][trial % 3]}
+        c["n_max"] = int(rng.integers(c["n_min"], 7))
+        _fused_vs_oracle(S, c, policy=["proposed", "ngram_first", "extension", "model_only", "ngram_only"][trial % 5],
+                         greedy=bool(trial % 2), budget=int(rng.integers(0, B * L + 3)),
+                         lam=float(rng.choice([0.0, 0.04, 0.3])), mvl=int(rng.integers(0, 16)))
 
 
 # ------------------------------------------------------------------ chain verification
