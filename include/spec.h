@@ -126,6 +126,8 @@ typedef struct {
   size_t off_rowkey;     /* uint64 [max_rows]: packed row argmax             */
   size_t off_partial;    /* float2 [(max_rows + max_batch K) x units]        */
   size_t off_partial2;   /* double [max_batch x units]                       */
+  size_t off_keys;       /* uint32 [SPEC_MAX_PRICE_BATCH x SPEC_MAX_L]:
+                            allocation keys of the pricing step            */
   int32_t units;         /* ceil(vocab / 2048)                               */
   int32_t pad_;
 } spec_workspace;

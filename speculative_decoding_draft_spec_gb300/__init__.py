@@ -46,7 +46,7 @@ class WorkspaceStruct(C.Structure):
         ("max_batch", C.c_int32), ("max_rows", C.c_int32), ("K", C.c_int32), ("vocab", C.c_int32),
         ("off_counter", C.c_size_t), ("off_counter2", C.c_size_t), ("off_record", C.c_size_t),
         ("off_rowkey", C.c_size_t), ("off_partial", C.c_size_t), ("off_partial2", C.c_size_t),
-        ("units", C.c_int32), ("pad_", C.c_int32),
+        ("off_keys", C.c_size_t), ("units", C.c_int32), ("pad_", C.c_int32),
     ]
 
 

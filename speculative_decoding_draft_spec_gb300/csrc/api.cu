@@ -23,14 +23,14 @@ cudaError_t spec_launch_price(int32_t batch, int32_t K, int32_t L, const int32_t
                               int32_t budget, int32_t mvl, int32_t policy, int32_t draft_greedy,
                               int32_t* chain, float* S, int32_t* chain_len, int32_t* source,
                               int32_t* verify_len, int32_t* row_off, uint8_t* point_mass,
-                              uint32_t* status, cudaStream_t stream);
+                              uint32_t* status, uint32_t* keys, cudaStream_t stream);
 cudaError_t spec_launch_draft_price(
     const int32_t* hist, int64_t stride, const int32_t* hist_len, int32_t batch, int32_t n_min, int32_t n_max,
     int32_t cap, int32_t* g, int32_t* g_len, int32_t* match_n, int32_t* agree, int32_t* copy_len, int32_t K,
     int32_t L, const int32_t* d, const float* c, const int32_t* d_len, const spec_estimator* est,
     const float* table, float lambda, int32_t budget, int32_t mvl, int32_t policy, int32_t draft_greedy,
     int32_t* chain, float* S, int32_t* chain_len, int32_t* source, int32_t* verify_len, int32_t* row_off,
-    uint8_t* point_mass, uint32_t* status, cudaStream_t stream, int* unsupported);
+    uint8_t* point_mass, uint32_t* status, uint32_t* keys, cudaStream_t stream, int* unsupported);
 cudaError_t spec_launch_verify_chain(int32_t batch, int32_t vocab, int32_t dtype, const void* logits,
                                      const int32_t* row_off, const void* draft, int32_t K,
                                      const int32_t* chain, int32_t L, const int32_t* verify_len,
@@ -83,6 +83,8 @@ bool layout(int32_t max_batch, int32_t max_rows, int32_t K, int32_t vocab, spec_
   off = align256(off + sizeof(float2) * (size_t)units * ((size_t)max_rows + (size_t)max_batch * K));
   w->off_partial2 = off;
   off = align256(off + sizeof(double) * (size_t)units * (size_t)max_batch);
+  w->off_keys = off;  // sized for the largest pricing batch, whatever max_batch is
+  off = align256(off + sizeof(uint32_t) * (size_t)SPEC_MAX_PRICE_BATCH * SPEC_MAX_L);
   w->bytes = off;
   w->max_batch = max_batch;
   w->max_rows = max_rows;
@@ -94,10 +96,16 @@ bool layout(int32_t max_batch, int32_t max_rows, int32_t K, int32_t vocab, spec_
 }
 
 bool ws_ok(const spec_workspace* ws) {
-  return ws && ws->base && (reinterpret_cast<uintptr_t>(ws->base) & 255u) == 0;
+  return ws && ws->base && (reinterpret_cast<uintptr_t>(ws->base) & 255u) == 0 &&
+         ws->off_keys % 256 == 0 &&
+         ws->bytes >= ws->off_keys + sizeof(uint32_t) * (size_t)SPEC_MAX_PRICE_BATCH * SPEC_MAX_L;
 }
 
 uint32_t* status_of(const spec_workspace* ws) { return static_cast<uint32_t*>(ws->base); }
+
+uint32_t* keys_of(const spec_workspace* ws) {
+  return reinterpret_cast<uint32_t*>(static_cast<char*>(ws->base) + ws->off_keys);
+}
 
 }  // namespace
 
@@ -202,7 +210,7 @@ spec_status spec_price_and_allocate(
   return from_cuda(spec_launch_price(batch, K, L, d, c, d_len, g, g_len, match_n, agree, copy_len,
                                      est, est_table, lambda, budget, max_verify_len, (int32_t)policy,
                                      draft_greedy ? 1 : 0, chain, S, chain_len, source, verify_len,
-                                     row_off, point_mass, status_of(ws), stream));
+                                     row_off, point_mass, status_of(ws), keys_of(ws), stream));
 }
 
 spec_status spec_draft_and_price(
@@ -237,8 +245,8 @@ spec_status spec_draft_and_price(
   const cudaError_t e = spec_launch_draft_price(
       hist, hist_stride < 1 ? 1 : hist_stride, hist_len, batch, n_min, n_max, copy_cap, g, g_len, match_n, agree,
       copy_len, K, L, d, c, d_len, est, est_table, lambda, budget, max_verify_len, (int32_t)policy,
-      draft_greedy ? 1 : 0, chain, S, chain_len, source, verify_len, row_off, point_mass, status_of(ws), stream,
-      &unsupported);
+      draft_greedy ? 1 : 0, chain, S, chain_len, source, verify_len, row_off, point_mass, status_of(ws), keys_of(ws),
+      stream, &unsupported);
   if (unsupported) return SPEC_ERR_UNSUPPORTED;
   return from_cuda(e);
 }

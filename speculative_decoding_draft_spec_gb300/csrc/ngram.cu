@@ -91,13 +91,13 @@ __global__ void __launch_bounds__(SPEC_CTA_THREADS, 1) ngram_kernel(NgramParams 
   const bool valid = (T >= 0) && ((int64_t)T <= p.stride);
   // fused pricing: warp 0 of rank 0 fetches the model drafter's chain now, while
   // the history copy is in flight
-  __shared__ int32_t s_dv[SPEC_MAX_L], s_gv[SPEC_MAX_L], s_dl;
-  __shared__ float s_cv[SPEC_MAX_L];
+  __shared__ PriceStage s_ps;
+  __shared__ int32_t s_dl;
   if (PRICE && rank == 0 && tid < 32) {
     if (tid == 0) s_dl = p.d_len[r];
     if (tid < p.cx.K) {
-      s_dv[tid] = p.d[(int64_t)r * p.cx.K + tid];
-      s_cv[tid] = p.c[(int64_t)r * p.cx.K + tid];
+      s_ps.d[tid] = p.d[(int64_t)r * p.cx.K + tid];
+      s_ps.c[tid] = p.c[(int64_t)r * p.cx.K + tid];
     }
   }
   const int32_t nc = valid && T >= 2 ? T - 1 : 0;  // candidate end positions 0..T-2
@@ -232,9 +232,9 @@ __global__ void __launch_bounds__(SPEC_CTA_THREADS, 1) ngram_kernel(NgramParams 
       __shared__ int32_t s_last;
       if (tid < 32) {
         uint32_t st = 0;
-        if (tid < p.L) s_gv[tid] = tid < len ? tok_at(jb + 1 + tid) : -1;
+        if (tid < p.L) s_ps.g[tid] = tid < len ? tok_at(jb + 1 + tid) : -1;
         __syncwarp();
-        price_request_warp(p.cx, r, tid, s_gv, len, n_out, a_out, m_out, s_dv, s_cv, s_dl, st);
+        price_request_warp(p.cx, r, tid, s_ps, len, n_out, a_out, m_out, s_dl, st);
         if (st) set_status(p.status, st);
         __syncwarp();
         if (tid == 0) {
@@ -356,7 +356,7 @@ extern "C" cudaError_t spec_launch_draft_price(
     int32_t L, const int32_t* d, const float* c, const int32_t* d_len, const spec_estimator* est,
     const float* table, float lambda, int32_t budget, int32_t mvl, int32_t policy, int32_t draft_greedy,
     int32_t* chain, float* S, int32_t* chain_len, int32_t* source, int32_t* verify_len, int32_t* row_off,
-    uint8_t* point_mass, uint32_t* status, cudaStream_t stream, int* unsupported) {
+    uint8_t* point_mass, uint32_t* status, uint32_t* keys, cudaStream_t stream, int* unsupported) {
   *unsupported = 0;
   spec::NgramParams p;
   ngram_common(&p, hist, stride, hist_len, batch, n_min, n_max, L, cap, g, g_len, match_n, agree, copy_len,
@@ -378,12 +378,12 @@ extern "C" cudaError_t spec_launch_draft_price(
   p.cx.chain_len = chain_len;
   p.cx.source = source;
   p.cx.point_mass = point_mass;
+  p.cx.mvl = mvl;
+  p.cx.keys = keys;
   p.sc.batch = batch;
   p.sc.L = L;
   p.sc.budget = budget;
-  p.sc.mvl = mvl;
-  p.sc.S = S;
-  p.sc.chain_len = chain_len;
+  p.sc.keys = keys;
   p.sc.verify_len = verify_len;
   p.sc.row_off = row_off;
   p.arrive = status + 2;  // the third word of the workspace header

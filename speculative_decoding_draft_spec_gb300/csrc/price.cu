@@ -11,15 +11,15 @@
 // All products and sums use explicit round-to-nearest intrinsics in a fixed
 // order so that the selection is reproducible bit for bit.
 //
-// GB300 layout, one launch: phase 1 gives every request one warp (lane k holds
-// position k+1: its table entry, draft tokens and confidence arrive in one
-// coalesced round trip; the survivals and chain values are formed left to right
-// by broadcasting the terms in order, so the fp32 results equal the sequential
-// definition bit for bit).  Phase 2 runs in the last CTA to arrive (an
-// acquire-release counter, no waiting): the b-th largest survival is found by a
-// 4-pass 8-bit radix select over the fp32 bit patterns with warp-aggregated
-// shared-memory histograms, ties at the threshold are resolved in (request,
-// position) order by a block scan, and a second scan builds the row offsets.
+// GB300 layout, one launch: phase 1 gives every request one warp (lane k stages
+// position k+1 of the request's rows in shared memory in one coalesced round
+// trip; the survivals and chain values are then formed left to right, so the
+// fp32 results equal the sequential definition bit for bit) and writes one
+// allocation key per slot.  Phase 2 runs in the last CTA to arrive (an
+// acquire-release counter, no waiting): the budget-th largest key is found by
+// a four-pass radix select with per-warp shared-memory histograms, and one
+// block scan of the per-request (above, tie) counts gives verify_len and the
+// row offsets.
 #include "pricing.cuh"
 
 namespace spec {
@@ -106,6 +106,7 @@ struct PriceParams {
 // waiting) allocates the budget for the whole batch with one warp.
 __global__ void __launch_bounds__(PR_THREADS, 1) price_kernel(PriceParams p) {
   extern __shared__ __align__(16) int32_t s_scratch[];  // select_scratch_ints(batch, L)
+  __shared__ PriceStage s_ps[PR_WARPS];
   __shared__ int32_t s_last;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   {
@@ -113,8 +114,15 @@ __global__ void __launch_bounds__(PR_THREADS, 1) price_kernel(PriceParams p) {
     const int r = blockIdx.x * PR_WARPS + warp;
     if (r < p.batch) {
       const int32_t K = p.cx.K, L = p.cx.L;
-      price_request_warp(p.cx, r, lane, p.g + (int64_t)r * L, p.g_len[r], p.match_n[r], p.agree[r],
-                         p.copy_len[r], p.d + (int64_t)r * K, p.c + (int64_t)r * K, p.d_len[r], st);
+      const int32_t gl = p.g_len[r], n = p.match_n[r], a = p.agree[r], m = p.copy_len[r], dl = p.d_len[r];
+      PriceStage& ps = s_ps[warp];
+      if (lane < L) ps.g[lane] = p.g[(int64_t)r * L + lane];
+      if (lane < K) {
+        ps.d[lane] = p.d[(int64_t)r * K + lane];
+        ps.c[lane] = p.c[(int64_t)r * K + lane];
+      }
+      __syncwarp();
+      price_request_warp(p.cx, r, lane, ps, gl, n, a, m, dl, st);
     }
     if (st) set_status(p.status, st);
   }
@@ -168,7 +176,7 @@ extern "C" cudaError_t spec_launch_price(
     const int32_t* copy_len, const spec_estimator* est, const float* table, float lambda,
     int32_t budget, int32_t mvl, int32_t policy, int32_t draft_greedy, int32_t* chain, float* S,
     int32_t* chain_len, int32_t* source, int32_t* verify_len, int32_t* row_off,
-    uint8_t* point_mass, uint32_t* status, cudaStream_t stream) {
+    uint8_t* point_mass, uint32_t* status, uint32_t* keys, cudaStream_t stream) {
   spec::PriceParams p;
   p.batch = batch;
   p.d = d;
@@ -193,12 +201,12 @@ extern "C" cudaError_t spec_launch_price(
   p.cx.chain_len = chain_len;
   p.cx.source = source;
   p.cx.point_mass = point_mass;
+  p.cx.mvl = mvl;
+  p.cx.keys = keys;
   p.sc.batch = batch;
   p.sc.L = L;
   p.sc.budget = budget;
-  p.sc.mvl = mvl;
-  p.sc.S = S;
-  p.sc.chain_len = chain_len;
+  p.sc.keys = keys;
   p.sc.verify_len = verify_len;
   p.sc.row_off = row_off;
   p.status = status;

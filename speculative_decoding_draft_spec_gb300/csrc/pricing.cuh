@@ -25,18 +25,18 @@ struct PriceCtx {
   const float* table;
   int32_t tab_const, n_full, m_cap;
   float lambda;
-  int32_t policy, draft_greedy;
+  int32_t policy, draft_greedy, mvl;
   int32_t* chain;
   float* S;
   int32_t* chain_len;
   int32_t* source;
   uint8_t* point_mass;
+  uint32_t* keys;  // [batch x L] allocation keys (workspace)
 };
 
 struct SelectCtx {
-  int32_t batch, L, budget, mvl;
-  const float* S;
-  const int32_t* chain_len;
+  int32_t batch, L, budget;
+  const uint32_t* keys;
   int32_t* verify_len;
   int32_t* row_off;
 };
@@ -67,15 +67,24 @@ __device__ __forceinline__ const float* table_row(const PriceCtx& cx, int32_t n,
   return nullptr;
 }
 
-// Chain choice and survivals of request r by one warp.  Every lane reads the
-// request's whole (short) rows -- the same addresses, so one broadcast load per
-// element -- and forms the sequential products and sums itself, left to right
-// in k, one correctly rounded fp32 operation at a time; lane k then writes
-// position k+1.  `gt`/`dt`/`ct` are the n-gram tokens, model tokens and
-// confidences (global or shared memory, any lane may read any entry).
-__device__ __forceinline__ void price_request_warp(const PriceCtx& cx, int r, int lane, const int32_t* gt,
-                                                   int32_t gl, int32_t n, int32_t a, int32_t m,
-                                                   const int32_t* dt, const float* ct, int32_t dl,
+// One request's short rows, staged in shared memory by the warp that prices it.
+struct PriceStage {
+  float h[32];    // h_1..h_gl (filled by price_request_warp)
+  int32_t g[32];  // n-gram chain
+  int32_t d[32];  // model drafter's chain
+  float c[32];    // model drafter's confidences (clamped in place)
+};
+
+// Chain choice, survivals and allocation keys of request r by one warp (all 32
+// lanes call it).  On entry ps.g[0, min(gl, L)), ps.d[0, K) and ps.c[0, K) hold
+// the request's n-gram tokens, model tokens and raw confidences, written by
+// this warp before a __syncwarp.  Lane j stages h_{j+1}; then every lane runs
+// the same left-to-right recurrence over the staged rows, one correctly
+// rounded fp32 operation at a time, and keeps the values of position j+1,
+// which it writes.  The loops stay rolled: this code runs once per request and
+// its latency, not its throughput, is on the critical path of the round.
+__device__ __forceinline__ void price_request_warp(const PriceCtx& cx, int r, int lane, PriceStage& ps,
+                                                   int32_t gl, int32_t n, int32_t a, int32_t m, int32_t dl,
                                                    uint32_t& st) {
   const int32_t K = cx.K, L = cx.L;
   if (dl < 0 || dl > K) {
@@ -91,34 +100,25 @@ __device__ __forceinline__ void price_request_warp(const PriceCtx& cx, int r, in
     a = 1;
   }
   const float* hrow = table_row(cx, n, a, m, gl, st);
-  float hv[SPEC_MAX_L], cv[SPEC_MAX_L];
-  int32_t gv[SPEC_MAX_L], dv[SPEC_MAX_L];
-#pragma unroll
-  for (int j = 0; j < SPEC_MAX_L; ++j) {
-    hv[j] = (j < gl && hrow) ? __ldg(hrow + (cx.tab_const ? 0 : j)) : 0.0f;
-    gv[j] = j < gl ? gt[j] : -1;
-    dv[j] = j < dl ? dt[j] : -1;
-    cv[j] = j < dl ? ct[j] : 0.0f;
-  }
-  uint32_t st_c = 0;
-#pragma unroll
-  for (int j = 0; j < SPEC_MAX_L; ++j)
-    if (j < dl) cv[j] = clamp_conf(cv[j], st_c);
-  if (lane == 0) st |= st_c;
-  // survivals and chain values, left to right
-  float sg[SPEC_MAX_L], sd[SPEC_MAX_L];
-  float run_g = 1.0f, run_d = 1.0f, vg = 0.0f, vd = 0.0f;
-  bool d_prefix = dl >= 1 && gl > dl;
-#pragma unroll
-  for (int j = 0; j < SPEC_MAX_L; ++j) {
-    run_g = __fmul_rn(run_g, hv[j]);
-    run_d = __fmul_rn(run_d, cv[j]);
-    sg[j] = run_g;
-    sd[j] = run_d;
-    if (j < gl) vg = __fadd_rn(vg, fmaxf(__fsub_rn(run_g, cx.lambda), 0.0f));
+  if (lane < gl) ps.h[lane] = hrow ? __ldg(hrow + (cx.tab_const ? 0 : lane)) : 0.0f;
+  if (lane < dl) ps.c[lane] = clamp_conf(ps.c[lane], st);
+  __syncwarp();
+  // S^g_k, S^d_k and the chain values, k = 1, 2, ... in order
+  float run_g = 1.0f, run_d = 1.0f, vg = 0.0f, vd = 0.0f, my_g = 0.0f, my_d = 0.0f;
+  bool d_prefix = dl >= 1 && gl > dl;  // d is a proper prefix of g (contains rule)
+  const int32_t jn = gl > dl ? gl : dl;
+#pragma unroll 1
+  for (int j = 0; j < jn; ++j) {
+    if (j < gl) {
+      run_g = __fmul_rn(run_g, ps.h[j]);
+      vg = __fadd_rn(vg, fmaxf(__fsub_rn(run_g, cx.lambda), 0.0f));
+      if (j == lane) my_g = run_g;
+    }
     if (j < dl) {
+      run_d = __fmul_rn(run_d, ps.c[j]);
       vd = __fadd_rn(vd, fmaxf(__fsub_rn(run_d, cx.lambda), 0.0f));
-      if (gv[j] != dv[j]) d_prefix = false;
+      if (j == lane) my_d = run_d;
+      d_prefix = d_prefix && ps.g[j] == ps.d[j];
     }
   }
   int32_t src = SPEC_SRC_MODEL;
@@ -141,50 +141,49 @@ __device__ __forceinline__ void price_request_warp(const PriceCtx& cx, int r, in
   }
   const int32_t len = (src == SPEC_SRC_MODEL) ? dl : gl;
   const uint8_t model_pm = cx.draft_greedy ? 1 : 0;
-  // lane k emits position k+1 (register arrays are read at constant indices)
-  const int k = lane;
   int32_t tok = -1;
   float sv = 0.0f;
   uint8_t pm = 0;
-  float prev = 1.0f;
-#pragma unroll
-  for (int j = 0; j < SPEC_MAX_L; ++j) {
-    if (j < len) {
-      int32_t tj;
-      float sj;
-      uint8_t pj;
-      if (src == SPEC_SRC_MODEL) {
-        tj = dv[j];
-        sj = sd[j];
-        pj = model_pm;
-      } else if (src == SPEC_SRC_NGRAM) {
-        tj = gv[j];
-        sj = sg[j];
-        pj = 1;
-      } else {
-        // contains rule / extension: the first dl positions take max(S^g, S^d)
-        // (contains) or S^d (extension); the tail continues S_j = S_{j-1} h_j
-        tj = gv[j];
-        if (j < dl) {
-          sj = (src == SPEC_SRC_CONTAINS) ? fmaxf(sg[j], sd[j]) : sd[j];
-          pj = (src == SPEC_SRC_EXTENSION) ? model_pm : (uint8_t)1;
-        } else {
-          sj = __fmul_rn(prev, hv[j]);
-          pj = 1;
-        }
-        prev = sj;
-      }
-      if (j == k) {
-        tok = tj;
-        sv = sj;
-        pm = pj;
+  if (src == SPEC_SRC_MODEL) {
+    if (lane < dl) {
+      tok = ps.d[lane];
+      sv = my_d;
+      pm = model_pm;
+    }
+  } else if (src == SPEC_SRC_NGRAM) {
+    if (lane < gl) {
+      tok = ps.g[lane];
+      sv = my_g;
+      pm = 1;
+    }
+  } else {
+    // contains rule / extension: the first dl positions take max(S^g, S^d)
+    // (contains) or S^d (extension); the tail continues S_j = S_{j-1} h_j
+    const bool contains = (src == SPEC_SRC_CONTAINS);
+    if (lane < gl) tok = ps.g[lane];
+    if (lane < dl) {
+      sv = contains ? fmaxf(my_g, my_d) : my_d;
+      pm = contains ? (uint8_t)1 : model_pm;
+    }
+    float prev = __shfl_sync(0xFFFFFFFFu, sv, dl - 1);  // dl >= 1 on this branch
+#pragma unroll 1
+    for (int j = dl; j < gl; ++j) {
+      prev = __fmul_rn(prev, ps.h[j]);
+      if (j == lane) {
+        sv = prev;
+        pm = 1;
       }
     }
   }
-  if (k < L) {
-    cx.chain[(int64_t)r * L + k] = tok;
-    cx.S[(int64_t)r * L + k] = sv;
-    cx.point_mass[(int64_t)r * L + k] = pm;
+  if (lane < L) {
+    const int64_t q = (int64_t)r * L + lane;
+    cx.chain[q] = tok;
+    cx.S[q] = sv;
+    cx.point_mass[q] = pm;
+    // allocation key: survival bits + 1 for a slot that may be verified, 0
+    // otherwise (S >= 0, so the bits order like the values; S <= 1 keeps the
+    // key below 2^30)
+    cx.keys[q] = (lane < len && lane < cx.mvl) ? __float_as_uint(sv) + 1u : 0u;
   }
   if (lane == 0) {
     cx.chain_len[r] = len;
@@ -193,16 +192,20 @@ __device__ __forceinline__ void price_request_warp(const PriceCtx& cx, int r, in
 }
 
 // ---------------------------------------------------------------------------
-// Batch-wide allocation by one CTA (all its threads call this).
-// Slot q = r * L + k (request, position order); its key is w = bits(S) + 1 for
-// a valid slot (k < min(chain_len, max_verify_len)), 0 otherwise (survivals
-// are >= 0, so their bits order like their values, and S <= 1.0f keeps w below
-// 2^30).  theta, the budget-th largest survival, is the largest t with
-// count(w >= t + 1) >= budget, built two bits per step from the top with one
-// barrier per step; slots above theta are taken, then the ties at theta in
-// slot order until the budget is spent.
+// Batch-wide allocation by one CTA of exactly 256 threads (all call this).
+// Slot q = r * L + k is taken when its key exceeds theta, or equals theta and
+// lies among the first `need` such slots in slot order; theta and need follow
+// from the budget: none (theta = ~0), every valid slot (budget >= number of
+// valid slots: theta = 0), else theta = the key of the budget-th slot in the
+// order (key desc, slot asc), found by a four-pass radix select over the key
+// bits 29..22 | 21..14 | 13..6 | 5..0 from the top.  Survivals fall along a
+// chain (products of factors in [0, 1]) and ties go to the lower position, so
+// every request takes a prefix: ell_r = above_r + min(eq_r, max(0, need - E_r))
+// with E_r the ties of the requests before r, and
+// row_off[r] = r + sum_{r' < r} above_r' + min(need, E_r), one block scan of
+// the pair (above, eq).
 // Shared scratch: select_scratch_ints(batch, L) ints.
-__host__ __device__ inline int select_scratch_ints(int batch, int L) { return batch * L + batch + 64; }
+__host__ __device__ inline int select_scratch_ints(int batch, int L) { return batch * L + 2 * 8 * 256 + 96; }
 
 static __device__ __forceinline__ int32_t cta_sum(int32_t v, int32_t* red /*[2][32]*/, int& parity) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -217,141 +220,149 @@ static __device__ __forceinline__ int32_t cta_sum(int32_t v, int32_t* red /*[2][
   return t;
 }
 
-static __device__ __forceinline__ void select_budget_cta(const SelectCtx& sc, int32_t* scratch) {
-  const int B = sc.batch, L = sc.L;
-  const int nslots = B * L;
-  const int tid = threadIdx.x, nt = blockDim.x;
-  uint32_t* s_key = reinterpret_cast<uint32_t*>(scratch);  // [nslots]
-  int32_t* s_ell = scratch + nslots;                        // [B]
-  int32_t* red = s_ell + B;                                 // [64]
-  int parity = 0;
-  // keys: batches of 8 slots per thread, every load issued before any is used
-  int32_t my_valid = 0;
-  for (int q0 = 0; q0 < nslots; q0 += 8 * nt) {
-    float sv[8];
-    int32_t len[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int q = q0 + tid + i * nt;
-      sv[i] = q < nslots ? __ldcg(sc.S + q) : 0.0f;
-      len[i] = q < nslots ? __ldcg(sc.chain_len + q / L) : 0;
-    }
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int q = q0 + tid + i * nt;
-      if (q < nslots) {
-        const int k = q - (q / L) * L;
-        const bool valid = k < len[i] && k < sc.mvl;
-        s_key[q] = valid ? __float_as_uint(sv[i]) + 1u : 0u;
-        my_valid += valid;
-      }
-    }
-  }
-  for (int r = tid; r < B; r += nt) s_ell[r] = 0;
-  const int32_t n_valid = cta_sum(my_valid, red, parity);  // (its barrier orders the stores above)
-  const int32_t budget = sc.budget;
-  if (budget >= n_valid || budget == 0) {
-    for (int r = tid; r < B; r += nt) {
-      const int32_t len = __ldcg(sc.chain_len + r);
-      s_ell[r] = budget > 0 ? (len < sc.mvl ? len : sc.mvl) : 0;
-    }
-  } else {
-    uint32_t t = 0u;  // bits of theta, two at a time from bit 29
-    for (int shift = 28; shift >= 0; shift -= 2) {
-      const uint32_t c1 = (t | (1u << shift)) + 1u, c2 = (t | (2u << shift)) + 1u, c3 = (t | (3u << shift)) + 1u;
-      int32_t n1 = 0, n2 = 0, n3 = 0;
-      for (int q = tid; q < nslots; q += nt) {
-        const uint32_t w = s_key[q];
-        n1 += w >= c1;
-        n2 += w >= c2;
-        n3 += w >= c3;
-      }
-      n1 = __reduce_add_sync(0xFFFFFFFFu, n1);
-      n2 = __reduce_add_sync(0xFFFFFFFFu, n2);
-      n3 = __reduce_add_sync(0xFFFFFFFFu, n3);
-      int32_t* buf = red + 32 * parity;
-      const int lane = tid & 31, warp = tid >> 5;
-      if (lane == 0) {
-        buf[warp] = n1;
-        buf[warp + 8] = n2;
-        buf[warp + 16] = n3;
-      }
-      __syncthreads();
-      int32_t m1 = 0, m2 = 0, m3 = 0;
-      for (int q = 0; q < (nt >> 5); ++q) {
-        m1 += buf[q];
-        m2 += buf[q + 8];
-        m3 += buf[q + 16];
-      }
-      parity ^= 1;
-      const uint32_t j = m3 >= budget ? 3u : (m2 >= budget ? 2u : (m1 >= budget ? 1u : 0u));
-      t |= j << shift;
-    }
-    const uint32_t key_eq = t + 1u;
-    int32_t above = 0;
-    for (int q = tid; q < nslots; q += nt) above += s_key[q] > key_eq;
-    const int32_t need = budget - cta_sum(above, red, parity);  // ties at theta to take
-    // ties in slot order: contiguous slot ranges per thread, one block scan
-    const int per = (nslots + nt - 1) / nt;
-    const int q_lo = tid * per, q_hi = min(nslots, q_lo + per);
-    int32_t eq = 0;
-    for (int q = q_lo; q < q_hi; ++q) eq += s_key[q] == key_eq;
-    const int lane = tid & 31, warp = tid >> 5;
-    int32_t incl = eq;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-      if (lane >= o) incl += v;
-    }
-    int32_t* buf = red + 32 * parity;
-    if (lane == 31) buf[warp] = incl;
-    __syncthreads();
-    int32_t rank = incl - eq;
-    for (int q = 0; q < warp; ++q) rank += buf[q];
-    int cur_r = -1, cur_n = 0;
-    for (int q = q_lo; q < q_hi; ++q) {
-      const uint32_t w = s_key[q];
-      const bool sel = w > key_eq || (w == key_eq && rank++ < need);
-      if (sel) {
-        const int r = q / L;
-        if (r != cur_r) {
-          if (cur_n) atomicAdd(&s_ell[cur_r], cur_n);
-          cur_r = r;
-          cur_n = 0;
-        }
-        ++cur_n;
-      }
-    }
-    if (cur_n) atomicAdd(&s_ell[cur_r], cur_n);
-    parity ^= 1;
-  }
-  __syncthreads();
-  // row offsets: contiguous request ranges per thread, one block scan
-  const int rp = (B + nt - 1) / nt;
-  const int r_lo = tid * rp, r_hi = min(B, r_lo + rp);
-  int32_t mine = 0;
-  for (int r = r_lo; r < r_hi; ++r) mine += s_ell[r] + 1;
-  const int lane = tid & 31, warp = tid >> 5;
-  int32_t incl = mine;
+// inclusive prefix sum over the CTA in thread order; *total gets the sum
+static __device__ __forceinline__ int32_t cta_incl_scan(int32_t v, int32_t* red, int& parity, int32_t* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int32_t incl = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const int32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-    if (lane >= o) incl += v;
+    const int32_t t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += t;
   }
   int32_t* buf = red + 32 * parity;
   if (lane == 31) buf[warp] = incl;
   __syncthreads();
-  int32_t off = incl - mine, total = 0;
-  for (int q = 0; q < (nt >> 5); ++q) {
-    if (q < warp) off += buf[q];
-    total += buf[q];
+  int32_t before = 0, all = 0;
+  const int nw = (blockDim.x + 31) >> 5;
+  for (int q = 0; q < nw; ++q) {
+    const int32_t b = buf[q];
+    before += q < warp ? b : 0;
+    all += b;
   }
+  parity ^= 1;
+  *total = all;
+  return incl + before;
+}
+
+static __device__ __forceinline__ void select_budget_cta(const SelectCtx& sc, int32_t* scratch) {
+  constexpr int NW = 8;  // warps (256 threads)
+  const int B = sc.batch, L = sc.L;
+  const int nslots = B * L;
+  const int tid = threadIdx.x, nt = blockDim.x;
+  const int lane = tid & 31, warp = tid >> 5;
+  uint32_t* s_key = reinterpret_cast<uint32_t*>(scratch);  // [nslots]
+  int32_t* s_hist = scratch + nslots;                       // [2][NW][256]
+  int32_t* red = s_hist + 2 * NW * 256;                     // [2][32]
+  int32_t* bc = red + 64;                                   // [2][2] digit, remaining
+  int parity = 0;
+  for (int i = tid; i < 2 * NW * 256; i += nt) s_hist[i] = 0;
+  // keys: batches of 8 slots per thread, every load issued before any is used
+  int32_t my_valid = 0;
+  for (int q0 = 0; q0 < nslots; q0 += 8 * nt) {
+    uint32_t w[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int q = q0 + tid + i * nt;
+      w[i] = q < nslots ? __ldcg(sc.keys + q) : 0u;
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int q = q0 + tid + i * nt;
+      if (q < nslots) s_key[q] = w[i];
+      my_valid += w[i] != 0u;
+    }
+  }
+  const int32_t n_valid = cta_sum(my_valid, red, parity);  // (its barrier orders the stores above)
+  const int32_t budget = sc.budget;
+  uint32_t theta;
+  int32_t need;
+  if (budget == 0) {
+    theta = 0xFFFFFFFFu;
+    need = 0;
+  } else if (budget >= n_valid) {
+    theta = 0u;
+    need = 0;
+  } else {
+    uint32_t prefix = 0u;
+    int32_t rem = budget;  // slots still to take among those matching the prefix
+#pragma unroll 1
+    for (int pass = 0; pass < 4; ++pass) {
+      const int shift = pass < 3 ? 22 - 8 * pass : 0;
+      const int hi = pass == 0 ? 30 : shift + (pass < 3 ? 8 : 6);
+      const uint32_t mask = pass < 3 ? 0xFFu : 0x3Fu;
+      int32_t* hist = s_hist + (pass & 1) * NW * 256;
+      int32_t* mine = hist + warp * 256;
+      // per-warp histogram of the matching keys' digits; equal digits within
+      // one warp instruction are merged first, so each entry has one writer
+#pragma unroll 1
+      for (int q0 = 0; q0 < nslots; q0 += nt) {
+        const int q = q0 + tid;
+        const uint32_t w = q < nslots ? s_key[q] : 0u;
+        const bool take = q < nslots && (w >> hi) == (prefix >> hi);
+        const uint32_t dgt = take ? ((w >> shift) & mask) : 0x100u;
+        const uint32_t peers = __match_any_sync(0xFFFFFFFFu, dgt);
+        if (take && lane == __ffs(peers) - 1) mine[dgt] += __popc(peers);
+        __syncwarp();
+      }
+      __syncthreads();
+      // thread t owns digit 255 - t (descending), sums the warps' counts and
+      // zeroes them for the pass after next
+      const int dg = 255 - tid;
+      int32_t cnt = 0;
+#pragma unroll
+      for (int w8 = 0; w8 < NW; ++w8) {
+        cnt += hist[w8 * 256 + dg];
+        hist[w8 * 256 + dg] = 0;
+      }
+      int32_t tot;
+      const int32_t incl = cta_incl_scan(cnt, red, parity, &tot);
+      const int32_t excl = incl - cnt;
+      int32_t* b = bc + 2 * (pass & 1);
+      if (excl < rem && incl >= rem) {
+        b[0] = dg;
+        b[1] = rem - excl;
+      }
+      __syncthreads();
+      prefix |= (uint32_t)b[0] << shift;
+      rem = b[1];
+    }
+    theta = prefix;
+    need = rem;
+  }
+  // per request: slots above theta and ties at theta; contiguous request
+  // ranges per thread, packed (above << 16 | eq): each is at most
+  // 1024 x 31 slots, so neither field overflows
+  const int rp = (B + nt - 1) / nt;
+  const int r_lo = min(B, tid * rp), r_hi = min(B, r_lo + rp);
+  int32_t mine = 0;
   for (int r = r_lo; r < r_hi; ++r) {
-    sc.verify_len[r] = s_ell[r];
-    sc.row_off[r] = off;
-    off += s_ell[r] + 1;
+    int32_t above = 0, eq = 0;
+#pragma unroll 4
+    for (int k = 0; k < L; ++k) {
+      const uint32_t w = s_key[r * L + k];
+      above += w > theta;
+      eq += w == theta;
+    }
+    mine += (above << 16) | eq;
   }
-  if (tid == 0) sc.row_off[B] = total;
+  int32_t tot;
+  const int32_t incl = cta_incl_scan(mine, red, parity, &tot);
+  int32_t A = (incl - mine) >> 16, E = (incl - mine) & 0xFFFF;
+  for (int r = r_lo; r < r_hi; ++r) {
+    int32_t above = 0, eq = 0;
+#pragma unroll 4
+    for (int k = 0; k < L; ++k) {
+      const uint32_t w = s_key[r * L + k];
+      above += w > theta;
+      eq += w == theta;
+    }
+    const int32_t take = min(eq, max(0, need - E));
+    sc.verify_len[r] = above + take;
+    sc.row_off[r] = r + A + min(need, E);
+    A += above;
+    E += eq;
+  }
+  if (tid == 0) sc.row_off[B] = B + (tot >> 16) + min(need, tot & 0xFFFF);
 }
 
 }  // namespace spec

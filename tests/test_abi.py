@@ -94,6 +94,8 @@ def _ws(spec):
     w = spec.WorkspaceStruct()
     w.base = 256 * 1024  # a fake, aligned device address; never dereferenced on these paths
     w.max_batch, w.max_rows, w.K, w.vocab = 4, 64, 7, 1024
+    w.off_keys = 256  # the pricing keys' region, inside the stated size
+    w.bytes = 256 + 4 * 1024 * 31
     return w
 
 
@@ -111,10 +113,13 @@ def test_host_validation_rejects_bad_arguments_without_a_gpu(spec):
     assert lib.spec_ngram_propose(*args(1, 40, 15, 256)) == UNS
     # null pointer
     assert lib.spec_ngram_propose(P, 64, None, 4, 1, 3, 15, 256, P, P, P, P, P, C.byref(w), None) == INV
-    # misaligned workspace
+    # misaligned workspace; one too small for the pricing keys
     w2 = _ws(spec)
     w2.base = 256 * 1024 + 8
     assert lib.spec_ngram_propose(*args(1, 3, 15, 256)[:-2], C.byref(w2), None) == WSE
+    w3 = _ws(spec)
+    w3.bytes = 1024
+    assert lib.spec_ngram_propose(*args(1, 3, 15, 256)[:-2], C.byref(w3), None) == WSE
     # pricing: K > L, negative budget, bad policy, oversized batch
     e = spec.make_estimator({"beta": [0.0] * 15})
     def price(B=4, K=7, L=15, budget=8, policy=0, lam=0.1, tb=1 << 20):
