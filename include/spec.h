@@ -242,10 +242,9 @@ spec_status spec_price_and_allocate(
  * Steps 1 + 2 fused: spec_ngram_propose followed by spec_price_and_allocate
  * in one launch, with identical outputs (every argument has the meaning it has
  * in those two calls; max_propose = L).  Each request's n-gram CTA prices its
- * own request from on-chip values ([HS] sec. 4.2: "the scan already computes
- * n, a, and m, so the estimate adds only one fused elementwise step per
- * request"), and the last request to finish allocates the budget for the
- * batch.  Limits: those of both calls.
+ * own request from on-chip values (the n-gram scan already yields the Eq. (1)
+ * features n, a and m, [HS] sec. 4.2), and the last request to finish
+ * allocates the budget for the batch.  Limits: those of both calls.
  * ------------------------------------------------------------------------ */
 spec_status spec_draft_and_price(
     const int32_t* hist, int64_t hist_stride, const int32_t* hist_len, int32_t batch, int32_t n_min,
@@ -255,6 +254,43 @@ spec_status spec_draft_and_price(
     int32_t budget, int32_t max_verify_len, spec_policy policy, int32_t draft_greedy, int32_t* chain,
     float* S, int32_t* chain_len, int32_t* source, int32_t* verify_len, int32_t* row_off,
     uint8_t* point_mass, const spec_workspace* ws, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
+ * spec_price_and_allocate_static: step 2 without a workspace.  The method has
+ * no counterpart of this call; it is an interface variant of
+ * spec_price_and_allocate for callers that cannot hand the library device
+ * memory -- for example a scheduler whose device memory is planned up front
+ * and that may not allocate while a decoding step is in flight, or a host
+ * thread that must not call into an allocator.  Every argument except
+ * `status_word` has its meaning in spec_price_and_allocate, and the outputs
+ * are identical to that call's on the same inputs.
+ *
+ * Scratch: a fixed array of (64 + SPEC_STATIC_PRICE_MAX_BATCH * SPEC_MAX_L)
+ * 32-bit words (32,000 bytes) in this library's device memory; this call and
+ * its kernel allocate nothing.
+ * Set-up: the first call on each device looks up that array's device address
+ * (cudaGetSymbolAddress, with the device current) and keeps it; make that
+ * first call before the stream is captured into a graph.
+ * Limits: batch <= SPEC_STATIC_PRICE_MAX_BATCH, else SPEC_ERR_UNSUPPORTED
+ * before any device work; the other limits of spec_price_and_allocate.
+ * Zero state: the array's arrival counter must be zero when a call's kernel
+ * starts; it is zero when the library's device code loads into a context, and
+ * every call leaves it at zero.  The allocation keys need no initial value.
+ * Concurrency: every call on one device shares the one array, so calls whose
+ * kernels may overlap on the device (different streams without an order
+ * between them, or several host threads) race; keep them in one stream order.
+ * status_word: device address of a caller-owned 32-bit word into which device
+ * errors are OR-ed (SPEC_DEV_*), or NULL to discard them.
+ * ------------------------------------------------------------------------ */
+#define SPEC_STATIC_PRICE_MAX_BATCH 256
+spec_status spec_price_and_allocate_static(
+    int32_t batch, int32_t K, int32_t L, const int32_t* d, const float* c, const int32_t* d_len,
+    const int32_t* g, const int32_t* g_len, const int32_t* match_n, const int32_t* agree,
+    const int32_t* copy_len, const spec_estimator* est, const float* est_table,
+    size_t est_table_bytes, float lambda,
+    int32_t budget, int32_t max_verify_len, spec_policy policy, int32_t draft_greedy,
+    int32_t* chain, float* S, int32_t* chain_len, int32_t* source, int32_t* verify_len,
+    int32_t* row_off, uint8_t* point_mass, uint32_t* status_word, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------
  * Step 3: chain verification ([HS] sec. 2 "accepts the longest prefix that

@@ -24,7 +24,7 @@ from ._build import build
 
 __all__ = [
     "build", "load", "Workspace", "EstimatorTable", "SpecError", "spec_ngram_propose",
-    "spec_price_and_allocate", "spec_draft_and_price", "spec_verify_chain", "spec_verify_tree", "POLICY", "DEV_BITS",
+    "spec_price_and_allocate", "spec_price_and_allocate_static", "spec_draft_and_price", "spec_verify_chain", "spec_verify_tree", "POLICY", "DEV_BITS",
 ]
 
 SPEC_OK, SPEC_ERR_INVALID_ARG, SPEC_ERR_CUDA, SPEC_ERR_UNSUPPORTED, SPEC_ERR_WORKSPACE = 0, 1, 2, 3, 4
@@ -80,6 +80,9 @@ SIGNATURES = {
     "spec_price_and_allocate": ([_i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _ESTP, _vp,
                                  _sz, _f32, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                  _WSP, _vp], _i32),
+    "spec_price_and_allocate_static": ([_i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _ESTP, _vp,
+                                        _sz, _f32, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                        _vp, _vp], _i32),
     "spec_draft_and_price": ([_vp, _i64, _vp, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _i32, _i32,
                               _vp, _vp, _vp, _ESTP, _vp, _sz, _f32, _i32, _i32, _i32, _i32, _vp, _vp, _vp,
                               _vp, _vp, _vp, _vp, _WSP, _vp], _i32),
@@ -218,6 +221,23 @@ def spec_price_and_allocate(d, c, d_len, g, g_len, match_n, agree, copy_len, est
         _ptr(copy_len), C.byref(est.est), _ptr(est.table), est.table.numel() * 4, float(lam), int(budget), int(max_verify_len),
         pol, 1 if draft_greedy else 0, _ptr(chain), _ptr(S), _ptr(chain_len), _ptr(source),
         _ptr(verify_len), _ptr(row_off), _ptr(point_mass), ws.ref, _stream(stream)))
+
+
+def spec_price_and_allocate_static(d, c, d_len, g, g_len, match_n, agree, copy_len, est: EstimatorTable, lam,
+                                   budget, max_verify_len, policy, draft_greedy, chain, S, chain_len, source,
+                                   verify_len, row_off, point_mass, status_word=None, stream=None):
+    """spec_price_and_allocate with its scratch in the library's fixed device
+    array instead of a workspace (nothing is allocated; batch <= 256; calls
+    that may overlap on one device race).  status_word: optional int32 device
+    tensor of one element that receives the device error bits."""
+    B, K = d.shape
+    L = g.shape[1]
+    pol = POLICY[policy] if isinstance(policy, str) else int(policy)
+    _check("spec_price_and_allocate_static", load().spec_price_and_allocate_static(
+        B, K, L, _ptr(d), _ptr(c), _ptr(d_len), _ptr(g), _ptr(g_len), _ptr(match_n), _ptr(agree),
+        _ptr(copy_len), C.byref(est.est), _ptr(est.table), est.table.numel() * 4, float(lam), int(budget),
+        int(max_verify_len), pol, 1 if draft_greedy else 0, _ptr(chain), _ptr(S), _ptr(chain_len), _ptr(source),
+        _ptr(verify_len), _ptr(row_off), _ptr(point_mass), _ptr(status_word), _stream(stream)))
 
 
 def spec_draft_and_price(hist, hist_len, n_min, n_max, copy_cap, g, g_len, match_n, agree, copy_len, d, c,

@@ -7,6 +7,15 @@
 
 #include "common.cuh"
 
+// pricing with the fixed scratch array (price.cu; internal, not exported)
+__attribute__((visibility("hidden"))) cudaError_t spec_launch_price_static(
+    int32_t batch, int32_t K, int32_t L, const int32_t* d, const float* c, const int32_t* d_len,
+    const int32_t* g, const int32_t* g_len, const int32_t* match_n, const int32_t* agree,
+    const int32_t* copy_len, const spec_estimator* est, const float* table, float lambda, int32_t budget,
+    int32_t mvl, int32_t policy, int32_t draft_greedy, int32_t* chain, float* S, int32_t* chain_len,
+    int32_t* source, int32_t* verify_len, int32_t* row_off, uint8_t* point_mass, uint32_t* status_word,
+    cudaStream_t stream);
+
 extern "C" {
 cudaError_t spec_launch_ngram(const int32_t* hist, int64_t stride, const int32_t* hist_len,
                               int32_t batch, int32_t n_min, int32_t n_max, int32_t L, int32_t cap,
@@ -211,6 +220,32 @@ spec_status spec_price_and_allocate(
                                      est, est_table, lambda, budget, max_verify_len, (int32_t)policy,
                                      draft_greedy ? 1 : 0, chain, S, chain_len, source, verify_len,
                                      row_off, point_mass, status_of(ws), keys_of(ws), stream));
+}
+
+spec_status spec_price_and_allocate_static(
+    int32_t batch, int32_t K, int32_t L, const int32_t* d, const float* c, const int32_t* d_len,
+    const int32_t* g, const int32_t* g_len, const int32_t* match_n, const int32_t* agree,
+    const int32_t* copy_len, const spec_estimator* est, const float* est_table,
+    size_t est_table_bytes, float lambda, int32_t budget, int32_t max_verify_len, spec_policy policy,
+    int32_t draft_greedy, int32_t* chain, float* S, int32_t* chain_len, int32_t* source,
+    int32_t* verify_len, int32_t* row_off, uint8_t* point_mass, uint32_t* status_word,
+    cudaStream_t stream) {
+  // the checks of spec_price_and_allocate, then the fixed scratch's batch limit
+  if (batch < 0 || K < 0 || L < 1 || K > L || budget < 0 || max_verify_len < 0 || !est ||
+      !(lambda == lambda) || (int)policy < 0 || (int)policy > 4)
+    return SPEC_ERR_INVALID_ARG;
+  if (L > SPEC_MAX_L || batch > SPEC_STATIC_PRICE_MAX_BATCH) return SPEC_ERR_UNSUPPORTED;
+  if (!est_table || !row_off) return SPEC_ERR_INVALID_ARG;
+  if (batch > 0 && (!d_len || !g || !g_len || !match_n || !agree || !copy_len || !chain || !S ||
+                    !chain_len || !source || !verify_len || !point_mass || (K > 0 && (!d || !c))))
+    return SPEC_ERR_INVALID_ARG;
+  if (!est->use_constant_h && (est->m_cap < 1 || est->m_cap > SPEC_MAX_COPY_CAP)) return SPEC_ERR_INVALID_ARG;
+  const size_t need = spec_estimator_table_bytes(est, L);
+  if (need == 0 || est_table_bytes < need) return SPEC_ERR_INVALID_ARG;
+  return from_cuda(spec_launch_price_static(batch, K, L, d, c, d_len, g, g_len, match_n, agree, copy_len, est,
+                                            est_table, lambda, budget, max_verify_len, (int32_t)policy,
+                                            draft_greedy ? 1 : 0, chain, S, chain_len, source, verify_len,
+                                            row_off, point_mass, status_word, stream));
 }
 
 spec_status spec_draft_and_price(

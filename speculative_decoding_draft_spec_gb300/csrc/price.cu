@@ -22,6 +22,8 @@
 // row offsets.
 #include "pricing.cuh"
 
+#include <mutex>
+
 namespace spec {
 
 // ------------------------------------------------------------------ Eq. (1)
@@ -214,6 +216,96 @@ extern "C" cudaError_t spec_launch_price(
   const int blocks = batch > 0 ? (batch + PR_WARPS - 1) / PR_WARPS : 1;
   const size_t smem = (size_t)spec::select_scratch_ints(batch > 0 ? batch : 1, L) * sizeof(int32_t);
   cudaError_t e = cudaFuncSetAttribute(spec::price_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  spec::price_kernel<<<blocks, PR_THREADS, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Pricing without a workspace: the scratch of one call (status word, arrival
+// counter, allocation keys) lives in a fixed array of this library's device
+// memory, so neither the call nor its kernel allocates.  For callers that own
+// no device workspace; calls that may overlap on one device race on the array.
+// ---------------------------------------------------------------------------
+namespace spec {
+constexpr int kStaticHeaderWords = 64;  // [0] status word, [1] arrival counter
+static __device__ __align__(256) uint32_t
+    g_static_price_scratch[kStaticHeaderWords + SPEC_STATIC_PRICE_MAX_BATCH * SPEC_MAX_L];
+}  // namespace spec
+
+namespace {
+constexpr int kMaxDevices = 256;
+std::mutex g_static_mu;
+uint32_t* g_static_addr[kMaxDevices] = {};
+}  // namespace
+
+// Device address of the fixed scratch array on the current device, looked up
+// once per device.  (Internal: not exported from the library.)
+__attribute__((visibility("hidden"))) cudaError_t spec_static_price_scratch(uint32_t** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  if (!g_static_addr[dev]) {
+    void* addr = nullptr;
+    e = cudaGetSymbolAddress(&addr, spec::g_static_price_scratch);
+    if (e != cudaSuccess) return e;
+    g_static_addr[dev] = static_cast<uint32_t*>(addr);
+  }
+  *out = g_static_addr[dev];
+  return cudaSuccess;
+}
+
+__attribute__((visibility("hidden"))) cudaError_t spec_launch_price_static(
+    int32_t batch, int32_t K, int32_t L, const int32_t* d, const float* c, const int32_t* d_len,
+    const int32_t* g, const int32_t* g_len, const int32_t* match_n, const int32_t* agree,
+    const int32_t* copy_len, const spec_estimator* est, const float* table, float lambda,
+    int32_t budget, int32_t mvl, int32_t policy, int32_t draft_greedy, int32_t* chain, float* S,
+    int32_t* chain_len, int32_t* source, int32_t* verify_len, int32_t* row_off,
+    uint8_t* point_mass, uint32_t* status_word, cudaStream_t stream) {
+  if (batch > SPEC_STATIC_PRICE_MAX_BATCH || L > SPEC_MAX_L) return cudaErrorInvalidValue;
+  uint32_t* scratch = nullptr;
+  cudaError_t e = spec_static_price_scratch(&scratch);
+  if (e != cudaSuccess) return e;
+  uint32_t* keys = scratch + spec::kStaticHeaderWords;
+  spec::PriceParams p;
+  p.batch = batch;
+  p.d = d;
+  p.c = c;
+  p.d_len = d_len;
+  p.g = g;
+  p.g_len = g_len;
+  p.match_n = match_n;
+  p.agree = agree;
+  p.copy_len = copy_len;
+  p.cx.K = K;
+  p.cx.L = L;
+  p.cx.table = table;
+  p.cx.tab_const = est->use_constant_h;
+  p.cx.n_full = est->n_full;
+  p.cx.m_cap = est->m_cap;
+  p.cx.lambda = lambda;
+  p.cx.policy = policy;
+  p.cx.draft_greedy = draft_greedy;
+  p.cx.chain = chain;
+  p.cx.S = S;
+  p.cx.chain_len = chain_len;
+  p.cx.source = source;
+  p.cx.point_mass = point_mass;
+  p.cx.mvl = mvl;
+  p.cx.keys = keys;
+  p.sc.batch = batch;
+  p.sc.L = L;
+  p.sc.budget = budget;
+  p.sc.keys = keys;
+  p.sc.verify_len = verify_len;
+  p.sc.row_off = row_off;
+  p.status = status_word ? status_word : scratch;  // scratch[0]: a word nobody reads
+  p.arrive = scratch + 1;
+  const int blocks = batch > 0 ? (batch + PR_WARPS - 1) / PR_WARPS : 1;
+  const size_t smem = (size_t)spec::select_scratch_ints(batch > 0 ? batch : 1, L) * sizeof(int32_t);
+  e = cudaFuncSetAttribute(spec::price_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   spec::price_kernel<<<blocks, PR_THREADS, smem, stream>>>(p);
   return cudaGetLastError();
