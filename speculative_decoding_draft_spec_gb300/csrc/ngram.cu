@@ -72,6 +72,10 @@ __device__ __forceinline__ void top2_insert(unsigned long long& b1, unsigned lon
   }
 }
 
+#define NG_SHORT 8  // tokens a thread extends a candidate by itself
+#define NG_QCAP 64  // queued long candidates per warp
+#define NG_UNROLL 4 // 16-byte groups per thread in flight in the candidate filter
+
 template <bool CLUSTER, bool PRICE>
 __global__ void __launch_bounds__(SPEC_CTA_THREADS, 1) ngram_kernel(NgramParams p) {
   extern __shared__ __align__(16) int32_t smem_tok[];
@@ -114,7 +118,10 @@ __global__ void __launch_bounds__(SPEC_CTA_THREADS, 1) ngram_kernel(NgramParams 
   int32_t* win = smem_tok;               // x[w0 .. w1)
   int32_t* suf = smem_tok + p.win_cap;   // x[s0 .. s1)
 
+  __shared__ int32_t s_q[SPEC_WARPS_PER_CTA][NG_QCAP];  // queued long candidates per warp
+  __shared__ int32_t s_qn[SPEC_WARPS_PER_CTA];
   if (tid == 0) s_flag = 0;
+  if (tid < SPEC_WARPS_PER_CTA) s_qn[tid] = 0;
   if (work) {
     if (p.use_bulk) {
       if (tid == 0) {
@@ -142,21 +149,97 @@ __global__ void __launch_bounds__(SPEC_CTA_THREADS, 1) ngram_kernel(NgramParams 
   }
   __syncthreads();
 
+  // Each thread extends its candidates up to NG_SHORT tokens; one still
+  // matching there goes to its warp's queue, and the warp then extends the
+  // queued candidates 32 positions per step (one ballot per step), so a long
+  // copy costs l / 32 steps instead of l dependent compares.
+  const int warp = tid >> 5, lane = tid & 31;
   unsigned long long b1 = 0ull, b2 = 0ull;  // packed (l << 32 | j); 0 = none
   if (work && s_flag == 0) {
     const int32_t* wv = win - w0;  // wv[t] = x[t]
     const int32_t* sv = suf - s0;
-    const int32_t last = sv[T - 1];
-    for (int32_t j = j0 + tid; j < j1; j += blockDim.x) {
-      if (wv[j] != last) continue;
+    // the suffix's last NG_SHORT tokens in registers (entries past the
+    // staged suffix are never compared: k < lim <= min(cap, T - 1))
+    int32_t sk[NG_SHORT];
+#pragma unroll
+    for (int k = 0; k < NG_SHORT; ++k) sk[k] = (k < p.cap && k < T) ? sv[T - 1 - k] : 0;
+    const int32_t last = sk[0];
+    // l(j) up to NG_SHORT by independent compares; a candidate still matching
+    // there is queued for its warp (or, with the queue full, extended alone)
+    auto extend = [&](int32_t j) {
       const int32_t lim = min(p.cap, j + 1);
-      int32_t l = 1;
-      while (l < lim && wv[j - l] == sv[T - 1 - l]) ++l;
+      uint32_t ok = 0u;
+#pragma unroll
+      for (int k = 1; k < NG_SHORT; ++k) ok |= (uint32_t)(k < lim && wv[j - k] == sk[k]) << (k - 1);
+      int32_t l = __ffs(~ok);  // the first k that fails, or NG_SHORT
+      if (l == NG_SHORT && l < lim) {
+        const int slot = atomicAdd(&s_qn[warp], 1);
+        if (slot < NG_QCAP) {
+          s_q[warp][slot] = j;
+          return;
+        }
+        while (l < lim && wv[j - l] == sv[T - 1 - l]) ++l;
+      }
       if (l >= p.n_min) top2_insert(b1, b2, ((unsigned long long)l << 32) | (uint32_t)j);
+    };
+    // with n_min >= 2 a candidate must also match the second-to-last token
+    // (and then j >= 1 and cap >= 2)
+    const bool two = p.n_min >= 2;
+    const int32_t s1 = two ? sk[1] : 0;
+    {
+      // candidate filter on 16-byte groups: thread t reads groups t, t + 256, ...
+      // (consecutive lanes, consecutive 16 bytes), NG_UNROLL groups in flight;
+      // wv is 16-byte aligned at multiples of 4 (the staged window starts at
+      // w0 = 0 mod 4 and holds x[w0, w1), w1 = j1 rounded up to 4)
+      const int32_t jb = j0 & ~3;
+      const int32_t gstride = 4 * (int32_t)blockDim.x;
+      for (int32_t c0 = jb + 4 * tid; c0 < j1; c0 += NG_UNROLL * gstride) {
+        int4 v[NG_UNROLL];
+        int32_t prev[NG_UNROLL];  // x[c - 1], read only when position c is in range
+#pragma unroll
+        for (int u = 0; u < NG_UNROLL; ++u) {
+          const int32_t c = c0 + u * gstride;
+          v[u] = c < j1 ? *reinterpret_cast<const int4*>(wv + c) : make_int4(0, 0, 0, 0);
+          prev[u] = (two && c < j1 && c >= j0 && c >= 1) ? wv[c - 1] : 0;
+        }
+#pragma unroll
+        for (int u = 0; u < NG_UNROLL; ++u) {
+          const int32_t c = c0 + u * gstride;
+          uint32_t m = (uint32_t)(v[u].x == last) | ((uint32_t)(v[u].y == last) << 1) |
+                       ((uint32_t)(v[u].z == last) << 2) | ((uint32_t)(v[u].w == last) << 3);
+          if (two)
+            m &= (uint32_t)(prev[u] == s1 && c >= 1) | ((uint32_t)(v[u].x == s1) << 1) |
+                 ((uint32_t)(v[u].y == s1) << 2) | ((uint32_t)(v[u].z == s1) << 3);
+          if (c < j0) m &= 0xFu << (j0 - c);                 // before this CTA's range
+          if (c + 4 > j1) m &= (1u << max(0, j1 - c)) - 1u;  // past it
+          while (m) {
+            const int e = __ffs(m) - 1;
+            m &= m - 1u;
+            extend(c + e);
+          }
+        }
+      }
+    }
+    __syncwarp();
+    const int nq = min(s_qn[warp], NG_QCAP);
+    for (int i = 0; i < nq; ++i) {
+      const int32_t j = s_q[warp][i];
+      const int32_t lim = min(p.cap, j + 1);
+      int32_t l = NG_SHORT;
+      while (l < lim) {
+        const int32_t t = l + lane;
+        const bool ok = t < lim && wv[j - t] == sv[T - 1 - t];
+        const uint32_t bad = __ballot_sync(0xFFFFFFFFu, !ok);
+        if (bad) {
+          l += __ffs(bad) - 1;
+          break;
+        }
+        l += 32;
+      }
+      if (lane == 0 && l >= p.n_min) top2_insert(b1, b2, ((unsigned long long)l << 32) | (uint32_t)j);
     }
   }
   warp_top2(b1, b2);
-  const int warp = tid >> 5, lane = tid & 31;
   if (lane == 0) {
     warp_best[warp][0] = b1;
     warp_best[warp][1] = b2;

@@ -197,15 +197,19 @@ __device__ __forceinline__ void price_request_warp(const PriceCtx& cx, int r, in
 // lies among the first `need` such slots in slot order; theta and need follow
 // from the budget: none (theta = ~0), every valid slot (budget >= number of
 // valid slots: theta = 0), else theta = the key of the budget-th slot in the
-// order (key desc, slot asc), found by a four-pass radix select over the key
-// bits 29..22 | 21..14 | 13..6 | 5..0 from the top.  Survivals fall along a
-// chain (products of factors in [0, 1]) and ties go to the lower position, so
-// every request takes a prefix: ell_r = above_r + min(eq_r, max(0, need - E_r))
-// with E_r the ties of the requests before r, and
-// row_off[r] = r + sum_{r' < r} above_r' + min(need, E_r), one block scan of
-// the pair (above, eq).
+// order (key desc, slot asc).  That key is found from the top bits down: a
+// 1024-bin shared-memory histogram of bits 29..20 (then 19..10, 9..0 while the
+// chosen bin still holds more than 256 keys) locates it, and the keys of the
+// chosen bin are then ranked against each other directly.  Survivals fall
+// along a chain (products of factors in [0, 1]) and ties go to the lower
+// position, so every request takes a prefix:
+// ell_r = above_r + min(eq_r, max(0, need - E_r)) with E_r the ties of the
+// requests before r, and row_off[r] = r + sum_{r' < r} above_r' + min(need, E_r),
+// one block scan of the pair (above, eq).
 // Shared scratch: select_scratch_ints(batch, L) ints.
-__host__ __device__ inline int select_scratch_ints(int batch, int L) { return batch * L + 2 * 8 * 256 + 96; }
+__host__ __device__ inline int select_scratch_ints(int batch, int L) {
+  return ((batch * L + 3) & ~3) + 2 * 1024 + 256 + 96;
+}
 
 static __device__ __forceinline__ int32_t cta_sum(int32_t v, int32_t* red /*[2][32]*/, int& parity) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -245,17 +249,19 @@ static __device__ __forceinline__ int32_t cta_incl_scan(int32_t v, int32_t* red,
 }
 
 static __device__ __forceinline__ void select_budget_cta(const SelectCtx& sc, int32_t* scratch) {
-  constexpr int NW = 8;  // warps (256 threads)
+  constexpr int NB = 1024;   // histogram bins (10 key bits per level)
+  constexpr int NCAND = 256; // keys ranked directly
   const int B = sc.batch, L = sc.L;
   const int nslots = B * L;
   const int tid = threadIdx.x, nt = blockDim.x;
-  const int lane = tid & 31, warp = tid >> 5;
-  uint32_t* s_key = reinterpret_cast<uint32_t*>(scratch);  // [nslots]
-  int32_t* s_hist = scratch + nslots;                       // [2][NW][256]
-  int32_t* red = s_hist + 2 * NW * 256;                     // [2][32]
-  int32_t* bc = red + 64;                                   // [2][2] digit, remaining
+  uint32_t* s_key = reinterpret_cast<uint32_t*>(scratch);          // [nslots]
+  int32_t* s_hist = scratch + ((nslots + 3) & ~3);                  // [2][NB], 16-byte aligned
+  uint32_t* s_cand = reinterpret_cast<uint32_t*>(s_hist + 2 * NB);  // [NCAND]
+  int32_t* red = reinterpret_cast<int32_t*>(s_cand + NCAND);        // [2][32]
+  int32_t* bc = red + 64;                                           // [2][4] + candidate count
   int parity = 0;
-  for (int i = tid; i < 2 * NW * 256; i += nt) s_hist[i] = 0;
+  for (int i = tid; i < 2 * NB; i += nt) s_hist[i] = 0;
+  if (tid == 0) bc[8] = 0;
   // keys: batches of 8 slots per thread, every load issued before any is used
   int32_t my_valid = 0;
   for (int q0 = 0; q0 < nslots; q0 += 8 * nt) {
@@ -283,51 +289,89 @@ static __device__ __forceinline__ void select_budget_cta(const SelectCtx& sc, in
     theta = 0u;
     need = 0;
   } else {
-    uint32_t prefix = 0u;
-    int32_t rem = budget;  // slots still to take among those matching the prefix
+    uint32_t prefix = 0u;  // key bits at and above `hi` fixed so far
+    int hi = 30;           // keys are below 2^30
+    int32_t rem = budget;  // slots still to take among the keys matching the prefix
+    int32_t cnt = nslots;
 #pragma unroll 1
-    for (int pass = 0; pass < 4; ++pass) {
-      const int shift = pass < 3 ? 22 - 8 * pass : 0;
-      const int hi = pass == 0 ? 30 : shift + (pass < 3 ? 8 : 6);
-      const uint32_t mask = pass < 3 ? 0xFFu : 0x3Fu;
-      int32_t* hist = s_hist + (pass & 1) * NW * 256;
-      int32_t* mine = hist + warp * 256;
-      // per-warp histogram of the matching keys' digits; equal digits within
-      // one warp instruction are merged first, so each entry has one writer
-#pragma unroll 1
-      for (int q0 = 0; q0 < nslots; q0 += nt) {
-        const int q = q0 + tid;
-        const uint32_t w = q < nslots ? s_key[q] : 0u;
-        const bool take = q < nslots && (w >> hi) == (prefix >> hi);
-        const uint32_t dgt = take ? ((w >> shift) & mask) : 0x100u;
-        const uint32_t peers = __match_any_sync(0xFFFFFFFFu, dgt);
-        if (take && lane == __ffs(peers) - 1) mine[dgt] += __popc(peers);
-        __syncwarp();
+    for (int level = 0; level < 3; ++level) {
+      const int shift = hi - 10;
+      int32_t* hist = s_hist + (level & 1) * NB;
+      for (int q = tid; q < nslots; q += nt) {
+        const uint32_t w = s_key[q];
+        if ((w >> hi) == (prefix >> hi)) atomicAdd(&hist[(w >> shift) & (NB - 1)], 1);
       }
       __syncthreads();
-      // thread t owns digit 255 - t (descending), sums the warps' counts and
-      // zeroes them for the pass after next
-      const int dg = 255 - tid;
-      int32_t cnt = 0;
-#pragma unroll
-      for (int w8 = 0; w8 < NW; ++w8) {
-        cnt += hist[w8 * 256 + dg];
-        hist[w8 * 256 + dg] = 0;
-      }
+      // thread t owns bins 1023 - 4t .. 1020 - 4t (descending) and zeroes them
+      // for the level after next
+      const int base = NB - 4 - 4 * tid;
+      const int4 h4 = *reinterpret_cast<const int4*>(hist + base);
+      *reinterpret_cast<int4*>(hist + base) = make_int4(0, 0, 0, 0);
+      const int32_t c4 = h4.x + h4.y + h4.z + h4.w;
       int32_t tot;
-      const int32_t incl = cta_incl_scan(cnt, red, parity, &tot);
-      const int32_t excl = incl - cnt;
-      int32_t* b = bc + 2 * (pass & 1);
-      if (excl < rem && incl >= rem) {
+      const int32_t incl = cta_incl_scan(c4, red, parity, &tot);
+      int32_t e = incl - c4;
+      int32_t* b = bc + 4 * (level & 1);
+      if (e < rem && incl >= rem) {
+        int dg = base + 3;
+        int32_t c = h4.w;
+        if (e + c < rem) {
+          e += c;
+          dg = base + 2;
+          c = h4.z;
+          if (e + c < rem) {
+            e += c;
+            dg = base + 1;
+            c = h4.y;
+            if (e + c < rem) {
+              e += c;
+              dg = base;
+              c = h4.x;
+            }
+          }
+        }
         b[0] = dg;
-        b[1] = rem - excl;
+        b[1] = rem - e;
+        b[2] = c;
       }
       __syncthreads();
       prefix |= (uint32_t)b[0] << shift;
       rem = b[1];
+      cnt = b[2];
+      hi = shift;
+      if (cnt <= NCAND || hi == 0) break;
     }
-    theta = prefix;
-    need = rem;
+    if (hi == 0) {
+      // every key bit fixed: the bin holds copies of one key
+      theta = prefix;
+      need = rem;
+    } else {
+      // the chosen bin's keys, ranked directly: theta is the value v with
+      // #(keys > v) < rem <= #(keys >= v)
+      for (int q = tid; q < nslots; q += nt) {
+        const uint32_t w = s_key[q];
+        if ((w >> hi) == (prefix >> hi)) s_cand[atomicAdd(&bc[8], 1)] = w;
+      }
+      __syncthreads();
+      int32_t* b = bc + 4 * 2;  // words 8..11: [8] count (done), [9] theta, [10] need
+      if (tid < cnt) {
+        const uint32_t v = s_cand[tid];
+        int32_t gt = 0, ge = 0;
+#pragma unroll 4
+        for (int i = 0; i < cnt; ++i) {
+          const uint32_t u = s_cand[i];
+          gt += u > v;
+          ge += u >= v;
+        }
+        if (gt < rem && rem <= ge) {  // every copy of v writes the same values
+          b[1] = (int32_t)v;
+          b[2] = rem - gt;
+        }
+      }
+      __syncthreads();
+      theta = (uint32_t)b[1];
+      need = b[2];
+    }
   }
   // per request: slots above theta and ties at theta; contiguous request
   // ranges per thread, packed (above << 16 | eq): each is at most
