@@ -50,11 +50,59 @@ def peaks():
     return 6800.0, "fallback"
 
 
+KERNEL_SOURCES = ["speculative_decoding_draft_spec_gb300/csrc/verify.cu",
+                  "speculative_decoding_draft_spec_gb300/csrc/common.cuh"]
+
+
+def source_hash(paths):
+    """sha256 of the sources with comments and blank space removed: a change to the
+    code changes it, a change to a comment does not."""
+    import hashlib
+    import re
+
+    h = hashlib.sha256()
+    for rel in paths:
+        with open(os.path.join(ROOT, rel)) as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(" ".join(text.split()).encode())
+    return h.hexdigest()
+
+
+def measured_traffic(kernel, workload):
+    """DRAM bytes per launch of `kernel` on `workload` from the committed ncu summary
+    (profiles/traffic.json), or None when the kernel's sources changed since."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    rec = json.load(open(p)).get(kernel, {}).get(workload)
+    if not rec or rec.get("source_sha256") != source_hash(KERNEL_SOURCES):
+        return None
+    return rec["dram_bytes_per_launch"]
+
+
 def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return rank, world, local
+
+
+def reduce_over_ranks(ms, tokens, rows, world, device="cpu"):
+    """Whole-job figures of a weak-scaling run: the slowest rank's time and the
+    tokens and rows of every rank (one all-reduce each; the path itself
+    exchanges nothing)."""
+    if world == 1:
+        return ms, tokens, rows
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    n = torch.tensor([tokens, rows], dtype=torch.int64, device=device)
+    dist.all_reduce(n, op=dist.ReduceOp.SUM)
+    return float(t.item()), int(n[0].item()), int(n[1].item())
 
 
 def build_workload(rank):
@@ -86,7 +134,7 @@ class ClockSampler:
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits", "-lms", "100",
+                ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits", "-lms", "50",
                  "-i", str(self.dev)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -193,12 +241,96 @@ def run_reference(args):
 
 
 # --------------------------------------------------------------------------- GPU arm
+def make_rounds(S, torch, W, cfg, nbuf):
+    """nbuf ChainRounds holding the workload, their logits laid out as the
+    device allocation asks (the allocation is run once to learn the layout)."""
+    from speculative_decoding_draft_spec_gb300.round import ChainRound
+
+    B, K, L, V = cfg["B"], cfg["K"], cfg["L"], cfg["V"]
+    max_rows = B * (L + 1)
+    rounds = []
+    for _ in range(nbuf):
+        rnd = ChainRound(B, cfg["hist"].shape[1], K, L, V, torch.bfloat16, max_rows, cfg["coef"], cfg["n_min"],
+                         cfg["n_max"], cfg["copy_cap"])
+        rnd.load(cfg["hist"], cfg["hist_len"], cfg["d"], cfg["c"], cfg["d_len"])
+        rounds.append(rnd)
+    rounds[0].draft_and_price(cfg["lam"], cfg["budget"], cfg["max_verify_len"], cfg["policy"], True)
+    torch.cuda.synchronize()
+    row_off = rounds[0].row_off.cpu().numpy()
+    vlen = rounds[0].verify_len.cpu().numpy()
+    n_rows, n_tok = int(row_off[-1]), int(vlen.sum())
+    logits = W.compact_logits(cfg, row_off, vlen)
+    lt = torch.from_numpy(logits.view(np.int16)).view(torch.bfloat16).to("cuda")
+    for rnd in rounds:
+        rnd.logits[:n_rows].copy_(lt)
+    torch.cuda.synchronize()
+    return rounds, n_rows, n_tok, logits
+
+
+def round_step(S, cfg, rnd, stream, rec=None):
+    """One round: spec_draft_and_price, then spec_verify_chain (T = 0), on `stream`;
+    rec: three CUDA events around the two launches."""
+    if rec:
+        rec[0].record(stream)
+    S.spec_draft_and_price(rnd.hist, rnd.hist_len, rnd.n_min, rnd.n_max, rnd.copy_cap, rnd.g, rnd.g_len,
+                           rnd.match_n, rnd.agree, rnd.copy_len, rnd.d, rnd.c, rnd.d_len, rnd.est, cfg["lam"],
+                           cfg["budget"], cfg["max_verify_len"], cfg["policy"], True, rnd.chain, rnd.S,
+                           rnd.chain_len, rnd.source, rnd.verify_len, rnd.row_off, rnd.point_mass, rnd.ws, stream)
+    if rec:
+        rec[1].record(stream)
+    S.spec_verify_chain(rnd.logits, rnd.row_off, rnd.max_rows, rnd.chain, rnd.verify_len, rnd.out_tokens,
+                        rnd.n_accepted, rnd.n_emitted, rnd.ws, point_mass=rnd.point_mass, temperature=0.0,
+                        stream=stream)
+    if rec:
+        rec[2].record(stream)
+
+
+def timed_rounds(S, torch, cfg, rounds, steps, warmup, barrier=lambda: None, sampler=None):
+    """W untimed rounds, then `steps` timed rounds between a barrier and a device
+    synchronisation (rounds rotate over the input sets); returns the elapsed ms
+    and the mean per-kernel times (us) from events on the launching stream."""
+    import contextlib
+
+    stream = torch.cuda.current_stream()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    for i in range(warmup):
+        round_step(S, cfg, rounds[i % len(rounds)], stream)
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with (sampler if sampler is not None else contextlib.nullcontext()):
+        t_start.record(stream)
+        for i in range(steps):
+            round_step(S, cfg, rounds[i % len(rounds)], stream, ev[i])
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    comp = {k: statistics.mean(e[a].elapsed_time(e[b]) for e in ev) * 1e3
+            for k, (a, b) in {"draft_price": (0, 1), "verify": (1, 2)}.items()}
+    return t_start.elapsed_time(t_end), comp
+
+
+def measure_bs4(S, torch, W, steps, warmup, hbm):
+    """The batch-4 code-editing configuration (T = 0): same round, same timing;
+    ten rotating input sets (10 x 19.5 MB of logits > L2)."""
+    cfg = W.edit_bs4()
+    rounds, n_rows, n_tok, _ = make_rounds(S, torch, W, cfg, 10)
+    ms, comp = timed_rounds(S, torch, cfg, rounds, steps, warmup)
+    achieved = n_rows * cfg["V"] * 2 / (comp["verify"] * 1e-6) / 1e9
+    return {"workload": "edit_bs4: B=4, V=151936, history 2048, budget 64, lambda 0.04, T=0, bf16 logits",
+            "value": n_tok * steps / (ms * 1e-3), "unit": UNIT, "rows_per_s": n_rows * steps / (ms * 1e-3),
+            "ms_per_step": ms / steps, "steps": steps, "verified_tokens_per_step": n_tok,
+            "verify_rows_per_step": n_rows, "components_us": {k: round(v, 3) for k, v in comp.items()},
+            "verify_roofline_frac": round(achieved / hbm, 4),
+            "l2": "10 rotating input sets (10 x 19.5 MB > L2)"}
+
+
 def run_gpu(args):
     import torch
 
     import speculative_decoding_draft_spec_gb300 as S
     import workloads as W
-    from speculative_decoding_draft_spec_gb300.round import ChainRound
 
     rank, world, local = dist_env()
     torch.cuda.set_device(local)
@@ -208,48 +340,9 @@ def run_gpu(args):
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     S.build()
     cfg = build_workload(rank)
-    B, K, L, V = cfg["B"], cfg["K"], cfg["L"], cfg["V"]
-    max_rows = B * (L + 1)
-    rounds = []
-    for k in range(NBUF):
-        rnd = ChainRound(B, cfg["hist"].shape[1], K, L, V, torch.bfloat16, max_rows, cfg["coef"], cfg["n_min"],
-                         cfg["n_max"], cfg["copy_cap"])
-        rnd.load(cfg["hist"], cfg["hist_len"], cfg["d"], cfg["c"], cfg["d_len"])
-        rounds.append(rnd)
+    B, L, V = cfg["B"], cfg["L"], cfg["V"]
+    rounds, n_rows, n_tok, logits = make_rounds(S, torch, W, cfg, NBUF)
     kw = dict(lam=cfg["lam"], budget=cfg["budget"], max_verify_len=cfg["max_verify_len"])
-    # the allocation (on the device) fixes the layout of the target rows
-    rounds[0].draft_and_price(**kw)
-    torch.cuda.synchronize()
-    row_off = rounds[0].row_off.cpu().numpy()
-    vlen = rounds[0].verify_len.cpu().numpy()
-    n_rows, n_tok = int(row_off[-1]), int(vlen.sum())
-    logits = W.compact_logits(cfg, row_off, vlen)
-    lt = torch.from_numpy(logits.view(np.int16)).view(torch.bfloat16)
-    for rnd in rounds:
-        rnd.logits[:n_rows].copy_(lt.to("cuda"))
-    torch.cuda.synchronize()
-
-    stream = torch.cuda.current_stream()
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
-
-    def step(i, rec=None):
-        rnd = rounds[i % NBUF]
-        if rec:
-            rec[0].record(stream)
-        S.spec_draft_and_price(rnd.hist, rnd.hist_len, rnd.n_min, rnd.n_max, rnd.copy_cap, rnd.g, rnd.g_len,
-                               rnd.match_n, rnd.agree, rnd.copy_len, rnd.d, rnd.c, rnd.d_len, rnd.est, cfg["lam"],
-                               cfg["budget"], cfg["max_verify_len"], cfg["policy"], True, rnd.chain, rnd.S,
-                               rnd.chain_len, rnd.source, rnd.verify_len, rnd.row_off, rnd.point_mass, rnd.ws)
-        if rec:
-            rec[1].record(stream)
-        S.spec_verify_chain(rnd.logits, rnd.row_off, max_rows, rnd.chain, rnd.verify_len, rnd.out_tokens,
-                            rnd.n_accepted, rnd.n_emitted, rnd.ws, point_mass=rnd.point_mass, temperature=0.0)
-        if rec:
-            rec[2].record(stream)
-
-    for i in range(args.warmup):
-        step(i)
-    torch.cuda.synchronize()
 
     def barrier():
         if world > 1:
@@ -257,31 +350,16 @@ def run_gpu(args):
 
             dist.barrier()
 
-    barrier()
-    torch.cuda.synchronize()
-    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local) as clk:
-        t_start.record(stream)
-        for i in range(args.steps):
-            step(i, ev[i])
-        t_end.record(stream)
-        torch.cuda.synchronize()
-    barrier()
-    ms = t_start.elapsed_time(t_end)
-    if world > 1:
-        import torch.distributed as dist
-
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    comp = {k: statistics.mean(e[a].elapsed_time(e[b]) for e in ev) * 1e3
-            for k, (a, b) in {"draft_price": (0, 1), "verify": (1, 2)}.items()}
+    clk = ClockSampler(local)
+    ms, comp = timed_rounds(S, torch, cfg, rounds, args.steps, args.warmup, barrier, clk)
+    ms, job_tok, job_rows = reduce_over_ranks(ms, n_tok, n_rows, world, "cuda")
     ok = all(int(r.ws.status()) == 0 for r in rounds)
     if args.legs == "timed":
         if rank == 0:
             print(json.dumps({"legs": "timed", "ms_per_step": ms / args.steps, "components_us": comp,
                               "status_clean": ok}), flush=True)
         return
+    stream = torch.cuda.current_stream()
 
     # graph-captured round time (one graph per input set)
     graphs = []
@@ -291,12 +369,13 @@ def run_gpu(args):
     g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     for i in range(args.warmup):
         graphs[i % NBUF].replay()
+    g_steps = min(args.steps, 5000)
     g0.record(stream)
-    for i in range(args.steps):
+    for i in range(g_steps):
         graphs[i % NBUF].replay()
     g1.record(stream)
     torch.cuda.synchronize()
-    graph_us = g0.elapsed_time(g1) * 1e3 / args.steps
+    graph_us = g0.elapsed_time(g1) * 1e3 / g_steps
 
     # end to end through the public API with host buffers: H2D of the step's inputs
     # (histories, drafter chain, confidences, logits) from pinned memory, the round,
@@ -324,32 +403,36 @@ def run_gpu(args):
         h_na.copy_(rnd.n_accepted, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / e_steps
+    e2e_ms = reduce_over_ranks(e0.elapsed_time(e1) / e_steps, 0, 0, world, "cuda")[0]
 
+    hbm, peak_kind = peaks()
+    bs4 = measure_bs4(S, torch, W, min(args.steps, 5000), args.warmup, hbm)
     if rank != 0:
         return
-    hbm, peak_kind = peaks()
     verify_us = comp["verify"]
     alg_bytes = n_rows * V * 2
     achieved = alg_bytes / (verify_us * 1e-6) / 1e9
     cpu = cpu_baseline(cfg, oracle_layout(cfg), logits, seconds=args.cpu_seconds) if args.cpu_seconds > 0 else None
     line = {
-        "metric": METRIC, "value": world * n_tok * args.steps / (ms * 1e-3), "unit": UNIT, "n_gpus": world,
+        "metric": METRIC, "value": job_tok * args.steps / (ms * 1e-3), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": config_json(cfg),
-        "rows_per_s": world * n_rows * args.steps / (ms * 1e-3),
+        "rows_per_s": job_rows * args.steps / (ms * 1e-3),
         "verified_tokens_per_step": n_tok, "verify_rows_per_step": n_rows,
         "components_us": {k: round(v, 3) for k, v in comp.items()},
         "graph_round_us": round(graph_us, 3),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
-                     "frac": round(achieved / hbm, 4), "traffic": None, "peak_kind": peak_kind,
+                     "frac": round(achieved / hbm, 4),
+                     "traffic": measured_traffic("verify_rows_kernel<bf16, greedy>", WORKLOAD),
+                     "peak_kind": peak_kind,
                      "kernel": "verify_rows_kernel<bf16, greedy>", "algorithmic_bytes": alg_bytes},
         "cpu_baseline": cpu,
-        "e2e": {"value": world * n_tok / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+        "e2e": {"value": job_tok / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": 2 * args.steps,
         "clocks": clk.summary(),
+        "bs4": bs4,
         "status_clean": ok,
     }
     print(json.dumps(line), flush=True)
@@ -358,8 +441,8 @@ def run_gpu(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--legs", default="all", choices=["all", "timed"],

@@ -171,8 +171,8 @@ spec_status spec_estimator_build(const spec_estimator* est, int32_t L, float* ta
                                  size_t table_bytes, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------
- * Step 1: n-gram prompt lookup ([HS] sec. 4.1 "One step", sec. 4.2 feature
- * list, sec. 5.1 "longest match wins").
+ * Step 1: n-gram prompt lookup ([HS] sec. 4.1, sec. 4.2 feature list,
+ * sec. 5.1: the longest match is the one used).
  *
  * For request r with history x = hist[r * hist_stride ...], T = hist_len[r]:
  * every earlier end position j <= T-2 has a match length l(j), the length of
@@ -293,8 +293,9 @@ spec_status spec_price_and_allocate_static(
     int32_t* row_off, uint8_t* point_mass, uint32_t* status_word, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------
- * Step 3: chain verification ([HS] sec. 2 "accepts the longest prefix that
- * passes rejection sampling, plus one token of its own", App. H point masses;
+ * Step 3: chain verification ([HS] sec. 2: the target keeps the longest
+ * draft prefix that survives rejection sampling and adds one token of its
+ * own; App. H point masses;
  * [LS] sec. 2.1: accept y_i with probability min(1, p_i(y_i)/q_i(y_i)), at the
  * first rejection draw from norm(max(0, p_i - q_i)), after B acceptances draw
  * a bonus from p_{B+1}; r accepted => r + 1 tokens).

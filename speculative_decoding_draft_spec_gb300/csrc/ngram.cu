@@ -1,21 +1,26 @@
-// ngram.cu -- step 1 of the round: n-gram prompt lookup.
+// ngram.cu -- step 1 of the round: n-gram prompt lookup (and, fused with it,
+// step 2 in spec_draft_and_price).
 //
-// Hybrid Spark sec. 4.1 ("One step"): the n-gram drafter proposes up to L
-// tokens following the longest earlier occurrence of the request's last
-// n_min..n_max tokens (sec. 5.1: longest match wins); sec. 4.2 defines the
-// features n (match length), a (runner-up agreement) and m (copy length,
-// capped).  Every earlier end position j <= T-2 has a match length l(j), the
+// Hybrid Spark sec. 4.1: the n-gram drafter proposes up to L tokens following
+// the longest earlier occurrence of the request's last n_min..n_max tokens
+// (sec. 5.1: the longest match is the one used); sec. 4.2 defines the features
+// n (match length), a (runner-up agreement) and m (copy length, capped).
+// Every earlier end position j <= T-2 has a match length l(j), the
 // common-suffix length of x[..j] and x[..T-1] capped at copy_cap; candidates
 // (l(j) >= n_min) rank by (l(j), j) descending.
 //
-// GB300 layout: one thread-block cluster per request.  The cluster's CTAs
-// split the candidate positions into contiguous chunks; each CTA stages its
-// chunk (plus a copy_cap halo behind it) and the request's last copy_cap
-// tokens into shared memory with one-dimensional bulk async copies completed
-// on an mbarrier, compares suffixes from shared memory (one position per
-// thread, early exit on the first mismatch), and reduces a top-2 of packed
-// (l, j) keys with warp shuffles.  Cluster rank 0 merges the CTAs' top-2
-// through distributed shared memory and writes the proposal and features.
+// GB300 layout: one CTA per request, or one thread-block cluster per request
+// for histories over 8192 tokens.  A cluster's CTAs split the candidate
+// positions into contiguous chunks; each CTA stages its chunk (plus a copy_cap
+// halo behind it) and the request's last copy_cap tokens into shared memory
+// with one-dimensional bulk async copies completed on an mbarrier (bounded
+// wait).  Candidates are found four positions per 16-byte shared-memory load
+// (with n_min >= 2 they must also match the second-to-last token); match
+// lengths up to 8 come from independent compares against the suffix held in
+// registers, and longer matches are queued and extended by the whole warp,
+// 32 positions per ballot.  A top-2 of packed (l, j) keys is reduced with
+// warp shuffles; cluster rank 0 merges the CTAs' top-2 through distributed
+// shared memory and writes the proposal and features.
 #include <cooperative_groups.h>
 
 #include "pricing.cuh"

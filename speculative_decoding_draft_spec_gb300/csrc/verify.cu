@@ -10,16 +10,23 @@
 // at its parent's row and its parent is accepted; commit the path and the
 // argmax after it.
 //
-// GB300 layout.  The HBM-bound part is one pass over every verify row.  A
-// persistent grid (SMs x resident CTAs) hands out work items of one warp =
-// one 2048-entry unit of one row, in row-major order, so every warp streams a
-// contiguous 4 KB (bf16) / 8 KB (fp32) block with 16-byte non-allocating
-// loads, all issued before use.  Per unit a warp produces
-//   greedy rows:  a packed 64-bit (ordered value, ~index) key, folded into the
-//                 row's key with one atomicMax (largest value, lowest index);
-//   sampled rows: (max, sum of 2^((z - max) log2e / T)) in the workspace.
+// GB300 layout.  The HBM-bound part is one pass over every verify row.  One
+// CTA per SM, 12 warps each; the work is the sequence of 8 KB chunks of the
+// rows (4096 bf16 / 2048 fp32 entries) in (request, row, chunk) order, and
+// every warp takes an equal contiguous range of it.  Each warp streams its
+// range through its own ring of two 8 KB shared-memory stages filled by
+// one-dimensional bulk async copies (completion on an mbarrier, bounded
+// wait), moves a landed chunk into registers and refills the stage at once,
+// so two copies per warp stay in flight while it computes.  Per chunk a warp
+// produces
+//   greedy rows:  a packed 64-bit (ordered value, ~index) key; keys of one
+//                 row fold in registers and reach the row's workspace key with
+//                 one atomicMax per run of the row (largest value, lowest
+//                 index);
+//   sampled rows: (max, sum of 2^((z - max) log2e / T)) per 2048-entry unit
+//                 in the workspace.
 // Each request has an arrival counter; the warp that completes a request's
-// last unit (threadfence + atomicAdd, no waiting) finalizes it: argmax
+// last chunk (acquire-release atomic, no waiting) finalizes it: argmax
 // compare or Philox accept tests, and for a draw the inverse CDF in
 // vocabulary order located first over the units' sums and then inside the
 // one unit that holds the crossing (a second read of 4-8 KB, not of the row).

@@ -1,5 +1,5 @@
 """Pins of the oracle's n-gram lookup (Hybrid Spark sec. 4.1, sec. 4.2 features,
-sec. 5.1 "longest match wins"): hand-built histories whose match is known by
+sec. 5.1, where the longest match is the one used): hand-built histories whose match is known by
 construction, and an independent restatement by substring search on tiny inputs."""
 import numpy as np
 import pytest

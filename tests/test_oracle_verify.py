@@ -1,6 +1,6 @@
 """Pins of the oracle's chain verification (Hybrid Spark sec. 2 and App. H;
-the fixed-cost parallel drafter page's accept / resample rule and its
-"r accepted => r + 1 tokens").
+the fixed-cost parallel drafter page's accept / resample rule, under which a
+round that accepts r drafts emits r + 1 tokens).
 
 The central pin is exact losslessness: on tiny vocabularies the law of the
 tokens a round emits, continued by the target itself, equals the target's own
