@@ -326,6 +326,98 @@ def measure_bs4(S, torch, W, steps, warmup, hbm):
             "l2": "10 rotating input sets (10 x 19.5 MB > L2)"}
 
 
+def measure_long_sampled(S, torch, W, steps, warmup, hbm):
+    """The batch-64 long-context workload: draft + price over 32768-token
+    histories (clusters of CTAs per request), then sampled chain verification
+    at T = 0.7 over fp32 logits materialised as 16 rows per request; two input
+    sets (2 x 622 MB > L2)."""
+    from speculative_decoding_draft_spec_gb300.round import ChainRound
+
+    cfg = W.long_bs64()
+    B, K, L, V, rows = cfg["B"], cfg["K"], cfg["L"], cfg["V"], cfg["rows_per_request"]
+    ro = torch.as_tensor(cfg["row_off_materialised"]).to("cuda")
+    logits = torch.from_numpy(W.materialised_logits(cfg)).to("cuda")
+    rounds = []
+    for k in range(2):
+        rnd = ChainRound(B, cfg["hist"].shape[1], K, L, V, torch.float32, B * rows, cfg["coef"], cfg["n_min"],
+                         cfg["n_max"], cfg["copy_cap"])
+        rnd.load(cfg["hist"], cfg["hist_len"], cfg["d"], cfg["c"], cfg["d_len"])
+        rnd.logits.copy_(logits)
+        rounds.append(rnd)
+    del logits
+    stream = torch.cuda.current_stream()
+
+    def one(i, rec=None):
+        rnd = rounds[i % 2]
+        if rec:
+            rec[0].record(stream)
+        rnd.draft_and_price(cfg["lam"], cfg["budget"], cfg["max_verify_len"], cfg["policy"], True, stream)
+        if rec:
+            rec[1].record(stream)
+        rnd.verify(temperature=cfg["temperature"], seed=0, step=i, row_off=ro, stream=stream)
+        if rec:
+            rec[2].record(stream)
+
+    for i in range(warmup):
+        one(i)
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(steps):
+        one(i, ev[i])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1)
+    comp = {k: statistics.mean(e[a].elapsed_time(e[b]) for e in ev) * 1e3
+            for k, (a, b) in {"draft_price": (0, 1), "verify": (1, 2)}.items()}
+    vlen = rounds[0].verify_len.cpu().numpy()
+    n_tok = int(vlen.sum())
+    n_rows = int((vlen + 1).sum())
+    achieved = n_rows * V * 4 / (comp["verify"] * 1e-6) / 1e9
+    return {"workload": "long_bs64: B=64, history 32768, n <= 4, budget 512, lambda 0.3, T=0.7, fp32 logits "
+                        "materialised as 16 rows per request",
+            "value": n_tok * steps / (ms * 1e-3), "unit": UNIT, "rows_per_s": n_rows * steps / (ms * 1e-3),
+            "ms_per_step": ms / steps, "steps": steps, "verified_tokens_per_step": n_tok,
+            "verify_rows_per_step": n_rows, "components_us": {k: round(v, 3) for k, v in comp.items()},
+            "verify_roofline_frac": round(achieved / hbm, 4),
+            "status_clean": all(int(r.ws.status()) == 0 for r in rounds),
+            "l2": "2 rotating input sets (2 x 622 MB > L2)"}
+
+
+def measure_tree(S, torch, W, steps, warmup, hbm):
+    """Greedy tree verification, batch 32 trees of 16 rows (bf16 V = 151936);
+    two input sets (2 x 156 MB > L2)."""
+    cfg = W.tree_bs32(width=16)
+    B, V, n = cfg["B"], cfg["V"], cfg["width"]
+    rows = int(cfg["node_off"][-1])
+    lt = torch.from_numpy(cfg["logits"].view(np.int16)).view(torch.bfloat16).to("cuda")
+    sets = [lt, lt.clone()]
+    dev = lambda a: torch.as_tensor(np.ascontiguousarray(a)).to("cuda")
+    node_off, tok, parent = dev(cfg["node_off"]), dev(cfg["tok"]), dev(cfg["parent"])
+    i32 = dict(dtype=torch.int32, device="cuda")
+    path, out = torch.empty((B, n), **i32), torch.empty((B, n), **i32)
+    acc = torch.empty(B, **i32)
+    ws = S.Workspace(B, rows, 1, V)
+    stream = torch.cuda.current_stream()
+    for i in range(warmup):
+        S.spec_verify_tree(sets[i % 2], node_off, rows, tok, parent, n, path, acc, out, ws, stream)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for i in range(steps):
+        ev[i][0].record(stream)
+        S.spec_verify_tree(sets[i % 2], node_off, rows, tok, parent, n, path, acc, out, ws, stream)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    us = statistics.mean(a.elapsed_time(b) for a, b in ev) * 1e3
+    accepted = int(acc.sum().item())
+    return {"workload": "tree_bs32: B=32 trees of 16 rows, bf16 V=151936", "tree_rows_per_s": rows / (us * 1e-6),
+            "accepted_tokens_per_s": accepted / (us * 1e-6), "us_per_step": round(us, 3), "steps": steps,
+            "rows_per_step": rows, "accepted_per_step": accepted,
+            "verify_roofline_frac": round(rows * V * 2 / (us * 1e-6) / 1e9 / hbm, 4),
+            "status_clean": int(ws.status()) == 0, "l2": "2 rotating input sets (2 x 156 MB > L2)"}
+
+
 def run_gpu(args):
     import torch
 
@@ -407,6 +499,8 @@ def run_gpu(args):
 
     hbm, peak_kind = peaks()
     bs4 = measure_bs4(S, torch, W, min(args.steps, 5000), args.warmup, hbm)
+    long_sampled = measure_long_sampled(S, torch, W, min(args.steps, 1000), args.warmup, hbm)
+    tree = measure_tree(S, torch, W, min(args.steps, 2000), args.warmup, hbm)
     if rank != 0:
         return
     verify_us = comp["verify"]
@@ -433,6 +527,8 @@ def run_gpu(args):
         "gpu_launches": 2 * args.steps,
         "clocks": clk.summary(),
         "bs4": bs4,
+        "long_bs64_sampled": long_sampled,
+        "tree_bs32": tree,
         "status_clean": ok,
     }
     print(json.dumps(line), flush=True)
