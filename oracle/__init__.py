@@ -13,7 +13,8 @@ Sources, cited by title and section in the C file:
     the Drafter (n-gram lookup, Eq. (1) estimator, chain value Eq. (3),
     contains rule, adaptive-verification allocation, lossless policies);
   * AdaSpark: Adaptive DSpark with Online Learning for Tree Verification and
-    N-gram Fill (greedy tree verification, sec. 2.2);
+    N-gram Fill (greedy tree verification, sec. 2.2; the candidate tree and
+    its best-first order, sec. 3.1, sec. 3.3 Eq. (6));
   * Efficient speculative decoding with a fixed-cost parallel drafter
     (accept / resample rule, r accepted => r + 1 tokens);
   * Salmon et al., "Parallel random numbers: as easy as 1, 2, 3" (Philox).
@@ -133,6 +134,9 @@ def _declare(L):
     L.oracle_verify_tree.restype = C.c_int
     L.oracle_row_argmax.argtypes = [C.c_void_p, C.c_int32, C.c_int32]
     L.oracle_row_argmax.restype = C.c_int32
+    L.oracle_build_tree.argtypes = [C.c_int32, C.c_int32, C.c_int32, _i32p, _i32p, _f32p, _i32p, C.c_int32,
+                                    _i32p, _f32p, _f32p, C.c_int32, _i32p, _i32p, _i32p, _i32p, _f64p]
+    L.oracle_build_tree.restype = C.c_int
 
 
 def _p(a, ct):
@@ -339,3 +343,34 @@ def verify_tree(logits, node_off, tok, parent, max_nodes) -> TreeOut:
 def row_argmax(row) -> int:
     a, dt = _logits(row)
     return int(lib().oracle_row_argmax(a.ctypes.data, a.shape[-1], dt))
+
+
+# --------------------------------------------------------------------------- tree builder
+@dataclass
+class TreeBuild:
+    tok: np.ndarray       # [B x width], -1 past n_rows
+    parent: np.ndarray    # [B x width], local; -1 at the anchor and past n_rows
+    cand_id: np.ndarray   # [B x width]
+    n_rows: np.ndarray    # [B]
+    Q: np.ndarray         # [B x (1 + P Kc + Lg)], -1 past the last candidate
+    status: int
+
+
+def build_tree(anchor, cand_tok, cand_score, ng_tok, ng_len, ng_score, ng_adj, width) -> TreeBuild:
+    cand_tok, cand_score = _c(cand_tok, np.int32), _c(cand_score, np.float32)
+    B, P, Kc = cand_tok.shape
+    ng_tok = _c(ng_tok, np.int32).reshape(B, -1)
+    Lg = ng_tok.shape[1]
+    anchor, ng_len = _c(anchor, np.int32), _c(ng_len, np.int32)
+    ng_score, ng_adj = _c(ng_score, np.float32), _c(ng_adj, np.float32)
+    tok = np.empty((B, width), np.int32)
+    parent = np.empty((B, width), np.int32)
+    cid = np.empty((B, width), np.int32)
+    nr = np.empty(B, np.int32)
+    Q = np.empty((B, 1 + P * Kc + Lg))
+    st = lib().oracle_build_tree(B, P, Kc, _p(anchor, C.c_int32), _p(cand_tok, C.c_int32),
+                                 _p(cand_score, C.c_float), _p(ng_tok, C.c_int32), Lg, _p(ng_len, C.c_int32),
+                                 _p(ng_score, C.c_float), _p(ng_adj, C.c_float), int(width), _p(tok, C.c_int32),
+                                 _p(parent, C.c_int32), _p(cid, C.c_int32), _p(nr, C.c_int32),
+                                 _p(Q, C.c_double))
+    return TreeBuild(tok, parent, cid, nr, Q, _check(st))

@@ -719,3 +719,160 @@ int oracle_verify_tree(
   }
   return status;
 }
+
+/* ------------------------------------------------------------------------ */
+/* The candidate tree of one block-drafter round ([AS] sec. 2.2 tree shape; */
+/* sec. 3.3 n-gram candidates and Eq. (6); sec. 3.1, Prop. 1, best-first    */
+/* order; Algorithm 1: the first n-1 nodes, laid out depth-first).          */
+/*                                                                          */
+/* Candidates: 0 the anchor; 1 + i Kc + k the k-th ranked candidate of      */
+/* block position i (k = 0 the pick, k >= 1 its siblings); the picks form a */
+/* spine (pick i under pick i-1, pick 0 under the anchor) and the siblings  */
+/* of position i hang from the pick's parent as leaves.  The n-gram chain   */
+/* walks from the anchor: a step whose token equals a drafter child of the  */
+/* current node marks that child agreed and moves to it (the lowest index   */
+/* on duplicates); otherwise it appends an n-gram node under the current    */
+/* node and moves to it.  At every node the chain passes through, the       */
+/* drafter children other than the agreed one are contradicted.             */
+/* Scores: a drafter candidate keeps its given s, plus adj if agreed, minus */
+/* adj if contradicted (adj = max(0, logit p_src) from the caller; reading: */
+/* the agreed / contradiction bucket weights are zero, their prior); an     */
+/* n-gram node scores ng_score.  Scores are clamped to [-80, 80].           */
+/* q_j = exp(s_j) / (1 + sum over the children c of parent(j) of exp(s_c))  */
+/* (children summed in index order); Q_j = Q_parent(j) q_j, Q_0 = 1.  The   */
+/* order is Q descending, ties to the lower index; the tree is the anchor   */
+/* and the first width-1 candidates of the order, laid out depth-first with */
+/* children in increasing candidate index (reading: the page fixes no child */
+/* order).  All in double.                                                  */
+/* ------------------------------------------------------------------------ */
+int oracle_build_tree(int32_t batch, int32_t P, int32_t Kc, const int32_t* anchor,
+                      const int32_t* cand_tok, const float* cand_score,
+                      const int32_t* ng_tok, int32_t Lg, const int32_t* ng_len,
+                      const float* ng_score, const float* ng_adj, int32_t width,
+                      int32_t* tok, int32_t* parent, int32_t* cand_id, int32_t* n_rows,
+                      double* dbg_Q) {
+  if (batch < 0 || P < 0 || Kc < 1 || Lg < 0 || width < 1) return ORACLE_ERR_ARG;
+  const int32_t cap = 1 + P * Kc + Lg;
+  int32_t* ctok = (int32_t*)malloc(sizeof(int32_t) * (size_t)cap);
+  int32_t* cpar = (int32_t*)malloc(sizeof(int32_t) * (size_t)cap);
+  int32_t* drafter = (int32_t*)malloc(sizeof(int32_t) * (size_t)cap);
+  int32_t* flag = (int32_t*)malloc(sizeof(int32_t) * (size_t)cap); /* +1 agreed, -1 contradicted */
+  int32_t* chosen = (int32_t*)malloc(sizeof(int32_t) * (size_t)cap);
+  int32_t* order = (int32_t*)malloc(sizeof(int32_t) * (size_t)cap);
+  int32_t* pos = (int32_t*)malloc(sizeof(int32_t) * (size_t)cap);
+  double* s = (double*)malloc(sizeof(double) * (size_t)cap);
+  double* q = (double*)malloc(sizeof(double) * (size_t)cap);
+  double* Q = (double*)malloc(sizeof(double) * (size_t)cap);
+  int status = 0;
+  for (int32_t r = 0; r < batch; ++r) {
+    /* the drafter's block */
+    int32_t N = 1 + P * Kc;
+    ctok[0] = anchor[r];
+    cpar[0] = -1;
+    drafter[0] = 0;
+    flag[0] = 0;
+    s[0] = 0.0;
+    for (int32_t i = 0; i < P; ++i)
+      for (int32_t k = 0; k < Kc; ++k) {
+        const int32_t j = 1 + i * Kc + k;
+        ctok[j] = cand_tok[((int64_t)r * P + i) * Kc + k];
+        cpar[j] = (i == 0) ? 0 : 1 + (i - 1) * Kc;
+        drafter[j] = 1;
+        flag[j] = 0;
+        s[j] = (double)cand_score[((int64_t)r * P + i) * Kc + k];
+      }
+    /* the n-gram chain from the anchor */
+    int32_t gl = ng_len[r];
+    if (gl < 0 || gl > Lg) {
+      status |= ORACLE_ST_BAD_LENGTH;
+      gl = 0;
+    }
+    int32_t cur = 0;
+    for (int32_t t = 0; t < gl; ++t) {
+      const int32_t x = ng_tok[(int64_t)r * Lg + t];
+      int32_t hit = -1;
+      for (int32_t c = cur + 1; c < N; ++c)
+        if (drafter[c] && cpar[c] == cur && ctok[c] == x) {
+          hit = c;
+          break;
+        }
+      for (int32_t c = cur + 1; c < N; ++c)
+        if (drafter[c] && cpar[c] == cur && c != hit) flag[c] = -1;
+      if (hit >= 0) {
+        flag[hit] = 1;
+        cur = hit;
+      } else {
+        ctok[N] = x;
+        cpar[N] = cur;
+        drafter[N] = 0;
+        flag[N] = 0;
+        s[N] = (double)ng_score[r];
+        cur = N;
+        ++N;
+      }
+    }
+    const double adj = (double)ng_adj[r];
+    for (int32_t j = 1; j < N; ++j) {
+      if (drafter[j]) s[j] += (flag[j] > 0 ? adj : 0.0) - (flag[j] < 0 ? adj : 0.0);
+      if (s[j] > 80.0) s[j] = 80.0;
+      if (s[j] < -80.0) s[j] = -80.0;
+    }
+    /* Eq. (6): one softmax per parent over its children and "none" */
+    for (int32_t p = 0; p < N; ++p) {
+      double den = 1.0;
+      for (int32_t c = p + 1; c < N; ++c)
+        if (cpar[c] == p) den += exp(s[c]);
+      for (int32_t c = p + 1; c < N; ++c)
+        if (cpar[c] == p) q[c] = exp(s[c]) / den;
+    }
+    Q[0] = 1.0;
+    for (int32_t j = 1; j < N; ++j) Q[j] = Q[cpar[j]] * q[j];
+    if (dbg_Q) {
+      for (int32_t j = 0; j < cap; ++j) dbg_Q[(int64_t)r * cap + j] = j < N ? Q[j] : -1.0;
+    }
+    /* best-first order (insertion sort: Q descending, ties to the lower index) */
+    int32_t m = 0;
+    for (int32_t j = 1; j < N; ++j) {
+      int32_t at = m;
+      while (at > 0 && (Q[order[at - 1]] < Q[j])) --at;
+      for (int32_t z = m; z > at; --z) order[z] = order[z - 1];
+      order[at] = j;
+      ++m;
+    }
+    const int32_t take = (width - 1 < m) ? width - 1 : m;
+    for (int32_t j = 0; j < N; ++j) chosen[j] = (j == 0);
+    for (int32_t z = 0; z < take; ++z) chosen[order[z]] = 1;
+    /* depth-first layout, children in increasing candidate index */
+    int32_t n = 0;
+    int32_t* stack = order; /* reuse: the order is no longer needed */
+    int32_t sp = 0;
+    stack[sp++] = 0;
+    while (sp > 0) {
+      const int32_t j = stack[--sp];
+      pos[j] = n;
+      tok[(int64_t)r * width + n] = ctok[j];
+      parent[(int64_t)r * width + n] = (j == 0) ? -1 : pos[cpar[j]];
+      cand_id[(int64_t)r * width + n] = j;
+      ++n;
+      for (int32_t c = N - 1; c > j; --c) /* pushed in decreasing index: popped increasing */
+        if (chosen[c] && cpar[c] == j) stack[sp++] = c;
+    }
+    for (int32_t z = n; z < width; ++z) {
+      tok[(int64_t)r * width + z] = -1;
+      parent[(int64_t)r * width + z] = -1;
+      cand_id[(int64_t)r * width + z] = -1;
+    }
+    n_rows[r] = n;
+  }
+  free(ctok);
+  free(cpar);
+  free(drafter);
+  free(flag);
+  free(chosen);
+  free(order);
+  free(pos);
+  free(s);
+  free(q);
+  free(Q);
+  return status;
+}

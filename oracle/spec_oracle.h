@@ -140,6 +140,20 @@ int oracle_verify_tree(
     const int32_t* tok, const int32_t* parent, int32_t max_nodes,
     int32_t* path, int32_t* accept_len, int32_t* out_tokens);
 
+/* The candidate tree of one block-drafter round ([AS] sec. 2.2, sec. 3.1
+ * Prop. 1, sec. 3.3 Eq. (6), Algorithm 1).  cand_tok / cand_score
+ * [batch x P x Kc] (k = 0 the pick), ng_tok [batch x Lg] with ng_len[r]
+ * tokens, ng_score / ng_adj [batch].  Outputs [batch x width]: tok, parent
+ * (local, -1 at the anchor), cand_id (candidate index), unused rows -1;
+ * n_rows [batch].  dbg_Q [batch x (1 + P Kc + Lg)]: Q per candidate index
+ * (-1 past the last), may be NULL. */
+int oracle_build_tree(int32_t batch, int32_t P, int32_t Kc, const int32_t* anchor,
+                      const int32_t* cand_tok, const float* cand_score,
+                      const int32_t* ng_tok, int32_t Lg, const int32_t* ng_len,
+                      const float* ng_score, const float* ng_adj, int32_t width,
+                      int32_t* tok, int32_t* parent, int32_t* cand_id, int32_t* n_rows,
+                      double* dbg_Q);
+
 /* argmax of one row (lowest index on ties); NaN entries are skipped */
 int32_t oracle_row_argmax(const void* row, int32_t vocab, int32_t dtype);
 

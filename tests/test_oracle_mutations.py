@@ -13,6 +13,7 @@ from . import test_oracle_ngram as TN
 from . import test_oracle_philox as TP
 from . import test_oracle_price as TPR
 from . import test_oracle_tree as TT
+from . import test_oracle_tree_build as TB
 from . import test_oracle_verify as TV
 
 SRC = os.path.join(os.path.dirname(ORC.__file__), "spec_oracle.c")
@@ -77,6 +78,25 @@ MUTATIONS = [
     ("tree commits the last path token, not its argmax", "out_tokens[(int64_t)r * max_nodes + len - 1] = a;",
      "out_tokens[(int64_t)r * max_nodes + len - 1] = tok[base + cur];",
      [TT.test_path_by_brute_force_over_root_to_node_paths]),
+    # candidate-tree builder (AdaSpark sec. 2.2, sec. 3.1, sec. 3.3 Eq. (6))
+    ("tree builder drops the none outcome of Eq. (6)", "double den = 1.0;", "double den = 0.0;",
+     [TB.test_chain_only_tree_is_a_path_of_sigmoids, lambda o: TB.test_equal_scores_share_one_softmax_with_none(o, 4, -1.3)]),
+    ("tree builder ties to the higher index", "while (at > 0 && (Q[order[at - 1]] < Q[j])) --at;",
+     "while (at > 0 && (Q[order[at - 1]] <= Q[j])) --at;", [TB.test_ties_go_to_the_lower_index]),
+    ("tree builder rewards contradicted candidates", "- (flag[j] < 0 ? adj : 0.0);", "+ (flag[j] < 0 ? adj : 0.0);",
+     [TB.test_ngram_chain_agrees_with_picks_then_extends,
+      TB.test_ngram_chain_that_matches_no_candidate_contradicts_them_all]),
+    ("tree builder hangs siblings under their own pick",
+     "cpar[j] = (i == 0) ? 0 : 1 + (i - 1) * Kc;",
+     "cpar[j] = (k == 0) ? ((i == 0) ? 0 : 1 + (i - 1) * Kc) : 1 + i * Kc;",
+     [TB.test_picks_form_a_spine_and_siblings_are_leaves]),
+    ("tree builder lays children out in decreasing index",
+     "for (int32_t c = N - 1; c > j; --c) /* pushed", "for (int32_t c = j + 1; c < N; ++c) /* pushed",
+     [lambda o: TB.test_layout_is_depth_first_with_children_in_index_order(o, 0),
+      lambda o: TB.test_layout_is_depth_first_with_children_in_index_order(o, 1)]),
+    ("tree builder multiplies Q by the parent's q", "for (int32_t j = 1; j < N; ++j) Q[j] = Q[cpar[j]] * q[j];",
+     "for (int32_t j = 1; j < N; ++j) Q[j] = Q[cpar[j]] * q[cpar[j] > 0 ? cpar[j] : j];",
+     [TB.test_chain_only_tree_is_a_path_of_sigmoids, TB.test_ngram_chain_agrees_with_picks_then_extends]),
 ]
 
 
