@@ -386,36 +386,66 @@ def measure_long_sampled(S, torch, W, steps, warmup, hbm):
 
 
 def measure_tree(S, torch, W, steps, warmup, hbm):
-    """Greedy tree verification, batch 32 trees of 16 rows (bf16 V = 151936);
-    two input sets (2 x 156 MB > L2)."""
+    """The tree round, batch 32 trees of 16 rows (bf16 V = 151936): the candidate
+    tree built on the device from the drafter's block and the n-gram chain
+    (spec_build_tree), then greedy tree verification (spec_verify_tree); two
+    logit sets (2 x 156 MB > L2)."""
     cfg = W.tree_bs32(width=16)
     B, V, n = cfg["B"], cfg["V"], cfg["width"]
-    rows = int(cfg["node_off"][-1])
-    lt = torch.from_numpy(cfg["logits"].view(np.int16)).view(torch.bfloat16).to("cuda")
-    sets = [lt, lt.clone()]
-    dev = lambda a: torch.as_tensor(np.ascontiguousarray(a)).to("cuda")
-    node_off, tok, parent = dev(cfg["node_off"]), dev(cfg["tok"]), dev(cfg["parent"])
+    dev = lambda a, dt=None: torch.as_tensor(np.ascontiguousarray(a)).to("cuda") if dt is None else \
+        torch.as_tensor(np.ascontiguousarray(a)).to("cuda", dt)
+    blk = [dev(cfg[k]) for k in ("anchor", "cand_tok", "cand_score", "ng_tok", "ng_len", "ng_score", "ng_adj")]
     i32 = dict(dtype=torch.int32, device="cuda")
+    tok2, par2, cid2 = (torch.empty((B, n), **i32) for _ in range(3))
+    nrow = torch.empty(B, **i32)
+    ws_b = S.Workspace(B, 1, 1, 1)
+    S.spec_build_tree(*blk, n, tok2, par2, cid2, nrow, ws_b)
+    torch.cuda.synchronize()
+    node_off_h, tok_h, par_h = W.flatten_trees(tok2.cpu().numpy(), par2.cpu().numpy(), nrow.cpu().numpy())
+    rows = int(node_off_h[-1])
+    logits, _ = W.tree_logits(node_off_h, tok_h, par_h, V)
+    lt = torch.from_numpy(logits.view(np.int16)).view(torch.bfloat16).to("cuda")
+    sets = [lt, lt.clone()]
+    node_off = dev(node_off_h)
+    # the verify reads the builder's rows in place: [B x n] with every tree full
+    assert np.all(nrow.cpu().numpy() == n)
     path, out = torch.empty((B, n), **i32), torch.empty((B, n), **i32)
     acc = torch.empty(B, **i32)
     ws = S.Workspace(B, rows, 1, V)
     stream = torch.cuda.current_stream()
+
+    def one(i, rec=None):
+        if rec:
+            rec[0].record(stream)
+        S.spec_build_tree(*blk, n, tok2, par2, cid2, nrow, ws_b, stream)
+        if rec:
+            rec[1].record(stream)
+        S.spec_verify_tree(sets[i % 2], node_off, rows, tok2, par2, n, path, acc, out, ws, stream)
+        if rec:
+            rec[2].record(stream)
+
     for i in range(warmup):
-        S.spec_verify_tree(sets[i % 2], node_off, rows, tok, parent, n, path, acc, out, ws, stream)
+        one(i)
     torch.cuda.synchronize()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
     for i in range(steps):
-        ev[i][0].record(stream)
-        S.spec_verify_tree(sets[i % 2], node_off, rows, tok, parent, n, path, acc, out, ws, stream)
-        ev[i][1].record(stream)
+        one(i, ev[i])
+    t1.record(stream)
     torch.cuda.synchronize()
-    us = statistics.mean(a.elapsed_time(b) for a, b in ev) * 1e3
+    ms = t0.elapsed_time(t1)
+    comp = {k: statistics.mean(e[a].elapsed_time(e[b]) for e in ev) * 1e3
+            for k, (a, b) in {"build": (0, 1), "verify": (1, 2)}.items()}
     accepted = int(acc.sum().item())
-    return {"workload": "tree_bs32: B=32 trees of 16 rows, bf16 V=151936", "tree_rows_per_s": rows / (us * 1e-6),
-            "accepted_tokens_per_s": accepted / (us * 1e-6), "us_per_step": round(us, 3), "steps": steps,
-            "rows_per_step": rows, "accepted_per_step": accepted,
-            "verify_roofline_frac": round(rows * V * 2 / (us * 1e-6) / 1e9 / hbm, 4),
-            "status_clean": int(ws.status()) == 0, "l2": "2 rotating input sets (2 x 156 MB > L2)"}
+    return {"workload": "tree_bs32: B=32, block of 8 picks with top-4 candidates plus a 15-token n-gram chain, "
+                        "trees of 16 rows, bf16 V=151936",
+            "tree_rows_per_s": rows * steps / (ms * 1e-3), "accepted_tokens_per_s": accepted * steps / (ms * 1e-3),
+            "ms_per_step": ms / steps, "steps": steps, "rows_per_step": rows, "accepted_per_step": accepted,
+            "components_us": {k: round(v, 3) for k, v in comp.items()},
+            "verify_roofline_frac": round(rows * V * 2 / (comp["verify"] * 1e-6) / 1e9 / hbm, 4),
+            "status_clean": int(ws.status()) == 0 and int(ws_b.status()) == 0,
+            "l2": "2 rotating logit sets (2 x 156 MB > L2)"}
 
 
 def run_gpu(args):

@@ -256,6 +256,43 @@ spec_status spec_draft_and_price(
     uint8_t* point_mass, const spec_workspace* ws, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------
+ * spec_build_tree: the candidate tree of one block-drafter round ([AS]
+ * sec. 2.2 tree shape; sec. 3.3 n-gram candidates and Eq. (6); sec. 3.1 and
+ * Proposition 1, best-first order; Algorithm 1, the first n-1 nodes laid out
+ * depth-first).  Its output feeds spec_verify_tree.
+ *
+ * Per request r: anchor[r], the committed token the tree hangs from; a block
+ * of P positions with Kc ranked candidates each, cand_tok / cand_score
+ * [batch x P x Kc] (k = 0 the drafter's pick, k >= 1 its siblings; the score
+ * s of Eq. (6), from the caller's acceptance model); an n-gram chain from the
+ * anchor, ng_tok [batch x Lg] with ng_len[r] tokens; ng_score[r], the score of
+ * an n-gram node; ng_adj[r] = max(0, logit p_src), added to an agreed drafter
+ * candidate's score and subtracted from a contradicted one's.
+ * Candidates: 0 the anchor; 1 + i Kc + k position i's k-th candidate; then
+ * the n-gram nodes in chain order.  Pick i hangs from pick i-1 (pick 0 from
+ * the anchor); the siblings of position i hang from the pick's parent, as
+ * leaves.  The chain walks from the anchor: a step equal to a drafter child
+ * of the current node marks that child agreed (lowest index on duplicates)
+ * and moves to it, else it appends an n-gram node and moves to it; the other
+ * drafter children of every node it passes through are contradicted.
+ * Scores are clamped to [-80, 80].
+ * q_j = e^{s_j} / (1 + sum over the children c of parent(j) of e^{s_c}),
+ * Q_j = Q_parent(j) q_j (fp64); order: Q descending, ties to the lower index.
+ * Outputs [batch x width]: the anchor and the first width-1 candidates of the
+ * order, depth-first with children in increasing candidate index: tok,
+ * parent (row of the parent, -1 at the anchor), cand_id (candidate index);
+ * rows past n_rows[r] = min(width, number of candidates) are -1.
+ * ng_len[r] outside [0, Lg] sets SPEC_DEV_BAD_LENGTH (no chain).
+ * Limits: Kc >= 1, P >= 0, Lg >= 0, 1 + P Kc + Lg <= SPEC_MAX_TREE_NODES,
+ * 1 <= width <= SPEC_MAX_TREE_NODES.  The workspace serves only its status word.
+ * ------------------------------------------------------------------------ */
+spec_status spec_build_tree(int32_t batch, int32_t P, int32_t Kc, const int32_t* anchor,
+                            const int32_t* cand_tok, const float* cand_score, const int32_t* ng_tok,
+                            int32_t Lg, const int32_t* ng_len, const float* ng_score, const float* ng_adj,
+                            int32_t width, int32_t* tok, int32_t* parent, int32_t* cand_id, int32_t* n_rows,
+                            const spec_workspace* ws, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
  * spec_price_and_allocate_static: step 2 without a workspace.  The method has
  * no counterpart of this call; it is an interface variant of
  * spec_price_and_allocate for callers that cannot hand the library device

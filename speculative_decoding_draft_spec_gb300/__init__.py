@@ -24,7 +24,7 @@ from ._build import build
 
 __all__ = [
     "build", "load", "Workspace", "EstimatorTable", "SpecError", "spec_ngram_propose",
-    "spec_price_and_allocate", "spec_price_and_allocate_static", "spec_draft_and_price", "spec_verify_chain", "spec_verify_tree", "POLICY", "DEV_BITS",
+    "spec_price_and_allocate", "spec_price_and_allocate_static", "spec_draft_and_price", "spec_verify_chain", "spec_verify_tree", "spec_build_tree", "POLICY", "DEV_BITS",
 ]
 
 SPEC_OK, SPEC_ERR_INVALID_ARG, SPEC_ERR_CUDA, SPEC_ERR_UNSUPPORTED, SPEC_ERR_WORKSPACE = 0, 1, 2, 3, 4
@@ -88,6 +88,8 @@ SIGNATURES = {
                               _vp, _vp, _vp, _vp, _WSP, _vp], _i32),
     "spec_verify_chain": ([_i32, _i32, _i32, _vp, _vp, _i32, _vp, _i32, _vp, _i32, _vp, _vp, _f32,
                            _u64, _u64, _vp, _vp, _vp, _vp, _vp, _vp, _WSP, _vp], _i32),
+    "spec_build_tree": ([_i32, _i32, _i32, _vp, _vp, _vp, _vp, _i32, _vp, _vp, _vp, _i32, _vp, _vp, _vp, _vp,
+                         _WSP, _vp], _i32),
     "spec_verify_tree": ([_i32, _i32, _i32, _vp, _vp, _i32, _vp, _vp, _i32, _vp, _vp, _vp, _WSP, _vp],
                          _i32),
 }
@@ -277,3 +279,14 @@ def spec_verify_tree(logits, node_off, max_rows, tok, parent, max_nodes, path, a
     _check("spec_verify_tree", load().spec_verify_tree(
         B, V, _dtype_code(logits), _ptr(logits), _ptr(node_off), int(max_rows), _ptr(tok), _ptr(parent),
         int(max_nodes), _ptr(path), _ptr(accept_len), _ptr(out_tokens), ws.ref, _stream(stream)))
+
+
+def spec_build_tree(anchor, cand_tok, cand_score, ng_tok, ng_len, ng_score, ng_adj, width, tok, parent, cand_id,
+                    n_rows, ws: Workspace, stream=None):
+    """cand_tok / cand_score [B x P x Kc], ng_tok [B x Lg]; outputs tok / parent /
+    cand_id [B x width], n_rows [B] (all int32 device tensors)."""
+    B, P, Kc = cand_tok.shape
+    Lg = ng_tok.shape[1]
+    _check("spec_build_tree", load().spec_build_tree(
+        B, P, Kc, _ptr(anchor), _ptr(cand_tok), _ptr(cand_score), _ptr(ng_tok), Lg, _ptr(ng_len), _ptr(ng_score),
+        _ptr(ng_adj), int(width), _ptr(tok), _ptr(parent), _ptr(cand_id), _ptr(n_rows), ws.ref, _stream(stream)))

@@ -33,6 +33,11 @@ cudaError_t spec_launch_price(int32_t batch, int32_t K, int32_t L, const int32_t
                               int32_t* chain, float* S, int32_t* chain_len, int32_t* source,
                               int32_t* verify_len, int32_t* row_off, uint8_t* point_mass,
                               uint32_t* status, uint32_t* keys, cudaStream_t stream);
+cudaError_t spec_launch_build_tree(int32_t batch, int32_t P, int32_t Kc, const int32_t* anchor,
+                                   const int32_t* cand_tok, const float* cand_score, const int32_t* ng_tok,
+                                   int32_t Lg, const int32_t* ng_len, const float* ng_score, const float* ng_adj,
+                                   int32_t width, int32_t* tok, int32_t* parent, int32_t* cand_id,
+                                   int32_t* n_rows, uint32_t* status, cudaStream_t stream);
 cudaError_t spec_launch_draft_price(
     const int32_t* hist, int64_t stride, const int32_t* hist_len, int32_t batch, int32_t n_min, int32_t n_max,
     int32_t cap, int32_t* g, int32_t* g_len, int32_t* match_n, int32_t* agree, int32_t* copy_len, int32_t K,
@@ -246,6 +251,24 @@ spec_status spec_price_and_allocate_static(
                                             est_table, lambda, budget, max_verify_len, (int32_t)policy,
                                             draft_greedy ? 1 : 0, chain, S, chain_len, source, verify_len,
                                             row_off, point_mass, status_word, stream));
+}
+
+spec_status spec_build_tree(int32_t batch, int32_t P, int32_t Kc, const int32_t* anchor,
+                            const int32_t* cand_tok, const float* cand_score, const int32_t* ng_tok,
+                            int32_t Lg, const int32_t* ng_len, const float* ng_score, const float* ng_adj,
+                            int32_t width, int32_t* tok, int32_t* parent, int32_t* cand_id, int32_t* n_rows,
+                            const spec_workspace* ws, cudaStream_t stream) {
+  if (batch < 0 || P < 0 || Kc < 1 || Lg < 0 || width < 1) return SPEC_ERR_INVALID_ARG;
+  if ((int64_t)1 + (int64_t)P * Kc + Lg > SPEC_MAX_TREE_NODES || width > SPEC_MAX_TREE_NODES)
+    return SPEC_ERR_UNSUPPORTED;
+  if (batch > 0 && (!anchor || !ng_len || !ng_score || !ng_adj || !tok || !parent || !cand_id || !n_rows ||
+                    (P > 0 && (!cand_tok || !cand_score)) || (Lg > 0 && !ng_tok)))
+    return SPEC_ERR_INVALID_ARG;
+  if (!ws_ok(ws)) return SPEC_ERR_WORKSPACE;
+  if (batch == 0) return SPEC_OK;
+  return from_cuda(spec_launch_build_tree(batch, P, Kc, anchor, cand_tok, cand_score, ng_tok, Lg, ng_len,
+                                          ng_score, ng_adj, width, tok, parent, cand_id, n_rows, status_of(ws),
+                                          stream));
 }
 
 spec_status spec_draft_and_price(

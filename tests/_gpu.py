@@ -158,3 +158,34 @@ def gpu_draft_price(S, ws, est, hist, hist_len, n_min, n_max, cap, d, c, d_len, 
     return dict(g=host(g), g_len=host(gl), match_n=host(n), agree=host(a), copy_len=host(m), chain=host(chain),
                 S=host(Sv), chain_len=host(chain_len), source=host(source), verify_len=host(verify_len),
                 row_off=host(row_off), point_mass=host(pm))
+
+
+def gpu_build_tree(S, ws, anchor, cand_tok, cand_score, ng_tok, ng_len, ng_score, ng_adj, width):
+    B = len(anchor)
+    i32 = dict(dtype=torch.int32, device=DEV)
+    tok, parent, cid = (torch.full((B, width), -7, **i32) for _ in range(3))
+    nr = torch.full((B,), -7, **i32)
+    S.spec_build_tree(dev(anchor, torch.int32), dev(cand_tok, torch.int32), dev(cand_score, torch.float32),
+                      dev(np.asarray(ng_tok).reshape(B, -1), torch.int32), dev(ng_len, torch.int32),
+                      dev(ng_score, torch.float32), dev(ng_adj, torch.float32), width, tok, parent, cid, nr, ws)
+    torch.cuda.synchronize()
+    return dict(tok=host(tok), parent=host(parent), cand_id=host(cid), n_rows=host(nr))
+
+
+def assert_tree_equal(g, o, rel=1e-12):
+    """The built trees equal the oracle's, except where the oracle's Q has a
+    near-tie (relative gap <= rel) at the selection cut: there the two
+    selections may differ among the tied candidates, and the GPU's must still
+    be a tree of the same size whose sum of Q is within rel of the oracle's."""
+    for r in range(len(o.n_rows)):
+        n = int(o.n_rows[r])
+        assert int(g["n_rows"][r]) == n, r
+        if np.array_equal(g["cand_id"][r], o.cand_id[r]):
+            assert np.array_equal(g["tok"][r], o.tok[r]) and np.array_equal(g["parent"][r], o.parent[r]), r
+            continue
+        Q = o.Q[r]
+        sel_o, sel_g = set(o.cand_id[r, 1:n]), set(g["cand_id"][r, 1:n])
+        diff = sel_o ^ sel_g
+        cut = min(Q[list(sel_o)]) if sel_o else 1.0
+        assert all(abs(Q[c] - cut) <= rel * cut for c in diff), (r, sorted(diff))
+        assert abs(sum(Q[list(sel_g)]) - sum(Q[list(sel_o)])) <= rel * max(1.0, sum(Q[list(sel_o)])), r

@@ -132,6 +132,15 @@ def test_host_validation_rejects_bad_arguments_without_a_gpu(spec):
     assert price(B=5000) == UNS
     assert price(L=40, K=7) == UNS
     assert price(tb=100) == INV  # a table too small for L
+    # tree builder: Kc 0, width 0, too many candidates, too wide
+    def tree(B=4, P=8, Kc=4, Lg=15, width=16):
+        return lib.spec_build_tree(B, P, Kc, P_, P_, P_, P_, Lg, P_, P_, P_, width, P_, P_, P_, P_, C.byref(w), None)
+    P_ = P
+    assert tree(Kc=0) == INV
+    assert tree(width=0) == INV
+    assert tree(P=40, Kc=8) == UNS  # 1 + 320 + 15 candidates
+    assert tree(width=257) == UNS
+    assert lib.spec_build_tree(4, 8, 4, None, P, P, P, 15, P, P, P, 16, P, P, P, P, C.byref(w), None) == INV
     # verification: vocab 0, bad dtype, batch beyond the workspace, NaN temperature
     def chain(B=4, V=1024, dtype=1, max_rows=64, T=0.0, K=0, draft=None):
         return lib.spec_verify_chain(B, V, dtype, P, P, max_rows, draft, K, P, 15, P, None, T, 0, 0, P, P, P,

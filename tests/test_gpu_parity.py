@@ -377,12 +377,16 @@ def test_chain_invalid_inputs_are_flagged_not_faulted(S):
 @pytest.mark.parametrize("width", [4, 8, 12, 16])
 def test_tree_parity_full_size(S, width):
     t = W.tree_bs32(width=width)
-    ws = _ws(S, 32, int(t["node_off"][-1]), 1, t["V"])
-    g = gpu_tree(S, ws, t["logits"], t["node_off"], t["tok"], t["parent"], t["max_nodes"])
-    o = O.verify_tree(t["logits"], t["node_off"], t["tok"], t["parent"], t["max_nodes"])
+    tb = O.build_tree(t["anchor"], t["cand_tok"], t["cand_score"], t["ng_tok"], t["ng_len"], t["ng_score"],
+                      t["ng_adj"], width)
+    node_off, tok, parent = W.flatten_trees(tb.tok, tb.parent, tb.n_rows)
+    logits, planted = W.tree_logits(node_off, tok, parent, t["V"])
+    ws = _ws(S, 32, int(node_off[-1]), 1, t["V"])
+    g = gpu_tree(S, ws, logits, node_off, tok, parent, t["max_nodes"])
+    o = O.verify_tree(logits, node_off, tok, parent, t["max_nodes"])
     assert np.array_equal(g["path"], o.path) and np.array_equal(g["accept_len"], o.accept_len)
     assert np.array_equal(g["out"], o.out_tokens)
-    for r, p in enumerate(t["planted_paths"]):
+    for r, p in enumerate(planted):
         assert g["path"][r, :len(p)].tolist() == p
     assert ws.status() == 0
 

@@ -98,27 +98,15 @@ def _anc(parent, j):
 @pytest.mark.parametrize("width", [4, 8, 12, 16])
 def test_planted_paths_of_the_tree_workload_are_recovered(orc, width):
     cfg = W.tree_bs32(width=width, B=8)
-    tv = orc.verify_tree(cfg["logits"], cfg["node_off"], cfg["tok"], cfg["parent"], cfg["max_nodes"])
+    tb = orc.build_tree(cfg["anchor"], cfg["cand_tok"], cfg["cand_score"], cfg["ng_tok"], cfg["ng_len"],
+                        cfg["ng_score"], cfg["ng_adj"], width)
+    node_off, tok, parent = W.flatten_trees(tb.tok, tb.parent, tb.n_rows)
+    logits, planted = W.tree_logits(node_off, tok, parent, cfg["V"])
+    tv = orc.verify_tree(logits, node_off, tok, parent, cfg["max_nodes"])
     assert tv.status == 0
-    for r, path in enumerate(cfg["planted_paths"]):
+    for r, path in enumerate(planted):
         assert tv.path[r, :len(path)].tolist() == path
         assert tv.accept_len[r] == len(path) - 1
-
-
-def test_best_first_order_prefixes_are_trees(orc):
-    # Prop. 1: ordering by decreasing Q (ties to the lower index) makes every prefix a tree
-    rng = np.random.default_rng(23)
-    for trial in range(20):
-        tok, parent, info = W._build_tree(rng, 1000, 8, 4, rng.integers(0, 1000, 15), 16)
-        order, par = info["order"], info["par"]
-        seen = {0}
-        for j in order:
-            assert par[j] in seen
-            seen.add(j)
-        Q = info["Q"]
-        assert all(Q[a] >= Q[b] for a, b in zip(order, order[1:]))
-        # layout: depth-first, parents precede children, anchor first
-        assert parent[0] == -1 and all(0 <= parent[j] < j for j in range(1, len(parent)))
 
 
 def test_invalid_trees_are_flagged(orc):

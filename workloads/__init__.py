@@ -378,132 +378,96 @@ def compact_logits(cfg, row_off, verify_len, rng_seed=78):
 # --------------------------------------------------------------------------
 # trees (AdaSpark sec. 2.2 shape, Fig. 1; order by Q = prod q, Prop. 1)
 # --------------------------------------------------------------------------
-def _build_tree(rng, V, P, Kc, ngram_chain, width):
-    """Candidates of one block (P positions, Kc ranked candidates each) plus an n-gram
-    chain from the anchor; q from the prior of AdaSpark Eq. (6) (pick ln 2 + logit h,
-    sibling log r, n-gram 0); best-first by Q with ties to the lower index; the first
-    width-1 candidates, laid out depth-first.  Returns (tok, parent) of `width` nodes."""
-    toks = [int(zipf_tokens(rng, 1, V)[0])]  # anchor
-    par = [-1]
-    score = [0.0]
-    kind = ["anchor"]
-    prev_pick = 0
-    picks = []
-    for i in range(P):
-        h = float(np.clip(rng.beta(2.0, 2.0), 1e-4, 1 - 1e-4))
-        group = set()
-        pick_tok = int(zipf_tokens(rng, 1, V)[0])
-        group.add(pick_tok)
-        toks.append(pick_tok)
-        par.append(prev_pick)
-        score.append(np.log(2.0) + np.log(h / (1 - h)))
-        kind.append("pick")
-        pick_idx = len(toks) - 1
-        shares = rng.dirichlet(np.ones(Kc - 1))
-        for s in shares:
-            t = int(zipf_tokens(rng, 1, V)[0])
-            while t in group:
-                t = (t + 1) % V
-            group.add(t)
-            toks.append(t)
-            par.append(prev_pick)
-            score.append(float(np.log(max(s, 1e-6))))
-            kind.append("sibling")
-        picks.append(pick_idx)
-        prev_pick = pick_idx
-    # n-gram chain from the anchor: agree with an existing child, else add a node
-    cur = 0
-    for t in ngram_chain:
-        kids = [j for j in range(len(toks)) if par[j] == cur]
-        hit = [j for j in kids if toks[j] == int(t)]
-        if hit:
-            cur = hit[0]
-            continue
-        toks.append(int(t))
-        par.append(cur)
-        score.append(0.0)
-        kind.append("ngram")
-        cur = len(toks) - 1
-    n = len(toks)
-    # q per parent: softmax over its children and an explicit "none"
-    q = np.zeros(n)
-    for p_ in range(n):
-        kids = [j for j in range(n) if par[j] == p_]
-        if not kids:
-            continue
-        den = 1.0 + sum(np.exp(score[j]) for j in kids)
-        for j in kids:
-            q[j] = np.exp(score[j]) / den
-    Q = np.ones(n)
-    for j in range(1, n):
-        Q[j] = Q[par[j]] * q[j]
-    order = sorted(range(1, n), key=lambda j: (-Q[j], j))
-    chosen = set([0] + order[:width - 1])
-    # depth-first layout: children in increasing candidate index
-    local = {}
-    layout = []
-
-    def dfs(j):
-        local[j] = len(layout)
-        layout.append(j)
-        for ch in range(j + 1, n):
-            if par[ch] == j and ch in chosen:
-                dfs(ch)
-
-    dfs(0)
-    tok = np.array([toks[j] for j in layout], np.int32)
-    parent = np.array([-1 if par[j] < 0 else local[par[j]] for j in layout], np.int32)
-    return tok, parent, {"Q": Q, "order": order, "par": par, "kind": kind}
-
-
-def tree_bs32(seed=1003, width=16, B=32):
-    """Greedy tree verification: batch 32, block of 8 picks with top-4 ranked candidates
-    (pick + 3 siblings, confidences Beta(2,2)), an n-gram chain from the anchor taken
-    from a planted earlier occurrence in a 4096-token history, trees of `width` rows by
-    best-first order; bf16 V=151936 logits N(0,1) with a planted true path (accept
-    length geometric with mean 3, capped by the tree), margin +8 on the path child and
-    a last-node argmax that matches none of its children."""
-    rng = np.random.default_rng(seed + 17 * width)
-    V, P, Kc = 151936, 8, 4
-    toks, pars, offs, planted = [], [], [0], []
-    hists = []
+def tree_blocks(seed=1003, B=32, P=8, Kc=4, V=151936):
+    """Inputs of the candidate-tree builder for B requests: a block of P positions
+    with Kc ranked candidates each (distinct tokens per position), scored with the
+    shape of the acceptance model's prior on the tree-verification page (pick:
+    ln 2 + logit h with the confidence head h ~ Beta(2, 2); sibling: log r with r
+    its share of the siblings' total, r ~ Dirichlet(1)); a 4096-token Zipf history
+    whose last 6 tokens repeat an earlier passage, and the 15 tokens that followed
+    that passage as the n-gram chain from the anchor (scored 0: a source
+    precision of 1/2, so no agreement adjustment)."""
+    rng = np.random.default_rng(seed)
+    anchor = np.empty(B, np.int32)
+    cand_tok = np.empty((B, P, Kc), np.int32)
+    cand_score = np.empty((B, P, Kc), np.float32)
+    hist = np.empty((B, 4096), np.int32)
+    ng_tok = np.empty((B, 15), np.int32)
     for r in range(B):
-        hist = zipf_tokens(rng, 4096, V)
+        h = zipf_tokens(rng, 4096, V)
         at = int(rng.integers(0, 2048))
-        hist[4096 - 6:] = hist[at:at + 6]  # suffix of 6 repeats an earlier passage
-        chain = hist[at + 6:at + 6 + 15].copy()
-        hists.append(hist)
-        tok, parent, _ = _build_tree(rng, V, P, Kc, chain, width)
-        toks.append(tok)
-        pars.append(parent)
-        offs.append(offs[-1] + len(tok))
-    N = offs[-1]
+        h[4096 - 6:] = h[at:at + 6]
+        hist[r] = h
+        ng_tok[r] = h[at + 6:at + 6 + 15]
+        anchor[r] = h[-1]
+        for i in range(P):
+            toks = []
+            while len(toks) < Kc:
+                t = int(zipf_tokens(rng, 1, V)[0])
+                if t not in toks:
+                    toks.append(t)
+            cand_tok[r, i] = toks
+            hc = float(np.clip(rng.beta(2.0, 2.0), 1e-4, 1 - 1e-4))
+            cand_score[r, i, 0] = np.log(2.0) + np.log(hc / (1 - hc))
+            if Kc > 1:
+                cand_score[r, i, 1:] = np.log(np.maximum(rng.dirichlet(np.ones(Kc - 1)), 1e-6))
+    # a few requests follow the block with the chain, so that it agrees with picks
+    for r in range(0, B, 4):
+        ng_tok[r, :min(P, 15)] = cand_tok[r, :min(P, 15), 0]
+    return {"B": B, "P": P, "Kc": Kc, "V": V, "anchor": anchor, "cand_tok": cand_tok, "cand_score": cand_score,
+            "ng_tok": ng_tok, "ng_len": np.full(B, 15, np.int32), "ng_score": np.zeros(B, np.float32),
+            "ng_adj": np.zeros(B, np.float32), "hist": hist}
+
+
+def flatten_trees(tok, parent, n_rows):
+    """[B x width] tree rows (valid up to n_rows[r]) -> node_off [B + 1] and the
+    rows of all requests back to back."""
+    n_rows = np.asarray(n_rows, np.int64)
+    node_off = np.concatenate([[0], np.cumsum(n_rows)]).astype(np.int32)
+    t = np.concatenate([np.asarray(tok)[r, :n_rows[r]] for r in range(len(n_rows))]).astype(np.int32)
+    p = np.concatenate([np.asarray(parent)[r, :n_rows[r]] for r in range(len(n_rows))]).astype(np.int32)
+    return node_off, t, p
+
+
+def tree_logits(node_off, tok, parent, V, seed=1005, dtype="bf16", margin=8.0):
+    """bf16 (or fp32) logits N(0, 1) for the rows of given trees, with a planted
+    true path per request: from the anchor, a geometric number of steps (mean 3)
+    each to a uniformly chosen child, the target's argmax at a row being the
+    token of the next path node (margin +margin); at the path's last node the
+    argmax is a token that matches none of its children.  Returns (logits,
+    planted paths as row indices)."""
+    rng = np.random.default_rng(seed)
+    N = int(node_off[-1])
     row_truth = np.full(N, -1, np.int32)
-    for r in range(B):
-        tok, parent, base = toks[r], pars[r], offs[r]
-        n = len(tok)
-        A = int(rng.geometric(0.25)) - 1  # mean 3
+    planted = []
+    for r in range(len(node_off) - 1):
+        base, n = int(node_off[r]), int(node_off[r + 1] - node_off[r])
+        A = int(rng.geometric(0.25)) - 1
         cur, depth, path = 0, 0, [0]
         while depth < A:
-            kids = [j for j in range(n) if parent[j] == cur]
+            kids = [j for j in range(n) if parent[base + j] == cur]
             if not kids:
                 break
             nxt = kids[int(rng.integers(0, len(kids)))]
-            row_truth[base + cur] = tok[nxt]
+            row_truth[base + cur] = tok[base + nxt]
             cur = nxt
             path.append(cur)
             depth += 1
-        kid_toks = {int(tok[j]) for j in range(n) if parent[j] == cur}
+        kid_toks = {int(tok[base + j]) for j in range(n) if parent[base + j] == cur}
         t = int(rng.integers(0, V))
         while t in kid_toks:
             t = (t + 1) % V
         row_truth[base + cur] = t
         planted.append(path)
-    logits = target_logits(rng, row_truth, V, "bf16", 8.0)
-    return {
-        "name": f"tree_bs32_w{width}", "B": B, "V": V, "width": width,
-        "node_off": np.array(offs, np.int32), "tok": np.concatenate(toks).astype(np.int32),
-        "parent": np.concatenate(pars).astype(np.int32), "logits": logits,
-        "planted_paths": planted, "max_nodes": width, "dtype": "bf16",
-        "hist": np.stack(hists).astype(np.int32),
-    }
+    return target_logits(rng, row_truth, V, dtype, margin), planted
+
+
+def tree_bs32(seed=1003, width=16, B=32):
+    """Greedy tree verification, batch 32: the builder inputs of tree_blocks (8
+    picks with top-4 ranked candidates, confidences Beta(2,2), an n-gram chain
+    from a planted repeat in a 4096-token history) and the tree width (4, 8, 12
+    or 16 rows).  The tree itself comes from the builder; tree_logits plants a
+    true path on it."""
+    cfg = tree_blocks(seed=seed + 17 * width, B=B)
+    cfg.update({"name": f"tree_bs32_w{width}", "width": width, "max_nodes": width, "dtype": "bf16"})
+    return cfg
