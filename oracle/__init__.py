@@ -137,6 +137,9 @@ def _declare(L):
     L.oracle_build_tree.argtypes = [C.c_int32, C.c_int32, C.c_int32, _i32p, _i32p, _f32p, _i32p, C.c_int32,
                                     _i32p, _f32p, _f32p, C.c_int32, _i32p, _i32p, _i32p, _i32p, _f64p]
     L.oracle_build_tree.restype = C.c_int
+    L.oracle_size_budget.argtypes = [C.c_int32, C.c_int32, _f32p, _i32p, C.c_int32, C.c_double, C.c_double,
+                                     _i32p, _f64p, _f64p]
+    L.oracle_size_budget.restype = C.c_int
 
 
 def _p(a, ct):
@@ -374,3 +377,24 @@ def build_tree(anchor, cand_tok, cand_score, ng_tok, ng_len, ng_score, ng_adj, w
                                  _p(parent, C.c_int32), _p(cid, C.c_int32), _p(nr, C.c_int32),
                                  _p(Q, C.c_double))
     return TreeBuild(tok, parent, cid, nr, Q, _check(st))
+
+
+# --------------------------------------------------------------------------- budget sizing
+@dataclass
+class BudgetOut:
+    b_star: int
+    lam: float
+    G: np.ndarray  # G(b) for b = 0..#slots
+
+
+def size_budget(S, chain_len, max_verify_len, C0, p) -> BudgetOut:
+    S = _c(S, np.float32)
+    B, L = S.shape
+    chain_len = _c(chain_len, np.int32)
+    b = np.zeros(1, np.int32)
+    lam = np.zeros(1)
+    G = np.empty(B * L + 1)
+    _check(lib().oracle_size_budget(B, L, _p(S, C.c_float), _p(chain_len, C.c_int32), int(max_verify_len),
+                                    float(C0), float(p), _p(b, C.c_int32), _p(lam, C.c_double), _p(G, C.c_double)))
+    n = int(np.minimum(np.minimum(chain_len, max_verify_len), L).clip(0).sum())
+    return BudgetOut(int(b[0]), float(lam[0]), G[:n + 1])

@@ -876,3 +876,50 @@ int oracle_build_tree(int32_t batch, int32_t P, int32_t Kc, const int32_t* ancho
   free(Q);
   return status;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Budget sizing ([HS] sec. 2 adaptive verification, sec. 4.3 Eq. (2), sec. */
+/* 4.4, App. F cost model, App. O stale sizing).  Over the slots that may   */
+/* be verified (k < min(chain_len[r], max_verify_len)), with survivals     */
+/* s_(1) >= s_(2) >= ... :                                                  */
+/*   A(b) = batch + sum_{i <= b} s_(i)     (expected emitted tokens)        */
+/*   C(b) = C0 + p b                       (App. F, the linear step cost)   */
+/*   G(b) = A(b) / C(b);  b* = the smallest b in [0, #slots] maximising G;  */
+/*   lambda = G(b*) p, the slot price of Eq. (2).                           */
+/* The sums run in the sorted order, in double.  Reading: the eager-step    */
+/* branch of App. F Eq. (4) is not modelled (one linear cost for every b).  */
+/* ------------------------------------------------------------------------ */
+static int cmp_desc_float(const void* a, const void* b) {
+  const float x = *(const float*)a, y = *(const float*)b;
+  return (x < y) - (x > y);
+}
+
+int oracle_size_budget(int32_t batch, int32_t L, const float* S, const int32_t* chain_len,
+                       int32_t max_verify_len, double C0, double p, int32_t* b_star,
+                       double* lambda, double* G_out) {
+  if (batch < 0 || L < 1 || max_verify_len < 0 || !(C0 > 0.0) || !(p > 0.0)) return ORACLE_ERR_ARG;
+  float* s = (float*)malloc(sizeof(float) * ((size_t)batch * L + 1));
+  int32_t n = 0;
+  for (int32_t r = 0; r < batch; ++r) {
+    int32_t len = chain_len[r] < max_verify_len ? chain_len[r] : max_verify_len;
+    if (len > L) len = L;
+    for (int32_t k = 0; k < len; ++k) s[n++] = S[(int64_t)r * L + k];
+  }
+  qsort(s, (size_t)n, sizeof(float), cmp_desc_float);
+  double A = (double)batch, best = A / C0;
+  int32_t bs = 0;
+  if (G_out) G_out[0] = best;
+  for (int32_t b = 1; b <= n; ++b) {
+    A += (double)s[b - 1];
+    const double G = A / (C0 + p * (double)b);
+    if (G_out) G_out[b] = G;
+    if (G > best) {
+      best = G;
+      bs = b;
+    }
+  }
+  *b_star = bs;
+  *lambda = best * p;
+  free(s);
+  return 0;
+}

@@ -154,6 +154,14 @@ int oracle_build_tree(int32_t batch, int32_t P, int32_t Kc, const int32_t* ancho
                       int32_t* tok, int32_t* parent, int32_t* cand_id, int32_t* n_rows,
                       double* dbg_Q);
 
+/* Budget sizing ([HS] sec. 2, sec. 4.3 Eq. (2), sec. 4.4, App. F): over the
+ * slots k < min(chain_len[r], max_verify_len) with survivals S [batch x L],
+ * b* = the smallest maximiser of G(b) = (batch + sum of the b largest S) /
+ * (C0 + p b), lambda = G(b*) p.  G_out (may be NULL) gets G(0..#slots). */
+int oracle_size_budget(int32_t batch, int32_t L, const float* S, const int32_t* chain_len,
+                       int32_t max_verify_len, double C0, double p, int32_t* b_star,
+                       double* lambda, double* G_out);
+
 /* argmax of one row (lowest index on ties); NaN entries are skipped */
 int32_t oracle_row_argmax(const void* row, int32_t vocab, int32_t dtype);
 

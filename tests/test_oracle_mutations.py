@@ -12,6 +12,7 @@ import oracle as ORC
 from . import test_oracle_ngram as TN
 from . import test_oracle_philox as TP
 from . import test_oracle_price as TPR
+from . import test_oracle_budget as TBU
 from . import test_oracle_tree as TT
 from . import test_oracle_tree_build as TB
 from . import test_oracle_verify as TV
@@ -97,6 +98,16 @@ MUTATIONS = [
     ("tree builder multiplies Q by the parent's q", "for (int32_t j = 1; j < N; ++j) Q[j] = Q[cpar[j]] * q[j];",
      "for (int32_t j = 1; j < N; ++j) Q[j] = Q[cpar[j]] * q[cpar[j] > 0 ? cpar[j] : j];",
      [TB.test_chain_only_tree_is_a_path_of_sigmoids, TB.test_ngram_chain_agrees_with_picks_then_extends]),
+    # budget sizing (Hybrid Spark sec. 2, sec. 4.3 Eq. (2), App. F)
+    ("budget forgets the one token every request emits", "double A = (double)batch, best = A / C0;",
+     "double A = 0.0, best = A / C0;", [lambda o: TBU.test_budget_against_exact_rationals(o, 3)]),
+    ("budget ties to the larger b", "    if (G > best) {\n      best = G;\n      bs = b;",
+     "    if (G >= best) {\n      best = G;\n      bs = b;", [lambda o: TBU.test_equal_survivals_closed_form(o, 0.5, 8.0, 1.0)]),
+    ("budget counts slots past max_verify_len",
+     "int32_t len = chain_len[r] < max_verify_len ? chain_len[r] : max_verify_len;",
+     "int32_t len = chain_len[r];", [TBU.test_only_verifiable_slots_count]),
+    ("budget takes the smallest survivals first", "return (x < y) - (x > y);", "return (x > y) - (x < y);",
+     [lambda o: TBU.test_slot_price_rule_of_eq_2(o, 0)]),
 ]
 
 
