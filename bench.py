@@ -527,6 +527,24 @@ def run_gpu(args):
     torch.cuda.synchronize()
     e2e_ms = reduce_over_ranks(e0.elapsed_time(e1) / e_steps, 0, 0, world, "cuda")[0]
 
+    # budget sizing for a later step (spec_size_budget), from this batch's survivals;
+    # the pipeline runs it on a side stream, here it is timed alone
+    bsz = S.Workspace(1, 1, 1, 1)
+    b_out = torch.zeros(1, dtype=torch.int32, device="cuda")
+    l_out = torch.zeros(1, dtype=torch.float32, device="cuda")
+    for _ in range(args.warmup):
+        S.spec_size_budget(rounds[0].S, rounds[0].chain_len, cfg["max_verify_len"], 256.0, 1.0, b_out, l_out, bsz)
+    torch.cuda.synchronize()
+    sz_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(200)]
+    for a, b in sz_ev:
+        a.record(stream)
+        S.spec_size_budget(rounds[0].S, rounds[0].chain_len, cfg["max_verify_len"], 256.0, 1.0, b_out, l_out, bsz)
+        b.record(stream)
+    torch.cuda.synchronize()
+    sizing = {"us": round(statistics.mean(a.elapsed_time(b) for a, b in sz_ev) * 1e3, 3),
+              "slots": int(np.minimum(rounds[0].chain_len.cpu().numpy(), cfg["max_verify_len"]).sum()),
+              "C0": 256.0, "p": 1.0, "b_star": int(b_out.item()), "lambda": float(l_out.item())}
+
     hbm, peak_kind = peaks()
     bs4 = measure_bs4(S, torch, W, min(args.steps, 5000), args.warmup, hbm)
     long_sampled = measure_long_sampled(S, torch, W, min(args.steps, 1000), args.warmup, hbm)
@@ -559,6 +577,7 @@ def run_gpu(args):
         "bs4": bs4,
         "long_bs64_sampled": long_sampled,
         "tree_bs32": tree,
+        "budget_sizing": sizing,
         "status_clean": ok,
     }
     print(json.dumps(line), flush=True)

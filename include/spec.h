@@ -293,6 +293,31 @@ spec_status spec_build_tree(int32_t batch, int32_t P, int32_t Kc, const int32_t*
                             const spec_workspace* ws, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------
+ * spec_size_budget: the next verification budget and slot price from one
+ * step's survivals ([HS] sec. 2 adaptive verification, sec. 4.3 Eq. (2),
+ * sec. 4.4, App. F cost model, App. O stale sizing).
+ *
+ * Over the slots (r, k) with k < min(chain_len[r], max_verify_len), whose
+ * survivals S [batch x L] are the output of spec_price_and_allocate, sorted
+ * descending s_(1) >= s_(2) >= ...:
+ *   G(b) = (batch + sum_{i <= b} s_(i)) / (C0 + p b)   (fp64),
+ *   *out_budget = b*, the smallest maximiser of G over b in [0, #slots],
+ *   *out_lambda = G(b*) p, rounded to fp32.
+ * C0 (base step cost) and p (cost of one verification slot) are host
+ * scalars from the caller's cost model (App. F); only their ratio matters.
+ * The host reads the two device scalars back asynchronously and passes them
+ * as `budget` and `lambda` to the pricing step two steps later ([HS] sec.
+ * 4.4: the GPU allocates from fresh survivals, the host sizes from stale
+ * ones).  The sums associate by segments of the sorted list, so G may differ
+ * from a left-to-right sum in its last bits.  The workspace serves only its
+ * status word (the call may overlap other calls on it).
+ * Limits: 1 <= L <= SPEC_MAX_L, batch <= SPEC_MAX_PRICE_BATCH; C0, p > 0.
+ * ------------------------------------------------------------------------ */
+spec_status spec_size_budget(int32_t batch, int32_t L, const float* S, const int32_t* chain_len,
+                             int32_t max_verify_len, double C0, double p, int32_t* out_budget,
+                             float* out_lambda, const spec_workspace* ws, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
  * spec_price_and_allocate_static: step 2 without a workspace.  The method has
  * no counterpart of this call; it is an interface variant of
  * spec_price_and_allocate for callers that cannot hand the library device

@@ -24,7 +24,7 @@ from ._build import build
 
 __all__ = [
     "build", "load", "Workspace", "EstimatorTable", "SpecError", "spec_ngram_propose",
-    "spec_price_and_allocate", "spec_price_and_allocate_static", "spec_draft_and_price", "spec_verify_chain", "spec_verify_tree", "spec_build_tree", "POLICY", "DEV_BITS",
+    "spec_price_and_allocate", "spec_price_and_allocate_static", "spec_draft_and_price", "spec_verify_chain", "spec_verify_tree", "spec_build_tree", "spec_size_budget", "POLICY", "DEV_BITS",
 ]
 
 SPEC_OK, SPEC_ERR_INVALID_ARG, SPEC_ERR_CUDA, SPEC_ERR_UNSUPPORTED, SPEC_ERR_WORKSPACE = 0, 1, 2, 3, 4
@@ -90,6 +90,7 @@ SIGNATURES = {
                            _u64, _u64, _vp, _vp, _vp, _vp, _vp, _vp, _WSP, _vp], _i32),
     "spec_build_tree": ([_i32, _i32, _i32, _vp, _vp, _vp, _vp, _i32, _vp, _vp, _vp, _i32, _vp, _vp, _vp, _vp,
                          _WSP, _vp], _i32),
+    "spec_size_budget": ([_i32, _i32, _vp, _vp, _i32, C.c_double, C.c_double, _vp, _vp, _WSP, _vp], _i32),
     "spec_verify_tree": ([_i32, _i32, _i32, _vp, _vp, _i32, _vp, _vp, _i32, _vp, _vp, _vp, _WSP, _vp],
                          _i32),
 }
@@ -290,3 +291,12 @@ def spec_build_tree(anchor, cand_tok, cand_score, ng_tok, ng_len, ng_score, ng_a
     _check("spec_build_tree", load().spec_build_tree(
         B, P, Kc, _ptr(anchor), _ptr(cand_tok), _ptr(cand_score), _ptr(ng_tok), Lg, _ptr(ng_len), _ptr(ng_score),
         _ptr(ng_adj), int(width), _ptr(tok), _ptr(parent), _ptr(cand_id), _ptr(n_rows), ws.ref, _stream(stream)))
+
+
+def spec_size_budget(S, chain_len, max_verify_len, C0, p, out_budget, out_lambda, ws: Workspace, stream=None):
+    """b* and lambda for a later step from survivals S [B x L] (device); out_budget:
+    int32 device tensor of one element, out_lambda: float32 device tensor of one."""
+    B, L = S.shape
+    _check("spec_size_budget", load().spec_size_budget(
+        B, L, _ptr(S), _ptr(chain_len), int(max_verify_len), float(C0), float(p), _ptr(out_budget),
+        _ptr(out_lambda), ws.ref, _stream(stream)))

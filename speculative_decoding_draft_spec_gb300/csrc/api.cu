@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 #include <string.h>
+#include <math.h>
 
 #include "common.cuh"
 
@@ -38,6 +39,9 @@ cudaError_t spec_launch_build_tree(int32_t batch, int32_t P, int32_t Kc, const i
                                    int32_t Lg, const int32_t* ng_len, const float* ng_score, const float* ng_adj,
                                    int32_t width, int32_t* tok, int32_t* parent, int32_t* cand_id,
                                    int32_t* n_rows, uint32_t* status, cudaStream_t stream);
+cudaError_t spec_launch_size_budget(int32_t batch, int32_t L, const float* S, const int32_t* chain_len,
+                                    int32_t mvl, double C0, double p, int32_t* out_budget, float* out_lambda,
+                                    cudaStream_t stream);
 cudaError_t spec_launch_draft_price(
     const int32_t* hist, int64_t stride, const int32_t* hist_len, int32_t batch, int32_t n_min, int32_t n_max,
     int32_t cap, int32_t* g, int32_t* g_len, int32_t* match_n, int32_t* agree, int32_t* copy_len, int32_t K,
@@ -269,6 +273,19 @@ spec_status spec_build_tree(int32_t batch, int32_t P, int32_t Kc, const int32_t*
   return from_cuda(spec_launch_build_tree(batch, P, Kc, anchor, cand_tok, cand_score, ng_tok, Lg, ng_len,
                                           ng_score, ng_adj, width, tok, parent, cand_id, n_rows, status_of(ws),
                                           stream));
+}
+
+spec_status spec_size_budget(int32_t batch, int32_t L, const float* S, const int32_t* chain_len,
+                             int32_t max_verify_len, double C0, double p, int32_t* out_budget,
+                             float* out_lambda, const spec_workspace* ws, cudaStream_t stream) {
+  if (batch < 0 || L < 1 || max_verify_len < 0 || !(C0 > 0.0) || !(p > 0.0) || !(C0 < INFINITY) ||
+      !(p < INFINITY))
+    return SPEC_ERR_INVALID_ARG;
+  if (L > SPEC_MAX_L || batch > SPEC_MAX_PRICE_BATCH) return SPEC_ERR_UNSUPPORTED;
+  if (!out_budget || !out_lambda || (batch > 0 && (!S || !chain_len))) return SPEC_ERR_INVALID_ARG;
+  if (!ws_ok(ws)) return SPEC_ERR_WORKSPACE;
+  return from_cuda(spec_launch_size_budget(batch, L, S, chain_len, max_verify_len, C0, p, out_budget, out_lambda,
+                                           stream));
 }
 
 spec_status spec_draft_and_price(

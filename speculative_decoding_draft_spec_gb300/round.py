@@ -12,7 +12,7 @@ from __future__ import annotations
 import torch
 
 from . import (EstimatorTable, Workspace, spec_draft_and_price, spec_ngram_propose,
-               spec_price_and_allocate, spec_verify_chain)
+               spec_price_and_allocate, spec_size_budget, spec_verify_chain)
 
 
 class ChainRound:
@@ -88,3 +88,55 @@ class ChainRound:
             self.run(**kw)
         self.graph = g
         return g
+
+
+class BudgetSizer:
+    """Stale budget sizing (Hybrid Spark sec. 4.4, App. O): after the allocation
+    of step t, spec_size_budget computes b* and lambda from step t's survivals
+    on a side stream and copies them to pinned host memory; step t + 2 passes
+    them to the pricing step as host scalars.  Steps 0 and 1 use the given
+    initial values.  The next step's lookup waits for the sizing kernel (it
+    overwrites the survivals the sizing reads), never for the host copy."""
+
+    def __init__(self, C0, p, budget0, lam0, max_verify_len, device="cuda"):
+        self.C0, self.p, self.mvl = float(C0), float(p), int(max_verify_len)
+        self.dev_b = torch.zeros(2, dtype=torch.int32, device=device)
+        self.dev_l = torch.zeros(2, dtype=torch.float32, device=device)
+        self.host_b = torch.zeros(2, dtype=torch.int32).pin_memory()
+        self.host_l = torch.zeros(2, dtype=torch.float32).pin_memory()
+        self.copied = [None, None]
+        self.sized = None
+        self.init = (int(budget0), float(lam0))
+        self.side = torch.cuda.Stream(device=device)
+        self.ws = Workspace(1, 1, 1, 1, device=device)
+
+    def params(self, step):
+        """(budget, lambda) for `step`: sized from step - 2's survivals."""
+        slot = step % 2
+        ev = self.copied[slot]
+        if step < 2 or ev is None:
+            return self.init
+        ev.synchronize()  # recorded two steps ago: normally long complete
+        return int(self.host_b[slot]), float(self.host_l[slot])
+
+    def size(self, rnd, step, stream=None):
+        """Enqueue the sizing of `step`'s survivals (after its allocation on `stream`)."""
+        stream = stream or torch.cuda.current_stream()
+        slot = step % 2
+        self.side.wait_stream(stream)
+        with torch.cuda.stream(self.side):
+            spec_size_budget(rnd.S, rnd.chain_len, self.mvl, self.C0, self.p, self.dev_b[slot:slot + 1],
+                             self.dev_l[slot:slot + 1], self.ws, self.side)
+            self.sized = torch.cuda.Event()
+            self.sized.record(self.side)
+            self.host_b[slot].copy_(self.dev_b[slot], non_blocking=True)
+            self.host_l[slot].copy_(self.dev_l[slot], non_blocking=True)
+            ev = torch.cuda.Event()
+            ev.record(self.side)
+            self.copied[slot] = ev
+
+    def before_next_step(self, stream=None):
+        """Order the next step's lookup after the sizing kernel that reads this
+        step's survivals (a device-side wait)."""
+        if self.sized is not None:
+            (stream or torch.cuda.current_stream()).wait_event(self.sized)
