@@ -140,6 +140,9 @@ def _declare(L):
     L.oracle_size_budget.argtypes = [C.c_int32, C.c_int32, _f32p, _i32p, C.c_int32, C.c_double, C.c_double,
                                      _i32p, _f64p, _f64p]
     L.oracle_size_budget.restype = C.c_int
+    L.oracle_sample_drafts.argtypes = [C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_void_p, C.c_double,
+                                       C.c_uint64, C.c_uint64, _f64p, _i32p, _f64p, _f64p]
+    L.oracle_sample_drafts.restype = C.c_int
 
 
 def _p(a, ct):
@@ -398,3 +401,26 @@ def size_budget(S, chain_len, max_verify_len, C0, p) -> BudgetOut:
                                     float(C0), float(p), _p(b, C.c_int32), _p(lam, C.c_double), _p(G, C.c_double)))
     n = int(np.minimum(np.minimum(chain_len, max_verify_len), L).clip(0).sum())
     return BudgetOut(int(b[0]), float(lam[0]), G[:n + 1])
+
+
+# --------------------------------------------------------------------------- probabilistic drafting
+@dataclass
+class DraftOut:
+    y: np.ndarray   # [B x K]
+    u: np.ndarray   # [B x K] the uniforms
+    q: np.ndarray   # [B x K] q of the drawn token (-1 for a flagged row)
+    status: int
+
+
+def sample_drafts(draft_logits, temperature, seed=0, step=0, u_override=None) -> DraftOut:
+    """draft_logits [B x K x V] fp32, or bf16 bits (uint16)."""
+    lg, dt = _logits(draft_logits)
+    B, K, V = lg.shape
+    y = np.empty((B, K), np.int32)
+    u = np.empty((B, K))
+    q = np.empty((B, K))
+    uo = None if u_override is None else _c(u_override, np.float64)
+    st = lib().oracle_sample_drafts(B, K, V, dt, lg.ctypes.data, float(temperature), int(seed), int(step),
+                                    None if uo is None else _p(uo, C.c_double), _p(y, C.c_int32),
+                                    _p(u, C.c_double), _p(q, C.c_double))
+    return DraftOut(y, u, q, _check(st))

@@ -923,3 +923,51 @@ int oracle_size_budget(int32_t batch, int32_t L, const float* S, const int32_t* 
   free(s);
   return 0;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Probabilistic drafting ([HS] sec. 4.5, App. H): the drafter's token at   */
+/* position k (1-based) is drawn from q_k = softmax(z_k / T) over its       */
+/* logit row, by inverse CDF in vocabulary order at the uniform u = word 0  */
+/* of Philox4x32-10 with counter (r, 0x40000000 + k, lo32(step),            */
+/* hi32(step)) and key (lo32(seed), hi32(seed)) -- a counter domain apart   */
+/* from verification's (r, i <= 32, ...).  Reading: the positions are drawn */
+/* independently from the given rows; a drafter whose logits depend on the  */
+/* previous token (DSpark's Markov head) produces its rows inside its own   */
+/* network.  A row holding NaN or +Inf is flagged and drafts its argmax.    */
+/* ------------------------------------------------------------------------ */
+int oracle_sample_drafts(int32_t batch, int32_t K, int32_t vocab, int32_t dtype,
+                         const void* draft_logits, double temperature, uint64_t seed,
+                         uint64_t step, const double* u_override, int32_t* y, double* dbg_u,
+                         double* dbg_q) {
+  if (batch < 0 || K < 1 || vocab < 1 || (dtype != 0 && dtype != 1) || !(temperature > 0.0))
+    return ORACLE_ERR_ARG;
+  int status = 0;
+  double* q = (double*)malloc(sizeof(double) * (size_t)vocab);
+  for (int32_t r = 0; r < batch; ++r)
+    for (int32_t k = 1; k <= K; ++k) {
+      const int64_t row = (int64_t)r * K + (k - 1);
+      double u;
+      if (u_override) {
+        u = u_override[row];
+      } else {
+        uint32_t ctr[4] = {(uint32_t)r, 0x40000000u + (uint32_t)k, (uint32_t)step, (uint32_t)(step >> 32)};
+        uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
+        uint32_t out[4];
+        oracle_philox4x32_10(ctr, key, out);
+        u = oracle_u01(out[0]);
+      }
+      if (dbg_u) dbg_u[row] = u;
+      if (row_nonfinite(draft_logits, row, vocab, dtype)) {
+        status |= ORACLE_ST_NONFINITE;
+        y[row] = row_argmax(draft_logits, row, vocab, dtype);
+        if (dbg_q) dbg_q[row] = -1.0;
+        continue;
+      }
+      row_softmax(draft_logits, row, vocab, dtype, temperature, q);
+      const int32_t x = inverse_cdf(q, vocab, u);
+      y[row] = x;
+      if (dbg_q) dbg_q[row] = q[x];
+    }
+  free(q);
+  return status;
+}

@@ -162,6 +162,16 @@ int oracle_size_budget(int32_t batch, int32_t L, const float* S, const int32_t* 
                        int32_t max_verify_len, double C0, double p, int32_t* b_star,
                        double* lambda, double* G_out);
 
+/* Probabilistic drafting ([HS] sec. 4.5, App. H): y [batch x K], y[r,k-1] =
+ * inverse CDF of softmax(z / T) over draft_logits row r K + k - 1 at the
+ * uniform of Philox counter (r, 0x40000000 + k, lo32(step), hi32(step)).
+ * u_override [batch x K] replaces the uniforms; dbg_u / dbg_q (may be NULL)
+ * get the uniform and q of the drawn token. */
+int oracle_sample_drafts(int32_t batch, int32_t K, int32_t vocab, int32_t dtype,
+                         const void* draft_logits, double temperature, uint64_t seed,
+                         uint64_t step, const double* u_override, int32_t* y, double* dbg_u,
+                         double* dbg_q);
+
 /* argmax of one row (lowest index on ties); NaN entries are skipped */
 int32_t oracle_row_argmax(const void* row, int32_t vocab, int32_t dtype);
 

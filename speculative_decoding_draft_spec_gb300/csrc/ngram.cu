@@ -349,15 +349,23 @@ template <bool PRICE>
 cudaError_t launch_ngram_kernel(const spec::NgramParams& p, int64_t C, size_t smem, int32_t batch,
                                 cudaStream_t stream) {
   if (C == 1) {
-    // one CTA per request: a plain launch, no cluster barrier or DSMEM
+    // one CTA per request: a plain launch, no cluster barrier or DSMEM.  The
+    // largest shared-memory carve-out, the one the verification kernel that
+    // follows needs, so that the SMs keep one L1 / shared-memory split
     cudaError_t e = cudaFuncSetAttribute(spec::ngram_kernel<false, PRICE>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(spec::ngram_kernel<false, PRICE>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
     spec::ngram_kernel<false, PRICE><<<batch, SPEC_CTA_THREADS, smem, stream>>>(p);
     return cudaGetLastError();
   }
   cudaError_t e = cudaFuncSetAttribute(spec::ngram_kernel<true, PRICE>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(spec::ngram_kernel<true, PRICE>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           (int)cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(batch * C), 1, 1);

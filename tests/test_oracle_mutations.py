@@ -13,6 +13,7 @@ from . import test_oracle_ngram as TN
 from . import test_oracle_philox as TP
 from . import test_oracle_price as TPR
 from . import test_oracle_budget as TBU
+from . import test_oracle_draft_sampling as TDS
 from . import test_oracle_tree as TT
 from . import test_oracle_tree_build as TB
 from . import test_oracle_verify as TV
@@ -108,6 +109,12 @@ MUTATIONS = [
      "int32_t len = chain_len[r];", [TBU.test_only_verifiable_slots_count]),
     ("budget takes the smallest survivals first", "return (x < y) - (x > y);", "return (x > y) - (x < y);",
      [lambda o: TBU.test_slot_price_rule_of_eq_2(o, 0)]),
+    # probabilistic drafting (Hybrid Spark sec. 4.5, App. H)
+    ("drafts draw with verification's counters", "0x40000000u + (uint32_t)k, (uint32_t)step",
+     "(uint32_t)k, (uint32_t)step", [TDS.test_uniform_counter_domain]),
+    ("drafts ignore the temperature", "row_softmax(draft_logits, row, vocab, dtype, temperature, q);",
+     "row_softmax(draft_logits, row, vocab, dtype, 1.0, q);",
+     [lambda o: TDS.test_temperature_half_squares_the_odds(o, 0.08, 1)]),
 ]
 
 
