@@ -326,6 +326,79 @@ def measure_bs4(S, torch, W, steps, warmup, hbm):
             "l2": "10 rotating input sets (10 x 19.5 MB > L2)"}
 
 
+def measure_bs4_probabilistic(S, torch, W, steps, warmup, hbm):
+    """Batch-4 code editing at T = 1 with probabilistic drafting (extension
+    policy): the drafter's 7 tokens sampled on the device from its bf16 rows
+    (spec_sample_drafts), draft + price, then sampled verification against
+    the draft rows; ten rotating input sets (10 x (19.5 + 8.5) MB > L2).  The
+    sampling step counter is held fixed so that every round has the same
+    layout; the work does not depend on the drawn values."""
+    from speculative_decoding_draft_spec_gb300.round import ChainRound
+
+    cfg = W.edit_bs4(temperature=1.0, probabilistic=True)
+    B, K, L, V = cfg["B"], cfg["K"], cfg["L"], cfg["V"]
+    max_rows = B * (L + 1)
+    dl = torch.from_numpy(cfg["draft_logits"].view(np.int16)).view(torch.bfloat16).to("cuda")
+    rounds = []
+    for _ in range(10):
+        rnd = ChainRound(B, cfg["hist"].shape[1], K, L, V, torch.bfloat16, max_rows, cfg["coef"], cfg["n_min"],
+                         cfg["n_max"], cfg["copy_cap"], with_draft=True)
+        rnd.load(cfg["hist"], cfg["hist_len"], cfg["d"], cfg["c"], cfg["d_len"])
+        rnd.draft_logits.copy_(dl)
+        rounds.append(rnd)
+    stream = torch.cuda.current_stream()
+
+    def sample(rnd):
+        S.spec_sample_drafts(rnd.draft_logits, 1.0, rnd.d, rnd.ws, seed=0, step=0, stream=stream)
+
+    sample(rounds[0])
+    rounds[0].draft_and_price(cfg["lam"], cfg["budget"], cfg["max_verify_len"], cfg["policy"], False, stream)
+    torch.cuda.synchronize()
+    row_off = rounds[0].row_off.cpu().numpy()
+    vlen = rounds[0].verify_len.cpu().numpy()
+    n_rows, n_tok = int(row_off[-1]), int(vlen.sum())
+    lt = torch.from_numpy(W.compact_logits(cfg, row_off, vlen).view(np.int16)).view(torch.bfloat16).to("cuda")
+    for rnd in rounds:
+        rnd.logits[:n_rows].copy_(lt)
+
+    def one(i, rec=None):
+        rnd = rounds[i % len(rounds)]
+        if rec:
+            rec[0].record(stream)
+        sample(rnd)
+        if rec:
+            rec[1].record(stream)
+        rnd.draft_and_price(cfg["lam"], cfg["budget"], cfg["max_verify_len"], cfg["policy"], False, stream)
+        if rec:
+            rec[2].record(stream)
+        rnd.verify(temperature=1.0, seed=0, step=i, stream=stream)
+        if rec:
+            rec[3].record(stream)
+
+    for i in range(warmup):
+        one(i)
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(steps):
+        one(i, ev[i])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1)
+    comp = {k: statistics.mean(e[a].elapsed_time(e[b]) for e in ev) * 1e3
+            for k, (a, b) in {"sample_drafts": (0, 1), "draft_price": (1, 2), "verify": (2, 3)}.items()}
+    draft_bytes = B * K * V * 2
+    return {"workload": "edit_bs4 probabilistic: B=4, T=1, drafts sampled on the device, extension policy, "
+                        "bf16 V=151936",
+            "value": n_tok * steps / (ms * 1e-3), "unit": UNIT, "ms_per_step": ms / steps, "steps": steps,
+            "verified_tokens_per_step": n_tok, "verify_rows_per_step": n_rows,
+            "components_us": {k: round(v, 3) for k, v in comp.items()},
+            "sample_drafts_roofline_frac": round(draft_bytes / (comp["sample_drafts"] * 1e-6) / 1e9 / hbm, 4),
+            "status_clean": all(int(r.ws.status()) == 0 for r in rounds),
+            "l2": "10 rotating input sets (10 x 28 MB > L2)"}
+
+
 def measure_long_sampled(S, torch, W, steps, warmup, hbm):
     """The batch-64 long-context workload: draft + price over 32768-token
     histories (clusters of CTAs per request), then sampled chain verification
@@ -547,6 +620,7 @@ def run_gpu(args):
 
     hbm, peak_kind = peaks()
     bs4 = measure_bs4(S, torch, W, min(args.steps, 5000), args.warmup, hbm)
+    bs4_prob = measure_bs4_probabilistic(S, torch, W, min(args.steps, 3000), args.warmup, hbm)
     long_sampled = measure_long_sampled(S, torch, W, min(args.steps, 1000), args.warmup, hbm)
     tree = measure_tree(S, torch, W, min(args.steps, 2000), args.warmup, hbm)
     if rank != 0:
@@ -575,6 +649,7 @@ def run_gpu(args):
         "gpu_launches": 2 * args.steps,
         "clocks": clk.summary(),
         "bs4": bs4,
+        "bs4_probabilistic": bs4_prob,
         "long_bs64_sampled": long_sampled,
         "tree_bs32": tree,
         "budget_sizing": sizing,

@@ -128,6 +128,8 @@ typedef struct {
   size_t off_partial2;   /* double [max_batch x units]                       */
   size_t off_keys;       /* uint32 [SPEC_MAX_PRICE_BATCH x SPEC_MAX_L]:
                             allocation keys of the pricing step            */
+  size_t off_counter3;   /* uint32 [max_batch x max(K, 1)]: per draft-row
+                            arrival counters of spec_sample_drafts          */
   int32_t units;         /* ceil(vocab / 2048)                               */
   int32_t pad_;
 } spec_workspace;
@@ -291,6 +293,29 @@ spec_status spec_build_tree(int32_t batch, int32_t P, int32_t Kc, const int32_t*
                             int32_t Lg, const int32_t* ng_len, const float* ng_score, const float* ng_adj,
                             int32_t width, int32_t* tok, int32_t* parent, int32_t* cand_id, int32_t* n_rows,
                             const spec_workspace* ws, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
+ * spec_sample_drafts: probabilistic drafting ([HS] sec. 4.5 and App. H;
+ * the drafter samples its tokens from its own distribution q).
+ *
+ * draft_logits [batch x K x vocab] (fp32 or bf16) holds the drafter's logit
+ * row of every position; y [batch x K] gets y[r, k-1] ~ q_k = softmax(z / T)
+ * by inverse CDF in vocabulary order at the uniform u = word 0 of
+ * Philox4x32-10 with counter (r, 0x40000000 + k, lo32(step), hi32(step)) and
+ * key (lo32(seed), hi32(seed)) -- a counter domain apart from
+ * spec_verify_chain's.  The positions are drawn independently from the given
+ * rows (a drafter whose row depends on the previous token produces its rows
+ * inside its own network).  dbg_u / dbg_q [batch x K] (may be NULL): the
+ * uniform and q of the drawn token.  The per-unit (max, sum) of every row are
+ * left in the workspace slots that spec_verify_chain uses for q rows.
+ * T must be > 0.  A row holding NaN or +Inf sets SPEC_DEV_NONFINITE.
+ * Limits: batch <= the workspace's max_batch, 1 <= K <= its K, vocab <= its
+ * vocab.
+ * ------------------------------------------------------------------------ */
+spec_status spec_sample_drafts(int32_t batch, int32_t K, int32_t vocab, spec_dtype dtype,
+                               const void* draft_logits, float temperature, uint64_t seed, uint64_t step,
+                               int32_t* y, float* dbg_u, float* dbg_q, const spec_workspace* ws,
+                               cudaStream_t stream);
 
 /* ------------------------------------------------------------------------
  * spec_size_budget: the next verification budget and slot price from one

@@ -24,7 +24,8 @@ from ._build import build
 
 __all__ = [
     "build", "load", "Workspace", "EstimatorTable", "SpecError", "spec_ngram_propose",
-    "spec_price_and_allocate", "spec_price_and_allocate_static", "spec_draft_and_price", "spec_verify_chain", "spec_verify_tree", "spec_build_tree", "spec_size_budget", "POLICY", "DEV_BITS",
+    "spec_price_and_allocate", "spec_price_and_allocate_static", "spec_draft_and_price", "spec_verify_chain", "spec_verify_tree", "spec_build_tree", "spec_size_budget", "spec_sample_drafts", "POLICY",
+    "DEV_BITS",
 ]
 
 SPEC_OK, SPEC_ERR_INVALID_ARG, SPEC_ERR_CUDA, SPEC_ERR_UNSUPPORTED, SPEC_ERR_WORKSPACE = 0, 1, 2, 3, 4
@@ -46,7 +47,7 @@ class WorkspaceStruct(C.Structure):
         ("max_batch", C.c_int32), ("max_rows", C.c_int32), ("K", C.c_int32), ("vocab", C.c_int32),
         ("off_counter", C.c_size_t), ("off_counter2", C.c_size_t), ("off_record", C.c_size_t),
         ("off_rowkey", C.c_size_t), ("off_partial", C.c_size_t), ("off_partial2", C.c_size_t),
-        ("off_keys", C.c_size_t), ("units", C.c_int32), ("pad_", C.c_int32),
+        ("off_keys", C.c_size_t), ("off_counter3", C.c_size_t), ("units", C.c_int32), ("pad_", C.c_int32),
     ]
 
 
@@ -91,6 +92,7 @@ SIGNATURES = {
     "spec_build_tree": ([_i32, _i32, _i32, _vp, _vp, _vp, _vp, _i32, _vp, _vp, _vp, _i32, _vp, _vp, _vp, _vp,
                          _WSP, _vp], _i32),
     "spec_size_budget": ([_i32, _i32, _vp, _vp, _i32, C.c_double, C.c_double, _vp, _vp, _WSP, _vp], _i32),
+    "spec_sample_drafts": ([_i32, _i32, _i32, _i32, _vp, _f32, _u64, _u64, _vp, _vp, _vp, _WSP, _vp], _i32),
     "spec_verify_tree": ([_i32, _i32, _i32, _vp, _vp, _i32, _vp, _vp, _i32, _vp, _vp, _vp, _WSP, _vp],
                          _i32),
 }
@@ -300,3 +302,12 @@ def spec_size_budget(S, chain_len, max_verify_len, C0, p, out_budget, out_lambda
     _check("spec_size_budget", load().spec_size_budget(
         B, L, _ptr(S), _ptr(chain_len), int(max_verify_len), float(C0), float(p), _ptr(out_budget),
         _ptr(out_lambda), ws.ref, _stream(stream)))
+
+
+def spec_sample_drafts(draft_logits, temperature, y, ws: Workspace, seed=0, step=0, dbg_u=None, dbg_q=None,
+                       stream=None):
+    """y [B x K] ~ softmax(draft_logits [B x K x V] / T) per position (device tensors)."""
+    B, K, V = draft_logits.shape
+    _check("spec_sample_drafts", load().spec_sample_drafts(
+        B, K, V, _dtype_code(draft_logits), _ptr(draft_logits), float(temperature), int(seed), int(step), _ptr(y),
+        _ptr(dbg_u), _ptr(dbg_q), ws.ref, _stream(stream)))

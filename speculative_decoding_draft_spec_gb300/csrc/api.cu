@@ -42,6 +42,10 @@ cudaError_t spec_launch_build_tree(int32_t batch, int32_t P, int32_t Kc, const i
 cudaError_t spec_launch_size_budget(int32_t batch, int32_t L, const float* S, const int32_t* chain_len,
                                     int32_t mvl, double C0, double p, int32_t* out_budget, float* out_lambda,
                                     cudaStream_t stream);
+cudaError_t spec_launch_sample_drafts(int32_t batch, int32_t K, int32_t vocab, int32_t dtype,
+                                      const void* draft_logits, float temperature, uint64_t seed, uint64_t step,
+                                      int32_t* y, float* dbg_u, float* dbg_q, const spec_workspace* ws,
+                                      int num_sms, cudaStream_t stream);
 cudaError_t spec_launch_draft_price(
     const int32_t* hist, int64_t stride, const int32_t* hist_len, int32_t batch, int32_t n_min, int32_t n_max,
     int32_t cap, int32_t* g, int32_t* g_len, int32_t* match_n, int32_t* agree, int32_t* copy_len, int32_t K,
@@ -103,6 +107,8 @@ bool layout(int32_t max_batch, int32_t max_rows, int32_t K, int32_t vocab, spec_
   off = align256(off + sizeof(double) * (size_t)units * (size_t)max_batch);
   w->off_keys = off;  // sized for the largest pricing batch, whatever max_batch is
   off = align256(off + sizeof(uint32_t) * (size_t)SPEC_MAX_PRICE_BATCH * SPEC_MAX_L);
+  w->off_counter3 = off;
+  off = align256(off + sizeof(uint32_t) * (size_t)max_batch * (size_t)(K > 1 ? K : 1));
   w->bytes = off;
   w->max_batch = max_batch;
   w->max_rows = max_rows;
@@ -286,6 +292,24 @@ spec_status spec_size_budget(int32_t batch, int32_t L, const float* S, const int
   if (!ws_ok(ws)) return SPEC_ERR_WORKSPACE;
   return from_cuda(spec_launch_size_budget(batch, L, S, chain_len, max_verify_len, C0, p, out_budget, out_lambda,
                                            stream));
+}
+
+spec_status spec_sample_drafts(int32_t batch, int32_t K, int32_t vocab, spec_dtype dtype,
+                               const void* draft_logits, float temperature, uint64_t seed, uint64_t step,
+                               int32_t* y, float* dbg_u, float* dbg_q, const spec_workspace* ws,
+                               cudaStream_t stream) {
+  if (batch < 0 || K < 1 || vocab < 1 || !(temperature > 0.0f) || !(temperature < INFINITY))
+    return SPEC_ERR_INVALID_ARG;
+  if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_INVALID_ARG;
+  if (K > SPEC_MAX_L || batch > kMaxVerifyBatch) return SPEC_ERR_UNSUPPORTED;
+  if (batch > 0 && (!draft_logits || !y)) return SPEC_ERR_INVALID_ARG;
+  if (!ws_ok(ws)) return SPEC_ERR_WORKSPACE;
+  if (batch > ws->max_batch || K > ws->K || vocab > ws->vocab) return SPEC_ERR_WORKSPACE;
+  if (batch == 0) return SPEC_OK;
+  const int sms = device_sms();
+  if (sms <= 0) return SPEC_ERR_CUDA;
+  return from_cuda(spec_launch_sample_drafts(batch, K, vocab, (int32_t)dtype, draft_logits, temperature, seed, step,
+                                             y, dbg_u, dbg_q, ws, sms, stream));
 }
 
 spec_status spec_draft_and_price(

@@ -166,6 +166,7 @@ struct WsView {
   uint32_t* status;
   uint32_t* counter;
   uint32_t* counter2;
+  uint32_t* counter3;  // per draft-row arrival counters (probabilistic drafting)
   unsigned char* record;
   unsigned long long* rowkey;
   float2* partial;

@@ -1369,6 +1369,112 @@ __global__ void __launch_bounds__(SPEC_CTA_THREADS) resample_kernel(VerifyParams
   }
 }
 
+// ------------------------------------------------------------------ probabilistic drafting
+// y_k ~ softmax(z_k / T) for the drafter's rows (Hybrid Spark sec. 4.5, App. H).
+// One pass over each row: per 8 KB chunk, (max, sum of 2^((z - max) log2e / T))
+// per 2048-entry unit into the workspace partials -- the slots the verification
+// kernel uses for the same q rows -- and the warp that completes a row draws
+// from it: the crossing unit from the units' weights, then the crossing entry
+// inside that unit (a second read of one 4-8 KB unit).  The uniform is word 0
+// of Philox counter (r, 0x40000000 + k, lo32(step), hi32(step)), key
+// (lo32(seed), hi32(seed)), a counter domain apart from verification's.
+template <int DT>
+__device__ void draw_draft(const VerifyParams& p, int row, int r, int k, int slot, int lane) {
+  const float2 mz = merge_row(p, slot, lane);
+  const float m = mz.x;
+  uint32_t o[4];
+  philox4x32_10((uint32_t)r, 0x40000000u + (uint32_t)(k + 1), (uint32_t)p.step, (uint32_t)(p.step >> 32),
+                (uint32_t)p.seed, (uint32_t)(p.seed >> 32), o);
+  const float u = (float)(o[0] >> 8) * (1.0f / 16777216.0f);
+  const char* base = static_cast<const char*>(p.draft) + (int64_t)row * p.vocab * (DT == 1 ? 2 : 4);
+  int y = 0;
+  float q_at = 0.0f;
+  double total = 0.0;
+  if (m != -INFINITY) {
+    auto w_plain = [&](int uu) -> double {
+      const float2 t = __ldcg(&p.ws.partial[(int64_t)slot * p.ws.units + uu]);
+      if (t.x == -INFINITY) return 0.0;
+      return (double)(t.y * ex2((t.x - m) * p.c));
+    };
+    double ls = 0.0;
+    for (int uu = lane; uu < p.units; uu += 32) ls += w_plain(uu);
+    total = warp_sum_d(ls);
+    const double t = (double)u * total;
+    const Crossing cr = find_unit(p.units, t, lane, w_plain);
+    float v[64];
+    const int e0 = cr.unit * SPEC_UNIT;
+    const int n_el = min(SPEC_UNIT, p.vocab - e0);
+    load_unit_contig<DT>(base, e0, n_el, p.vec_ok != 0, lane, v);
+    const float mc = m * p.c;
+#pragma unroll
+    for (int j = 0; j < 64; ++j) v[j] = (v[j] == -INFINITY) ? 0.0f : ex2(fmaf(v[j], p.c, -mc));
+    const int pick = find_in_unit(v, cr.before, t, lane, &q_at);
+    y = e0 + pick;
+  }
+  if (lane == 0) {
+    p.out_tokens[row] = y;
+    if (p.dbg_u) p.dbg_u[row] = u;
+    if (p.dbg_resid) p.dbg_resid[row] = total > 0.0 ? (float)((double)q_at / total) : 0.0f;
+  }
+}
+
+template <int DT>
+__global__ void __launch_bounds__(SPEC_CTA_THREADS) sample_drafts_kernel(VerifyParams p) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  constexpr int CH = Vec<DT>::CH, SUB = Vec<DT>::SUB;
+  const int chunks = (p.vocab + CH - 1) / CH;
+  const int rows = p.batch * p.K;
+  const int64_t total = (int64_t)rows * chunks;
+  const int64_t nwarps = (int64_t)gridDim.x * SPEC_WARPS_PER_CTA;
+  const size_t esz = DT == 1 ? 2 : 4;
+  const bool vec = p.vec_ok != 0;
+  int bad = 0;
+  for (int64_t w = (int64_t)blockIdx.x * SPEC_WARPS_PER_CTA + warp; w < total; w += nwarps) {
+    const int row = (int)(w / chunks), ch = (int)(w - (int64_t)row * chunks);
+    const int r = row / p.K, k = row - r * p.K;  // position k + 1
+    const int slot = q_slot_of(p, r, k + 1);
+    const char* base = static_cast<const char*>(p.draft) + (int64_t)row * p.vocab * esz;
+    const int e0 = ch * CH, n_el = min(CH, p.vocab - e0);
+    float2 ms[SUB];
+    if (vec) {
+      uint4 v[Vec<DT>::NV];
+      vec_load_global<DT>(base + (size_t)e0 * esz, n_el, lane, v);
+      if (DT == 1) {
+        ms[0] = unit_softmax_vec<DT, 0, 8>(v, p.c, bad);
+        if (SUB > 1) ms[SUB - 1] = unit_softmax_vec<DT, 8, 8>(v, p.c, bad);
+      } else {
+        ms[0] = unit_softmax_vec<DT, 0, 16>(v, p.c, bad);
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < SUB; ++j) {
+        const int e1 = e0 + j * SPEC_UNIT;
+        const int n1 = min(SPEC_UNIT, p.vocab - e1);
+        ms[j] = n1 <= 0 ? make_float2(-INFINITY, 0.0f)
+                        : unit_softmax_scalar<DT>(base + (size_t)e1 * esz, n1, lane, p.c, bad);
+      }
+    }
+    int last = 0;
+    if (lane == 0) {
+#pragma unroll
+      for (int j = 0; j < SUB; ++j) {
+        const int uu = ch * SUB + j;
+        if (uu * SPEC_UNIT < p.vocab) __stcg(&p.ws.partial[(int64_t)slot * p.ws.units + uu], ms[j]);
+      }
+      // release this chunk's partials, acquire the row's others
+      const uint32_t old = atomic_add_acq_rel(&p.ws.counter3[row], 1u);
+      last = (old + 1u == (uint32_t)chunks);
+    }
+    last = __shfl_sync(0xFFFFFFFFu, last, 0);
+    if (last) {
+      __syncwarp();  // orders every lane after lane 0's acquire
+      if (lane == 0) p.ws.counter3[row] = 0u;
+      draw_draft<DT>(p, row, r, k, slot, lane);
+    }
+  }
+  if (bad && lane == 0) set_status(p.ws.status, SPEC_DEV_NONFINITE);
+}
+
 }  // namespace spec
 
 // ---------------------------------------------------------------------------
@@ -1416,6 +1522,7 @@ spec::WsView ws_view(const spec_workspace* ws) {
   v.status = reinterpret_cast<uint32_t*>(b);
   v.counter = reinterpret_cast<uint32_t*>(b + ws->off_counter);
   v.counter2 = reinterpret_cast<uint32_t*>(b + ws->off_counter2);
+  v.counter3 = reinterpret_cast<uint32_t*>(b + ws->off_counter3);
   v.record = reinterpret_cast<unsigned char*>(b + ws->off_record);
   v.rowkey = reinterpret_cast<unsigned long long*>(b + ws->off_rowkey);
   v.partial = reinterpret_cast<float2*>(b + ws->off_partial);
@@ -1502,4 +1609,36 @@ extern "C" cudaError_t spec_launch_verify_tree(int32_t batch, int32_t vocab, int
   if (batch == 0) return cudaSuccess;
   return dtype == SPEC_BF16 ? launch_rows<1, spec::MODE_TREE>(p, num_sms, stream)
                             : launch_rows<0, spec::MODE_TREE>(p, num_sms, stream);
+}
+
+extern "C" cudaError_t spec_launch_sample_drafts(int32_t batch, int32_t K, int32_t vocab, int32_t dtype,
+                                                 const void* draft_logits, float temperature, uint64_t seed,
+                                                 uint64_t step, int32_t* y, float* dbg_u, float* dbg_q,
+                                                 const spec_workspace* ws, int num_sms, cudaStream_t stream) {
+  spec::VerifyParams p = {};
+  p.batch = batch;
+  p.vocab = vocab;
+  p.max_rows = ws->max_rows;
+  p.draft = draft_logits;
+  p.K = K;
+  p.c = (float)(1.4426950408889634 / (double)temperature);
+  p.seed = seed;
+  p.step = step;
+  p.out_tokens = y;
+  p.dbg_u = dbg_u;
+  p.dbg_resid = dbg_q;
+  p.units = (vocab + SPEC_UNIT - 1) / SPEC_UNIT;
+  const size_t esz = dtype == SPEC_BF16 ? 2 : 4;
+  p.vec_ok = (((size_t)vocab * esz) % 16 == 0 && (reinterpret_cast<uintptr_t>(draft_logits) & 15u) == 0) ? 1 : 0;
+  p.ws = ws_view(ws);
+  if (batch == 0) return cudaSuccess;
+  const int ch = dtype == SPEC_BF16 ? spec::Vec<1>::CH : spec::Vec<0>::CH;
+  const int64_t chunks = (int64_t)batch * K * ((vocab + ch - 1) / ch);
+  const int64_t want = (chunks + SPEC_WARPS_PER_CTA - 1) / SPEC_WARPS_PER_CTA;
+  const int grid = (int)(want < (int64_t)num_sms * 8 ? want : (int64_t)num_sms * 8);
+  if (dtype == SPEC_BF16)
+    spec::sample_drafts_kernel<1><<<grid, SPEC_CTA_THREADS, 0, stream>>>(p);
+  else
+    spec::sample_drafts_kernel<0><<<grid, SPEC_CTA_THREADS, 0, stream>>>(p);
+  return cudaGetLastError();
 }
