@@ -333,9 +333,14 @@ spec_status spec_sample_drafts(int32_t batch, int32_t K, int32_t vocab, spec_dty
  * The host reads the two device scalars back asynchronously and passes them
  * as `budget` and `lambda` to the pricing step two steps later ([HS] sec.
  * 4.4: the GPU allocates from fresh survivals, the host sizes from stale
- * ones).  The sums associate by segments of the sorted list, so G may differ
- * from a left-to-right sum in its last bits.  The workspace serves only its
- * status word (the call may overlap other calls on it).
+ * ones).  The maximum is found without sorting, by Dinkelbach's iteration on
+ * the ratio (the set that maximises A - lambda C takes every slot above
+ * lambda p), with the survivals summed exactly in 2^-48 fixed point, so
+ * near-ties of G may resolve differently from a left-to-right fp64 sum in
+ * the last bits.  A survival outside [0, 1] (or NaN) among the verifiable
+ * slots sets SPEC_DEV_BAD_VALUE and counts as clamped to [0, 1] (NaN as 0).
+ * The workspace serves only its status word (the call may overlap other
+ * calls on it).
  * Limits: 1 <= L <= SPEC_MAX_L, batch <= SPEC_MAX_PRICE_BATCH; C0, p > 0.
  * ------------------------------------------------------------------------ */
 spec_status spec_size_budget(int32_t batch, int32_t L, const float* S, const int32_t* chain_len,

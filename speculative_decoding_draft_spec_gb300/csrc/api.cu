@@ -41,7 +41,7 @@ cudaError_t spec_launch_build_tree(int32_t batch, int32_t P, int32_t Kc, const i
                                    int32_t* n_rows, uint32_t* status, cudaStream_t stream);
 cudaError_t spec_launch_size_budget(int32_t batch, int32_t L, const float* S, const int32_t* chain_len,
                                     int32_t mvl, double C0, double p, int32_t* out_budget, float* out_lambda,
-                                    cudaStream_t stream);
+                                    uint32_t* status, cudaStream_t stream);
 cudaError_t spec_launch_sample_drafts(int32_t batch, int32_t K, int32_t vocab, int32_t dtype,
                                       const void* draft_logits, float temperature, uint64_t seed, uint64_t step,
                                       int32_t* y, float* dbg_u, float* dbg_q, const spec_workspace* ws,
@@ -291,7 +291,7 @@ spec_status spec_size_budget(int32_t batch, int32_t L, const float* S, const int
   if (!out_budget || !out_lambda || (batch > 0 && (!S || !chain_len))) return SPEC_ERR_INVALID_ARG;
   if (!ws_ok(ws)) return SPEC_ERR_WORKSPACE;
   return from_cuda(spec_launch_size_budget(batch, L, S, chain_len, max_verify_len, C0, p, out_budget, out_lambda,
-                                           stream));
+                                           status_of(ws), stream));
 }
 
 spec_status spec_sample_drafts(int32_t batch, int32_t K, int32_t vocab, spec_dtype dtype,

@@ -9,22 +9,19 @@
 // this kernel produces them on the device so that the host only copies two
 // scalars back, asynchronously.
 //
-// GB300 layout: one CTA of 1024 threads.  The survivals of the verifiable
-// slots are gathered into shared memory, sorted descending by a bitonic sort
-// over the next power of two, then each thread takes a contiguous segment of
-// the sorted list: segment sums in fp64, one block scan, a walk that forms
-// A(b) and G(b) for its b, and a block-wide argmax (largest G, then smallest
-// b).  The sums associate by segment, not left to right, so G may differ from
-// a sequential sum in the last bits.
+// GB300 layout: one CTA of 256 threads.  The survivals of the verifiable
+// slots are gathered into shared memory (no sort), then Dinkelbach's
+// iteration below finds the maximising ratio with one block-wide count and
+// exact fixed-point sum per round (fp64 work runs on a narrow pipe on this
+// part, so only the ratio is formed in fp64).  The sums differ from a
+// left-to-right fp64 sum in the last bits, so near-ties of G may resolve
+// differently.
 #include "common.cuh"
 
 namespace spec {
 
-#define BU_THREADS 1024
-#define BU_WARPS (BU_THREADS / 32)
-
 struct BudgetParams {
-  int32_t batch, L, mvl, n_pad;
+  int32_t batch, L, mvl;
   const float* S;
   const int32_t* chain_len;
   double C0, p;
@@ -32,118 +29,138 @@ struct BudgetParams {
   float* out_lambda;
 };
 
-__global__ void __launch_bounds__(BU_THREADS, 1) size_budget_kernel(BudgetParams p) {
-  extern __shared__ __align__(16) float s_val[];  // [n_pad]
+#define BU_THREADS 256
+
+// A survival in [0, 1] as a multiple of 2^-48, truncated: integer sums of
+// these are exact, and at most 1024 x 31 of them stay below 2^63.  The
+// truncation moves a sum by less than 2^-48 per term, far less than the
+// rounding of a left-to-right fp64 sum of the same terms.
+__device__ __forceinline__ uint64_t fixed48(float v) {
+  const uint32_t bits = __float_as_uint(v);
+  const int32_t e = (int32_t)(bits >> 23);
+  if (e == 0) return 0ull;  // zero or subnormal: below 2^-126
+  const uint64_t m = (uint64_t)((bits & 0x7FFFFFu) | 0x800000u);
+  const int32_t sh = e - 102;  // v = m 2^(e - 150), so v 2^48 = m 2^(e - 102)
+  return sh >= 0 ? (m << sh) : (sh > -64 ? (m >> -sh) : 0ull);
+}
+
+__global__ void __launch_bounds__(BU_THREADS) size_budget_kernel(BudgetParams p, uint32_t* status) {
+  extern __shared__ __align__(16) float s_val[];  // [batch x L]: the verifiable survivals
   __shared__ int32_t s_n;
-  __shared__ double s_part[BU_WARPS];
-  __shared__ double s_bestG[BU_WARPS];
-  __shared__ int32_t s_bestb[BU_WARPS];
+  __shared__ unsigned long long s_part[BU_THREADS / 32];
+  __shared__ int32_t s_cnt[BU_THREADS / 32];
+  __shared__ float s_thr;
+  __shared__ int32_t s_b, s_done;
+  __shared__ double s_lam;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (tid == 0) s_n = 0;
-  for (int32_t i = tid; i < p.n_pad; i += BU_THREADS) s_val[i] = -1.0f;  // below every survival
-  __syncthreads();
-  // gather the verifiable survivals (their order does not matter: they are sorted next)
-  const int32_t nslots = p.batch * p.L;
-  for (int32_t q = tid; q < nslots; q += BU_THREADS) {
-    const int32_t r = q / p.L, k = q - r * p.L;
-    int32_t len = __ldg(p.chain_len + r);
-    len = len < p.mvl ? len : p.mvl;
-    if (k < len) s_val[atomicAdd(&s_n, 1)] = __ldg(p.S + q);
+  if (tid == 0) {
+    s_n = 0;
+    s_b = 0;
+    s_lam = (double)p.batch / p.C0;  // G(0)
+    s_thr = __double2float_rd(s_lam * p.p);
+    s_done = 0;
   }
+  __syncthreads();
+  // gather the verifiable survivals (their order does not matter): batches of
+  // 8 slots per thread with every load issued before any is used; one shared
+  // atomic per warp and batch places them
+  const int32_t nslots = p.batch * p.L;
+  bool bad = false;
+  for (int32_t q0 = 0; q0 < nslots; q0 += 8 * BU_THREADS) {
+    float v[8];
+    int32_t len[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int32_t q = q0 + j * BU_THREADS + tid;
+      v[j] = q < nslots ? __ldg(p.S + q) : 0.0f;
+      len[j] = q < nslots ? __ldg(p.chain_len + q / p.L) : 0;
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int32_t q = q0 + j * BU_THREADS + tid;
+      const int32_t k = q - (q / p.L) * p.L;
+      const bool valid = q < nslots && k < min(len[j], p.mvl);
+      if (valid && !(v[j] >= 0.0f && v[j] <= 1.0f)) {  // survivals are probabilities
+        bad = true;
+        v[j] = v[j] > 1.0f ? 1.0f : 0.0f;
+      }
+      const unsigned b = __ballot_sync(0xFFFFFFFFu, valid);
+      int32_t base = 0;
+      if (lane == 0 && b != 0u) base = atomicAdd(&s_n, __popc(b));
+      base = __shfl_sync(0xFFFFFFFFu, base, 0);
+      if (valid) s_val[base + __popc(b & ((1u << lane) - 1u))] = v[j];
+    }
+  }
+  if (bad) set_status(status, SPEC_DEV_BAD_VALUE);
   __syncthreads();
   const int32_t n = s_n;
-  // bitonic sort, descending
-  for (int32_t size = 2; size <= p.n_pad; size <<= 1) {
-    for (int32_t stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int32_t i = tid; i < p.n_pad / 2; i += BU_THREADS) {
-        const int32_t lo = 2 * i - (i & (stride - 1));  // pairs (lo, lo + stride)
-        const int32_t hi = lo + stride;
-        const bool desc = ((lo & size) == 0);
-        const float a = s_val[lo], b = s_val[hi];
-        if (desc ? (a < b) : (a > b)) {
-          s_val[lo] = b;
-          s_val[hi] = a;
-        }
+  // Dinkelbach's iteration for the ratio G = A / C: given the ratio lam of
+  // the current set, the set maximising A(b) - lam C(b) takes every slot whose
+  // survival exceeds lam p (a slot equal to it adds nothing, and leaving it
+  // out keeps the smallest b); its ratio is the next lam.  lam rises to
+  // max_b G(b) and the set stops changing there, in a few rounds.  Each round
+  // is one block-wide count and exact integer sum; only the ratio itself is
+  // formed in fp64, by one thread.
+  for (int it = 0; it < 64 && !s_done; ++it) {
+    // v > lam p for an fp32 v exactly when v > (lam p rounded down to fp32)
+    const float thr = s_thr;
+    int32_t cnt = 0;
+    uint64_t sum = 0;
+    for (int32_t i = tid; i < n; i += BU_THREADS) {
+      const float v = s_val[i];
+      if (v > thr) {
+        ++cnt;
+        sum += fixed48(v);
       }
-      __syncthreads();
     }
-  }
-  // contiguous segments of the sorted list: sums, scan, then G(b) for b in the segment
-  const int32_t per = (n + BU_THREADS - 1) / BU_THREADS;
-  const int32_t b0 = tid * per, b1 = min(n, b0 + per);
-  double seg = 0.0;
-  for (int32_t i = b0; i < b1; ++i) seg += (double)s_val[i];
-  double incl = seg;
+    cnt = __reduce_add_sync(0xFFFFFFFFu, cnt);
 #pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const double v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-    if (lane >= o) incl += v;
-  }
-  if (lane == 31) s_part[warp] = incl;
-  __syncthreads();
-  double before = 0.0;
-  for (int w = 0; w < warp; ++w) before += s_part[w];
-  double A = (double)p.batch + (before + (incl - seg));  // A at b = b0
-  double bestG = -1.0;
-  int32_t bestb = 0;
-  if (tid == 0) {
-    bestG = A / p.C0;  // b = 0
-    bestb = 0;
-  }
-  for (int32_t i = b0; i < b1; ++i) {
-    A += (double)s_val[i];
-    const int32_t b = i + 1;
-    const double G = A / (p.C0 + p.p * (double)b);
-    if (G > bestG) {
-      bestG = G;
-      bestb = b;
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
+    if (lane == 0) {
+      s_part[warp] = sum;
+      s_cnt[warp] = cnt;
     }
-  }
-  // argmax over the block: largest G, ties to the smallest b
+    __syncthreads();
+    if (tid == 0) {
+      int32_t c = 0;
+      uint64_t sm = 0;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const double g2 = __shfl_down_sync(0xFFFFFFFFu, bestG, o);
-    const int32_t b2 = __shfl_down_sync(0xFFFFFFFFu, bestb, o);
-    if (g2 > bestG || (g2 == bestG && b2 < bestb)) {
-      bestG = g2;
-      bestb = b2;
-    }
-  }
-  if (lane == 0) {
-    s_bestG[warp] = bestG;
-    s_bestb[warp] = bestb;
-  }
-  __syncthreads();
-  if (tid == 0) {
-    double g = s_bestG[0];
-    int32_t b = s_bestb[0];
-    for (int w = 1; w < BU_WARPS; ++w)
-      if (s_bestG[w] > g || (s_bestG[w] == g && s_bestb[w] < b)) {
-        g = s_bestG[w];
-        b = s_bestb[w];
+      for (int w = 0; w < BU_THREADS / 32; ++w) {
+        c += s_cnt[w];
+        sm += s_part[w];
       }
-    *p.out_budget = b;
-    *p.out_lambda = (float)(g * p.p);
+      const double lam_new = ((double)p.batch + (double)sm * 0x1p-48) / (p.C0 + p.p * (double)c);
+      if (c == s_b || !(lam_new > s_lam)) {
+        s_done = 1;  // the set stopped changing (or the ratio stopped rising)
+      } else {
+        s_b = c;
+        s_lam = lam_new;
+        s_thr = __double2float_rd(lam_new * p.p);
+      }
+    }
+    __syncthreads();
+  }
+  if (tid == 0) {
+    *p.out_budget = s_b;
+    *p.out_lambda = (float)(s_lam * p.p);
   }
 }
 
 }  // namespace spec
 
 extern "C" size_t spec_budget_smem_bytes(int32_t batch, int32_t L) {
-  int64_t n = 1;
-  while (n < (int64_t)batch * L) n <<= 1;
-  return (size_t)(n < 2 ? 2 : n) * sizeof(float);
+  const int64_t n = (int64_t)batch * L;
+  return (size_t)(n < 1 ? 1 : n) * sizeof(float);
 }
 
 extern "C" cudaError_t spec_launch_size_budget(int32_t batch, int32_t L, const float* S, const int32_t* chain_len,
                                                int32_t mvl, double C0, double p, int32_t* out_budget,
-                                               float* out_lambda, cudaStream_t stream) {
+                                               float* out_lambda, uint32_t* status, cudaStream_t stream) {
   spec::BudgetParams bp;
   bp.batch = batch;
   bp.L = L;
   bp.mvl = mvl;
   const size_t smem = spec_budget_smem_bytes(batch, L);
-  bp.n_pad = (int32_t)(smem / sizeof(float));
   bp.S = S;
   bp.chain_len = chain_len;
   bp.C0 = C0;
@@ -153,6 +170,6 @@ extern "C" cudaError_t spec_launch_size_budget(int32_t batch, int32_t L, const f
   cudaError_t e = cudaFuncSetAttribute(spec::size_budget_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
-  spec::size_budget_kernel<<<1, BU_THREADS, smem, stream>>>(bp);
+  spec::size_budget_kernel<<<1, BU_THREADS, smem, stream>>>(bp, status);
   return cudaGetLastError();
 }

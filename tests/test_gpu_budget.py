@@ -103,3 +103,17 @@ def test_stale_pipeline_uses_the_survivals_of_two_steps_before(S):
         if b != o.b_star:
             assert abs(o.G[b] - o.G[o.b_star]) <= 1e-12 * o.G[o.b_star]
         assert abs(lam - np.float32(o.lam)) <= 1e-6 * o.lam
+
+
+def test_survival_outside_unit_interval_is_flagged_and_clamped(S):
+    Sv = np.full((2, 3), 0.6, np.float32)
+    Sv[1, 0] = 1.5
+    ws = S.Workspace(1, 1, 1, 1)
+    b = torch.full((1,), -7, dtype=torch.int32, device="cuda")
+    lam = torch.full((1,), -7.0, dtype=torch.float32, device="cuda")
+    S.spec_size_budget(torch.as_tensor(Sv).cuda(), torch.full((2,), 3, dtype=torch.int32, device="cuda"), 3, 4.0, 1.0,
+                       b, lam, ws)
+    torch.cuda.synchronize()
+    assert ws.status() & 0x10
+    o = O.size_budget(np.clip(Sv, 0, 1), np.full(2, 3, np.int32), 3, 4.0, 1.0)
+    assert int(b.item()) == o.b_star
