@@ -86,7 +86,16 @@ __device__ __forceinline__ double warp_sum_d(double v) {
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
   return v;
 }
-// inclusive prefix sum over lanes in lane order
+// inclusive prefix sums over lanes in lane order
+__device__ __forceinline__ float warp_incl_scan(float v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float t = __shfl_up_sync(0xFFFFFFFFu, v, o);
+    if (lane >= o) v += t;
+  }
+  return v;
+}
 __device__ __forceinline__ double warp_incl_scan_d(double v) {
   const int lane = threadIdx.x & 31;
 #pragma unroll

@@ -560,55 +560,85 @@ __device__ __forceinline__ float2 merge_row_lane(const VerifyParams& p, int slot
   return make_float2(m, s0 + s1);
 }
 
-// Inverse CDF over unit weights w_u (unit order) held as 3+ consecutive units
-// per lane: returns the unit holding the crossing of t and the weight before it.
-// units_per_lane consecutive units belong to each lane, so lane order is unit order.
+// Inverse CDF over unit weights w_u (unit order), at the fraction u of their
+// total: returns the unit holding the crossing of t = u * total, the weight
+// before it, the total and t.  Each lane owns `per` consecutive units, so lane
+// order is unit order; a lane keeps its first four weights in registers for
+// the walk that locates the crossing.  The sums run in fp32 (the weights are
+// fp32 products, and fp64 work runs on a narrow pipe on this part).
 struct Crossing {
   int unit;
-  double before;
-  double total;
+  float before;  // weight of the units before `unit`; -1: t at or above the total
+  float total;
+  float t;
 };
 
 template <typename WFn>
-__device__ __forceinline__ Crossing find_unit(int units, double t, int lane, WFn wfn) {
+__device__ __forceinline__ Crossing find_unit(int units, float u, int lane, WFn wfn) {
   const int per = (units + 31) / 32;
   const int u0 = lane * per;
-  double lsum = 0.0;
+  float w4[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) w4[q] = (q < per && u0 + q < units) ? wfn(u0 + q) : 0.0f;
+  float lsum = 0.0f;
   int last_pos = -1;
-  for (int q = 0; q < per; ++q) {
-    const int u = u0 + q;
-    if (u < units) {
-      const double w = wfn(u);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    lsum += w4[q];
+    if (w4[q] > 0.0f) last_pos = u0 + q;
+  }
+  for (int q = 4; q < per; ++q) {
+    const int uu = u0 + q;
+    if (uu < units) {
+      const float w = wfn(uu);
       lsum += w;
-      if (w > 0.0) last_pos = u;
+      if (w > 0.0f) last_pos = uu;
     }
   }
-  const double incl = warp_incl_scan_d(lsum);
-  const double excl = incl - lsum;
-  const double total = __shfl_sync(0xFFFFFFFFu, incl, 31);
-  const unsigned hit = __ballot_sync(0xFFFFFFFFu, incl > t && lsum > 0.0);
+  const float incl = warp_incl_scan(lsum);
+  const float excl = incl - lsum;
   Crossing c;
-  c.total = total;
+  c.total = __shfl_sync(0xFFFFFFFFu, incl, 31);
+  c.t = u * c.total;
+  const float t = c.t;
+  const unsigned hit = __ballot_sync(0xFFFFFFFFu, incl > t && lsum > 0.0f);
   if (hit) {
     const int src = __ffs(hit) - 1;
     int unit = -1;
-    double before = 0.0;
+    float before = 0.0f;
     if (lane == src) {
-      double run = excl;
-      for (int q = 0; q < per; ++q) {
-        const int u = u0 + q;
-        if (u >= units) break;
-        const double w = wfn(u);
-        if (run + w > t && w > 0.0) {
-          unit = u;
+      float run = excl;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float w = w4[q];
+        if (unit < 0 && q < per && u0 + q < units) {
+          if (run + w > t && w > 0.0f) {
+            unit = u0 + q;
+            before = run;
+          }
+          run += w;
+        }
+      }
+      for (int q = 4; q < per && unit < 0; ++q) {
+        const int uu = u0 + q;
+        if (uu >= units) break;
+        const float w = wfn(uu);
+        if (run + w > t && w > 0.0f) {
+          unit = uu;
           before = run;
-          break;
         }
         run += w;
       }
       if (unit < 0) {  // rounding inside the lane: its last unit with mass
         unit = last_pos;
-        before = incl - (last_pos >= 0 ? wfn(last_pos) : 0.0);
+        float wl = 0.0f;
+        if (last_pos >= 0) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            if (u0 + q == last_pos) wl = w4[q];
+          if (last_pos >= u0 + 4) wl = wfn(last_pos);
+        }
+        before = incl - wl;
       }
     }
     c.unit = __shfl_sync(0xFFFFFFFFu, unit, src);
@@ -619,7 +649,7 @@ __device__ __forceinline__ Crossing find_unit(int units, double t, int lane, WFn
     const int src = has ? 31 - __clz(has) : 0;
     const int lp = __shfl_sync(0xFFFFFFFFu, last_pos, src);
     c.unit = lp < 0 ? 0 : lp;
-    c.before = -1.0;  // marker: take the last positive entry of the unit
+    c.before = -1.0f;  // marker: take the last positive entry of the unit
   }
   return c;
 }
@@ -627,34 +657,46 @@ __device__ __forceinline__ Crossing find_unit(int units, double t, int lane, WFn
 // inside one unit: the smallest index whose running sum (from `before`)
 // exceeds t, over residual values r[64] in contiguous lane layout.  Returns
 // (index within the unit, r at that index); falls back to the last positive.
-__device__ __forceinline__ int find_in_unit(const float r[64], double before, double t, int lane,
-                                            float* r_at) {
-  double lsum = 0.0;
+// The sums inside the unit run from the unit's start, against t - before.
+__device__ __forceinline__ int find_in_unit(const float r[64], float before, float t, int lane, float* r_at) {
+  float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
 #pragma unroll
-  for (int j = 0; j < 64; ++j) lsum += (double)r[j];
-  const double incl = warp_incl_scan_d(lsum) + (before < 0.0 ? 0.0 : before);
-  const double excl = incl - lsum;
+  for (int j = 0; j < 64; j += 4) {
+    a0 += r[j];
+    a1 += r[j + 1];
+    a2 += r[j + 2];
+    a3 += r[j + 3];
+  }
+  const float lsum = (a0 + a1) + (a2 + a3);
+  const float incl = warp_incl_scan(lsum);
+  const float excl = incl - lsum;
+  const float tr = t - before;
   int pick = -1;
   float rv = 0.0f;
-  const bool last_mode = before < 0.0;
-  const unsigned hit = last_mode ? 0u : __ballot_sync(0xFFFFFFFFu, incl > t && lsum > 0.0);
+  const bool last_mode = before < 0.0f;
+  const unsigned hit = last_mode ? 0u : __ballot_sync(0xFFFFFFFFu, incl > tr && lsum > 0.0f);
   if (hit) {
     const int src = __ffs(hit) - 1;
     if (lane == src) {
-      double run = excl;
+      // unrolled without an early exit, so r[] stays in registers
+      float run = excl, lastv = 0.0f;
       int lastp = -1;
+#pragma unroll
       for (int j = 0; j < 64; ++j) {
-        if (r[j] > 0.0f) lastp = j;
-        run += (double)r[j];
-        if (run > t && r[j] > 0.0f) {
+        const float x = r[j];
+        if (x > 0.0f) {
+          lastp = j;
+          lastv = x;
+        }
+        run += x;
+        if (pick < 0 && run > tr && x > 0.0f) {
           pick = 64 * lane + j;
-          rv = r[j];
-          break;
+          rv = x;
         }
       }
       if (pick < 0 && lastp >= 0) {
         pick = 64 * lane + lastp;
-        rv = r[lastp];
+        rv = lastv;
       }
     }
     pick = __shfl_sync(0xFFFFFFFFu, pick, src);
@@ -832,42 +874,35 @@ __device__ void finalize_chain_sample(const VerifyParams& p, int r, int base, in
   const int u_y = yv >= 0 ? yv / SPEC_UNIT : -1;
   const bool vec = p.vec_ok != 0;
   // weight of the unit holding y with y removed: a rescan of that one unit
-  double w_y = 0.0;
+  float w_y = 0.0f;
   if (u_y >= 0) {
     float v[64];
     const int e0 = u_y * SPEC_UNIT;
     const int n_el = min(SPEC_UNIT, p.vocab - e0);
     load_unit_contig<DT>(row, e0, n_el, vec, lane, v);
     const float mc = m * p.c;
-    double ls = 0.0;
+    float a0 = 0.0f, a1 = 0.0f;
 #pragma unroll
-    for (int j = 0; j < 64; ++j)
-      if (e0 + 64 * lane + j != yv && v[j] != -INFINITY) ls += (double)ex2(fmaf(v[j], p.c, -mc));
-    w_y = warp_sum_d(ls);
+    for (int j = 0; j < 64; ++j) {
+      const float w = (e0 + 64 * lane + j != yv && v[j] != -INFINITY) ? ex2(fmaf(v[j], p.c, -mc)) : 0.0f;
+      if (j & 1)
+        a1 += w;
+      else
+        a0 += w;
+    }
+    w_y = warp_sum(a0 + a1);
   }
-  auto w_plain = [&](int uu) -> double {
+  auto w_plain = [&](int uu) -> float {
     const float2 t = __ldcg(&p.ws.partial[(int64_t)slot * p.ws.units + uu]);
-    if (t.x == -INFINITY) return 0.0;
-    return (double)(t.y * ex2((t.x - m) * p.c));
+    if (t.x == -INFINITY) return 0.0f;
+    return t.y * ex2((t.x - m) * p.c);
   };
-  auto w_removed = [&](int uu) -> double { return uu == u_y ? w_y : w_plain(uu); };
-  // residual mass (unnormalised); a residual at or below 1e-30 of the row's
-  // mass falls back to p itself
-  bool remove = false;
-  double total;
-  if (yv >= 0) {
-    double ls = 0.0;
-    for (int uu = lane; uu < p.units; uu += 32) ls += w_removed(uu);
-    total = warp_sum_d(ls);
-    remove = total > 1e-30 * (double)s;
-  }
-  if (!remove) {
-    double ls = 0.0;
-    for (int uu = lane; uu < p.units; uu += 32) ls += w_plain(uu);
-    total = warp_sum_d(ls);
-  }
-  const double t = (double)u2_stop * total;
-  const Crossing cr = remove ? find_unit(p.units, t, lane, w_removed) : find_unit(p.units, t, lane, w_plain);
+  auto w_removed = [&](int uu) -> float { return uu == u_y ? w_y : w_plain(uu); };
+  // the draw removes y when the residual mass (unnormalised) exceeds 1e-30
+  // of the row's mass, else it falls back to p itself
+  Crossing cr = find_unit(p.units, u2_stop, lane, w_removed);
+  const bool remove = yv >= 0 && cr.total > 1e-30f * s;
+  if (yv >= 0 && !remove) cr = find_unit(p.units, u2_stop, lane, w_plain);
   float v[64];
   const int e0 = cr.unit * SPEC_UNIT;
   const int n_el = min(SPEC_UNIT, p.vocab - e0);
@@ -879,10 +914,10 @@ __device__ void finalize_chain_sample(const VerifyParams& p, int r, int base, in
     v[j] = ((remove && gi == yv) || v[j] == -INFINITY) ? 0.0f : ex2(fmaf(v[j], p.c, -mc));
   }
   float r_at;
-  const int pick = find_in_unit(v, cr.before, t, lane, &r_at);
+  const int pick = find_in_unit(v, cr.before, cr.t, lane, &r_at);
   if (lane == 0) {
     p.out_tokens[(int64_t)r * (p.L + 1) + n_acc] = e0 + pick;
-    if (p.dbg_resid) p.dbg_resid[r] = (float)((double)r_at / total);
+    if (p.dbg_resid) p.dbg_resid[r] = r_at / cr.total;
   }
 }
 
@@ -1310,11 +1345,14 @@ __global__ void __launch_bounds__(SPEC_CTA_THREADS) resample_kernel(VerifyParams
       float vp[64], vq[64];
       load_unit_contig<DT>(prow, e0, n_el, vec, lane, vp);
       load_unit_contig<DT>(qrow, e0, n_el, vec, lane, vq);
-      double ls = 0.0;
+      float a0 = 0.0f, a1 = 0.0f;
 #pragma unroll
-      for (int j = 0; j < 64; ++j) ls += (double)resid(vp, vq, j);
-      const double ws = warp_sum_d(ls);
-      if (lane == 0) __stcg(&p.ws.partial2[(int64_t)r * p.ws.units + u], ws);
+      for (int j = 0; j < 64; j += 2) {
+        a0 += resid(vp, vq, j);
+        a1 += resid(vp, vq, j + 1);
+      }
+      const float ws = warp_sum(a0 + a1);
+      if (lane == 0) __stcg(&p.ws.partial2[(int64_t)r * p.ws.units + u], (double)ws);
     }
     int last = 0;
     if (lane == 0) {
@@ -1325,31 +1363,17 @@ __global__ void __launch_bounds__(SPEC_CTA_THREADS) resample_kernel(VerifyParams
     last = __shfl_sync(0xFFFFFFFFu, last, 0);
     if (!last) continue;
     __threadfence();
-    // total residual mass; at or below 1e-30 the draw falls back to p
-    double Z;
-    {
-      double ls = 0.0;
-      for (int uu = lane; uu < units; uu += 32) ls += __ldcg(&p.ws.partial2[(int64_t)r * p.ws.units + uu]);
-      Z = warp_sum_d(ls);
-    }
-    const bool fallback = !(Z > 1e-30);
+    // the residual mass; at or below 1e-30 the draw falls back to p
     const int pslot = rec.prow;
-    auto w_res = [&](int uu) -> double { return __ldcg(&p.ws.partial2[(int64_t)r * p.ws.units + uu]); };
-    auto w_p = [&](int uu) -> double {
+    auto w_res = [&](int uu) -> float { return (float)__ldcg(&p.ws.partial2[(int64_t)r * p.ws.units + uu]); };
+    auto w_p = [&](int uu) -> float {
       const float2 t = __ldcg(&p.ws.partial[(int64_t)pslot * p.ws.units + uu]);
-      if (t.x == -INFINITY) return 0.0;
-      return (double)(t.y * ex2((t.x - rec.mp) * p.c) * ip);
+      if (t.x == -INFINITY) return 0.0f;
+      return t.y * ex2((t.x - rec.mp) * p.c) * ip;
     };
-    Crossing cr;
-    double tot;
-    if (fallback) {
-      tot = find_unit(units, 0.0, lane, w_p).total;
-      cr = find_unit(units, (double)rec.u2 * tot, lane, w_p);
-    } else {
-      tot = Z;
-      cr = find_unit(units, (double)rec.u2 * tot, lane, w_res);
-    }
-    const double t = (double)rec.u2 * tot;
+    Crossing cr = find_unit(units, rec.u2, lane, w_res);
+    const bool fallback = !(cr.total > 1e-30f);
+    if (fallback) cr = find_unit(units, rec.u2, lane, w_p);
     const int e0 = cr.unit * SPEC_UNIT, n_el = min(SPEC_UNIT, p.vocab - e0);
     float vp[64], vq[64], rr[64];
     load_unit_contig<DT>(prow, e0, n_el, vec, lane, vp);
@@ -1358,10 +1382,10 @@ __global__ void __launch_bounds__(SPEC_CTA_THREADS) resample_kernel(VerifyParams
     for (int j = 0; j < 64; ++j)
       rr[j] = fallback ? (vp[j] == -INFINITY ? 0.0f : ex2(fmaf(vp[j], p.c, -mpc)) * ip) : resid(vp, vq, j);
     float r_at;
-    const int pick = find_in_unit(rr, cr.before, t, lane, &r_at);
+    const int pick = find_in_unit(rr, cr.before, cr.t, lane, &r_at);
     if (lane == 0) {
       p.out_tokens[(int64_t)r * (p.L + 1) + rec.pos - 1] = e0 + pick;
-      if (p.dbg_resid) p.dbg_resid[r] = (float)((double)r_at / tot);
+      if (p.dbg_resid) p.dbg_resid[r] = r_at / cr.total;
       Record* wr = reinterpret_cast<Record*>(p.ws.record) + r;
       wr->flag = 0;
       p.ws.counter2[r] = 0u;
@@ -1389,18 +1413,15 @@ __device__ void draw_draft(const VerifyParams& p, int row, int r, int k, int slo
   const char* base = static_cast<const char*>(p.draft) + (int64_t)row * p.vocab * (DT == 1 ? 2 : 4);
   int y = 0;
   float q_at = 0.0f;
-  double total = 0.0;
+  float total = 0.0f;
   if (m != -INFINITY) {
-    auto w_plain = [&](int uu) -> double {
+    auto w_plain = [&](int uu) -> float {
       const float2 t = __ldcg(&p.ws.partial[(int64_t)slot * p.ws.units + uu]);
-      if (t.x == -INFINITY) return 0.0;
-      return (double)(t.y * ex2((t.x - m) * p.c));
+      if (t.x == -INFINITY) return 0.0f;
+      return t.y * ex2((t.x - m) * p.c);
     };
-    double ls = 0.0;
-    for (int uu = lane; uu < p.units; uu += 32) ls += w_plain(uu);
-    total = warp_sum_d(ls);
-    const double t = (double)u * total;
-    const Crossing cr = find_unit(p.units, t, lane, w_plain);
+    const Crossing cr = find_unit(p.units, u, lane, w_plain);
+    total = cr.total;
     float v[64];
     const int e0 = cr.unit * SPEC_UNIT;
     const int n_el = min(SPEC_UNIT, p.vocab - e0);
@@ -1408,13 +1429,13 @@ __device__ void draw_draft(const VerifyParams& p, int row, int r, int k, int slo
     const float mc = m * p.c;
 #pragma unroll
     for (int j = 0; j < 64; ++j) v[j] = (v[j] == -INFINITY) ? 0.0f : ex2(fmaf(v[j], p.c, -mc));
-    const int pick = find_in_unit(v, cr.before, t, lane, &q_at);
+    const int pick = find_in_unit(v, cr.before, cr.t, lane, &q_at);
     y = e0 + pick;
   }
   if (lane == 0) {
     p.out_tokens[row] = y;
     if (p.dbg_u) p.dbg_u[row] = u;
-    if (p.dbg_resid) p.dbg_resid[row] = total > 0.0 ? (float)((double)q_at / total) : 0.0f;
+    if (p.dbg_resid) p.dbg_resid[row] = total > 0.0f ? q_at / total : 0.0f;
   }
 }
 
