@@ -8,9 +8,12 @@ batch-128 mixed editing / chat configuration (context 4096, budget 256,
 V = 151936 bf16 logits, T = 0); its logits are synthetic, laid out exactly as
 the allocation asks (the target forward itself is not part of the path).
 
-Timing: W warm-up steps, then K steps between a barrier and a device
-synchronisation, CUDA events on the launching stream; three input sets rotate
-so that every step reads logits that are not in L2 (3 x 117 MB > 129 MB).
+Timing: each input set's two launches are captured as two CUDA graphs; W
+warm-up steps, then K steps of graph replays between a barrier and a device
+synchronisation, with CUDA events on the launching stream before, between and
+after the two graphs (replays keep the device queue ahead of the host, so the
+events time the kernels, not host launch gaps); three input sets rotate so
+that every step reads logits that are not in L2 (3 x 117 MB > 129 MB).
 `value` = verified draft tokens per second (sum of verify_len per step);
 rows/s, per-kernel times, the verify kernel's HBM roofline fraction, an
 end-to-end figure through host buffers, the oracle's CPU time and the SM
@@ -29,6 +32,7 @@ import os
 import statistics
 import subprocess
 import sys
+import threading
 import time
 
 import numpy as np
@@ -123,6 +127,11 @@ def config_json(cfg, extra=None):
 
 # --------------------------------------------------------------------------- clocks
 class ClockSampler:
+    """nvidia-smi samples (every 50 ms) around a timed region: the sampler waits
+    for its first sample before the region starts and for one taken after it
+    ends, and keeps the last sample before the region, every sample inside it
+    and the first after it (a region shorter than the interval is bracketed by
+    its neighbours)."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -130,31 +139,55 @@ class ClockSampler:
     def __init__(self, device_index):
         self.dev = device_index
         self.proc = None
+        self.lines = []
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            if ln.strip():
+                self._stamped.append((time.monotonic(), ln))
+
+    def _wait(self, pred, limit=5.0):
+        t = time.monotonic()
+        while not pred() and time.monotonic() - t < limit:
+            time.sleep(0.005)
 
     def __enter__(self):
+        self._stamped = []
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits", "-lms", "50",
                  "-i", str(self.dev)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
+            return self
+        self._thread = threading.Thread(target=self._read, daemon=True)
+        self._thread.start()
+        self._wait(lambda: len(self._stamped) > 0)
+        self.t0 = time.monotonic()
         return self
 
     def __exit__(self, *a):
-        self.lines = []
-        if self.proc is not None:
-            self.proc.terminate()
-            try:
-                out, _ = self.proc.communicate(timeout=5)
-            except subprocess.TimeoutExpired:
-                self.proc.kill()
-                out, _ = self.proc.communicate()
-            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+        if self.proc is None:
+            return
+        t1 = time.monotonic()
+        self._wait(lambda: any(t > t1 for t, _ in list(self._stamped)))
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            self.proc.wait()
+        self._thread.join(timeout=5)
+        st = list(self._stamped)
+        before = [x for x in st if x[0] < self.t0][-1:]
+        inside = [x for x in st if self.t0 <= x[0] <= t1]
+        after = [x for x in st if x[0] > t1][:1]
+        self.lines = [ln for _, ln in before + inside + after]
 
     def summary(self):
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in getattr(self, "lines", []):
+        for ln in self.lines:
             f = [x.strip() for x in ln.split(",")]
             if len(f) < 9:
                 continue
@@ -267,34 +300,44 @@ def make_rounds(S, torch, W, cfg, nbuf):
     return rounds, n_rows, n_tok, logits
 
 
-def round_step(S, cfg, rnd, stream, rec=None):
-    """One round: spec_draft_and_price, then spec_verify_chain (T = 0), on `stream`;
-    rec: three CUDA events around the two launches."""
-    if rec:
-        rec[0].record(stream)
-    S.spec_draft_and_price(rnd.hist, rnd.hist_len, rnd.n_min, rnd.n_max, rnd.copy_cap, rnd.g, rnd.g_len,
-                           rnd.match_n, rnd.agree, rnd.copy_len, rnd.d, rnd.c, rnd.d_len, rnd.est, cfg["lam"],
-                           cfg["budget"], cfg["max_verify_len"], cfg["policy"], True, rnd.chain, rnd.S,
-                           rnd.chain_len, rnd.source, rnd.verify_len, rnd.row_off, rnd.point_mass, rnd.ws, stream)
-    if rec:
-        rec[1].record(stream)
-    S.spec_verify_chain(rnd.logits, rnd.row_off, rnd.max_rows, rnd.chain, rnd.verify_len, rnd.out_tokens,
-                        rnd.n_accepted, rnd.n_emitted, rnd.ws, point_mass=rnd.point_mass, temperature=0.0,
-                        stream=stream)
-    if rec:
-        rec[2].record(stream)
+def capture(torch, fn):
+    """fn(stream) captured into a CUDA graph, after one run on a side stream."""
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fn(s)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn(torch.cuda.current_stream())
+    return g
 
 
-def timed_rounds(S, torch, cfg, rounds, steps, warmup, barrier=lambda: None, sampler=None):
-    """W untimed rounds, then `steps` timed rounds between a barrier and a device
-    synchronisation (rounds rotate over the input sets); returns the elapsed ms
-    and the mean per-kernel times (us) from events on the launching stream."""
+def timed_parts(torch, sets, names, steps, warmup, barrier=lambda: None, sampler=None, launches=30):
+    """`sets` holds, per input set, one function per component of a step (in
+    step order), each taking the stream to launch on.
+
+    The timed region: every set's whole step is captured as one CUDA graph; W
+    untimed steps, then `steps` timed steps between a barrier and a device
+    synchronisation, step i replaying set i % len(sets)'s graph; CUDA events
+    on the launching stream around the region.
+
+    Per-component times: for each component, one graph of `launches`
+    back-to-back launches of it, cycling over the sets, replayed after the
+    timed region and timed with events around each replay; its mean per
+    launch (the kernels' own time, with the device's gap between consecutive
+    kernels but without host launch gaps).
+
+    Returns the region's elapsed ms and the mean us per launch of each
+    component."""
     import contextlib
 
     stream = torch.cuda.current_stream()
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    nset = len(sets)
+    steps_g = [capture(torch, lambda st, fns=fns: [f(st) for f in fns]) for fns in sets]
     for i in range(warmup):
-        round_step(S, cfg, rounds[i % len(rounds)], stream)
+        steps_g[i % nset].replay()
     torch.cuda.synchronize()
     barrier()
     torch.cuda.synchronize()
@@ -302,13 +345,49 @@ def timed_rounds(S, torch, cfg, rounds, steps, warmup, barrier=lambda: None, sam
     with (sampler if sampler is not None else contextlib.nullcontext()):
         t_start.record(stream)
         for i in range(steps):
-            round_step(S, cfg, rounds[i % len(rounds)], stream, ev[i])
+            steps_g[i % nset].replay()
         t_end.record(stream)
         torch.cuda.synchronize()
     barrier()
-    comp = {k: statistics.mean(e[a].elapsed_time(e[b]) for e in ev) * 1e3
-            for k, (a, b) in {"draft_price": (0, 1), "verify": (1, 2)}.items()}
+    comp = {}
+    reps = 10
+    for j, name in enumerate(names):
+        g = capture(torch, lambda st, j=j: [sets[i % nset][j](st) for i in range(launches)])
+        for _ in range(2):
+            g.replay()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        for a, b in ev:
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+        torch.cuda.synchronize()
+        comp[name] = statistics.mean(a.elapsed_time(b) for a, b in ev) * 1e3 / launches
     return t_start.elapsed_time(t_end), comp
+
+
+def round_parts(S, torch, cfg, rnd):
+    """The two launches of one round on `rnd`'s inputs, as functions of the
+    stream: spec_draft_and_price and spec_verify_chain (T = 0)."""
+    def draft(stream):
+        S.spec_draft_and_price(rnd.hist, rnd.hist_len, rnd.n_min, rnd.n_max, rnd.copy_cap, rnd.g, rnd.g_len,
+                               rnd.match_n, rnd.agree, rnd.copy_len, rnd.d, rnd.c, rnd.d_len, rnd.est, cfg["lam"],
+                               cfg["budget"], cfg["max_verify_len"], cfg["policy"], True, rnd.chain, rnd.S,
+                               rnd.chain_len, rnd.source, rnd.verify_len, rnd.row_off, rnd.point_mass, rnd.ws,
+                               stream)
+
+    def verify(stream):
+        S.spec_verify_chain(rnd.logits, rnd.row_off, rnd.max_rows, rnd.chain, rnd.verify_len, rnd.out_tokens,
+                            rnd.n_accepted, rnd.n_emitted, rnd.ws, point_mass=rnd.point_mass, temperature=0.0,
+                            stream=stream)
+
+    return [draft, verify]
+
+
+def timed_rounds(S, torch, cfg, rounds, steps, warmup, barrier=lambda: None, sampler=None):
+    """The chain round (draft + price, verify) timed over per-round graphs, one
+    per input set; returns the elapsed ms and the mean per-kernel us."""
+    sets = [round_parts(S, torch, cfg, rnd) for rnd in rounds]
+    return timed_parts(torch, sets, ["draft_price", "verify"], steps, warmup, barrier, sampler)
 
 
 def measure_bs4(S, torch, W, steps, warmup, hbm):
@@ -361,33 +440,15 @@ def measure_bs4_probabilistic(S, torch, W, steps, warmup, hbm):
     for rnd in rounds:
         rnd.logits[:n_rows].copy_(lt)
 
-    def one(i, rec=None):
-        rnd = rounds[i % len(rounds)]
-        if rec:
-            rec[0].record(stream)
-        sample(rnd)
-        if rec:
-            rec[1].record(stream)
-        rnd.draft_and_price(cfg["lam"], cfg["budget"], cfg["max_verify_len"], cfg["policy"], False, stream)
-        if rec:
-            rec[2].record(stream)
-        rnd.verify(temperature=1.0, seed=0, step=i, stream=stream)
-        if rec:
-            rec[3].record(stream)
-
-    for i in range(warmup):
-        one(i)
-    torch.cuda.synchronize()
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
-    for i in range(steps):
-        one(i, ev[i])
-    t1.record(stream)
-    torch.cuda.synchronize()
-    ms = t0.elapsed_time(t1)
-    comp = {k: statistics.mean(e[a].elapsed_time(e[b]) for e in ev) * 1e3
-            for k, (a, b) in {"sample_drafts": (0, 1), "draft_price": (1, 2), "verify": (2, 3)}.items()}
+    # one graph per component and input set; the verification's Philox step is
+    # the set's index (the work does not depend on the uniforms' values)
+    sets = [[lambda st, rnd=rnd: S.spec_sample_drafts(rnd.draft_logits, 1.0, rnd.d, rnd.ws, seed=0, step=0,
+                                                      stream=st),
+             lambda st, rnd=rnd: rnd.draft_and_price(cfg["lam"], cfg["budget"], cfg["max_verify_len"], cfg["policy"],
+                                                     False, st),
+             lambda st, rnd=rnd, k=k: rnd.verify(temperature=1.0, seed=0, step=k, stream=st)]
+            for k, rnd in enumerate(rounds)]
+    ms, comp = timed_parts(torch, sets, ["sample_drafts", "draft_price", "verify"], steps, warmup)
     draft_bytes = B * K * V * 2
     return {"workload": "edit_bs4 probabilistic: B=4, T=1, drafts sampled on the device, extension policy, "
                         "bf16 V=151936",
@@ -420,30 +481,12 @@ def measure_long_sampled(S, torch, W, steps, warmup, hbm):
     del logits
     stream = torch.cuda.current_stream()
 
-    def one(i, rec=None):
-        rnd = rounds[i % 2]
-        if rec:
-            rec[0].record(stream)
-        rnd.draft_and_price(cfg["lam"], cfg["budget"], cfg["max_verify_len"], cfg["policy"], True, stream)
-        if rec:
-            rec[1].record(stream)
-        rnd.verify(temperature=cfg["temperature"], seed=0, step=i, row_off=ro, stream=stream)
-        if rec:
-            rec[2].record(stream)
-
-    for i in range(warmup):
-        one(i)
-    torch.cuda.synchronize()
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
-    for i in range(steps):
-        one(i, ev[i])
-    t1.record(stream)
-    torch.cuda.synchronize()
-    ms = t0.elapsed_time(t1)
-    comp = {k: statistics.mean(e[a].elapsed_time(e[b]) for e in ev) * 1e3
-            for k, (a, b) in {"draft_price": (0, 1), "verify": (1, 2)}.items()}
+    sets = [[lambda st, rnd=rnd: rnd.draft_and_price(cfg["lam"], cfg["budget"], cfg["max_verify_len"], cfg["policy"],
+                                                     True, st),
+             lambda st, rnd=rnd, k=k: rnd.verify(temperature=cfg["temperature"], seed=0, step=k, row_off=ro,
+                                                 stream=st)]
+            for k, rnd in enumerate(rounds)]
+    ms, comp = timed_parts(torch, sets, ["draft_price", "verify"], steps, warmup)
     vlen = rounds[0].verify_len.cpu().numpy()
     n_tok = int(vlen.sum())
     n_rows = int((vlen + 1).sum())
@@ -487,29 +530,10 @@ def measure_tree(S, torch, W, steps, warmup, hbm):
     ws = S.Workspace(B, rows, 1, V)
     stream = torch.cuda.current_stream()
 
-    def one(i, rec=None):
-        if rec:
-            rec[0].record(stream)
-        S.spec_build_tree(*blk, n, tok2, par2, cid2, nrow, ws_b, stream)
-        if rec:
-            rec[1].record(stream)
-        S.spec_verify_tree(sets[i % 2], node_off, rows, tok2, par2, n, path, acc, out, ws, stream)
-        if rec:
-            rec[2].record(stream)
-
-    for i in range(warmup):
-        one(i)
-    torch.cuda.synchronize()
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
-    for i in range(steps):
-        one(i, ev[i])
-    t1.record(stream)
-    torch.cuda.synchronize()
-    ms = t0.elapsed_time(t1)
-    comp = {k: statistics.mean(e[a].elapsed_time(e[b]) for e in ev) * 1e3
-            for k, (a, b) in {"build": (0, 1), "verify": (1, 2)}.items()}
+    build = lambda st: S.spec_build_tree(*blk, n, tok2, par2, cid2, nrow, ws_b, st)
+    sets = [[build, lambda st, lg=lg: S.spec_verify_tree(lg, node_off, rows, tok2, par2, n, path, acc, out, ws, st)]
+            for lg in sets]
+    ms, comp = timed_parts(torch, sets, ["build", "verify"], steps, warmup)
     accepted = int(acc.sum().item())
     return {"workload": "tree_bs32: B=32, block of 8 picks with top-4 candidates plus a 15-token n-gram chain, "
                         "trees of 16 rows, bf16 V=151936",
@@ -556,22 +580,6 @@ def run_gpu(args):
         return
     stream = torch.cuda.current_stream()
 
-    # graph-captured round time (one graph per input set)
-    graphs = []
-    for rnd in rounds:
-        graphs.append(rnd.capture(**kw))
-    torch.cuda.synchronize()
-    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    for i in range(args.warmup):
-        graphs[i % NBUF].replay()
-    g_steps = min(args.steps, 5000)
-    g0.record(stream)
-    for i in range(g_steps):
-        graphs[i % NBUF].replay()
-    g1.record(stream)
-    torch.cuda.synchronize()
-    graph_us = g0.elapsed_time(g1) * 1e3 / g_steps
-
     # end to end through the public API with host buffers: H2D of the step's inputs
     # (histories, drafter chain, confidences, logits) from pinned memory, the round,
     # D2H of the emitted tokens and counts
@@ -605,16 +613,10 @@ def run_gpu(args):
     bsz = S.Workspace(1, 1, 1, 1)
     b_out = torch.zeros(1, dtype=torch.int32, device="cuda")
     l_out = torch.zeros(1, dtype=torch.float32, device="cuda")
-    for _ in range(args.warmup):
-        S.spec_size_budget(rounds[0].S, rounds[0].chain_len, cfg["max_verify_len"], 256.0, 1.0, b_out, l_out, bsz)
-    torch.cuda.synchronize()
-    sz_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(200)]
-    for a, b in sz_ev:
-        a.record(stream)
-        S.spec_size_budget(rounds[0].S, rounds[0].chain_len, cfg["max_verify_len"], 256.0, 1.0, b_out, l_out, bsz)
-        b.record(stream)
-    torch.cuda.synchronize()
-    sizing = {"us": round(statistics.mean(a.elapsed_time(b) for a, b in sz_ev) * 1e3, 3),
+    _, sz = timed_parts(torch, [[lambda st: S.spec_size_budget(rounds[0].S, rounds[0].chain_len, cfg["max_verify_len"],
+                                                              256.0, 1.0, b_out, l_out, bsz, st)]],
+                        ["size_budget"], 3, args.warmup)
+    sizing = {"us": round(sz["size_budget"], 3),
               "slots": int(np.minimum(rounds[0].chain_len.cpu().numpy(), cfg["max_verify_len"]).sum()),
               "C0": 256.0, "p": 1.0, "b_star": int(b_out.item()), "lambda": float(l_out.item())}
 
@@ -637,7 +639,6 @@ def run_gpu(args):
         "rows_per_s": job_rows * args.steps / (ms * 1e-3),
         "verified_tokens_per_step": n_tok, "verify_rows_per_step": n_rows,
         "components_us": {k: round(v, 3) for k, v in comp.items()},
-        "graph_round_us": round(graph_us, 3),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(achieved / hbm, 4),
                      "traffic": measured_traffic("verify_rows_kernel<bf16, greedy>", WORKLOAD),
