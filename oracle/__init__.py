@@ -135,7 +135,10 @@ def _declare(L):
     L.oracle_row_argmax.argtypes = [C.c_void_p, C.c_int32, C.c_int32]
     L.oracle_row_argmax.restype = C.c_int32
     L.oracle_build_tree.argtypes = [C.c_int32, C.c_int32, C.c_int32, _i32p, _i32p, _f32p, _i32p, C.c_int32,
-                                    _i32p, _f32p, _f32p, C.c_int32, _i32p, _i32p, _i32p, _i32p, _f64p]
+                                    C.c_int32, _i32p, _f32p, _f32p, C.c_int32, _i32p, _i32p, _i32p, _i32p, _f64p]
+    L.oracle_ngram_fill.argtypes = [_i32p, C.c_int64, _i32p, C.c_int32, C.c_int32, C.c_int32, _i32p, C.c_int32,
+                                    C.c_int32, C.c_int32, C.c_int32, _i32p, _i32p, _i32p]
+    L.oracle_ngram_fill.restype = C.c_int
     L.oracle_build_tree.restype = C.c_int
     L.oracle_size_budget.argtypes = [C.c_int32, C.c_int32, _f32p, _i32p, C.c_int32, C.c_double, C.c_double,
                                      _i32p, _f64p, _f64p]
@@ -363,23 +366,52 @@ class TreeBuild:
 
 
 def build_tree(anchor, cand_tok, cand_score, ng_tok, ng_len, ng_score, ng_adj, width) -> TreeBuild:
+    """ng_tok [B x Lg] with ng_len [B] (one chain, from the anchor), or
+    [B x C x Lg] with ng_len [B x C] (chain 0 from the anchor, chain c from
+    pick c-1)."""
     cand_tok, cand_score = _c(cand_tok, np.int32), _c(cand_score, np.float32)
     B, P, Kc = cand_tok.shape
-    ng_tok = _c(ng_tok, np.int32).reshape(B, -1)
-    Lg = ng_tok.shape[1]
-    anchor, ng_len = _c(anchor, np.int32), _c(ng_len, np.int32)
+    ng_tok = _c(ng_tok, np.int32)
+    if ng_tok.ndim != 3:
+        ng_tok = ng_tok.reshape(B, 1, -1)
+    nc, Lg = ng_tok.shape[1], ng_tok.shape[2]
+    anchor, ng_len = _c(anchor, np.int32), _c(ng_len, np.int32).reshape(B, nc)
     ng_score, ng_adj = _c(ng_score, np.float32), _c(ng_adj, np.float32)
     tok = np.empty((B, width), np.int32)
     parent = np.empty((B, width), np.int32)
     cid = np.empty((B, width), np.int32)
     nr = np.empty(B, np.int32)
-    Q = np.empty((B, 1 + P * Kc + Lg))
+    Q = np.empty((B, 1 + P * Kc + nc * Lg))
     st = lib().oracle_build_tree(B, P, Kc, _p(anchor, C.c_int32), _p(cand_tok, C.c_int32),
-                                 _p(cand_score, C.c_float), _p(ng_tok, C.c_int32), Lg, _p(ng_len, C.c_int32),
+                                 _p(cand_score, C.c_float), _p(ng_tok, C.c_int32), nc, Lg, _p(ng_len, C.c_int32),
                                  _p(ng_score, C.c_float), _p(ng_adj, C.c_float), int(width), _p(tok, C.c_int32),
                                  _p(parent, C.c_int32), _p(cid, C.c_int32), _p(nr, C.c_int32),
                                  _p(Q, C.c_double))
     return TreeBuild(tok, parent, cid, nr, Q, _check(st))
+
+
+@dataclass
+class FillOut:
+    tok: np.ndarray  # [B x (P+1) x Lg], -1 past each chain's end
+    len: np.ndarray  # [B x (P+1)]
+    ev: np.ndarray   # [B x (P+1) x Lg]: copy length (> 0) or minus the follower count
+    status: int
+
+
+def ngram_fill(hist, hist_len, cand_tok, n_min, copy_cap, max_depth, Lg) -> FillOut:
+    """The n-gram chains of a candidate tree from the anchor and from each pick."""
+    hist = _c(hist, np.int32)
+    B, stride = hist.shape
+    cand_tok = _c(cand_tok, np.int32)
+    _, P, Kc = cand_tok.shape
+    hist_len = _c(hist_len, np.int32)
+    tok = np.empty((B, P + 1, Lg), np.int32)
+    ln = np.empty((B, P + 1), np.int32)
+    ev = np.empty((B, P + 1, Lg), np.int32)
+    st = lib().oracle_ngram_fill(_p(hist, C.c_int32), stride, _p(hist_len, C.c_int32), B, P, Kc,
+                                 _p(cand_tok, C.c_int32), int(n_min), int(copy_cap), int(max_depth), int(Lg),
+                                 _p(tok, C.c_int32), _p(ln, C.c_int32), _p(ev, C.c_int32))
+    return FillOut(tok, ln, ev, _check(st))
 
 
 # --------------------------------------------------------------------------- budget sizing

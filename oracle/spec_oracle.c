@@ -728,12 +728,17 @@ int oracle_verify_tree(
 /* Candidates: 0 the anchor; 1 + i Kc + k the k-th ranked candidate of      */
 /* block position i (k = 0 the pick, k >= 1 its siblings); the picks form a */
 /* spine (pick i under pick i-1, pick 0 under the anchor) and the siblings  */
-/* of position i hang from the pick's parent as leaves.  The n-gram chain   */
-/* walks from the anchor: a step whose token equals a drafter child of the  */
-/* current node marks that child agreed and moves to it (the lowest index   */
-/* on duplicates); otherwise it appends an n-gram node under the current    */
-/* node and moves to it.  At every node the chain passes through, the       */
-/* drafter children other than the agreed one are contradicted.             */
+/* of position i hang from the pick's parent as leaves.  n-gram chains: c = */
+/* 0 starts at the anchor, c >= 1 at pick c-1 (the chains branch from the   */
+/* anchor and from each pick), taken in order c = 0, 1, ...  A step whose   */
+/* token equals a drafter child of the current node marks that child agreed */
+/* and moves to it (the lowest index on duplicates); else, when an n-gram   */
+/* node with that token already hangs from the current node (an earlier     */
+/* chain's), it moves to it; else it appends an n-gram node under the       */
+/* current node and moves to it.  At every node a chain passes through, the */
+/* drafter children other than the one it moves to are contradicted.       */
+/* Reading: a candidate that one chain agrees with and another contradicts  */
+/* counts as agreed.                                                        */
 /* Scores: a drafter candidate keeps its given s, plus adj if agreed, minus */
 /* adj if contradicted (adj = max(0, logit p_src) from the caller; reading: */
 /* the agreed / contradiction bucket weights are zero, their prior); an     */
@@ -747,16 +752,18 @@ int oracle_verify_tree(
 /* ------------------------------------------------------------------------ */
 int oracle_build_tree(int32_t batch, int32_t P, int32_t Kc, const int32_t* anchor,
                       const int32_t* cand_tok, const float* cand_score,
-                      const int32_t* ng_tok, int32_t Lg, const int32_t* ng_len,
+                      const int32_t* ng_tok, int32_t n_chains, int32_t Lg, const int32_t* ng_len,
                       const float* ng_score, const float* ng_adj, int32_t width,
                       int32_t* tok, int32_t* parent, int32_t* cand_id, int32_t* n_rows,
                       double* dbg_Q) {
-  if (batch < 0 || P < 0 || Kc < 1 || Lg < 0 || width < 1) return ORACLE_ERR_ARG;
-  const int32_t cap = 1 + P * Kc + Lg;
+  if (batch < 0 || P < 0 || Kc < 1 || Lg < 0 || width < 1 || n_chains < 1 || n_chains > P + 1)
+    return ORACLE_ERR_ARG;
+  const int32_t cap = 1 + P * Kc + n_chains * Lg;
   int32_t* ctok = (int32_t*)malloc(sizeof(int32_t) * (size_t)cap);
   int32_t* cpar = (int32_t*)malloc(sizeof(int32_t) * (size_t)cap);
   int32_t* drafter = (int32_t*)malloc(sizeof(int32_t) * (size_t)cap);
-  int32_t* flag = (int32_t*)malloc(sizeof(int32_t) * (size_t)cap); /* +1 agreed, -1 contradicted */
+  int32_t* agreed = (int32_t*)malloc(sizeof(int32_t) * (size_t)cap);
+  int32_t* contra = (int32_t*)malloc(sizeof(int32_t) * (size_t)cap);
   int32_t* chosen = (int32_t*)malloc(sizeof(int32_t) * (size_t)cap);
   int32_t* order = (int32_t*)malloc(sizeof(int32_t) * (size_t)cap);
   int32_t* pos = (int32_t*)malloc(sizeof(int32_t) * (size_t)cap);
@@ -770,7 +777,7 @@ int oracle_build_tree(int32_t batch, int32_t P, int32_t Kc, const int32_t* ancho
     ctok[0] = anchor[r];
     cpar[0] = -1;
     drafter[0] = 0;
-    flag[0] = 0;
+    agreed[0] = contra[0] = 0;
     s[0] = 0.0;
     for (int32_t i = 0; i < P; ++i)
       for (int32_t k = 0; k < Kc; ++k) {
@@ -778,34 +785,46 @@ int oracle_build_tree(int32_t batch, int32_t P, int32_t Kc, const int32_t* ancho
         ctok[j] = cand_tok[((int64_t)r * P + i) * Kc + k];
         cpar[j] = (i == 0) ? 0 : 1 + (i - 1) * Kc;
         drafter[j] = 1;
-        flag[j] = 0;
+        agreed[j] = contra[j] = 0;
         s[j] = (double)cand_score[((int64_t)r * P + i) * Kc + k];
       }
-    /* the n-gram chain from the anchor */
-    int32_t gl = ng_len[r];
-    if (gl < 0 || gl > Lg) {
-      status |= ORACLE_ST_BAD_LENGTH;
-      gl = 0;
-    }
-    int32_t cur = 0;
-    for (int32_t t = 0; t < gl; ++t) {
-      const int32_t x = ng_tok[(int64_t)r * Lg + t];
-      int32_t hit = -1;
-      for (int32_t c = cur + 1; c < N; ++c)
-        if (drafter[c] && cpar[c] == cur && ctok[c] == x) {
-          hit = c;
-          break;
+    /* the n-gram chains, from the anchor (c = 0) and from pick c - 1 */
+    for (int32_t ch = 0; ch < n_chains; ++ch) {
+      int32_t gl = ng_len[(int64_t)r * n_chains + ch];
+      if (gl < 0 || gl > Lg) {
+        status |= ORACLE_ST_BAD_LENGTH;
+        gl = 0;
+      }
+      int32_t cur = (ch == 0) ? 0 : 1 + (ch - 1) * Kc;
+      for (int32_t t = 0; t < gl; ++t) {
+        const int32_t x = ng_tok[((int64_t)r * n_chains + ch) * Lg + t];
+        int32_t hit = -1;
+        for (int32_t c = cur + 1; c < N; ++c)
+          if (drafter[c] && cpar[c] == cur && ctok[c] == x) {
+            hit = c;
+            break;
+          }
+        for (int32_t c = cur + 1; c < N; ++c)
+          if (drafter[c] && cpar[c] == cur && c != hit) contra[c] = 1;
+        if (hit >= 0) {
+          agreed[hit] = 1;
+          cur = hit;
+          continue;
         }
-      for (int32_t c = cur + 1; c < N; ++c)
-        if (drafter[c] && cpar[c] == cur && c != hit) flag[c] = -1;
-      if (hit >= 0) {
-        flag[hit] = 1;
-        cur = hit;
-      } else {
+        int32_t old = -1;
+        for (int32_t c = 1 + P * Kc; c < N; ++c)
+          if (cpar[c] == cur && ctok[c] == x) {
+            old = c;
+            break;
+          }
+        if (old >= 0) {
+          cur = old;
+          continue;
+        }
         ctok[N] = x;
         cpar[N] = cur;
         drafter[N] = 0;
-        flag[N] = 0;
+        agreed[N] = contra[N] = 0;
         s[N] = (double)ng_score[r];
         cur = N;
         ++N;
@@ -813,7 +832,7 @@ int oracle_build_tree(int32_t batch, int32_t P, int32_t Kc, const int32_t* ancho
     }
     const double adj = (double)ng_adj[r];
     for (int32_t j = 1; j < N; ++j) {
-      if (drafter[j]) s[j] += (flag[j] > 0 ? adj : 0.0) - (flag[j] < 0 ? adj : 0.0);
+      if (drafter[j]) s[j] += agreed[j] ? adj : (contra[j] ? -adj : 0.0);
       if (s[j] > 80.0) s[j] = 80.0;
       if (s[j] < -80.0) s[j] = -80.0;
     }
@@ -867,13 +886,144 @@ int oracle_build_tree(int32_t batch, int32_t P, int32_t Kc, const int32_t* ancho
   free(ctok);
   free(cpar);
   free(drafter);
-  free(flag);
+  free(agreed);
+  free(contra);
   free(chosen);
   free(order);
   free(pos);
   free(s);
   free(q);
   free(Q);
+  return status;
+}
+
+/* ------------------------------------------------------------------------ */
+/* N-gram fill of the candidate tree ([AS] sec. 2.2: chains branch from the */
+/* anchor and from each pick and may run past the drafter's block; sec. 3.3 */
+/* "N-gram candidates"; the parameter table: last 3 tokens, depth 32).      */
+/*                                                                          */
+/* x = hist[r][0 .. T-1] is the request's committed text, ending with the   */
+/* anchor.  Chain c = 0 starts at the anchor (depth 0), chain c >= 1 at     */
+/* pick c-1 (depth c), with context ctx = x, pick_0, ..., pick_{c-1}.  Each */
+/* step appends one token y to the chain and to ctx:                        */
+/*  1. when the chain is reading along an earlier passage of x and the      */
+/*     passage continues (its next position is <= T-1), y is that token;   */
+/*  2. else the earlier occurrence of the current context: for every end    */
+/*     position j <= T-2 of x, l(j) = common-suffix length of x[..j] and    */
+/*     ctx, capped at copy_cap and j+1; candidates have l >= n_min, ranked  */
+/*     by (l, j) descending (the n-gram lookup's ranking); y = x[j+1] of    */
+/*     the best, and the chain reads on along x from j+2;                   */
+/*  3. else the most frequent follower of the last three tokens of ctx:     */
+/*     over j in [2, T-2] with x[j-2..j] equal to them, y = the follower    */
+/*     x[j+1] with the most occurrences, ties to the follower whose latest  */
+/*     occurrence is the most recent; the next step looks up again;         */
+/*  4. else the chain stops (nothing is proposed).                          */
+/* A chain stops at depth max_depth below the anchor (at most Lg tokens).   */
+/* ev: the evidence of each token: the length of the copy it continues (the */
+/* lookup's l, plus one per token read since, capped at copy_cap) for steps */
+/* 1-2, minus the follower's count for step 3.                              */
+/* Readings: "an earlier occurrence of the current context" takes the      */
+/* n-gram lookup's ranking with its minimum n_min (so step 3 can fire only  */
+/* when n_min > 3); a passage is read only within x.                        */
+/* ------------------------------------------------------------------------ */
+int oracle_ngram_fill(const int32_t* hist, int64_t hist_stride, const int32_t* hist_len, int32_t batch,
+                      int32_t P, int32_t Kc, const int32_t* cand_tok, int32_t n_min, int32_t copy_cap,
+                      int32_t max_depth, int32_t Lg, int32_t* ng_tok, int32_t* ng_len, int32_t* ng_ev) {
+  if (batch < 0 || P < 0 || Kc < 1 || n_min < 1 || copy_cap < n_min || max_depth < 0 || Lg < 0 ||
+      hist_stride < 0)
+    return ORACLE_ERR_ARG;
+  int status = 0;
+  const int32_t C = P + 1;
+  int32_t* ext = (int32_t*)malloc(sizeof(int32_t) * (size_t)(P + Lg + 1));
+  for (int32_t r = 0; r < batch; ++r) {
+    const int32_t* x = hist + (int64_t)r * hist_stride;
+    int32_t T = hist_len[r];
+    if (T < 0 || T > hist_stride) {
+      status |= ORACLE_ST_BAD_LENGTH;
+      T = 0;
+    }
+    for (int32_t c = 0; c < C; ++c) {
+      int32_t* out = ng_tok + ((int64_t)r * C + c) * Lg;
+      int32_t* ev = ng_ev + ((int64_t)r * C + c) * Lg;
+      for (int32_t k = 0; k < Lg; ++k) {
+        out[k] = -1;
+        ev[k] = 0;
+      }
+      int32_t cap = max_depth - c;
+      if (cap > Lg) cap = Lg;
+      int32_t n = 0;
+      /* ctx = x ++ ext[0 .. m-1]: the picks on the path, then the chain */
+      int32_t m = 0;
+      for (int32_t i = 0; i < c; ++i) ext[m++] = cand_tok[((int64_t)r * P + i) * Kc];
+      if (T < 1) cap = 0; /* no anchor */
+      int64_t q = -1;     /* the passage's next position in x, or -1 */
+      int32_t run = 0;    /* the length of the copy being continued */
+      while (n < cap) {
+        const int64_t len = (int64_t)T + m;
+#define CTX(i) ((i) < T ? x[(i)] : ext[(i) - T])
+        int32_t y = -1, e = 0, found = 0;
+        if (q >= 0 && q <= T - 1) {
+          found = 1;
+          y = x[q];
+          ++q;
+          ++run;
+          if (run > copy_cap) run = copy_cap;
+          e = run;
+        } else {
+          int32_t top_l = 0;
+          int64_t top_j = -1;
+          for (int64_t j = 0; j <= (int64_t)T - 2; ++j) {
+            int32_t l = 0;
+            while (l < copy_cap && l <= j && x[j - l] == CTX(len - 1 - l)) ++l;
+            if (l >= n_min && (l > top_l || (l == top_l && j > top_j))) {
+              top_l = l;
+              top_j = j;
+            }
+          }
+          if (top_j >= 0) {
+            found = 1;
+            y = x[top_j + 1];
+            q = top_j + 2;
+            run = top_l;
+            e = run;
+          } else if (len >= 3) {
+            /* followers of the last three tokens: counts and latest positions */
+            const int32_t a = CTX(len - 3), b = CTX(len - 2), d = CTX(len - 1);
+            int32_t best_cnt = 0;
+            int64_t best_last = -1;
+            for (int64_t j = 2; j <= (int64_t)T - 2; ++j) {
+              if (!(x[j - 2] == a && x[j - 1] == b && x[j] == d)) continue;
+              const int32_t f = x[j + 1];
+              int32_t cnt = 0;
+              int64_t last = -1;
+              for (int64_t i = 2; i <= (int64_t)T - 2; ++i)
+                if (x[i - 2] == a && x[i - 1] == b && x[i] == d && x[i + 1] == f) {
+                  ++cnt;
+                  last = i;
+                }
+              if (cnt > best_cnt || (cnt == best_cnt && last > best_last)) {
+                found = 1;
+                best_cnt = cnt;
+                best_last = last;
+                y = f;
+              }
+            }
+            q = -1;
+            run = 0;
+            e = -best_cnt;
+          }
+        }
+#undef CTX
+        if (!found) break; /* nothing proposed */
+        out[n] = y;
+        ev[n] = e;
+        ++n;
+        ext[m++] = y;
+      }
+      ng_len[(int64_t)r * C + c] = n;
+    }
+  }
+  free(ext);
   return status;
 }
 

@@ -142,17 +142,28 @@ int oracle_verify_tree(
 
 /* The candidate tree of one block-drafter round ([AS] sec. 2.2, sec. 3.1
  * Prop. 1, sec. 3.3 Eq. (6), Algorithm 1).  cand_tok / cand_score
- * [batch x P x Kc] (k = 0 the pick), ng_tok [batch x Lg] with ng_len[r]
- * tokens, ng_score / ng_adj [batch].  Outputs [batch x width]: tok, parent
- * (local, -1 at the anchor), cand_id (candidate index), unused rows -1;
- * n_rows [batch].  dbg_Q [batch x (1 + P Kc + Lg)]: Q per candidate index
- * (-1 past the last), may be NULL. */
+ * [batch x P x Kc] (k = 0 the pick), ng_tok [batch x n_chains x Lg] with
+ * ng_len[r][c] tokens (chain 0 from the anchor, chain c >= 1 from pick c-1;
+ * 1 <= n_chains <= P + 1), ng_score / ng_adj [batch].  Outputs
+ * [batch x width]: tok, parent (local, -1 at the anchor), cand_id
+ * (candidate index), unused rows -1; n_rows [batch].
+ * dbg_Q [batch x (1 + P Kc + n_chains Lg)]: Q per candidate index (-1 past
+ * the last), may be NULL. */
 int oracle_build_tree(int32_t batch, int32_t P, int32_t Kc, const int32_t* anchor,
                       const int32_t* cand_tok, const float* cand_score,
-                      const int32_t* ng_tok, int32_t Lg, const int32_t* ng_len,
+                      const int32_t* ng_tok, int32_t n_chains, int32_t Lg, const int32_t* ng_len,
                       const float* ng_score, const float* ng_adj, int32_t width,
                       int32_t* tok, int32_t* parent, int32_t* cand_id, int32_t* n_rows,
                       double* dbg_Q);
+
+/* The n-gram chains of a candidate tree ([AS] sec. 2.2, sec. 3.3): chain 0
+ * from the anchor (the last token of hist[r][0 .. hist_len[r]-1]) and chain
+ * c from pick c-1 (cand_tok[r][c-1][0]), for c = 0..P.  Outputs
+ * [batch x (P+1) x Lg]: ng_tok (-1 past the end), ng_ev (evidence: copy
+ * length > 0, or minus the follower count); ng_len [batch x (P+1)]. */
+int oracle_ngram_fill(const int32_t* hist, int64_t hist_stride, const int32_t* hist_len, int32_t batch,
+                      int32_t P, int32_t Kc, const int32_t* cand_tok, int32_t n_min, int32_t copy_cap,
+                      int32_t max_depth, int32_t Lg, int32_t* ng_tok, int32_t* ng_len, int32_t* ng_ev);
 
 /* Budget sizing ([HS] sec. 2, sec. 4.3 Eq. (2), sec. 4.4, App. F): over the
  * slots k < min(chain_len[r], max_verify_len) with survivals S [batch x L],

@@ -10,6 +10,7 @@ import pytest
 import oracle as ORC
 
 from . import test_oracle_ngram as TN
+from . import test_oracle_ngram_fill as TF
 from . import test_oracle_philox as TP
 from . import test_oracle_price as TPR
 from . import test_oracle_budget as TBU
@@ -85,7 +86,7 @@ MUTATIONS = [
      [TB.test_chain_only_tree_is_a_path_of_sigmoids, lambda o: TB.test_equal_scores_share_one_softmax_with_none(o, 4, -1.3)]),
     ("tree builder ties to the higher index", "while (at > 0 && (Q[order[at - 1]] < Q[j])) --at;",
      "while (at > 0 && (Q[order[at - 1]] <= Q[j])) --at;", [TB.test_ties_go_to_the_lower_index]),
-    ("tree builder rewards contradicted candidates", "- (flag[j] < 0 ? adj : 0.0);", "+ (flag[j] < 0 ? adj : 0.0);",
+    ("tree builder rewards contradicted candidates", "(contra[j] ? -adj : 0.0)", "(contra[j] ? adj : 0.0)",
      [TB.test_ngram_chain_agrees_with_picks_then_extends,
       TB.test_ngram_chain_that_matches_no_candidate_contradicts_them_all]),
     ("tree builder hangs siblings under their own pick",
@@ -99,6 +100,33 @@ MUTATIONS = [
     ("tree builder multiplies Q by the parent's q", "for (int32_t j = 1; j < N; ++j) Q[j] = Q[cpar[j]] * q[j];",
      "for (int32_t j = 1; j < N; ++j) Q[j] = Q[cpar[j]] * q[cpar[j] > 0 ? cpar[j] : j];",
      [TB.test_chain_only_tree_is_a_path_of_sigmoids, TB.test_ngram_chain_agrees_with_picks_then_extends]),
+    ("tree builder duplicates an n-gram node another chain made", "        if (old >= 0) {\n          cur = old;",
+     "        if (0) {\n          cur = old;", [TB.test_chains_from_picks_share_their_nodes]),
+    ("tree builder lets a contradiction beat an agreement", "agreed[j] ? adj : (contra[j] ? -adj : 0.0)",
+     "contra[j] ? -adj : (agreed[j] ? adj : 0.0)",
+     [TB.test_a_candidate_agreed_by_one_chain_and_contradicted_by_another_is_agreed]),
+    ("tree builder starts a pick's chain below the wrong pick", "int32_t cur = (ch == 0) ? 0 : 1 + (ch - 1) * Kc;",
+     "int32_t cur = (ch == 0) ? 0 : 1 + ch * Kc;",
+     [TB.test_chains_from_picks_share_their_nodes,
+      TB.test_a_candidate_agreed_by_one_chain_and_contradicted_by_another_is_agreed]),
+    # n-gram fill of the tree (AdaSpark sec. 2.2, sec. 3.3)
+    ("fill ties to the oldest occurrence", "(l == top_l && j > top_j)", "(l == top_l && j < top_j)",
+     [TF.test_equal_matches_go_to_the_most_recent]),
+    ("fill does not read on along the passage", "q = top_j + 2;", "q = -1;",
+     [TF.test_the_passage_is_read_on_even_where_a_new_lookup_would_leave_it]),
+    ("fill follower by recency only", "                  ++cnt;\n", "                  cnt = 1;\n",
+     [TF.test_follower_fallback_takes_the_most_frequent]),
+    ("fill follower ties to the oldest", "(cnt == best_cnt && last > best_last)", "(cnt == best_cnt && last < best_last)",
+     [TF.test_follower_ties_go_to_the_most_recent]),
+    ("fill counts followers of two tokens", "if (x[i - 2] == a && x[i - 1] == b && x[i] == d && x[i + 1] == f) {",
+     "if (x[i - 1] == b && x[i] == d && x[i + 1] == f) {",
+     [lambda o, s=s: TF.test_every_token_is_backed_by_its_evidence(o, s, 4, 5, 0.0) for s in range(4)]),
+    ("fill depth counted from the chain's start", "int32_t cap = max_depth - c;", "int32_t cap = max_depth;",
+     [TF.test_depth_limit_counts_from_the_anchor]),
+    ("fill forgets the picks on the path", "for (int32_t i = 0; i < c; ++i) ext[m++]",
+     "for (int32_t i = 0; i < 0; ++i) ext[m++]", [TF.test_chain_from_a_pick_continues_the_pick]),
+    ("fill passage overruns the text", "if (q >= 0 && q <= T - 1) {", "if (q >= 0 && q <= T) {",
+     [TF.test_chain_reads_along_an_earlier_passage]),
     # budget sizing (Hybrid Spark sec. 2, sec. 4.3 Eq. (2), App. F)
     ("budget forgets the one token every request emits", "double A = (double)batch, best = A / C0;",
      "double A = 0.0, best = A / C0;", [lambda o: TBU.test_budget_against_exact_rationals(o, 3)]),

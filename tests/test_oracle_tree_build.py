@@ -175,3 +175,108 @@ def test_layout_is_depth_first_with_children_in_index_order(orc, seed):
         kids = [k for k in range(n) if par[k] == j]
         assert list(cid[kids]) == sorted(cid[kids])
     assert np.all(o.tok[0, n:] == -1) and np.all(o.cand_id[0, n:] == -1)
+
+
+# ------------------------------------------------------------------ chains from the anchor and each pick
+def _chains(rows, Lg):
+    """[C x Lg] chain tokens (padded with -1) and their lengths"""
+    tok = np.full((1, len(rows), Lg), -1, np.int32)
+    for c, r in enumerate(rows):
+        tok[0, c, :len(r)] = r
+    return tok, np.array([[len(r) for r in rows]], np.int32)
+
+
+def test_chains_from_picks_share_their_nodes(orc):
+    # picks 10, 20 with siblings 11, 21.  Chain 0 agrees with both picks and adds
+    # 30; chain 1 (from pick 0) walks the same way and adds 40 below 30; chain 2
+    # (from pick 1) reuses 30 and adds 50 beside 40
+    tok = np.array([[[10, 11], [20, 21]]], np.int32)
+    ng, ln = _chains([[10, 20, 30], [20, 30, 40], [30, 50]], 4)
+    o = orc.build_tree([5], tok, np.zeros((1, 2, 2), np.float32), ng, ln, [0.0], [0.0], 32)
+    assert int((o.Q[0] >= 0).sum()) == 1 + 4 + 3
+    cid, par = _tree_of(o)
+    pc = dict(zip(cid, par))
+    assert pc[5] == 3 and pc[6] == 5 and pc[7] == 5
+    # 30 has two children, both n-gram nodes with score 0: e^0 / (1 + 2 e^0) each
+    np.testing.assert_allclose(o.Q[0, 6] / o.Q[0, 5], 1.0 / 3.0, rtol=1e-14)
+
+
+def test_a_candidate_agreed_by_one_chain_and_contradicted_by_another_is_agreed(orc):
+    adj = f32(0.9)
+    tok = np.array([[[10, 11], [20, 21]]], np.int32)
+    # chain 0: pick 10, then sibling 21 (20 contradicted); chain 1 from pick 0: 20 (21 contradicted)
+    ng, ln = _chains([[10, 21], [20]], 2)
+    o = orc.build_tree([5], tok, np.zeros((1, 2, 2), np.float32), ng, ln, [0.0], [adj], 16)
+    e = math.exp
+    q0 = e(adj) / (1 + e(adj) + e(-adj))  # pick 10 agreed, sibling 11 contradicted
+    np.testing.assert_allclose(o.Q[0, 1], q0, rtol=1e-13)
+    np.testing.assert_allclose(o.Q[0, 3], q0 * e(adj) / (1 + 2 * e(adj)), rtol=1e-13)
+    np.testing.assert_allclose(o.Q[0, 4], q0 * e(adj) / (1 + 2 * e(adj)), rtol=1e-13)
+
+
+def test_one_chain_in_the_chain_layout_equals_the_single_chain_call(orc):
+    rng = np.random.default_rng(5)
+    tok, score, chain, sg, adj = _random_case(rng, 4, 3, 6)
+    a = orc.build_tree([0], tok, score, chain, [6], sg, adj, 12)
+    b = orc.build_tree([0], tok, score, chain[:, None, :], [[6]], sg, adj, 12)
+    for f in ("tok", "parent", "cand_id", "n_rows"):
+        np.testing.assert_array_equal(getattr(a, f), getattr(b, f))
+    np.testing.assert_array_equal(a.Q, b.Q)
+
+
+def _random_chains(rng, tok, P, Lg):
+    rows = []
+    for c in range(P + 1):
+        r, pos = [], c
+        for _ in range(int(rng.integers(0, Lg + 1))):
+            if pos < P and rng.random() < 0.6:
+                r.append(int(tok[0, pos, int(rng.integers(0, tok.shape[2]))]))
+                pos += 1
+            else:
+                r.append(int(rng.integers(1000, 1004)))  # few values: chains meet again
+                pos = P
+        rows.append(r)
+    return _chains(rows, Lg)
+
+
+@pytest.mark.parametrize("seed", range(10))
+def test_proposition_1_by_brute_force_with_chains_from_every_pick(orc, seed):
+    rng = np.random.default_rng(200 + seed)
+    P, Kc, Lg = 2, 2, 2
+    tok, score = _block(rng, P, Kc)
+    ng, ln = _random_chains(rng, tok, P, Lg)
+    sg, adj = [float(rng.normal(0, 1))], [float(abs(rng.normal(0, 1)))]
+    full = orc.build_tree([0], tok, score, ng, ln, sg, adj, 64)
+    N = int((full.Q[0] >= 0).sum())
+    cid_full, par_full = _tree_of(full)
+    cpar = dict(zip(cid_full, par_full))
+    assert sorted(cid_full) == list(range(N))
+    Q = full.Q[0, :N]
+    prev = None
+    for width in range(2, min(N, 9) + 1):
+        o = orc.build_tree([0], tok, score, ng, ln, sg, adj, width)
+        got = set(_tree_of(o)[0]) - {0}
+        assert all(cpar[c] in got | {0} for c in got)
+        best = max(sum(Q[list(sub)]) for sub in itertools.combinations(range(1, N), width - 1)
+                   if all(cpar[c] in set(sub) | {0} for c in sub))
+        assert sum(Q[list(got)]) >= best - 1e-15
+        if prev is not None:
+            assert prev <= got
+        prev = got
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_layout_with_chains_from_every_pick(orc, seed):
+    rng = np.random.default_rng(300 + seed)
+    P, Kc, Lg = 5, 3, 6
+    tok, score = _block(rng, P, Kc)
+    ng, ln = _random_chains(rng, tok, P, Lg)
+    o = orc.build_tree([0], tok, score, ng, ln, [0.3], [0.5], 20)
+    n = int(o.n_rows[0])
+    par, cid = o.parent[0, :n], o.cand_id[0, :n]
+    assert par[0] == -1 and all(0 <= par[j] < j for j in range(1, n))
+    for j in range(n):
+        kids = [k for k in range(n) if par[k] == j]
+        assert list(cid[kids]) == sorted(cid[kids])
+        assert len({int(o.tok[0, k]) for k in kids if cid[k] > P * Kc}) == \
+            len([k for k in kids if cid[k] > P * Kc])  # n-gram children carry distinct tokens
