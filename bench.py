@@ -545,6 +545,64 @@ def measure_tree(S, torch, W, steps, warmup, hbm):
             "l2": "2 rotating logit sets (2 x 156 MB > L2)"}
 
 
+def measure_tree_fill(S, torch, W, steps, warmup, hbm):
+    """The filled tree round, batch 32 (bf16 V = 151936): n-gram chains from the
+    anchor and from each of the 8 picks made on the device from the requests'
+    4096-token texts (spec_ngram_fill), the candidate tree built from the block
+    and the 9 chains per request (spec_build_tree), then greedy tree
+    verification of 16 rows per request (spec_verify_tree); two logit sets
+    (2 x 156 MB > L2)."""
+    cfg = W.tree_fill_bs32(width=16)
+    B, V, n, P = cfg["B"], cfg["V"], cfg["width"], cfg["P"]
+    dev = lambda a: torch.as_tensor(np.ascontiguousarray(a)).to("cuda")
+    hist, hist_len, cand_tok = dev(cfg["hist"]), dev(cfg["hist_len"]), dev(cfg["cand_tok"])
+    blk = [dev(cfg[k]) for k in ("anchor", "cand_tok", "cand_score")]
+    sc = [dev(cfg[k]) for k in ("ng_score", "ng_adj")]
+    i32 = dict(dtype=torch.int32, device="cuda")
+    ng_tok, ng_ev = (torch.empty((B, P + 1, cfg["Lg"]), **i32) for _ in range(2))
+    ng_len = torch.empty((B, P + 1), **i32)
+    tok2, par2, cid2 = (torch.empty((B, n), **i32) for _ in range(3))
+    nrow = torch.empty(B, **i32)
+    ws_b = S.Workspace(B, 1, 1, 1)
+
+    def fill(st):
+        S.spec_ngram_fill(hist, hist_len, cand_tok, cfg["n_min"], cfg["copy_cap"], cfg["max_depth"], ng_tok, ng_len,
+                          ng_ev, ws_b, st)
+
+    def build(st):
+        S.spec_build_tree(*blk, ng_tok, ng_len, *sc, n, tok2, par2, cid2, nrow, ws_b, st)
+
+    fill(None)
+    build(None)
+    torch.cuda.synchronize()
+    node_off_h, tok_h, par_h = W.flatten_trees(tok2.cpu().numpy(), par2.cpu().numpy(), nrow.cpu().numpy())
+    rows = int(node_off_h[-1])
+    logits, _ = W.tree_logits(node_off_h, tok_h, par_h, V)
+    lt = torch.from_numpy(logits.view(np.int16)).view(torch.bfloat16).to("cuda")
+    lsets = [lt, lt.clone()]
+    node_off = dev(node_off_h)
+    assert np.all(nrow.cpu().numpy() == n)
+    path, out = torch.empty((B, n), **i32), torch.empty((B, n), **i32)
+    acc = torch.empty(B, **i32)
+    ws = S.Workspace(B, rows, 1, V)
+    sets = [[fill, build, lambda st, lg=lg: S.spec_verify_tree(lg, node_off, rows, tok2, par2, n, path, acc, out,
+                                                                ws, st)]
+            for lg in lsets]
+    ms, comp = timed_parts(torch, sets, ["fill", "build", "verify"], steps, warmup)
+    accepted = int(acc.sum().item())
+    chain_tokens = int(ng_len.sum().item())
+    return {"workload": "tree_fill_bs32: B=32, 4096-token texts, n-gram chains from the anchor and 8 picks "
+                        "(passage copy >= 4 tokens, else the most frequent follower of 3; depth 32), block of 8 "
+                        "picks with top-4 candidates, trees of 16 rows, bf16 V=151936",
+            "tree_rows_per_s": rows * steps / (ms * 1e-3), "accepted_tokens_per_s": accepted * steps / (ms * 1e-3),
+            "ms_per_step": ms / steps, "steps": steps, "rows_per_step": rows, "accepted_per_step": accepted,
+            "chain_tokens_per_step": chain_tokens,
+            "components_us": {k: round(v, 3) for k, v in comp.items()},
+            "verify_roofline_frac": round(rows * V * 2 / (comp["verify"] * 1e-6) / 1e9 / hbm, 4),
+            "status_clean": int(ws.status()) == 0 and int(ws_b.status()) == 0,
+            "l2": "2 rotating logit sets (2 x 156 MB > L2)"}
+
+
 def run_gpu(args):
     import torch
 
@@ -625,6 +683,7 @@ def run_gpu(args):
     bs4_prob = measure_bs4_probabilistic(S, torch, W, min(args.steps, 3000), args.warmup, hbm)
     long_sampled = measure_long_sampled(S, torch, W, min(args.steps, 1000), args.warmup, hbm)
     tree = measure_tree(S, torch, W, min(args.steps, 2000), args.warmup, hbm)
+    tree_fill = measure_tree_fill(S, torch, W, min(args.steps, 2000), args.warmup, hbm)
     if rank != 0:
         return
     verify_us = comp["verify"]
@@ -653,6 +712,7 @@ def run_gpu(args):
         "bs4_probabilistic": bs4_prob,
         "long_bs64_sampled": long_sampled,
         "tree_bs32": tree,
+        "tree_fill_bs32": tree_fill,
         "budget_sizing": sizing,
         "status_clean": ok,
     }

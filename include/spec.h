@@ -91,12 +91,16 @@ typedef enum {
 #define SPEC_DEV_BAD_VALUE 0x10u /* a confidence outside [0,1] (clamped), a feature
                                     outside the estimator table (h = 0)             */
 #define SPEC_DEV_TIMEOUT 0x20u   /* a bounded wait on an asynchronous copy ran out  */
+#define SPEC_DEV_OVERFLOW 0x40u  /* a fixed on-chip table was too small: the n-gram
+                                    fill met more than 2048 distinct followers of
+                                    one three-token context (that chain stops)     */
 
 /* limits */
 #define SPEC_MAX_L 31            /* longest chain (L) and n-gram proposal           */
 #define SPEC_MAX_N 32            /* largest n-gram match length n_max               */
 #define SPEC_MAX_PRICE_BATCH 1024
 #define SPEC_MAX_TREE_NODES 256
+#define SPEC_MAX_TREE_CANDIDATES 512 /* the builder's 1 + P Kc + n_chains Lg      */
 #define SPEC_MAX_COPY_CAP 4096
 
 const char* spec_status_string(spec_status s);
@@ -258,6 +262,43 @@ spec_status spec_draft_and_price(
     uint8_t* point_mass, const spec_workspace* ws, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------
+ * spec_ngram_fill: the n-gram chains of a candidate tree ([AS] sec. 2.2, the
+ * chains that branch from the anchor and from each pick and may run past the
+ * drafter's block; sec. 3.3 "N-gram candidates"; the parameter table's
+ * three-token follower context and 32-token depth).  Its output is
+ * spec_build_tree's chain input with n_chains = P + 1.
+ *
+ * Per request r the committed text x = hist[r][0 .. hist_len[r]-1] (row
+ * stride hist_stride) ends with the anchor.  Chain 0 starts at the anchor
+ * and chain c >= 1 at pick c-1 = cand_tok[r][c-1][0] (cand_tok
+ * [batch x P x Kc], the builder's block), with context ctx = x followed by
+ * pick_0 .. pick_{c-1}.  Each step appends one token y to the chain and ctx:
+ *   1. while reading along an earlier passage whose next position is
+ *      <= T-1, y is that token;
+ *   2. else, over end positions j <= T-2 with l(j) = common-suffix length of
+ *      x[..j] and ctx (capped at copy_cap and j+1) >= n_min, the largest
+ *      (l, j): y = x[j+1], and the chain reads on along x from j+2;
+ *   3. else the most frequent follower x[j+1] of ctx's last three tokens over
+ *      j in [2, T-2] (ties: the follower seen most recently);
+ *   4. else the chain stops.
+ * A chain stops at depth max_depth below the anchor (pick c-1 sits at depth
+ * c), so chain c holds at most min(Lg, max_depth - c) tokens.
+ * Outputs: ng_tok [batch x (P+1) x Lg] (-1 past each chain), ng_len
+ * [batch x (P+1)], ng_ev [batch x (P+1) x Lg] (each token's evidence: the
+ * length of the copy it continues, capped at copy_cap, for steps 1-2; minus
+ * the follower's count for step 3; 0 past the chain).
+ * hist_len[r] outside [0, hist_stride] sets SPEC_DEV_BAD_LENGTH (no chains);
+ * more than 2048 distinct followers of one context set SPEC_DEV_OVERFLOW and
+ * stop that chain.  Limits: P >= 0, Kc >= 1, 1 <= n_min <= copy_cap,
+ * max_depth >= 0, Lg >= 0, P + Lg <= 4096, batch <= 65535.  The workspace
+ * serves only its status word.
+ * ------------------------------------------------------------------------ */
+spec_status spec_ngram_fill(const int32_t* hist, int64_t hist_stride, const int32_t* hist_len, int32_t batch,
+                            int32_t P, int32_t Kc, const int32_t* cand_tok, int32_t n_min, int32_t copy_cap,
+                            int32_t max_depth, int32_t Lg, int32_t* ng_tok, int32_t* ng_len, int32_t* ng_ev,
+                            const spec_workspace* ws, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
  * spec_build_tree: the candidate tree of one block-drafter round ([AS]
  * sec. 2.2 tree shape; sec. 3.3 n-gram candidates and Eq. (6); sec. 3.1 and
  * Proposition 1, best-first order; Algorithm 1, the first n-1 nodes laid out
@@ -266,17 +307,21 @@ spec_status spec_draft_and_price(
  * Per request r: anchor[r], the committed token the tree hangs from; a block
  * of P positions with Kc ranked candidates each, cand_tok / cand_score
  * [batch x P x Kc] (k = 0 the drafter's pick, k >= 1 its siblings; the score
- * s of Eq. (6), from the caller's acceptance model); an n-gram chain from the
- * anchor, ng_tok [batch x Lg] with ng_len[r] tokens; ng_score[r], the score of
- * an n-gram node; ng_adj[r] = max(0, logit p_src), added to an agreed drafter
- * candidate's score and subtracted from a contradicted one's.
+ * s of Eq. (6), from the caller's acceptance model); n_chains n-gram chains,
+ * ng_tok [batch x n_chains x Lg] with ng_len[r][c] tokens, chain 0 from the
+ * anchor and chain c >= 1 from pick c-1 (1 <= n_chains <= P + 1; the layout
+ * spec_ngram_fill writes); ng_score[r], the score of an n-gram node;
+ * ng_adj[r] = max(0, logit p_src), added to an agreed drafter candidate's
+ * score and subtracted from a contradicted one's.
  * Candidates: 0 the anchor; 1 + i Kc + k position i's k-th candidate; then
- * the n-gram nodes in chain order.  Pick i hangs from pick i-1 (pick 0 from
- * the anchor); the siblings of position i hang from the pick's parent, as
- * leaves.  The chain walks from the anchor: a step equal to a drafter child
- * of the current node marks that child agreed (lowest index on duplicates)
- * and moves to it, else it appends an n-gram node and moves to it; the other
- * drafter children of every node it passes through are contradicted.
+ * the n-gram nodes in the order the chains make them.  Pick i hangs from
+ * pick i-1 (pick 0 from the anchor); the siblings of position i hang from
+ * the pick's parent, as leaves.  The chains walk in order c = 0, 1, ...: a
+ * step equal to a drafter child of the current node marks that child agreed
+ * (lowest index on duplicates) and moves to it; else a step equal to an
+ * n-gram child already there moves to it; else it appends an n-gram node and
+ * moves to it.  The other drafter children of every node a chain passes
+ * through are contradicted, unless some chain agrees with them.
  * Scores are clamped to [-80, 80].
  * q_j = e^{s_j} / (1 + sum over the children c of parent(j) of e^{s_c}),
  * Q_j = Q_parent(j) q_j (fp64); order: Q descending, ties to the lower index.
@@ -284,15 +329,16 @@ spec_status spec_draft_and_price(
  * order, depth-first with children in increasing candidate index: tok,
  * parent (row of the parent, -1 at the anchor), cand_id (candidate index);
  * rows past n_rows[r] = min(width, number of candidates) are -1.
- * ng_len[r] outside [0, Lg] sets SPEC_DEV_BAD_LENGTH (no chain).
- * Limits: Kc >= 1, P >= 0, Lg >= 0, 1 + P Kc + Lg <= SPEC_MAX_TREE_NODES,
- * 1 <= width <= SPEC_MAX_TREE_NODES.  The workspace serves only its status word.
+ * ng_len[r][c] outside [0, Lg] sets SPEC_DEV_BAD_LENGTH (that chain is empty).
+ * Limits: Kc >= 1, P >= 0, Lg >= 0, 1 + P Kc + n_chains Lg <=
+ * SPEC_MAX_TREE_CANDIDATES, 1 <= width <= SPEC_MAX_TREE_NODES.  The workspace
+ * serves only its status word.
  * ------------------------------------------------------------------------ */
 spec_status spec_build_tree(int32_t batch, int32_t P, int32_t Kc, const int32_t* anchor,
                             const int32_t* cand_tok, const float* cand_score, const int32_t* ng_tok,
-                            int32_t Lg, const int32_t* ng_len, const float* ng_score, const float* ng_adj,
-                            int32_t width, int32_t* tok, int32_t* parent, int32_t* cand_id, int32_t* n_rows,
-                            const spec_workspace* ws, cudaStream_t stream);
+                            int32_t n_chains, int32_t Lg, const int32_t* ng_len, const float* ng_score,
+                            const float* ng_adj, int32_t width, int32_t* tok, int32_t* parent, int32_t* cand_id,
+                            int32_t* n_rows, const spec_workspace* ws, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------
  * spec_sample_drafts: probabilistic drafting ([HS] sec. 4.5 and App. H;

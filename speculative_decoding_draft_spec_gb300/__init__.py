@@ -24,7 +24,7 @@ from ._build import build
 
 __all__ = [
     "build", "load", "Workspace", "EstimatorTable", "SpecError", "spec_ngram_propose",
-    "spec_price_and_allocate", "spec_price_and_allocate_static", "spec_draft_and_price", "spec_verify_chain", "spec_verify_tree", "spec_build_tree", "spec_size_budget", "spec_sample_drafts", "POLICY",
+    "spec_price_and_allocate", "spec_price_and_allocate_static", "spec_draft_and_price", "spec_verify_chain", "spec_verify_tree", "spec_build_tree", "spec_ngram_fill", "spec_size_budget", "spec_sample_drafts", "POLICY",
     "DEV_BITS",
 ]
 
@@ -32,7 +32,7 @@ SPEC_OK, SPEC_ERR_INVALID_ARG, SPEC_ERR_CUDA, SPEC_ERR_UNSUPPORTED, SPEC_ERR_WOR
 SPEC_F32, SPEC_BF16 = 0, 1
 POLICY = {"proposed": 0, "ngram_first": 1, "extension": 2, "model_only": 3, "ngram_only": 4}
 DEV_BITS = {"bad_token": 0x1, "nonfinite": 0x2, "bad_tree": 0x4, "bad_length": 0x8,
-            "bad_value": 0x10, "timeout": 0x20}
+            "bad_value": 0x10, "timeout": 0x20, "overflow": 0x40}
 
 
 class SpecError(RuntimeError):
@@ -89,8 +89,10 @@ SIGNATURES = {
                               _vp, _vp, _vp, _vp, _WSP, _vp], _i32),
     "spec_verify_chain": ([_i32, _i32, _i32, _vp, _vp, _i32, _vp, _i32, _vp, _i32, _vp, _vp, _f32,
                            _u64, _u64, _vp, _vp, _vp, _vp, _vp, _vp, _WSP, _vp], _i32),
-    "spec_build_tree": ([_i32, _i32, _i32, _vp, _vp, _vp, _vp, _i32, _vp, _vp, _vp, _i32, _vp, _vp, _vp, _vp,
-                         _WSP, _vp], _i32),
+    "spec_build_tree": ([_i32, _i32, _i32, _vp, _vp, _vp, _vp, _i32, _i32, _vp, _vp, _vp, _i32, _vp, _vp, _vp,
+                         _vp, _WSP, _vp], _i32),
+    "spec_ngram_fill": ([_vp, _i64, _vp, _i32, _i32, _i32, _vp, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _WSP, _vp],
+                        _i32),
     "spec_size_budget": ([_i32, _i32, _vp, _vp, _i32, C.c_double, C.c_double, _vp, _vp, _WSP, _vp], _i32),
     "spec_sample_drafts": ([_i32, _i32, _i32, _i32, _vp, _f32, _u64, _u64, _vp, _vp, _vp, _WSP, _vp], _i32),
     "spec_verify_tree": ([_i32, _i32, _i32, _vp, _vp, _i32, _vp, _vp, _i32, _vp, _vp, _vp, _WSP, _vp],
@@ -286,13 +288,29 @@ def spec_verify_tree(logits, node_off, max_rows, tok, parent, max_nodes, path, a
 
 def spec_build_tree(anchor, cand_tok, cand_score, ng_tok, ng_len, ng_score, ng_adj, width, tok, parent, cand_id,
                     n_rows, ws: Workspace, stream=None):
-    """cand_tok / cand_score [B x P x Kc], ng_tok [B x Lg]; outputs tok / parent /
-    cand_id [B x width], n_rows [B] (all int32 device tensors)."""
+    """cand_tok / cand_score [B x P x Kc]; ng_tok [B x Lg] with ng_len [B] (one
+    chain, from the anchor) or [B x C x Lg] with ng_len [B x C] (chain 0 from
+    the anchor, chain c from pick c-1); outputs tok / parent / cand_id
+    [B x width], n_rows [B] (all int32 device tensors)."""
     B, P, Kc = cand_tok.shape
-    Lg = ng_tok.shape[1]
+    nc, Lg = (ng_tok.shape[1], ng_tok.shape[2]) if ng_tok.dim() == 3 else (1, ng_tok.shape[1])
     _check("spec_build_tree", load().spec_build_tree(
-        B, P, Kc, _ptr(anchor), _ptr(cand_tok), _ptr(cand_score), _ptr(ng_tok), Lg, _ptr(ng_len), _ptr(ng_score),
-        _ptr(ng_adj), int(width), _ptr(tok), _ptr(parent), _ptr(cand_id), _ptr(n_rows), ws.ref, _stream(stream)))
+        B, P, Kc, _ptr(anchor), _ptr(cand_tok), _ptr(cand_score), _ptr(ng_tok), nc, Lg, _ptr(ng_len),
+        _ptr(ng_score), _ptr(ng_adj), int(width), _ptr(tok), _ptr(parent), _ptr(cand_id), _ptr(n_rows), ws.ref,
+        _stream(stream)))
+
+
+def spec_ngram_fill(hist, hist_len, cand_tok, n_min, copy_cap, max_depth, ng_tok, ng_len, ng_ev, ws: Workspace,
+                    stream=None):
+    """The n-gram chains of a candidate tree from the anchor and from each pick:
+    hist [B x stride], hist_len [B], cand_tok [B x P x Kc]; outputs ng_tok /
+    ng_ev [B x (P+1) x Lg], ng_len [B x (P+1)] (all int32 device tensors)."""
+    B, stride = hist.shape
+    P, Kc = cand_tok.shape[1], cand_tok.shape[2]
+    Lg = ng_tok.shape[2]
+    _check("spec_ngram_fill", load().spec_ngram_fill(
+        _ptr(hist), stride, _ptr(hist_len), B, P, Kc, _ptr(cand_tok), int(n_min), int(copy_cap), int(max_depth), Lg,
+        _ptr(ng_tok), _ptr(ng_len), _ptr(ng_ev), ws.ref, _stream(stream)))
 
 
 def spec_size_budget(S, chain_len, max_verify_len, C0, p, out_budget, out_lambda, ws: Workspace, stream=None):

@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libspecgb.so")
-SOURCES = ["api.cu", "ngram.cu", "price.cu", "verify.cu", "tree.cu", "budget.cu"]
+SOURCES = ["api.cu", "ngram.cu", "price.cu", "verify.cu", "tree.cu", "budget.cu", "fill.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -36,9 +36,14 @@ cudaError_t spec_launch_price(int32_t batch, int32_t K, int32_t L, const int32_t
                               uint32_t* status, uint32_t* keys, cudaStream_t stream);
 cudaError_t spec_launch_build_tree(int32_t batch, int32_t P, int32_t Kc, const int32_t* anchor,
                                    const int32_t* cand_tok, const float* cand_score, const int32_t* ng_tok,
-                                   int32_t Lg, const int32_t* ng_len, const float* ng_score, const float* ng_adj,
+                                   int32_t n_chains, int32_t Lg, const int32_t* ng_len, const float* ng_score,
+                                   const float* ng_adj,
                                    int32_t width, int32_t* tok, int32_t* parent, int32_t* cand_id,
                                    int32_t* n_rows, uint32_t* status, cudaStream_t stream);
+cudaError_t spec_launch_ngram_fill(const int32_t* hist, int64_t hist_stride, const int32_t* hist_len,
+                                   int32_t batch, int32_t P, int32_t Kc, const int32_t* cand_tok, int32_t n_min,
+                                   int32_t copy_cap, int32_t max_depth, int32_t Lg, int32_t* ng_tok,
+                                   int32_t* ng_len, int32_t* ng_ev, uint32_t* status, cudaStream_t stream);
 cudaError_t spec_launch_size_budget(int32_t batch, int32_t L, const float* S, const int32_t* chain_len,
                                     int32_t mvl, double C0, double p, int32_t* out_budget, float* out_lambda,
                                     uint32_t* status, cudaStream_t stream);
@@ -265,20 +270,39 @@ spec_status spec_price_and_allocate_static(
 
 spec_status spec_build_tree(int32_t batch, int32_t P, int32_t Kc, const int32_t* anchor,
                             const int32_t* cand_tok, const float* cand_score, const int32_t* ng_tok,
-                            int32_t Lg, const int32_t* ng_len, const float* ng_score, const float* ng_adj,
-                            int32_t width, int32_t* tok, int32_t* parent, int32_t* cand_id, int32_t* n_rows,
-                            const spec_workspace* ws, cudaStream_t stream) {
-  if (batch < 0 || P < 0 || Kc < 1 || Lg < 0 || width < 1) return SPEC_ERR_INVALID_ARG;
-  if ((int64_t)1 + (int64_t)P * Kc + Lg > SPEC_MAX_TREE_NODES || width > SPEC_MAX_TREE_NODES)
+                            int32_t n_chains, int32_t Lg, const int32_t* ng_len, const float* ng_score,
+                            const float* ng_adj, int32_t width, int32_t* tok, int32_t* parent, int32_t* cand_id,
+                            int32_t* n_rows, const spec_workspace* ws, cudaStream_t stream) {
+  if (batch < 0 || P < 0 || Kc < 1 || Lg < 0 || width < 1 || n_chains < 1 || n_chains > P + 1)
+    return SPEC_ERR_INVALID_ARG;
+  if ((int64_t)1 + (int64_t)P * Kc + (int64_t)n_chains * Lg > SPEC_MAX_TREE_CANDIDATES ||
+      width > SPEC_MAX_TREE_NODES)
     return SPEC_ERR_UNSUPPORTED;
   if (batch > 0 && (!anchor || !ng_len || !ng_score || !ng_adj || !tok || !parent || !cand_id || !n_rows ||
                     (P > 0 && (!cand_tok || !cand_score)) || (Lg > 0 && !ng_tok)))
     return SPEC_ERR_INVALID_ARG;
   if (!ws_ok(ws)) return SPEC_ERR_WORKSPACE;
   if (batch == 0) return SPEC_OK;
-  return from_cuda(spec_launch_build_tree(batch, P, Kc, anchor, cand_tok, cand_score, ng_tok, Lg, ng_len,
+  return from_cuda(spec_launch_build_tree(batch, P, Kc, anchor, cand_tok, cand_score, ng_tok, n_chains, Lg, ng_len,
                                           ng_score, ng_adj, width, tok, parent, cand_id, n_rows, status_of(ws),
                                           stream));
+}
+
+spec_status spec_ngram_fill(const int32_t* hist, int64_t hist_stride, const int32_t* hist_len, int32_t batch,
+                            int32_t P, int32_t Kc, const int32_t* cand_tok, int32_t n_min, int32_t copy_cap,
+                            int32_t max_depth, int32_t Lg, int32_t* ng_tok, int32_t* ng_len, int32_t* ng_ev,
+                            const spec_workspace* ws, cudaStream_t stream) {
+  if (batch < 0 || hist_stride < 0 || P < 0 || Kc < 1 || n_min < 1 || copy_cap < n_min || max_depth < 0 ||
+      Lg < 0)
+    return SPEC_ERR_INVALID_ARG;
+  if ((int64_t)P + Lg > 4096 || batch > 65535) return SPEC_ERR_UNSUPPORTED;
+  if (batch > 0 && (!hist_len || !ng_len || (hist_stride > 0 && !hist) || (P > 0 && !cand_tok) ||
+                    (Lg > 0 && (!ng_tok || !ng_ev))))
+    return SPEC_ERR_INVALID_ARG;
+  if (!ws_ok(ws)) return SPEC_ERR_WORKSPACE;
+  if (batch == 0) return SPEC_OK;
+  return from_cuda(spec_launch_ngram_fill(hist, hist_stride, hist_len, batch, P, Kc, cand_tok, n_min, copy_cap,
+                                          max_depth, Lg, ng_tok, ng_len, ng_ev, status_of(ws), stream));
 }
 
 spec_status spec_size_budget(int32_t batch, int32_t L, const float* S, const int32_t* chain_len,

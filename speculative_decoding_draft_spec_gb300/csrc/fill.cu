@@ -1,0 +1,224 @@
+// fill.cu -- the n-gram chains of a candidate tree.
+//
+// AdaSpark sec. 2.2 (n-gram chains branch from the anchor and from each pick
+// and may run past the drafter's block) and sec. 3.3 ("N-gram candidates"),
+// with the parameter table's three-token follower context and 32-token depth:
+// for request r with committed text x = hist[r][0 .. T-1] (its last token the
+// anchor), chain c = 0 starts at the anchor and chain c >= 1 at pick c-1, with
+// context ctx = x, pick_0 .. pick_{c-1}.  Each step appends one token y:
+//   1. reading along an earlier passage whose next position is <= T-1: y is
+//      that token;
+//   2. else the earlier occurrence of ctx: over end positions j <= T-2,
+//      l(j) = common-suffix length of x[..j] and ctx capped at copy_cap and
+//      j+1; among l >= n_min the largest (l, j); y = x[j+1] and the chain
+//      reads on from j+2;
+//   3. else the most frequent follower x[j+1] of the last three tokens of ctx
+//      over j in [2, T-2], ties to the follower seen most recently;
+//   4. else the chain stops.
+// A chain ends at depth max_depth below the anchor (Lg tokens at most).  ev
+// holds each token's evidence: the length of the copy it continues (capped at
+// copy_cap) for steps 1-2, minus the follower's count for step 3.
+//
+// GB300 layout: one CTA of 256 threads per (chain, request).  The chain's
+// steps are sequential; a lookup is one block-wide pass over the text (each
+// thread tests its end positions, extends the matches it finds, and the
+// block takes the max of (l << 32 | j)), a follower step one pass that counts
+// followers in a shared-memory hash table (atomics) and one max over it.  A
+// passage is read from a shared-memory copy of its next 64 tokens.  All
+// threads carry the same chain state, so every branch is block-uniform.
+#include "common.cuh"
+
+namespace spec {
+
+#define FL_THREADS 256
+#define FL_HASH 2048  // follower table entries (a power of two)
+#define FL_PBUF 64    // passage tokens staged at a time
+
+struct FillParams {
+  const int32_t* hist;
+  int64_t stride;
+  const int32_t* hist_len;
+  int32_t P, Kc;
+  const int32_t* cand_tok;
+  int32_t n_min, copy_cap, max_depth, Lg;
+  int32_t* ng_tok;
+  int32_t* ng_len;
+  int32_t* ng_ev;
+  uint32_t* status;
+};
+
+__device__ __forceinline__ unsigned long long block_max_u64(unsigned long long v, unsigned long long* s_red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const unsigned long long t = __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    v = t > v ? t : v;
+  }
+  if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  unsigned long long m = 0;
+#pragma unroll
+  for (int w = 0; w < FL_THREADS / 32; ++w) m = s_red[w] > m ? s_red[w] : m;
+  return m;
+}
+
+__global__ void __launch_bounds__(FL_THREADS) ngram_fill_kernel(FillParams p) {
+  extern __shared__ int32_t s_ext[];  // [P + Lg]: the picks on the path, then the chain
+  __shared__ unsigned long long s_key[FL_HASH];  // (1 << 32) | follower, 0 = empty
+  __shared__ int32_t s_cnt[FL_HASH], s_last[FL_HASH];
+  __shared__ unsigned long long s_red[FL_THREADS / 32];
+  __shared__ int32_t s_pbuf[FL_PBUF];
+  __shared__ int32_t s_overflow;
+  const int tid = threadIdx.x;
+  const int c = blockIdx.x, r = blockIdx.y;
+  const int C = p.P + 1;
+  const int32_t* x = p.hist + (int64_t)r * p.stride;
+  int32_t T = p.hist_len[r];
+  if (T < 0 || (int64_t)T > p.stride) {
+    if (tid == 0 && c == 0) set_status(p.status, SPEC_DEV_BAD_LENGTH);
+    T = 0;
+  }
+  int32_t cap = p.max_depth - c;
+  if (cap > p.Lg) cap = p.Lg;
+  if (T < 1 || cap < 0) cap = 0;  // no anchor
+  for (int i = tid; i < c; i += FL_THREADS) s_ext[i] = p.cand_tok[((int64_t)r * p.P + i) * p.Kc];
+  if (tid == 0) s_overflow = 0;
+  int32_t* out = p.ng_tok + ((int64_t)r * C + c) * p.Lg;
+  int32_t* ev = p.ng_ev + ((int64_t)r * C + c) * p.Lg;
+  __syncthreads();
+  // ctx = x ++ s_ext[0 .. m-1]
+  auto ctx = [&](int64_t i) -> int32_t { return i < T ? __ldg(x + i) : s_ext[i - T]; };
+  int32_t m = c, n = 0;
+  int64_t q = -1;            // the passage's next position in x, or -1
+  int32_t run = 0;           // the length of the copy being continued
+  int64_t pq0 = 0;           // s_pbuf holds x[pq0 .. pq0 + pn - 1]
+  int32_t pn = 0;
+  while (n < cap) {
+    int32_t y = -1, e = 0;
+    bool found = false;
+    if (q >= 0 && q <= T - 1) {
+      if (!(q >= pq0 && q < pq0 + pn)) {
+        pq0 = q;
+        pn = (int32_t)min((int64_t)FL_PBUF, (int64_t)T - q);
+        if (tid < pn) s_pbuf[tid] = __ldg(x + q + tid);
+        __syncthreads();
+      }
+      y = s_pbuf[q - pq0];
+      ++q;
+      run = min(run + 1, p.copy_cap);
+      e = run;
+      found = true;
+    } else {
+      // the earlier occurrence of ctx: the largest (l, j)
+      const int64_t len = (int64_t)T + m;
+      const int32_t last = ctx(len - 1);
+      unsigned long long best = 0;
+      for (int64_t j = tid; j <= (int64_t)T - 2; j += FL_THREADS) {
+        if (__ldg(x + j) != last) continue;
+        const int32_t lim = (int32_t)min((int64_t)p.copy_cap, j + 1);
+        int32_t l = 1;
+        while (l < lim && __ldg(x + j - l) == ctx(len - 1 - l)) ++l;
+        if (l >= p.n_min) {
+          const unsigned long long k = ((unsigned long long)l << 32) | (unsigned long long)j;
+          best = k > best ? k : best;
+        }
+      }
+      best = block_max_u64(best, s_red);
+      if (best != 0ull) {
+        const int64_t j = (int64_t)(uint32_t)best;
+        y = __ldg(x + j + 1);
+        q = j + 2;
+        run = (int32_t)(best >> 32);
+        e = run;
+        found = true;
+      } else if (len >= 3) {
+        // the most frequent follower of the last three tokens
+        const int32_t a = ctx(len - 3), b = ctx(len - 2), d = last;
+        for (int h = tid; h < FL_HASH; h += FL_THREADS) {
+          s_key[h] = 0ull;
+          s_cnt[h] = 0;
+          s_last[h] = -1;
+        }
+        __syncthreads();
+        for (int64_t j = 2 + tid; j <= (int64_t)T - 2; j += FL_THREADS) {
+          if (__ldg(x + j) != d || __ldg(x + j - 1) != b || __ldg(x + j - 2) != a) continue;
+          const int32_t f = __ldg(x + j + 1);
+          const unsigned long long key = (1ull << 32) | (unsigned long long)(uint32_t)f;
+          uint32_t h = ((uint32_t)f * 2654435761u) >> (32 - 11);
+          bool placed = false;
+          for (int probe = 0; probe < FL_HASH && !placed; ++probe) {
+            const unsigned long long prev = atomicCAS(&s_key[h], 0ull, key);
+            if (prev == 0ull || prev == key) {
+              atomicAdd(&s_cnt[h], 1);
+              atomicMax(&s_last[h], (int32_t)j);
+              placed = true;
+            }
+            h = (h + 1) & (FL_HASH - 1);
+          }
+          if (!placed) s_overflow = 1;
+        }
+        __syncthreads();
+        unsigned long long top = 0;
+        for (int h = tid; h < FL_HASH; h += FL_THREADS)
+          if (s_key[h] != 0ull) {
+            const unsigned long long k = ((unsigned long long)s_cnt[h] << 32) | (unsigned long long)s_last[h];
+            top = k > top ? k : top;
+          }
+        top = block_max_u64(top, s_red);
+        if (s_overflow) {
+          // more distinct followers than the table holds: the chain stops here
+          if (tid == 0) set_status(p.status, SPEC_DEV_OVERFLOW);
+        } else if (top != 0ull) {
+          y = __ldg(x + (int64_t)(uint32_t)top + 1);
+          e = -(int32_t)(top >> 32);
+          q = -1;
+          run = 0;
+          found = true;
+        }
+      }
+    }
+    if (!found) break;
+    if (tid == 0) {
+      out[n] = y;
+      ev[n] = e;
+      s_ext[m] = y;
+    }
+    ++n;
+    ++m;
+    __syncthreads();  // the new token is visible to every thread's ctx
+  }
+  for (int k = n + tid; k < p.Lg; k += FL_THREADS) {
+    out[k] = -1;
+    ev[k] = 0;
+  }
+  if (tid == 0) p.ng_len[(int64_t)r * C + c] = n;
+}
+
+}  // namespace spec
+
+extern "C" cudaError_t spec_launch_ngram_fill(const int32_t* hist, int64_t hist_stride, const int32_t* hist_len,
+                                              int32_t batch, int32_t P, int32_t Kc, const int32_t* cand_tok,
+                                              int32_t n_min, int32_t copy_cap, int32_t max_depth, int32_t Lg,
+                                              int32_t* ng_tok, int32_t* ng_len, int32_t* ng_ev, uint32_t* status,
+                                              cudaStream_t stream) {
+  spec::FillParams fp;
+  fp.hist = hist;
+  fp.stride = hist_stride;
+  fp.hist_len = hist_len;
+  fp.P = P;
+  fp.Kc = Kc;
+  fp.cand_tok = cand_tok;
+  fp.n_min = n_min;
+  fp.copy_cap = copy_cap;
+  fp.max_depth = max_depth;
+  fp.Lg = Lg;
+  fp.ng_tok = ng_tok;
+  fp.ng_len = ng_len;
+  fp.ng_ev = ng_ev;
+  fp.status = status;
+  const size_t smem = (size_t)(P + Lg + 1) * sizeof(int32_t);
+  cudaError_t e = cudaFuncSetAttribute(spec::ngram_fill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
+  if (e != cudaSuccess) return e;
+  spec::ngram_fill_kernel<<<dim3(P + 1, batch), FL_THREADS, smem, stream>>>(fp);
+  return cudaGetLastError();
+}

@@ -1,38 +1,47 @@
 // tree.cu -- the candidate tree of one block-drafter round.
 //
-// AdaSpark sec. 2.2 (tree shape), sec. 3.3 (n-gram candidates, Eq. (6)),
-// sec. 3.1 with Proposition 1 (best-first order) and Algorithm 1 (the first
-// n-1 nodes of the order, laid out depth-first):
+// AdaSpark sec. 2.2 (tree shape; n-gram chains branch from the anchor and from
+// each pick), sec. 3.3 (n-gram candidates, Eq. (6)), sec. 3.1 with
+// Proposition 1 (best-first order) and Algorithm 1 (the first n-1 nodes of
+// the order, laid out depth-first):
 //   candidates: 0 the anchor; 1 + i Kc + k the k-th ranked candidate of block
 //     position i (k = 0 the pick); pick i hangs from pick i-1 (pick 0 from the
 //     anchor), the siblings of position i from the pick's parent, as leaves;
-//   the n-gram chain walks from the anchor: a step equal to a drafter child of
-//     the current node marks it agreed (lowest index on duplicates) and moves
-//     to it, else it appends an n-gram node; the other drafter children of
-//     every node it passes through are contradicted;
-//   s: the given drafter score + adj if agreed - adj if contradicted, or the
-//     n-gram score; clamped to [-80, 80];
+//   n-gram chains, c = 0 from the anchor and c >= 1 from pick c-1, in order: a
+//     step equal to a drafter child of the current node marks it agreed
+//     (lowest index on duplicates) and moves to it; else a step equal to an
+//     n-gram child already there (an earlier chain's) moves to it; else it
+//     appends an n-gram node.  The other drafter children of every node a
+//     chain passes through are contradicted; agreed wins over contradicted;
+//   s: the given drafter score + adj if agreed, else - adj if contradicted; or
+//     the n-gram score; clamped to [-80, 80];
 //   q_j = e^{s_j} / (1 + sum over the children c of parent(j) of e^{s_c})
 //     (children summed in index order), Q_j = Q_parent(j) q_j, in fp64;
 //   order: Q descending, ties to the lower index; the tree: the anchor and the
 //     first width-1 candidates, depth-first with children in index order.
 //
-// GB300 layout: one CTA per request, one thread per candidate (at most 256),
-// everything in shared memory.  Warp 0 merges the n-gram chain (sequential in
-// its steps, lane-parallel over a node's children).  A node's children are a
-// known index range of drafter candidates plus at most one n-gram node, so the
-// per-parent sums and the depth-first offsets cost O(Kc) per node; the rank of
-// every candidate is a count over all candidates, the subtree sizes come from
-// shared-memory atomics along each path, and Q is formed level by level from
-// the anchor, one barrier per tree level.
+// GB300 layout: one CTA per request, one thread per candidate (at most 512),
+// everything in shared memory.  Warp 0 merges the chains depth by depth, one
+// lane per chain and a warp barrier per depth: a step's node depends only on
+// its token path from the anchor, so the steps at one depth resolve together
+// (against their parents' nodes and the other chains' steps at that depth);
+// meanwhile the other warps form e^s of every drafter candidate for its three
+// cases (fp64 runs on a narrow pipe on this part).  The new n-gram nodes are
+// numbered by a block-wide count in the order a sequential merge would make
+// them.  A node's children are a known index range of drafter candidates plus
+// a list of n-gram nodes in index order, so the per-parent sums and the
+// depth-first offsets cost O(children) per node; the rank of every candidate
+// is a count over all candidates, the subtree sizes come from shared-memory
+// atomics along each path, and Q is formed level by level from the anchor by
+// warp 0 over depth buckets.
 #include "common.cuh"
 
 namespace spec {
 
-#define TB_THREADS 256
+#define TB_THREADS 512
 
 struct TreeParams {
-  int32_t batch, P, Kc, Lg, width;
+  int32_t batch, P, Kc, n_chains, Lg, width;
   const int32_t* anchor;
   const int32_t* cand_tok;
   const float* cand_score;
@@ -48,140 +57,300 @@ struct TreeParams {
 };
 
 __global__ void __launch_bounds__(TB_THREADS) build_tree_kernel(TreeParams p) {
-  __shared__ int32_t s_tok[TB_THREADS], s_par[TB_THREADS], s_flag[TB_THREADS];
+  __shared__ int32_t s_tok[TB_THREADS], s_par[TB_THREADS], s_dk[TB_THREADS], s_depth[TB_THREADS];
+  __shared__ uint8_t s_agree[TB_THREADS], s_contra[TB_THREADS];
   __shared__ double s_e[TB_THREADS], s_den[TB_THREADS], s_Q[TB_THREADS];
-  __shared__ int32_t s_sel[TB_THREADS], s_size[TB_THREADS], s_before[TB_THREADS];
-  __shared__ int32_t s_chain[TB_THREADS];
-  __shared__ int32_t s_N, s_maxd, s_ngc, s_gl;
+  // e^s of the agreed and contradicted cases, until the denominators and Q take the space
+  double* const s_ea = s_den;
+  double* const s_ec = s_Q;
+  __shared__ int32_t s_size[TB_THREADS];
+  __shared__ int32_t s_ngfirst[TB_THREADS], s_ngnext[TB_THREADS];
+  __shared__ int32_t s_itok[TB_THREADS], s_ipar[TB_THREADS], s_node[TB_THREADS], s_final[TB_THREADS];
+  // the selection and the sibling offsets reuse the chain steps' tokens and parents
+  int32_t* const s_sel = s_itok;
+  int32_t* const s_before = s_ipar;
+  __shared__ int32_t s_bucket[TB_THREADS], s_bpar[TB_THREADS], s_dcnt[TB_THREADS + 1], s_doff[TB_THREADS + 1];
+  __shared__ int32_t s_N, s_maxd, s_levels, s_len[TB_THREADS], s_wcnt[TB_THREADS / 32];
   __shared__ float s_ngs, s_adj;
+  __shared__ double s_eng;
   const int r = blockIdx.x, j = threadIdx.x;
-  const int P = p.P, Kc = p.Kc;
+  const int lane = j & 31, warp = j >> 5;
+  const int P = p.P, Kc = p.Kc, NC = p.n_chains, Lg = p.Lg;
   const int ND = 1 + P * Kc;  // anchor + drafter candidates
   // every global input of the request, loaded at once: the drafter's block,
-  // its scores, the chain and the per-request scalars
-  float my_score = 0.0f;
+  // the chains and the per-request scalars
   if (j < ND) {
     if (j == 0) {
       s_tok[0] = p.anchor[r];
       s_par[0] = -1;
-      s_gl = p.ng_len[r];
+      s_depth[0] = 0;
       s_ngs = p.ng_score[r];
       s_adj = p.ng_adj[r];
+      s_dk[0] = P > 0 ? 1 : -1;
     } else {
-      const int i = (j - 1) / Kc;
+      const int i = (j - 1) / Kc, k = (j - 1) - i * Kc;
       s_tok[j] = p.cand_tok[(int64_t)r * P * Kc + (j - 1)];
-      my_score = p.cand_score[(int64_t)r * P * Kc + (j - 1)];
       s_par[j] = (i == 0) ? 0 : 1 + (i - 1) * Kc;
+      s_depth[j] = i + 1;
+      // a pick that is not the last has the next position's candidates as children
+      s_dk[j] = (k == 0 && i + 1 < P) ? j + Kc : -1;
     }
-    s_flag[j] = 0;
   }
+  s_agree[j] = 0;
+  s_contra[j] = 0;
+  s_ngfirst[j] = 0x7FFFFFFF;
+  s_ngnext[j] = -1;
   s_size[j] = 0;
-  if (j == 0) s_maxd = 0;
-  // the chain's tokens, staged for the sequential walk below
-  if (j < p.Lg) s_chain[j] = p.ng_tok[(int64_t)r * p.Lg + j];
+  s_dcnt[j] = 0;
+  if (j == 0) {
+    s_maxd = 0;
+    s_levels = 0;
+    s_dcnt[TB_THREADS] = 0;
+  }
+  // chain item j = c Lg + t: the t-th step of chain c
+  const int nct = NC * Lg;
+  if (j < nct) s_itok[j] = p.ng_tok[(int64_t)r * nct + j];
+  int32_t my_gl = 0;
+  if (j < NC) {
+    my_gl = p.ng_len[(int64_t)r * NC + j];
+    if (my_gl < 0 || my_gl > Lg) {
+      set_status(p.status, SPEC_DEV_BAD_LENGTH);
+      my_gl = 0;
+    }
+    s_len[j] = my_gl;
+  }
+  __syncthreads();  // s_levels is zero from here on
+  if (j < NC) atomicMax(&s_levels, j + my_gl);  // chain c's steps sit at depths c+1 .. c+gl
   __syncthreads();
-  // the n-gram chain from the anchor, by warp 0: each step depends on where
-  // the previous one went (lanes compare the current node's drafter children
-  // at once); once the chain leaves the drafter's block it only appends
-  // n-gram nodes, which the warp writes in parallel
-  if (j < 32) {
-    const int lane = j;
-    int32_t gl = s_gl;
-    if (gl < 0 || gl > p.Lg) {
-      if (lane == 0) set_status(p.status, SPEC_DEV_BAD_LENGTH);
-      gl = 0;
-    }
-    int32_t cur = 0;                  // current node
-    int32_t c0 = (P > 0) ? 1 : -1;    // its drafter children [c0, c0 + Kc), -1: none
-    int32_t pos = 0;                  // the block position of those children
-    int32_t t = 0;
-    for (; t < gl && c0 >= 0; ++t) {
-      const int32_t x = s_chain[t];
-      // the lowest-index drafter child with token x
-      int32_t hit = -1;
-      for (int32_t k0 = 0; k0 < Kc && hit < 0; k0 += 32) {
-        const int32_t k = k0 + lane;
-        const unsigned b = __ballot_sync(0xFFFFFFFFu, k < Kc && s_tok[c0 + k] == x);
-        if (b != 0u) hit = c0 + k0 + __ffs(b) - 1;
+  if (warp == 0) {
+    // the node of every step, depth by depth, by warp 0 (lane = chain; each
+    // chain has one step per depth).  A step's node depends only on its token
+    // path from the anchor: under a node with drafter children it is the
+    // lowest-index child with its token (agreed; the other children
+    // contradicted), else the n-gram child (parent, token), made by the first
+    // chain (in chain order) with that step at this depth -- among the lanes of
+    // one round of 32 chains the lowest lane of its __match_any_sync group.
+    // Provisional ids: drafter nodes their index, n-gram nodes ND + the item
+    // that makes them.
+    const int levels = s_levels;
+    if (NC <= 32) {
+      // one chain per lane, its current node in a register; the first chain
+      // with the same (parent, token) found by shuffles over the lower lanes
+      const int c = lane;
+      const int32_t gl = c < NC ? s_len[c] : 0;
+      int32_t cur = c == 0 ? 0 : 1 + (c - 1) * Kc;
+      for (int d = 1; d <= levels; ++d) {
+        const int t = d - c - 1;
+        const bool active = c < NC && t >= 0 && t < gl;
+        const int jj = c * Lg + t;
+        const int32_t xt = active ? s_itok[jj] : 0;
+        int32_t node = -1;
+        if (active) {
+          const int32_t c0 = cur < ND ? s_dk[cur] : -1;
+          if (c0 >= 0) {
+            for (int32_t k = 0; k < Kc; ++k)
+              if (node < 0 && s_tok[c0 + k] == xt) node = c0 + k;
+            for (int32_t k = 0; k < Kc; ++k)
+              if (c0 + k != node) s_contra[c0 + k] = 1;
+            if (node >= 0) s_agree[node] = 1;
+          }
+        }
+        const bool need = active && node < 0;
+        int first = lane;
+        for (int k = 0; k < NC - 1; ++k) {
+          const int32_t op = __shfl_sync(0xFFFFFFFFu, cur, k);
+          const int32_t ox = __shfl_sync(0xFFFFFFFFu, xt, k);
+          const bool on = __shfl_sync(0xFFFFFFFFu, need, k);
+          if (k < first && on && op == cur && ox == xt) first = k;
+        }
+        if (need) node = ND + first * Lg + (d - first - 1);
+        if (active) {
+          s_node[jj] = node;
+          s_ipar[jj] = cur;
+          cur = node;
+        }
       }
-      for (int32_t k = lane; k < Kc; k += 32)
-        if (c0 + k != hit) s_flag[c0 + k] = -1;
-      if (hit < 0) break;  // appended below, with every later step
-      if (lane == 0) s_flag[hit] = 1;
-      cur = hit;
-      // a pick's children are the next position's candidates; a sibling has none
-      const bool pick = (hit - c0) == 0;
-      ++pos;
-      c0 = (pick && pos < P) ? 1 + pos * Kc : -1;
+      __syncwarp();
+    } else {
+      for (int d = 1; d <= levels; ++d) {
+        for (int cb = 0; cb < NC; cb += 32) {
+          const int c = cb + lane, t = d - c - 1;
+          const bool active = c < NC && t >= 0 && t < s_len[c];
+          const int jj = c * Lg + t;
+          int32_t par = -1, xt = 0, node = -1;
+          if (active) {
+            par = t == 0 ? (c == 0 ? 0 : 1 + (c - 1) * Kc) : s_node[jj - 1];
+            xt = s_itok[jj];
+            const int32_t c0 = par < ND ? s_dk[par] : -1;
+            if (c0 >= 0) {
+              for (int32_t k = 0; k < Kc; ++k)
+                if (node < 0 && s_tok[c0 + k] == xt) node = c0 + k;
+              for (int32_t k = 0; k < Kc; ++k)
+                if (c0 + k != node) s_contra[c0 + k] = 1;
+              if (node >= 0) s_agree[node] = 1;
+            }
+          }
+          const bool need = active && node < 0;
+          const unsigned mask = __ballot_sync(0xFFFFFFFFu, need);
+          if (need) {
+            const unsigned long long key = ((unsigned long long)(uint32_t)par << 32) | (uint32_t)xt;
+            const unsigned grp = __match_any_sync(mask, key);
+            const int c1 = cb + __ffs(grp) - 1;
+            node = ND + c1 * Lg + (d - c1 - 1);
+            // chains of earlier rounds come first in chain order
+            for (int c2 = 0; c2 < cb; ++c2) {
+              const int t2 = d - c2 - 1;
+              if (t2 < 0 || t2 >= s_len[c2]) continue;
+              const int j2 = c2 * Lg + t2;
+              if (s_itok[j2] == xt && s_ipar[j2] == par) {
+                node = ND + j2;
+                break;
+              }
+            }
+          }
+          if (active) {
+            s_node[jj] = node;
+            s_ipar[jj] = par;
+          }
+          __syncwarp();
+        }
+      }
     }
-    // steps t .. gl-1 append a chain of n-gram nodes under cur
-    const int32_t rest = gl - t;
-    for (int32_t k = lane; k < rest; k += 32) {
-      s_tok[ND + k] = s_chain[t + k];
-      s_par[ND + k] = (k == 0) ? cur : ND + k - 1;
-      s_flag[ND + k] = 0;
+  } else {
+    // meanwhile: e^s of every drafter candidate for each of its three cases
+    // (plain, agreed, contradicted) and of an n-gram node, clamped to [-80, 80]
+    const double adj = (double)s_adj;
+    auto ex = [](double x) { return exp(x > 80.0 ? 80.0 : (x < -80.0 ? -80.0 : x)); };
+    // one exponential per thread: item w = 3 (v - 1) + case, then the n-gram node's
+    for (int w = j - 32; w <= 3 * (ND - 1); w += TB_THREADS - 32) {
+      if (w == 3 * (ND - 1)) {
+        s_eng = ex((double)s_ngs);
+        continue;
+      }
+      const int v = 1 + w / 3, cs = w - 3 * (v - 1);
+      const double sv = (double)p.cand_score[(int64_t)r * P * Kc + (v - 1)];
+      if (cs == 0)
+        s_e[v] = ex(sv);
+      else if (cs == 1)
+        s_ea[v] = ex(sv + adj);
+      else
+        s_ec[v] = ex(sv - adj);
     }
-    if (lane == 0) {
-      s_N = ND + rest;
-      s_ngc = rest > 0 ? cur : -1;  // the node the n-gram nodes hang from
+  }
+  __syncthreads();
+  // the n-gram nodes in the order the sequential merge makes them: a step that
+  // makes its node gets index ND + (the steps before it, in chain order, that
+  // make theirs)
+  const int my_c = Lg > 0 ? j / Lg : 0, my_t = Lg > 0 ? j - my_c * Lg : 0;
+  const bool item = j < nct && my_t < s_len[my_c];
+  const bool makes = item && s_node[j] == ND + j;
+  {
+    const unsigned bal = __ballot_sync(0xFFFFFFFFu, makes);
+    if (lane == 0) s_wcnt[warp] = __popc(bal);
+    __syncthreads();
+    int32_t before = __popc(bal & ((1u << lane) - 1u)), all = 0;
+#pragma unroll
+    for (int w = 0; w < TB_THREADS / 32; ++w) {
+      before += w < warp ? s_wcnt[w] : 0;
+      all += s_wcnt[w];
     }
+    if (makes) s_final[j] = ND + before;
+    if (j == 0) s_N = ND + all;
   }
   __syncthreads();
   const int N = s_N;
-  // scores and e^s
-  if (j >= 1 && j < N) {
-    double s;
-    if (j < ND) {
-      const double adj = (double)s_adj;
-      s = (double)my_score;
-      s += (s_flag[j] > 0 ? adj : 0.0) - (s_flag[j] < 0 ? adj : 0.0);
-    } else {
-      s = (double)s_ngs;
-    }
-    s = s > 80.0 ? 80.0 : (s < -80.0 ? -80.0 : s);
-    s_e[j] = exp(s);
+  if (makes) {
+    const int32_t v = s_final[j];
+    const int32_t par = s_ipar[j];
+    const int32_t pv = par < ND ? par : s_final[par - ND];
+    s_tok[v] = s_itok[j];
+    s_par[v] = pv;
+    s_depth[v] = my_c + my_t + 1;
+    atomicMin(&s_ngfirst[pv], v);
+  }
+  if (j < ND) {
+    atomicMax(&s_maxd, s_depth[j]);
+    atomicAdd(&s_dcnt[s_depth[j]], 1);
+  }
+  if (makes) {
+    atomicMax(&s_maxd, my_c + my_t + 1);
+    atomicAdd(&s_dcnt[my_c + my_t + 1], 1);
   }
   __syncthreads();
-  // every node's children: a range of Kc drafter candidates (under the anchor
-  // and under a pick that is not the last) and at most one n-gram node (the
-  // chain passes each node once); both in increasing index
-  const int32_t ngc = s_ngc;
-  auto drafter_kids = [&](int32_t v) -> int32_t {  // first drafter child, or -1
-    if (v == 0) return P > 0 ? 1 : -1;
-    if (v < ND && (v - 1) % Kc == 0 && (v - 1) / Kc + 1 < P) return v + Kc;
-    return -1;
-  };
-  auto ngram_kid = [&](int32_t v) -> int32_t {  // the n-gram child, or -1
-    if (v == ngc) return ND;
-    return (v >= ND && v + 1 < N) ? v + 1 : -1;
-  };
-  // Eq. (6) denominators: thread j sums its own children in index order
+  // each n-gram node's next sibling: the smallest larger index among the nodes
+  // made at its depth with its parent; e^s of every candidate
+  if (makes) {
+    const int32_t v = s_final[j], par = s_ipar[j], d = my_c + my_t + 1;
+    int32_t nx = 0x7FFFFFFF;
+    for (int c2 = 0; c2 < NC; ++c2) {
+      const int t2 = d - c2 - 1;
+      if (t2 < 0 || t2 >= s_len[c2]) continue;
+      const int j2 = c2 * Lg + t2;
+      if (s_node[j2] == ND + j2 && s_ipar[j2] == par) {
+        const int32_t w = s_final[j2];
+        if (w > v && w < nx) nx = w;
+      }
+    }
+    s_ngnext[v] = nx == 0x7FFFFFFF ? -1 : nx;
+  }
+  if (j < N) {
+    if (s_ngfirst[j] == 0x7FFFFFFF) s_ngfirst[j] = -1;
+    if (j >= 1 && j < ND)
+      s_e[j] = s_agree[j] ? s_ea[j] : (s_contra[j] ? s_ec[j] : s_e[j]);
+    else if (j >= ND)
+      s_e[j] = s_eng;
+  }
+  const int32_t maxd = s_maxd;
+  if (warp == 0) {  // offsets of the depth buckets
+    int32_t run = 0;
+    for (int32_t d0 = 0; d0 <= maxd; d0 += 32) {
+      const int32_t d = d0 + lane;
+      const int32_t v = d <= maxd ? s_dcnt[d] : 0;
+      int32_t x = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int32_t y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+        if (lane >= o) x += y;
+      }
+      if (d <= maxd) {
+        s_doff[d] = run + x - v;
+        s_dcnt[d] = run + x - v;  // the bucket's fill cursor
+      }
+      run += __shfl_sync(0xFFFFFFFFu, x, 31);
+    }
+    if (lane == 0) s_doff[maxd + 1] = run;
+  }
+  __syncthreads();
+  // Eq. (6) denominators: thread j sums its own children in index order, the
+  // drafter range first; and the depth buckets are filled
   if (j < N) {
     double den = 1.0;
-    const int32_t c0 = drafter_kids(j);
+    const int32_t c0 = j < ND ? s_dk[j] : -1;
     if (c0 >= 0)
       for (int32_t k = 0; k < Kc; ++k) den += s_e[c0 + k];
-    const int32_t g = ngram_kid(j);
-    if (g >= 0) den += s_e[g];
+    for (int32_t g = s_ngfirst[j]; g >= 0; g = s_ngnext[g]) den += s_e[g];
     s_den[j] = den;
+    const int32_t b = atomicAdd(&s_dcnt[s_depth[j]], 1);
+    s_bucket[b] = j;
+    s_bpar[b] = s_par[j];
   }
   __syncthreads();
-  // q_j, depths, then Q_j = Q_parent(j) q_j level by level from the anchor
-  // down (the order of the definition's products)
-  double qj = 1.0;
-  int32_t dj = 0;
-  if (j < N) {
-    if (j > 0) qj = s_e[j] / s_den[s_par[j]];
-    for (int32_t a = j; a != 0; a = s_par[a]) ++dj;
-    atomicMax(&s_maxd, dj);
-  }
-  if (j == 0) s_Q[0] = 1.0;
+  // q_j = e^{s_j} / den(parent); Q_j = Q_parent(j) q_j level by level from the
+  // anchor down (the order of the definition's products), by warp 0
+  if (j > 0 && j < N) s_Q[j] = s_e[j] / s_den[s_par[j]];  // q until its level turns it into Q
   __syncthreads();
-  const int32_t maxd = s_maxd;
-  for (int32_t d = 1; d <= maxd; ++d) {
-    if (j < N && dj == d) s_Q[j] = s_Q[s_par[j]] * qj;
-    __syncthreads();
+  if (warp == 0) {
+    if (lane == 0) s_Q[0] = 1.0;
+    __syncwarp();
+    for (int32_t d = 1; d <= maxd; ++d) {
+      for (int32_t b = s_doff[d] + lane; b < s_doff[d + 1]; b += 32) {
+        const int32_t v = s_bucket[b];
+        s_Q[v] = s_Q[s_bpar[b]] * s_Q[v];
+      }
+      __syncwarp();
+    }
   }
+  __syncthreads();
   // best-first rank (Q descending, ties to the lower index) and selection
   if (j < N) {
     bool sel = (j == 0);
@@ -210,15 +379,18 @@ __global__ void __launch_bounds__(TB_THREADS) build_tree_kernel(TreeParams p) {
   // before[c]: the rows that the selected earlier siblings of c occupy
   if (j < N && s_sel[j]) {
     int32_t run = 0;
-    const int32_t c0 = drafter_kids(j);
+    const int32_t c0 = j < ND ? s_dk[j] : -1;
     if (c0 >= 0)
       for (int32_t k = 0; k < Kc; ++k)
         if (s_sel[c0 + k]) {
           s_before[c0 + k] = run;
           run += s_size[c0 + k];
         }
-    const int32_t g = ngram_kid(j);
-    if (g >= 0 && s_sel[g]) s_before[g] = run;
+    for (int32_t g = s_ngfirst[j]; g >= 0; g = s_ngnext[g])
+      if (s_sel[g]) {
+        s_before[g] = run;
+        run += s_size[g];
+      }
   }
   __syncthreads();
   // depth-first position: one row per ancestor step, plus the earlier
@@ -245,7 +417,8 @@ __global__ void __launch_bounds__(TB_THREADS) build_tree_kernel(TreeParams p) {
 
 extern "C" cudaError_t spec_launch_build_tree(int32_t batch, int32_t P, int32_t Kc, const int32_t* anchor,
                                               const int32_t* cand_tok, const float* cand_score,
-                                              const int32_t* ng_tok, int32_t Lg, const int32_t* ng_len,
+                                              const int32_t* ng_tok, int32_t n_chains, int32_t Lg,
+                                              const int32_t* ng_len,
                                               const float* ng_score, const float* ng_adj, int32_t width,
                                               int32_t* tok, int32_t* parent, int32_t* cand_id, int32_t* n_rows,
                                               uint32_t* status, cudaStream_t stream) {
@@ -253,6 +426,7 @@ extern "C" cudaError_t spec_launch_build_tree(int32_t batch, int32_t P, int32_t 
   p.batch = batch;
   p.P = P;
   p.Kc = Kc;
+  p.n_chains = n_chains;
   p.Lg = Lg;
   p.width = width;
   p.anchor = anchor;

@@ -166,10 +166,23 @@ def gpu_build_tree(S, ws, anchor, cand_tok, cand_score, ng_tok, ng_len, ng_score
     tok, parent, cid = (torch.full((B, width), -7, **i32) for _ in range(3))
     nr = torch.full((B,), -7, **i32)
     S.spec_build_tree(dev(anchor, torch.int32), dev(cand_tok, torch.int32), dev(cand_score, torch.float32),
-                      dev(np.asarray(ng_tok).reshape(B, -1), torch.int32), dev(ng_len, torch.int32),
+                      dev(np.asarray(ng_tok) if np.ndim(ng_tok) == 3 else np.asarray(ng_tok).reshape(B, -1),
+                          torch.int32), dev(ng_len, torch.int32),
                       dev(ng_score, torch.float32), dev(ng_adj, torch.float32), width, tok, parent, cid, nr, ws)
     torch.cuda.synchronize()
     return dict(tok=host(tok), parent=host(parent), cand_id=host(cid), n_rows=host(nr))
+
+
+def gpu_ngram_fill(S, ws, hist, hist_len, cand_tok, n_min, copy_cap, max_depth, Lg):
+    B = len(hist_len)
+    P = np.shape(cand_tok)[1]
+    i32 = dict(dtype=torch.int32, device=DEV)
+    tok, ev = (torch.full((B, P + 1, Lg), -7, **i32) for _ in range(2))
+    ln = torch.full((B, P + 1), -7, **i32)
+    S.spec_ngram_fill(dev(hist, torch.int32), dev(hist_len, torch.int32), dev(cand_tok, torch.int32), n_min,
+                      copy_cap, max_depth, tok, ln, ev, ws)
+    torch.cuda.synchronize()
+    return dict(tok=host(tok), len=host(ln), ev=host(ev))
 
 
 def assert_tree_equal(g, o, rel=1e-12):

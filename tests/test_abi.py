@@ -133,14 +133,27 @@ def test_host_validation_rejects_bad_arguments_without_a_gpu(spec):
     assert price(L=40, K=7) == UNS
     assert price(tb=100) == INV  # a table too small for L
     # tree builder: Kc 0, width 0, too many candidates, too wide
-    def tree(B=4, P=8, Kc=4, Lg=15, width=16):
-        return lib.spec_build_tree(B, P, Kc, P_, P_, P_, P_, Lg, P_, P_, P_, width, P_, P_, P_, P_, C.byref(w), None)
+    def tree(B=4, P=8, Kc=4, Lg=15, width=16, nc=1):
+        return lib.spec_build_tree(B, P, Kc, P_, P_, P_, P_, nc, Lg, P_, P_, P_, width, P_, P_, P_, P_, C.byref(w),
+                                   None)
     P_ = P
     assert tree(Kc=0) == INV
     assert tree(width=0) == INV
-    assert tree(P=40, Kc=8) == UNS  # 1 + 320 + 15 candidates
+    assert tree(nc=0) == INV and tree(nc=10) == INV  # 1 <= n_chains <= P + 1
+    assert tree(P=70, Kc=8) == UNS  # 1 + 560 + 15 candidates
+    assert tree(nc=9, Lg=60) == UNS  # 1 + 32 + 540 candidates
     assert tree(width=257) == UNS
-    assert lib.spec_build_tree(4, 8, 4, None, P, P, P, 15, P, P, P, 16, P, P, P, P, C.byref(w), None) == INV
+    assert lib.spec_build_tree(4, 8, 4, None, P, P, P, 1, 15, P, P, P, 16, P, P, P, P, C.byref(w), None) == INV
+    # n-gram fill: n_min 0, copy_cap below n_min, negative depth, P + Lg too large, missing outputs
+    def fill(B=4, stride=64, npos=8, Kc=4, n_min=4, cap=256, depth=32, Lg=32, tok=P):
+        return lib.spec_ngram_fill(P, stride, P, B, npos, Kc, P, n_min, cap, depth, Lg, tok, P, P, C.byref(w), None)
+    assert fill(n_min=0) == INV
+    assert fill(n_min=5, cap=4) == INV
+    assert fill(depth=-1) == INV
+    assert fill(Kc=0) == INV
+    assert fill(npos=4000, Lg=200) == UNS
+    assert fill(tok=None) == INV
+    assert fill(B=0, tok=None) == 0  # nothing to do: no device work
     # verification: vocab 0, bad dtype, batch beyond the workspace, NaN temperature
     def chain(B=4, V=1024, dtype=1, max_rows=64, T=0.0, K=0, draft=None):
         return lib.spec_verify_chain(B, V, dtype, P, P, max_rows, draft, K, P, 15, P, None, T, 0, 0, P, P, P,

@@ -419,6 +419,35 @@ def tree_blocks(seed=1003, B=32, P=8, Kc=4, V=151936):
             "ng_adj": np.zeros(B, np.float32), "hist": hist}
 
 
+def tree_fill_bs32(seed=1011, width=16, B=32, P=8, Kc=4, V=151936):
+    """The tree round with its n-gram chains made by the fill from the request's
+    own text: tree_blocks' 4096-token histories (their last 6 tokens repeat an
+    earlier passage), with the drafter's picks following that passage's
+    continuation in every fourth request and for its first three positions in
+    the next one (so that chains agree with picks and chains from picks read
+    on).  Fill parameters: copy length >= 4 for a passage (so that contexts
+    matched only by their last three tokens take the follower rule), copies
+    capped at 256, chains to 32 tokens below the anchor."""
+    cfg = tree_blocks(seed=seed, B=B, P=P, Kc=Kc, V=V)
+    hist = cfg["hist"]
+    for r in range(B):
+        # where the history's last 6 tokens occurred before (the planted repeat)
+        tail = hist[r, -6:]
+        at = next(a for a in range(4096 - 6) if np.array_equal(hist[r, a:a + 6], tail))
+        follow = P if r % 4 == 0 else (3 if r % 4 == 1 else 0)
+        for i in range(follow):
+            t = int(hist[r, at + 6 + i])
+            row = cfg["cand_tok"][r, i]
+            if t in row[1:]:
+                row[list(row).index(t)] = row[0]
+            row[0] = t
+    cfg.update({"name": f"tree_fill_bs32_w{width}", "width": width, "max_nodes": width, "dtype": "bf16",
+                "hist_len": np.full(B, 4096, np.int32), "n_min": 4, "copy_cap": 256, "max_depth": 32,
+                "Lg": 32, "ng_score": np.zeros(B, np.float32),
+                "ng_adj": np.full(B, float(np.log(0.7 / 0.3)), np.float32)})
+    return cfg
+
+
 def flatten_trees(tok, parent, n_rows):
     """[B x width] tree rows (valid up to n_rows[r]) -> node_off [B + 1] and the
     rows of all requests back to back."""
