@@ -14,10 +14,13 @@
 // CTA per SM, 12 warps each; the work is the sequence of 8 KB chunks of the
 // rows (4096 bf16 / 2048 fp32 entries) in (request, row, chunk) order, and
 // every warp takes an equal contiguous range of it.  Each warp streams its
-// range through its own ring of two 8 KB shared-memory stages filled by
-// one-dimensional bulk async copies (completion on an mbarrier, bounded
-// wait), moves a landed chunk into registers and refills the stage at once,
-// so two copies per warp stay in flight while it computes.  Per chunk a warp
+// range through its own 8 KB shared-memory stage filled by one-dimensional
+// bulk async copies (completion on an mbarrier, bounded wait): it moves a
+// landed chunk into registers and refills the stage at once, so its next
+// copy is in flight while it computes.  One 8 KB copy per warp (96 KB per
+// SM, 15 MB over the GPU) keeps HBM busy; deeper rings measured slower, as
+// longer memory queues widen the spread of the warps' finish times.  Per
+// chunk a warp
 // produces
 //   greedy rows:  a packed 64-bit (ordered value, ~index) key; keys of one
 //                 row fold in registers and reach the row's workspace key with
@@ -41,7 +44,7 @@ namespace spec {
 enum { MODE_CHAIN_GREEDY = 0, MODE_CHAIN_SAMPLE = 1, MODE_TREE = 2 };
 
 // streaming kernel: 12 warps per CTA, one CTA per SM, each warp with its own
-// ring of 2 x 8 KB stages (192 KB of shared memory in flight per SM)
+// 8 KB stage (96 KB of shared memory in flight per SM)
 #define VR_WARPS 12
 #define VR_THREADS (32 * VR_WARPS)
 enum { KIND_POINT = 0, KIND_BONUS = 1, KIND_Q = 2 };
@@ -222,7 +225,7 @@ struct Vec {
   static constexpr int PER = DT == 1 ? 8 : 4;  // entries per vector
   static constexpr int CH = 32 * NV * PER;     // entries per chunk: 4096 bf16 / 2048 fp32
   static constexpr int BYTES = 8192;           // bytes per chunk (one pipeline stage)
-  static constexpr int STAGES = 2;
+  static constexpr int STAGES = 1;  // copies in flight per warp
   static constexpr int SUB = CH / SPEC_UNIT;   // 2048-entry units per chunk
   static constexpr uint32_t NEG = DT == 1 ? 0xFF80FF80u : 0xFF800000u;
 };
@@ -1231,8 +1234,8 @@ __global__ void __launch_bounds__(VR_THREADS, 1) verify_rows_kernel(VerifyParams
         aborted = 1;
         break;
       }
-      // copy the chunk to registers and refill the stage at once, so that two
-      // copies per warp stay in flight while it computes
+      // copy the chunk to registers and refill the stage at once, so that the
+      // next copy is in flight while the warp computes
       uint4 v[Vec<DT>::NV];
       vec_load_smem<DT>(stage + (size_t)s * UB, n_el, lane, v);
       __syncwarp();
