@@ -542,25 +542,69 @@ __device__ __forceinline__ float2 merge_row(const VerifyParams& p, int slot, int
   return make_float2(M, warp_sum(sc));
 }
 
-// (max, sum) of a whole row from its unit partials, by one lane: a max pass and
-// a rescaled-sum pass, each over independent loads
-__device__ __forceinline__ float2 merge_row_lane(const VerifyParams& p, int slot) {
-  const float2* pr = &p.ws.partial[(int64_t)slot * p.ws.units];
-  float m = -INFINITY;
-#pragma unroll 8
-  for (int u = 0; u < p.units; ++u) m = fmaxf(m, __ldcg(&pr[u]).x);
-  if (m == -INFINITY) return make_float2(m, 0.0f);
-  float s0 = 0.0f, s1 = 0.0f;
-#pragma unroll 8
-  for (int u = 0; u < p.units; ++u) {
-    const float2 t = __ldcg(&pr[u]);
-    const float w = t.x == -INFINITY ? 0.0f : t.y * ex2((t.x - m) * p.c);
-    if (u & 1)
-      s1 += w;
-    else
-      s0 += w;
+// (m, s) pairs merged: s rescaled to the larger max (empty pairs have m = -inf)
+__device__ __forceinline__ void merge_ms(float& m, float& s, float m2, float s2, float c) {
+  const float nm = fmaxf(m, m2);
+  if (nm == -INFINITY) return;
+  s = (m == -INFINITY ? 0.0f : s * ex2((m - nm) * c)) + (m2 == -INFINITY ? 0.0f : s2 * ex2((m2 - nm) * c));
+  m = nm;
+}
+
+// (max, sum) of R rows from their unit partials, by the whole warp at once.
+// Row k (its partials at slot_of(k); none when negative) is merged by G lanes,
+// G the largest power of two with R G <= 32: each lane takes every G-th unit
+// in batches of MB independent loads (one memory round trip per batch, with an
+// online rescale), then the G lanes combine by shuffles.  More than 32 rows
+// take several rounds.  Lane l receives row want_a(l)'s result in *a and row
+// want_b(l)'s in *b (negative: none, (-inf, 0)).
+template <typename SlotFn>
+__device__ __forceinline__ void merge_rows_warp(const VerifyParams& p, int R, SlotFn slot_of, int lane, int want_a,
+                                                float2* a, int want_b, float2* b) {
+  constexpr int MB = 20;
+  int G = 1;
+  while (G < 32 && R * 2 * G <= 32) G <<= 1;
+  const int rpr = 32 / G, sub = lane & (G - 1);
+  *a = make_float2(-INFINITY, 0.0f);
+  *b = make_float2(-INFINITY, 0.0f);
+  for (int k0 = 0; k0 < R; k0 += rpr) {
+    const int k = k0 + lane / G;
+    const int slot = k < R ? slot_of(k) : -1;
+    float m = -INFINITY, s = 0.0f;
+    if (slot >= 0) {
+      const float2* pr = &p.ws.partial[(int64_t)slot * p.ws.units];
+      for (int u0 = sub; u0 < p.units; u0 += MB * G) {
+        float2 t[MB];
+#pragma unroll
+        for (int q = 0; q < MB; ++q) {
+          const int u = u0 + q * G;
+          t[q] = u < p.units ? __ldcg(&pr[u]) : make_float2(-INFINITY, 0.0f);
+        }
+        float bm = -INFINITY;
+#pragma unroll
+        for (int q = 0; q < MB; ++q) bm = fmaxf(bm, t[q].x);
+        if (bm == -INFINITY) continue;
+        const float nm = fmaxf(m, bm);
+        float acc = (m == -INFINITY) ? 0.0f : s * ex2((m - nm) * p.c);
+#pragma unroll
+        for (int q = 0; q < MB; ++q)
+          if (t[q].x != -INFINITY) acc += t[q].y * ex2((t[q].x - nm) * p.c);
+        m = nm;
+        s = acc;
+      }
+    }
+    for (int o = G >> 1; o >= 1; o >>= 1) {
+      const float m2 = __shfl_xor_sync(0xFFFFFFFFu, m, o), s2 = __shfl_xor_sync(0xFFFFFFFFu, s, o);
+      merge_ms(m, s, m2, s2, p.c);
+    }
+    // rows k0 .. k0 + rpr - 1 sit at lanes (k - k0) G
+    const bool in_a = want_a >= k0 && want_a < k0 + rpr, in_b = want_b >= k0 && want_b < k0 + rpr;
+    const float ma = __shfl_sync(0xFFFFFFFFu, m, in_a ? (want_a - k0) * G : 0);
+    const float sa = __shfl_sync(0xFFFFFFFFu, s, in_a ? (want_a - k0) * G : 0);
+    const float mb = __shfl_sync(0xFFFFFFFFu, m, in_b ? (want_b - k0) * G : 0);
+    const float sb = __shfl_sync(0xFFFFFFFFu, s, in_b ? (want_b - k0) * G : 0);
+    if (in_a) *a = make_float2(ma, sa);
+    if (in_b) *b = make_float2(mb, sb);
   }
-  return make_float2(m, s0 + s1);
 }
 
 // Inverse CDF over unit weights w_u (unit order), at the fraction u of their
@@ -726,6 +770,141 @@ __device__ __forceinline__ int find_in_unit(const float r[64], float before, flo
   return pick;
 }
 
+
+// ---- one unit's weights for a draw, in compact code.  A draw runs once per
+// request, from cold instruction caches, so these loops stay rolled: lane l
+// owns the unit's entries [64 l, 64 l + 64), read through L1 in 16-byte
+// vectors (one memory round trip for the first pass; the rest hit L1).  The
+// weight of entry z is 2^(z c - mc), 0 for -inf and for the excluded index.
+template <int DT>
+__device__ __forceinline__ void unpack_vec(const uint4& w, float (&x)[DT == 1 ? 8 : 4]) {
+  if (DT == 1) {
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      x[2 * q] = bf16_lo(ws[q]);
+      x[2 * q + 1] = bf16_hi(ws[q]);
+    }
+  } else {
+    x[0] = __uint_as_float(w.x);
+    x[1] = __uint_as_float(w.y);
+    x[2] = __uint_as_float(w.z);
+    x[3] = __uint_as_float(w.w);
+  }
+}
+
+template <int DT>
+__device__ __forceinline__ float entry_l1(const void* row, int64_t i) {
+  if (DT == 1) return __uint_as_float((uint32_t)__ldca(static_cast<const unsigned short*>(row) + i) << 16);
+  return __ldca(static_cast<const float*>(row) + i);
+}
+
+// the lane's entries in order, from running sum `run`: mode 0 returns their
+// total weight; mode 1 stops at the first entry whose running sum exceeds t
+// (returning its unit index and weight), else returns the last entry with
+// positive weight (-1 if none)
+template <int DT, int MODE>
+__device__ __forceinline__ float unit_lane_pass(const void* row, int e0, int n_el, bool vec, int lane, float c,
+                                                float mc, int skip, float run, float t, int* pick, float* w_at) {
+  constexpr int PER = DT == 1 ? 8 : 4;
+  const int b = 64 * lane;
+  const int cnt = min(64, n_el - b);
+  float sum = 0.0f, lastw = 0.0f;
+  int last = -1;
+  if (MODE == 1) *pick = -1;
+  if (cnt <= 0) return 0.0f;
+  if (vec && cnt == 64) {
+    const uint4* rp = reinterpret_cast<const uint4*>(static_cast<const char*>(row) + (size_t)(e0 + b) * (DT == 1 ? 2 : 4));
+#pragma unroll 2
+    for (int i = 0; i < 64 / PER; ++i) {
+      float x[PER];
+      unpack_vec<DT>(__ldca(rp + i), x);
+#pragma unroll
+      for (int e = 0; e < PER; ++e) {
+        const int k = b + i * PER + e;
+        const float w = (k == skip || x[e] == -INFINITY) ? 0.0f : ex2(fmaf(x[e], c, -mc));
+        if (MODE == 0) {
+          sum += w;
+        } else if (w > 0.0f) {
+          run += w;
+          last = k;
+          lastw = w;
+          if (run > t) {
+            *pick = k;
+            *w_at = w;
+            return 0.0f;
+          }
+        }
+      }
+    }
+  } else {
+    for (int j = 0; j < cnt; ++j) {
+      const int k = b + j;
+      const float x = entry_l1<DT>(row, (int64_t)e0 + k);
+      const float w = (k == skip || x == -INFINITY) ? 0.0f : ex2(fmaf(x, c, -mc));
+      if (MODE == 0) {
+        sum += w;
+      } else if (w > 0.0f) {
+        run += w;
+        last = k;
+        lastw = w;
+        if (run > t) {
+          *pick = k;
+          *w_at = w;
+          return 0.0f;
+        }
+      }
+    }
+  }
+  if (MODE == 1) {
+    *pick = last;
+    *w_at = lastw;
+  }
+  return sum;
+}
+
+// weight of one unit of a row (entries e0 .. e0 + n_el - 1), skip excluded
+template <int DT>
+__device__ __forceinline__ float unit_weight(const void* row, int e0, int n_el, bool vec, int lane, float c, float mc,
+                                             int skip) {
+  int pk;
+  float wa;
+  return warp_sum(unit_lane_pass<DT, 0>(row, e0, n_el, vec, lane, c, mc, skip, 0.0f, 0.0f, &pk, &wa));
+}
+
+// inverse CDF inside one unit: the first entry (in index order) whose running
+// sum from `before` exceeds t; the last entry with positive weight when
+// rounding leaves none (before < 0: always the last).  Returns the unit index
+// and *w_at its weight.
+template <int DT>
+__device__ __forceinline__ int unit_draw(const void* row, int e0, int n_el, bool vec, int lane, float c, float mc,
+                                         int skip, float before, float t, float* w_at) {
+  int pk;
+  float wa;
+  const float lsum = unit_lane_pass<DT, 0>(row, e0, n_el, vec, lane, c, mc, skip, 0.0f, 0.0f, &pk, &wa);
+  const float incl = warp_incl_scan(lsum);
+  const float tr = t - before;
+  const unsigned hit = before < 0.0f ? 0u : __ballot_sync(0xFFFFFFFFu, incl > tr && lsum > 0.0f);
+  const unsigned has = __ballot_sync(0xFFFFFFFFu, lsum > 0.0f);
+  int src;
+  float run, tt;
+  if (hit) {
+    src = __ffs(hit) - 1;
+    run = incl - lsum;
+    tt = tr;
+  } else {
+    src = has ? 31 - __clz(has) : 0;
+    run = 0.0f;
+    tt = INFINITY;  // no crossing: the lane's last positive entry
+  }
+  int pick = -1;
+  float w = 0.0f;
+  if (lane == src) unit_lane_pass<DT, 1>(row, e0, n_el, vec, lane, c, mc, skip, run, tt, &pick, &w);
+  pick = __shfl_sync(0xFFFFFFFFu, pick, src);
+  *w_at = __shfl_sync(0xFFFFFFFFu, w, src);
+  return pick < 0 ? 0 : pick;
+}
+
 // ------------------------------------------------------------------ finalize
 __device__ __forceinline__ void write_invalid_chain(const VerifyParams& p, int r, int lane) {
   for (int j = lane; j <= p.L; j += 32) p.out_tokens[(int64_t)r * (p.L + 1) + j] = -1;
@@ -762,7 +941,7 @@ __device__ void finalize_chain_greedy(const VerifyParams& p, int r, int base, in
   const int a_stop = __shfl_sync(0xFFFFFFFFu, a, stop);
   for (int j = lane; j <= p.L; j += 32) {
     int t = -1;
-    if (j < n_acc) t = y[j];
+    if (j < n_acc) t = j == lane ? yi : y[j];  // lane j holds y[j] (L < 32)
     if (j == n_acc) t = a_stop;
     p.out_tokens[(int64_t)r * (p.L + 1) + j] = t;
   }
@@ -782,40 +961,49 @@ template <int DT>
 __device__ void finalize_chain_sample(const VerifyParams& p, int r, int base, int ell, int lane) {
   const int32_t* y = p.chain + (int64_t)r * p.L;
   const uint8_t* pmr = p.pm ? p.pm + (int64_t)r * p.L : nullptr;
-  // (max, sum) of each p row (lane i merges row i) and each q row (lane i-1
-  // merges the draft row of position i): every lane reads its own row's unit
-  // partials with independent loads
-  float mrow = 0.0f, srow = 0.0f, mq = 0.0f, sq = 0.0f;
-  int use_q_lane = 0;
-  if (lane <= ell) {
-    const float2 ms = merge_row_lane(p, base + lane);
-    mrow = ms.x;
-    srow = ms.y;
-  }
-  if (lane < ell) {
-    use_q_lane = (p.use_q && pmr && pmr[lane] == 0 && lane + 1 <= p.K) ? 1 : 0;
-    if (use_q_lane) {
-      const float2 ms = merge_row_lane(p, q_slot_of(p, r, lane + 1));
-      mq = ms.x;
-      sq = ms.y;
-    }
-  }
-  // accept tests: lane i-1 tests position i
+  // lane i-1 tests position i: its token's logits are loaded first, so that
+  // those loads overlap the merges below
   const bool tested = lane < ell;
-  float ratio = -1.0f, u = -1.0f, u2 = 0.0f;
-  bool acc = false;
-  int yi = -1;
+  int use_q_lane = 0, yi = -1;
+  float zp = 0.0f, zq = 0.0f;
   if (tested) {
     yi = y[lane];
+    use_q_lane = (p.use_q && pmr && pmr[lane] == 0 && lane + 1 <= p.K) ? 1 : 0;
+    if (yi >= 0 && yi < p.vocab) {
+      zp = load_one<DT>(p.logits, (int64_t)(base + lane) * p.vocab + yi);
+      if (use_q_lane) zq = load_one<DT>(p.draft, ((int64_t)r * p.K + lane) * p.vocab + yi);
+    }
+  }
+  // (max, sum) of the p rows 0 .. ell (row k = lane k) and of the q rows of
+  // the positions that carry one (row ell + 1 + j = the j-th such position),
+  // merged by the whole warp at once
+  const unsigned qmask = __ballot_sync(0xFFFFFFFFu, use_q_lane);
+  const int R = ell + 1 + __popc(qmask);
+  auto slot_of = [&](int k) -> int {
+    if (k <= ell) return base + k;
+    unsigned mm = qmask;
+    int i = 0;
+    for (int t = 0; t <= k - ell - 1; ++t) {
+      i = __ffs(mm) - 1;
+      mm &= mm - 1u;
+    }
+    return q_slot_of(p, r, i + 1);
+  };
+  float2 prow, qrow;
+  merge_rows_warp(p, R, slot_of, lane, lane <= ell ? lane : -1, &prow,
+                  use_q_lane ? ell + 1 + __popc(qmask & ((1u << lane) - 1u)) : -1, &qrow);
+  const float mrow = prow.x, srow = prow.y, mq = qrow.x, sq = qrow.y;
+  // accept tests
+  float ratio = -1.0f, u = -1.0f, u2 = 0.0f;
+  bool acc = false;
+  if (tested) {
     round_uniforms(p.seed, p.step, (uint32_t)r, (uint32_t)(lane + 1), &u, &u2);
     if (yi < 0 || yi >= p.vocab) {
       set_status(p.ws.status, SPEC_DEV_BAD_TOKEN);
       ratio = 0.0f;
     } else {
-      const float zp = load_one<DT>(p.logits, (int64_t)(base + lane) * p.vocab + yi);
       const float py = ex2((zp - mrow) * p.c) / srow;
       if (use_q_lane) {
-        const float zq = load_one<DT>(p.draft, ((int64_t)r * p.K + lane) * p.vocab + yi);
         const float qy = ex2((zq - mq) * p.c) / sq;
         ratio = py / qy;
       } else {
@@ -834,7 +1022,7 @@ __device__ void finalize_chain_sample(const VerifyParams& p, int r, int base, in
     if (p.dbg_u) p.dbg_u[(int64_t)r * p.L + j] = tj ? u : -1.0f;
   }
   for (int j = lane; j <= p.L; j += 32)
-    if (j != n_acc) p.out_tokens[(int64_t)r * (p.L + 1) + j] = j < n_acc ? y[j] : -1;
+    if (j != n_acc) p.out_tokens[(int64_t)r * (p.L + 1) + j] = j < n_acc ? (j == lane ? yi : y[j]) : -1;
   if (lane == 0) {
     p.n_accepted[r] = n_acc;
     p.n_emitted[r] = n_acc + 1;
@@ -876,48 +1064,36 @@ __device__ void finalize_chain_sample(const VerifyParams& p, int r, int base, in
   const int yv = (y_stop >= 0 && y_stop < p.vocab) ? y_stop : -1;  // point mass to remove
   const int u_y = yv >= 0 ? yv / SPEC_UNIT : -1;
   const bool vec = p.vec_ok != 0;
-  // weight of the unit holding y with y removed: a rescan of that one unit
-  float w_y = 0.0f;
-  if (u_y >= 0) {
-    float v[64];
-    const int e0 = u_y * SPEC_UNIT;
-    const int n_el = min(SPEC_UNIT, p.vocab - e0);
-    load_unit_contig<DT>(row, e0, n_el, vec, lane, v);
-    const float mc = m * p.c;
-    float a0 = 0.0f, a1 = 0.0f;
-#pragma unroll
-    for (int j = 0; j < 64; ++j) {
-      const float w = (e0 + 64 * lane + j != yv && v[j] != -INFINITY) ? ex2(fmaf(v[j], p.c, -mc)) : 0.0f;
-      if (j & 1)
-        a1 += w;
-      else
-        a0 += w;
-    }
-    w_y = warp_sum(a0 + a1);
-  }
+  const float zy = __shfl_sync(0xFFFFFFFFu, zp, stop);  // y's logit, loaded for its test
   auto w_plain = [&](int uu) -> float {
     const float2 t = __ldcg(&p.ws.partial[(int64_t)slot * p.ws.units + uu]);
     if (t.x == -INFINITY) return 0.0f;
     return t.y * ex2((t.x - m) * p.c);
   };
-  auto w_removed = [&](int uu) -> float { return uu == u_y ? w_y : w_plain(uu); };
+  // The unit holding y, with y removed: first its partial less y's own term
+  // (no rescan).  Where the residual mass is under 1/16 of the row's, that
+  // difference can lose the precision the draw needs, and the unit is
+  // rescanned instead.
+  const float w_self = yv >= 0 ? ex2(fmaf(zy, p.c, -m * p.c)) : 0.0f;
+  auto w_fast = [&](int uu) -> float {
+    const float w = w_plain(uu);
+    return uu == u_y ? fmaxf(w - w_self, 0.0f) : w;
+  };
+  Crossing cr = find_unit(p.units, u2_stop, lane, w_fast);
+  const float mc = m * p.c;
+  if (yv >= 0 && !(cr.total >= 0.0625f * s)) {
+    const int ey = u_y * SPEC_UNIT;
+    const float w_y = unit_weight<DT>(row, ey, min(SPEC_UNIT, p.vocab - ey), vec, lane, p.c, mc, yv - ey);
+    cr = find_unit(p.units, u2_stop, lane, [&](int uu) -> float { return uu == u_y ? w_y : w_plain(uu); });
+  }
   // the draw removes y when the residual mass (unnormalised) exceeds 1e-30
   // of the row's mass, else it falls back to p itself
-  Crossing cr = find_unit(p.units, u2_stop, lane, w_removed);
   const bool remove = yv >= 0 && cr.total > 1e-30f * s;
   if (yv >= 0 && !remove) cr = find_unit(p.units, u2_stop, lane, w_plain);
-  float v[64];
   const int e0 = cr.unit * SPEC_UNIT;
-  const int n_el = min(SPEC_UNIT, p.vocab - e0);
-  load_unit_contig<DT>(row, e0, n_el, vec, lane, v);
-  const float mc = m * p.c;
-#pragma unroll
-  for (int j = 0; j < 64; ++j) {
-    const int gi = e0 + 64 * lane + j;
-    v[j] = ((remove && gi == yv) || v[j] == -INFINITY) ? 0.0f : ex2(fmaf(v[j], p.c, -mc));
-  }
   float r_at;
-  const int pick = find_in_unit(v, cr.before, cr.t, lane, &r_at);
+  const int pick = unit_draw<DT>(row, e0, min(SPEC_UNIT, p.vocab - e0), vec, lane, p.c, mc,
+                                 remove ? yv - e0 : -1, cr.before, cr.t, &r_at);
   if (lane == 0) {
     p.out_tokens[(int64_t)r * (p.L + 1) + n_acc] = e0 + pick;
     if (p.dbg_resid) p.dbg_resid[r] = r_at / cr.total;
