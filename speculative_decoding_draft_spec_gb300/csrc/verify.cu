@@ -799,22 +799,40 @@ __device__ __forceinline__ float entry_l1(const void* row, int64_t i) {
   return __ldca(static_cast<const float*>(row) + i);
 }
 
-// the lane's entries in order, from running sum `run`: mode 0 returns their
-// total weight; mode 1 stops at the first entry whose running sum exceeds t
-// (returning its unit index and weight), else returns the last entry with
-// positive weight (-1 if none)
-template <int DT, int MODE>
-__device__ __forceinline__ float unit_lane_pass(const void* row, int e0, int n_el, bool vec, int lane, float c,
-                                                float mc, int skip, float run, float t, int* pick, float* w_at) {
+// the lane's entries in order, from running sum `run`, with weight wf(k, x)
+// of unit entry k with logit x: mode 0 returns their total; mode 1 stops at
+// the first entry whose running sum exceeds t (its unit index in *pick,
+// weight in *w_at), else gives the last entry with positive weight (-1 if none)
+template <int DT, int MODE, typename WF>
+__device__ __forceinline__ float unit_lane_pass(const void* row, int e0, int n_el, bool vec, int lane, float run,
+                                                float t, int* pick, float* w_at, WF wf) {
   constexpr int PER = DT == 1 ? 8 : 4;
+  constexpr size_t ESZ = DT == 1 ? 2 : 4;
   const int b = 64 * lane;
   const int cnt = min(64, n_el - b);
   float sum = 0.0f, lastw = 0.0f;
   int last = -1;
   if (MODE == 1) *pick = -1;
   if (cnt <= 0) return 0.0f;
+  auto take = [&](int k, float w) -> bool {  // true: crossing found
+    if (MODE == 0) {
+      sum += w;
+    } else if (w > 0.0f) {
+      run += w;
+      last = k;
+      lastw = w;
+      if (run > t) {
+        *pick = k;
+        *w_at = w;
+        return true;
+      }
+    }
+    return false;
+  };
   if (vec && cnt == 64) {
-    const uint4* rp = reinterpret_cast<const uint4*>(static_cast<const char*>(row) + (size_t)(e0 + b) * (DT == 1 ? 2 : 4));
+    const uint4* rp = reinterpret_cast<const uint4*>(static_cast<const char*>(row) + (size_t)(e0 + b) * ESZ);
+    if (DT != 1)  // the lane's 256 bytes span two 128-byte lines: ask for both at once
+      asm volatile("prefetch.global.L1 [%0];" ::"l"(rp + 8));
 #pragma unroll 2
     for (int i = 0; i < 64 / PER; ++i) {
       float x[PER];
@@ -822,38 +840,14 @@ __device__ __forceinline__ float unit_lane_pass(const void* row, int e0, int n_e
 #pragma unroll
       for (int e = 0; e < PER; ++e) {
         const int k = b + i * PER + e;
-        const float w = (k == skip || x[e] == -INFINITY) ? 0.0f : ex2(fmaf(x[e], c, -mc));
-        if (MODE == 0) {
-          sum += w;
-        } else if (w > 0.0f) {
-          run += w;
-          last = k;
-          lastw = w;
-          if (run > t) {
-            *pick = k;
-            *w_at = w;
-            return 0.0f;
-          }
-        }
+        if (take(k, wf(k, x[e]))) return 0.0f;
       }
     }
   } else {
     for (int j = 0; j < cnt; ++j) {
       const int k = b + j;
       const float x = entry_l1<DT>(row, (int64_t)e0 + k);
-      const float w = (k == skip || x == -INFINITY) ? 0.0f : ex2(fmaf(x, c, -mc));
-      if (MODE == 0) {
-        sum += w;
-      } else if (w > 0.0f) {
-        run += w;
-        last = k;
-        lastw = w;
-        if (run > t) {
-          *pick = k;
-          *w_at = w;
-          return 0.0f;
-        }
-      }
+      if (take(k, wf(k, x))) return 0.0f;
     }
   }
   if (MODE == 1) {
@@ -863,25 +857,16 @@ __device__ __forceinline__ float unit_lane_pass(const void* row, int e0, int n_e
   return sum;
 }
 
-// weight of one unit of a row (entries e0 .. e0 + n_el - 1), skip excluded
-template <int DT>
-__device__ __forceinline__ float unit_weight(const void* row, int e0, int n_el, bool vec, int lane, float c, float mc,
-                                             int skip) {
-  int pk;
-  float wa;
-  return warp_sum(unit_lane_pass<DT, 0>(row, e0, n_el, vec, lane, c, mc, skip, 0.0f, 0.0f, &pk, &wa));
-}
-
 // inverse CDF inside one unit: the first entry (in index order) whose running
 // sum from `before` exceeds t; the last entry with positive weight when
 // rounding leaves none (before < 0: always the last).  Returns the unit index
 // and *w_at its weight.
-template <int DT>
-__device__ __forceinline__ int unit_draw(const void* row, int e0, int n_el, bool vec, int lane, float c, float mc,
-                                         int skip, float before, float t, float* w_at) {
+template <int DT, typename WF>
+__device__ __forceinline__ int unit_draw(const void* row, int e0, int n_el, bool vec, int lane, float before, float t,
+                                         float* w_at, WF wf) {
   int pk;
   float wa;
-  const float lsum = unit_lane_pass<DT, 0>(row, e0, n_el, vec, lane, c, mc, skip, 0.0f, 0.0f, &pk, &wa);
+  const float lsum = unit_lane_pass<DT, 0>(row, e0, n_el, vec, lane, 0.0f, 0.0f, &pk, &wa, wf);
   const float incl = warp_incl_scan(lsum);
   const float tr = t - before;
   const unsigned hit = before < 0.0f ? 0u : __ballot_sync(0xFFFFFFFFu, incl > tr && lsum > 0.0f);
@@ -899,11 +884,20 @@ __device__ __forceinline__ int unit_draw(const void* row, int e0, int n_el, bool
   }
   int pick = -1;
   float w = 0.0f;
-  if (lane == src) unit_lane_pass<DT, 1>(row, e0, n_el, vec, lane, c, mc, skip, run, tt, &pick, &w);
+  if (lane == src) unit_lane_pass<DT, 1>(row, e0, n_el, vec, lane, run, tt, &pick, &w, wf);
   pick = __shfl_sync(0xFFFFFFFFu, pick, src);
   *w_at = __shfl_sync(0xFFFFFFFFu, w, src);
   return pick < 0 ? 0 : pick;
 }
+
+// the weight 2^(z c - mc) of a logit z (0 for -inf and for entry `skip`)
+struct SoftW {
+  float c, mc;
+  int skip;
+  __device__ __forceinline__ float operator()(int k, float x) const {
+    return (k == skip || x == -INFINITY) ? 0.0f : ex2(fmaf(x, c, -mc));
+  }
+};
 
 // ------------------------------------------------------------------ finalize
 __device__ __forceinline__ void write_invalid_chain(const VerifyParams& p, int r, int lane) {
@@ -1083,7 +1077,10 @@ __device__ void finalize_chain_sample(const VerifyParams& p, int r, int base, in
   const float mc = m * p.c;
   if (yv >= 0 && !(cr.total >= 0.0625f * s)) {
     const int ey = u_y * SPEC_UNIT;
-    const float w_y = unit_weight<DT>(row, ey, min(SPEC_UNIT, p.vocab - ey), vec, lane, p.c, mc, yv - ey);
+    int pk;
+    float wa;
+    const float w_y = warp_sum(unit_lane_pass<DT, 0>(row, ey, min(SPEC_UNIT, p.vocab - ey), vec, lane, 0.0f, 0.0f,
+                                                     &pk, &wa, SoftW{p.c, mc, yv - ey}));
     cr = find_unit(p.units, u2_stop, lane, [&](int uu) -> float { return uu == u_y ? w_y : w_plain(uu); });
   }
   // the draw removes y when the residual mass (unnormalised) exceeds 1e-30
@@ -1092,8 +1089,8 @@ __device__ void finalize_chain_sample(const VerifyParams& p, int r, int base, in
   if (yv >= 0 && !remove) cr = find_unit(p.units, u2_stop, lane, w_plain);
   const int e0 = cr.unit * SPEC_UNIT;
   float r_at;
-  const int pick = unit_draw<DT>(row, e0, min(SPEC_UNIT, p.vocab - e0), vec, lane, p.c, mc,
-                                 remove ? yv - e0 : -1, cr.before, cr.t, &r_at);
+  const int pick = unit_draw<DT>(row, e0, min(SPEC_UNIT, p.vocab - e0), vec, lane, cr.before, cr.t, &r_at,
+                                 SoftW{p.c, mc, remove ? yv - e0 : -1});
   if (lane == 0) {
     p.out_tokens[(int64_t)r * (p.L + 1) + n_acc] = e0 + pick;
     if (p.dbg_resid) p.dbg_resid[r] = r_at / cr.total;
