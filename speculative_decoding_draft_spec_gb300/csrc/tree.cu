@@ -56,6 +56,22 @@ struct TreeParams {
   uint32_t* status;
 };
 
+// the lowest-index drafter child c0 .. c0 + Kc - 1 with token x, or -1; the
+// first four tokens are loaded together (the merge's chain of steps waits on
+// this lookup)
+__device__ __forceinline__ int32_t child_with(const int32_t* s_tok, int32_t c0, int32_t Kc, int32_t x) {
+  int32_t t[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) t[k] = k < Kc ? s_tok[c0 + k] : 0;
+  int32_t node = -1;
+#pragma unroll
+  for (int k = 3; k >= 0; --k)
+    if (k < Kc && t[k] == x) node = c0 + k;
+  for (int32_t k = 4; k < Kc && node < 0; ++k)
+    if (s_tok[c0 + k] == x) node = c0 + k;
+  return node;
+}
+
 __global__ void __launch_bounds__(TB_THREADS) build_tree_kernel(TreeParams p) {
   __shared__ int32_t s_tok[TB_THREADS], s_par[TB_THREADS], s_dk[TB_THREADS], s_depth[TB_THREADS];
   __shared__ uint8_t s_agree[TB_THREADS], s_contra[TB_THREADS];
@@ -135,7 +151,7 @@ __global__ void __launch_bounds__(TB_THREADS) build_tree_kernel(TreeParams p) {
     const int levels = s_levels;
     if (NC <= 32) {
       // one chain per lane, its current node in a register; the first chain
-      // with the same (parent, token) found by shuffles over the lower lanes
+      // with the same (parent, token): the lowest lane of its match group
       const int c = lane;
       const int32_t gl = c < NC ? s_len[c] : 0;
       int32_t cur = c == 0 ? 0 : 1 + (c - 1) * Kc;
@@ -148,22 +164,19 @@ __global__ void __launch_bounds__(TB_THREADS) build_tree_kernel(TreeParams p) {
         if (active) {
           const int32_t c0 = cur < ND ? s_dk[cur] : -1;
           if (c0 >= 0) {
-            for (int32_t k = 0; k < Kc; ++k)
-              if (node < 0 && s_tok[c0 + k] == xt) node = c0 + k;
+            node = child_with(s_tok, c0, Kc, xt);
             for (int32_t k = 0; k < Kc; ++k)
               if (c0 + k != node) s_contra[c0 + k] = 1;
             if (node >= 0) s_agree[node] = 1;
           }
         }
         const bool need = active && node < 0;
-        int first = lane;
-        for (int k = 0; k < NC - 1; ++k) {
-          const int32_t op = __shfl_sync(0xFFFFFFFFu, cur, k);
-          const int32_t ox = __shfl_sync(0xFFFFFFFFu, xt, k);
-          const bool on = __shfl_sync(0xFFFFFFFFu, need, k);
-          if (k < first && on && op == cur && ox == xt) first = k;
+        const unsigned nmask = __ballot_sync(0xFFFFFFFFu, need);
+        if (need) {
+          const unsigned long long key = ((unsigned long long)(uint32_t)cur << 32) | (uint32_t)xt;
+          const int first = __ffs(__match_any_sync(nmask, key)) - 1;
+          node = ND + first * Lg + (d - first - 1);
         }
-        if (need) node = ND + first * Lg + (d - first - 1);
         if (active) {
           s_node[jj] = node;
           s_ipar[jj] = cur;
@@ -183,8 +196,7 @@ __global__ void __launch_bounds__(TB_THREADS) build_tree_kernel(TreeParams p) {
             xt = s_itok[jj];
             const int32_t c0 = par < ND ? s_dk[par] : -1;
             if (c0 >= 0) {
-              for (int32_t k = 0; k < Kc; ++k)
-                if (node < 0 && s_tok[c0 + k] == xt) node = c0 + k;
+              node = child_with(s_tok, c0, Kc, xt);
               for (int32_t k = 0; k < Kc; ++k)
                 if (c0 + k != node) s_contra[c0 + k] = 1;
               if (node >= 0) s_agree[node] = 1;
