@@ -19,20 +19,23 @@
 // holds each token's evidence: the length of the copy it continues (capped at
 // copy_cap) for steps 1-2, minus the follower's count for step 3.
 //
-// GB300 layout: one CTA of 256 threads per (chain, request).  The chain's
-// steps are sequential; a lookup is one block-wide pass over the text (each
-// thread tests its end positions, extends the matches it finds, and the
-// block takes the max of (l << 32 | j)), a follower step one pass that counts
-// followers in a shared-memory hash table (atomics) and one max over it.  A
-// passage is read from a shared-memory copy of its next 64 tokens.  All
-// threads carry the same chain state, so every branch is block-uniform.
+// GB300 layout: one CTA of 256 threads per (chain, request).  The request's
+// text is staged in shared memory once (when it fits: FL_STAGE_MAX tokens),
+// so the passes below read on-chip memory instead of making one memory round
+// trip per position.  The chain's steps are sequential; a lookup is one
+// block-wide pass over the text (each thread tests its end positions four at
+// a time, extends the matches it finds, and the block takes the max of
+// (l << 32 | j)), a follower step one pass that counts followers in a
+// shared-memory hash table (atomics) and one max over it.  Reading on along a
+// passage needs no lookup, so a whole run of such steps is one parallel copy.
+// All threads carry the same chain state, so every branch is block-uniform.
 #include "common.cuh"
 
 namespace spec {
 
 #define FL_THREADS 256
 #define FL_HASH 2048  // follower table entries (a power of two)
-#define FL_PBUF 64    // passage tokens staged at a time
+#define FL_STAGE_MAX 16384  // longest text staged in shared memory (64 KB)
 
 struct FillParams {
   const int32_t* hist;
@@ -41,6 +44,7 @@ struct FillParams {
   int32_t P, Kc;
   const int32_t* cand_tok;
   int32_t n_min, copy_cap, max_depth, Lg;
+  int32_t stage;  // the texts are staged in shared memory (stride <= FL_STAGE_MAX)
   int32_t* ng_tok;
   int32_t* ng_len;
   int32_t* ng_ev;
@@ -62,11 +66,12 @@ __device__ __forceinline__ unsigned long long block_max_u64(unsigned long long v
 }
 
 __global__ void __launch_bounds__(FL_THREADS) ngram_fill_kernel(FillParams p) {
-  extern __shared__ int32_t s_ext[];  // [P + Lg]: the picks on the path, then the chain
+  // [stride] the staged text (when p.stage), then [P + Lg + 1]: the picks on
+  // the path, then the chain
+  extern __shared__ __align__(16) int32_t s_dyn[];
   __shared__ unsigned long long s_key[FL_HASH];  // (1 << 32) | follower, 0 = empty
   __shared__ int32_t s_cnt[FL_HASH], s_last[FL_HASH];
   __shared__ unsigned long long s_red[FL_THREADS / 32];
-  __shared__ int32_t s_pbuf[FL_PBUF];
   __shared__ int32_t s_overflow;
   const int tid = threadIdx.x;
   const int c = blockIdx.x, r = blockIdx.y;
@@ -80,52 +85,76 @@ __global__ void __launch_bounds__(FL_THREADS) ngram_fill_kernel(FillParams p) {
   int32_t cap = p.max_depth - c;
   if (cap > p.Lg) cap = p.Lg;
   if (T < 1 || cap < 0) cap = 0;  // no anchor
+  int32_t* const s_x = s_dyn;
+  int32_t* const s_ext = s_dyn + (p.stage ? ((p.stride + 3) & ~3) : 0);
+  if (p.stage && cap > 0) {
+    // the text, four tokens per load where the row allows it
+    if ((p.stride & 3) == 0 && (reinterpret_cast<uintptr_t>(x) & 15u) == 0) {
+      const int4* x4 = reinterpret_cast<const int4*>(x);
+      for (int i = tid; 4 * i < T; i += FL_THREADS) reinterpret_cast<int4*>(s_x)[i] = __ldg(x4 + i);
+    } else {
+      for (int i = tid; i < T; i += FL_THREADS) s_x[i] = __ldg(x + i);
+    }
+  }
+  const int32_t* const xs = p.stage ? s_x : x;  // the text, staged or in memory
   for (int i = tid; i < c; i += FL_THREADS) s_ext[i] = p.cand_tok[((int64_t)r * p.P + i) * p.Kc];
   if (tid == 0) s_overflow = 0;
   int32_t* out = p.ng_tok + ((int64_t)r * C + c) * p.Lg;
   int32_t* ev = p.ng_ev + ((int64_t)r * C + c) * p.Lg;
   __syncthreads();
   // ctx = x ++ s_ext[0 .. m-1]
-  auto ctx = [&](int64_t i) -> int32_t { return i < T ? __ldg(x + i) : s_ext[i - T]; };
+  auto ctx = [&](int64_t i) -> int32_t { return i < T ? xs[i] : s_ext[i - T]; };
   int32_t m = c, n = 0;
   int64_t q = -1;            // the passage's next position in x, or -1
   int32_t run = 0;           // the length of the copy being continued
-  int64_t pq0 = 0;           // s_pbuf holds x[pq0 .. pq0 + pn - 1]
-  int32_t pn = 0;
   while (n < cap) {
     int32_t y = -1, e = 0;
     bool found = false;
     if (q >= 0 && q <= T - 1) {
-      if (!(q >= pq0 && q < pq0 + pn)) {
-        pq0 = q;
-        pn = (int32_t)min((int64_t)FL_PBUF, (int64_t)T - q);
-        if (tid < pn) s_pbuf[tid] = __ldg(x + q + tid);
-        __syncthreads();
+      // reading along the passage needs no lookup: the next k tokens of the
+      // text at once, each with the copy length it continues
+      const int32_t k = (int32_t)min((int64_t)(cap - n), (int64_t)T - q);
+      for (int i = tid; i < k; i += FL_THREADS) {
+        const int32_t t = xs[q + i];
+        out[n + i] = t;
+        ev[n + i] = min(run + 1 + i, p.copy_cap);
+        s_ext[m + i] = t;
       }
-      y = s_pbuf[q - pq0];
-      ++q;
-      run = min(run + 1, p.copy_cap);
-      e = run;
-      found = true;
+      n += k;
+      m += k;
+      q += k;
+      run = min(run + k, p.copy_cap);
+      __syncthreads();  // the new tokens are visible to every thread's ctx
+      continue;
     } else {
       // the earlier occurrence of ctx: the largest (l, j)
       const int64_t len = (int64_t)T + m;
       const int32_t last = ctx(len - 1);
       unsigned long long best = 0;
-      for (int64_t j = tid; j <= (int64_t)T - 2; j += FL_THREADS) {
-        if (__ldg(x + j) != last) continue;
-        const int32_t lim = (int32_t)min((int64_t)p.copy_cap, j + 1);
-        int32_t l = 1;
-        while (l < lim && __ldg(x + j - l) == ctx(len - 1 - l)) ++l;
-        if (l >= p.n_min) {
-          const unsigned long long k = ((unsigned long long)l << 32) | (unsigned long long)j;
-          best = k > best ? k : best;
+      for (int64_t j0 = tid; j0 <= (int64_t)T - 2; j0 += 4 * FL_THREADS) {
+        int32_t v[4];  // four end positions' tokens, loaded together
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int64_t j = j0 + u * FL_THREADS;
+          v[u] = j <= (int64_t)T - 2 ? xs[j] : ~last;
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          if (v[u] != last) continue;
+          const int64_t j = j0 + u * FL_THREADS;
+          const int32_t lim = (int32_t)min((int64_t)p.copy_cap, j + 1);
+          int32_t l = 1;
+          while (l < lim && xs[j - l] == ctx(len - 1 - l)) ++l;
+          if (l >= p.n_min) {
+            const unsigned long long k = ((unsigned long long)l << 32) | (unsigned long long)j;
+            best = k > best ? k : best;
+          }
         }
       }
       best = block_max_u64(best, s_red);
       if (best != 0ull) {
         const int64_t j = (int64_t)(uint32_t)best;
-        y = __ldg(x + j + 1);
+        y = xs[j + 1];
         q = j + 2;
         run = (int32_t)(best >> 32);
         e = run;
@@ -140,8 +169,8 @@ __global__ void __launch_bounds__(FL_THREADS) ngram_fill_kernel(FillParams p) {
         }
         __syncthreads();
         for (int64_t j = 2 + tid; j <= (int64_t)T - 2; j += FL_THREADS) {
-          if (__ldg(x + j) != d || __ldg(x + j - 1) != b || __ldg(x + j - 2) != a) continue;
-          const int32_t f = __ldg(x + j + 1);
+          if (xs[j] != d || xs[j - 1] != b || xs[j - 2] != a) continue;
+          const int32_t f = xs[j + 1];
           const unsigned long long key = (1ull << 32) | (unsigned long long)(uint32_t)f;
           uint32_t h = ((uint32_t)f * 2654435761u) >> (32 - 11);
           bool placed = false;
@@ -168,7 +197,7 @@ __global__ void __launch_bounds__(FL_THREADS) ngram_fill_kernel(FillParams p) {
           // more distinct followers than the table holds: the chain stops here
           if (tid == 0) set_status(p.status, SPEC_DEV_OVERFLOW);
         } else if (top != 0ull) {
-          y = __ldg(x + (int64_t)(uint32_t)top + 1);
+          y = xs[(int64_t)(uint32_t)top + 1];
           e = -(int32_t)(top >> 32);
           q = -1;
           run = 0;
@@ -215,7 +244,9 @@ extern "C" cudaError_t spec_launch_ngram_fill(const int32_t* hist, int64_t hist_
   fp.ng_len = ng_len;
   fp.ng_ev = ng_ev;
   fp.status = status;
-  const size_t smem = (size_t)(P + Lg + 1) * sizeof(int32_t);
+  fp.stage = hist_stride <= FL_STAGE_MAX ? 1 : 0;
+  const size_t smem =
+      ((fp.stage ? (size_t)((hist_stride + 3) & ~(int64_t)3) : 0) + (size_t)(P + Lg + 1)) * sizeof(int32_t);
   cudaError_t e = cudaFuncSetAttribute(spec::ngram_fill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
