@@ -524,24 +524,6 @@ __device__ __forceinline__ float2 unit_softmax_scalar(const void* unit, int n_el
 }
 
 // ------------------------------------------------------------------ helpers
-// (max, sum) of a whole row from its unit partials; every lane gets the result
-__device__ __forceinline__ float2 merge_row(const VerifyParams& p, int slot, int lane) {
-  float m = -INFINITY, s = 0.0f;
-  for (int u = lane; u < p.units; u += 32) {
-    const float2 t = __ldcg(&p.ws.partial[(int64_t)slot * p.ws.units + u]);
-    if (t.x == -INFINITY) continue;
-    if (t.x > m) {
-      s = s * ex2((m - t.x) * p.c) + t.y;
-      m = t.x;
-    } else {
-      s += t.y * ex2((t.x - m) * p.c);
-    }
-  }
-  const float M = warp_max(m);
-  const float sc = (m == -INFINITY) ? 0.0f : s * ex2((m - M) * p.c);
-  return make_float2(M, warp_sum(sc));
-}
-
 // (m, s) pairs merged: s rescaled to the larger max (empty pairs have m = -inf)
 __device__ __forceinline__ void merge_ms(float& m, float& s, float m2, float s2, float c) {
   const float nm = fmaxf(m, m2);
@@ -1502,10 +1484,15 @@ __global__ void __launch_bounds__(SPEC_CTA_THREADS) resample_kernel(VerifyParams
   for (int64_t w = (int64_t)blockIdx.x * SPEC_WARPS_PER_CTA + warp; w < total; w += nwarps) {
     const int r = (int)(w / units);
     const int u = (int)(w - (int64_t)r * units);
-    const Record* recp = reinterpret_cast<const Record*>(p.ws.record) + r;
-    const int flag = __ldcg(&recp->flag);
-    if (!flag) continue;
-    const Record rec = *recp;
+    // the whole record in one round trip (four 16-byte loads)
+    Record rec;
+    {
+      const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const Record*>(p.ws.record) + r);
+      uint4* dst = reinterpret_cast<uint4*>(&rec);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) dst[q] = __ldcg(src + q);
+    }
+    if (!rec.flag) continue;
     const void* prow = static_cast<const char*>(p.logits) + (int64_t)rec.prow * p.vocab * esz;
     const void* qrow = static_cast<const char*>(p.draft) +
                        ((int64_t)r * p.K + rec.pos - 1) * p.vocab * esz;
@@ -1580,8 +1567,18 @@ __global__ void __launch_bounds__(SPEC_CTA_THREADS) resample_kernel(VerifyParams
 // (lo32(seed), hi32(seed)), a counter domain apart from verification's.
 template <int DT>
 __device__ void draw_draft(const VerifyParams& p, int row, int r, int k, int slot, int lane) {
-  const float2 mz = merge_row(p, slot, lane);
-  const float m = mz.x;
+  // the row's unit partials, lane l holding units [per l, per l + per) (the
+  // layout find_unit walks), loaded once for the row max and the weights
+  const int per = (p.units + 31) / 32, u0 = lane * per;
+  const float2* pr = &p.ws.partial[(int64_t)slot * p.ws.units];
+  float2 t4[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    t4[q] = (q < per && u0 + q < p.units) ? __ldcg(&pr[u0 + q]) : make_float2(-INFINITY, 0.0f);
+  float lm = fmaxf(fmaxf(t4[0].x, t4[1].x), fmaxf(t4[2].x, t4[3].x));
+  for (int q = 4; q < per; ++q)
+    if (u0 + q < p.units) lm = fmaxf(lm, __ldcg(&pr[u0 + q]).x);
+  const float m = warp_max(lm);
   uint32_t o[4];
   philox4x32_10((uint32_t)r, 0x40000000u + (uint32_t)(k + 1), (uint32_t)p.step, (uint32_t)(p.step >> 32),
                 (uint32_t)p.seed, (uint32_t)(p.seed >> 32), o);
@@ -1592,7 +1589,8 @@ __device__ void draw_draft(const VerifyParams& p, int row, int r, int k, int slo
   float total = 0.0f;
   if (m != -INFINITY) {
     auto w_plain = [&](int uu) -> float {
-      const float2 t = __ldcg(&p.ws.partial[(int64_t)slot * p.ws.units + uu]);
+      const int q = uu - u0;
+      const float2 t = q == 0 ? t4[0] : q == 1 ? t4[1] : q == 2 ? t4[2] : q == 3 ? t4[3] : __ldcg(&pr[uu]);
       if (t.x == -INFINITY) return 0.0f;
       return t.y * ex2((t.x - m) * p.c);
     };
