@@ -187,10 +187,13 @@ __global__ void __launch_bounds__(SPEC_CTA_THREADS, 1) ngram_kernel(NgramParams 
       }
       if (l >= p.n_min) top2_insert(b1, b2, ((unsigned long long)l << 32) | (uint32_t)j);
     };
-    // with n_min >= 2 a candidate must also match the second-to-last token
-    // (and then j >= 1 and cap >= 2)
-    const bool two = p.n_min >= 2;
-    const int32_t s1 = two ? sk[1] : 0;
+    // a candidate that also matches the second-to-last token (j >= 1, cap >=
+    // 2) is extended; one that does not has l = 1 exactly, so it needs no
+    // extension: with n_min = 1 it enters the top two as (1, j), with n_min >= 2
+    // it is dropped
+    const bool two_ok = p.cap >= 2 && T >= 2;
+    const int32_t s1 = two_ok ? sk[1] : 0;
+    const bool keep_ones = p.n_min <= 1;
     {
       // candidate filter on 16-byte groups: thread t reads groups t, t + 256, ...
       // (consecutive lanes, consecutive 16 bytes), NG_UNROLL groups in flight;
@@ -205,21 +208,32 @@ __global__ void __launch_bounds__(SPEC_CTA_THREADS, 1) ngram_kernel(NgramParams 
         for (int u = 0; u < NG_UNROLL; ++u) {
           const int32_t c = c0 + u * gstride;
           v[u] = c < j1 ? *reinterpret_cast<const int4*>(wv + c) : make_int4(0, 0, 0, 0);
-          prev[u] = (two && c < j1 && c >= j0 && c >= 1) ? wv[c - 1] : 0;
+          prev[u] = (two_ok && c < j1 && c >= j0 && c >= 1) ? wv[c - 1] : 0;
         }
 #pragma unroll
         for (int u = 0; u < NG_UNROLL; ++u) {
           const int32_t c = c0 + u * gstride;
           uint32_t m = (uint32_t)(v[u].x == last) | ((uint32_t)(v[u].y == last) << 1) |
                        ((uint32_t)(v[u].z == last) << 2) | ((uint32_t)(v[u].w == last) << 3);
-          if (two)
-            m &= (uint32_t)(prev[u] == s1 && c >= 1) | ((uint32_t)(v[u].x == s1) << 1) |
-                 ((uint32_t)(v[u].y == s1) << 2) | ((uint32_t)(v[u].z == s1) << 3);
           if (c < j0) m &= 0xFu << (j0 - c);                 // before this CTA's range
           if (c + 4 > j1) m &= (1u << max(0, j1 - c)) - 1u;  // past it
-          while (m) {
-            const int e = __ffs(m) - 1;
-            m &= m - 1u;
+          const uint32_t m2 =
+              two_ok ? m & ((uint32_t)(prev[u] == s1 && c >= 1) | ((uint32_t)(v[u].x == s1) << 1) |
+                            ((uint32_t)(v[u].y == s1) << 2) | ((uint32_t)(v[u].z == s1) << 3))
+                     : 0u;
+          if (keep_ones && (m & ~m2)) {
+            // single matches (l = 1) enter the top two as (1, j): no extension
+            uint32_t m1 = m & ~m2;
+            while (m1) {
+              const int e = __ffs(m1) - 1;
+              m1 &= m1 - 1u;
+              top2_insert(b1, b2, (1ull << 32) | (uint32_t)(c + e));
+            }
+          }
+          uint32_t mx = m2;
+          while (mx) {
+            const int e = __ffs(mx) - 1;
+            mx &= mx - 1u;
             extend(c + e);
           }
         }
