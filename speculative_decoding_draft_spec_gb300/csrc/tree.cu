@@ -39,6 +39,12 @@
 namespace spec {
 
 #define TB_THREADS 512
+#define TB_MERGE_WARPS 8  // warps that merge up to 32 chains (named barrier 1)
+
+// the merging warps' own barrier, so that the other warps keep working
+__device__ __forceinline__ void merge_bar() {
+  asm volatile("bar.sync 1, %0;" ::"n"(32 * TB_MERGE_WARPS) : "memory");
+}
 
 struct TreeParams {
   int32_t batch, P, Kc, n_chains, Lg, width;
@@ -138,103 +144,26 @@ __global__ void __launch_bounds__(TB_THREADS) build_tree_kernel(TreeParams p) {
   __syncthreads();  // s_levels is zero from here on
   if (j < NC) atomicMax(&s_levels, j + my_gl);  // chain c's steps sit at depths c+1 .. c+gl
   __syncthreads();
-  if (warp == 0) {
-    // the node of every step, depth by depth, by warp 0 (lane = chain; each
-    // chain has one step per depth).  A step's node depends only on its token
-    // path from the anchor: under a node with drafter children it is the
-    // lowest-index child with its token (agreed; the other children
-    // contradicted), else the n-gram child (parent, token), made by the first
-    // chain (in chain order) with that step at this depth -- among the lanes of
-    // one round of 32 chains the lowest lane of its __match_any_sync group.
-    // Provisional ids: drafter nodes their index, n-gram nodes ND + the item
-    // that makes them.
-    const int levels = s_levels;
-    if (NC <= 32) {
-      // one chain per lane, its current node in a register; the first chain
-      // with the same (parent, token): the lowest lane of its match group
-      const int c = lane;
-      const int32_t gl = c < NC ? s_len[c] : 0;
-      int32_t cur = c == 0 ? 0 : 1 + (c - 1) * Kc;
-      for (int d = 1; d <= levels; ++d) {
-        const int t = d - c - 1;
-        const bool active = c < NC && t >= 0 && t < gl;
-        const int jj = c * Lg + t;
-        const int32_t xt = active ? s_itok[jj] : 0;
-        int32_t node = -1;
-        if (active) {
-          const int32_t c0 = cur < ND ? s_dk[cur] : -1;
-          if (c0 >= 0) {
-            node = child_with(s_tok, c0, Kc, xt);
-            for (int32_t k = 0; k < Kc; ++k)
-              if (c0 + k != node) s_contra[c0 + k] = 1;
-            if (node >= 0) s_agree[node] = 1;
-          }
-        }
-        const bool need = active && node < 0;
-        const unsigned nmask = __ballot_sync(0xFFFFFFFFu, need);
-        if (need) {
-          const unsigned long long key = ((unsigned long long)(uint32_t)cur << 32) | (uint32_t)xt;
-          const int first = __ffs(__match_any_sync(nmask, key)) - 1;
-          node = ND + first * Lg + (d - first - 1);
-        }
-        if (active) {
-          s_node[jj] = node;
-          s_ipar[jj] = cur;
-          cur = node;
-        }
-      }
-      __syncwarp();
-    } else {
-      for (int d = 1; d <= levels; ++d) {
-        for (int cb = 0; cb < NC; cb += 32) {
-          const int c = cb + lane, t = d - c - 1;
-          const bool active = c < NC && t >= 0 && t < s_len[c];
-          const int jj = c * Lg + t;
-          int32_t par = -1, xt = 0, node = -1;
-          if (active) {
-            par = t == 0 ? (c == 0 ? 0 : 1 + (c - 1) * Kc) : s_node[jj - 1];
-            xt = s_itok[jj];
-            const int32_t c0 = par < ND ? s_dk[par] : -1;
-            if (c0 >= 0) {
-              node = child_with(s_tok, c0, Kc, xt);
-              for (int32_t k = 0; k < Kc; ++k)
-                if (c0 + k != node) s_contra[c0 + k] = 1;
-              if (node >= 0) s_agree[node] = 1;
-            }
-          }
-          const bool need = active && node < 0;
-          const unsigned mask = __ballot_sync(0xFFFFFFFFu, need);
-          if (need) {
-            const unsigned long long key = ((unsigned long long)(uint32_t)par << 32) | (uint32_t)xt;
-            const unsigned grp = __match_any_sync(mask, key);
-            const int c1 = cb + __ffs(grp) - 1;
-            node = ND + c1 * Lg + (d - c1 - 1);
-            // chains of earlier rounds come first in chain order
-            for (int c2 = 0; c2 < cb; ++c2) {
-              const int t2 = d - c2 - 1;
-              if (t2 < 0 || t2 >= s_len[c2]) continue;
-              const int j2 = c2 * Lg + t2;
-              if (s_itok[j2] == xt && s_ipar[j2] == par) {
-                node = ND + j2;
-                break;
-              }
-            }
-          }
-          if (active) {
-            s_node[jj] = node;
-            s_ipar[jj] = par;
-          }
-          __syncwarp();
-        }
-      }
-    }
-  } else {
-    // meanwhile: e^s of every drafter candidate for each of its three cases
-    // (plain, agreed, contradicted) and of an n-gram node, clamped to [-80, 80]
-    const double adj = (double)s_adj;
-    auto ex = [](double x) { return exp(x > 80.0 ? 80.0 : (x < -80.0 ? -80.0 : x)); };
-    // one exponential per thread: item w = 3 (v - 1) + case, then the n-gram node's
-    for (int w = j - 32; w <= 3 * (ND - 1); w += TB_THREADS - 32) {
+  // the node of every chain step.  A step's node depends only on its token
+  // path from the anchor (chain c's path: pick_0 .. pick_{c-1}, then its own
+  // tokens): while the path follows the picks it is the next pick; at the first
+  // step that leaves them, the lowest-index sibling with that step's token
+  // (when that position has candidates), else an n-gram node; below, n-gram
+  // nodes.  An n-gram node is shared by every chain whose path is the same up
+  // to its depth and is made by the first of them in chain order.  The parent
+  // of a step with drafter children has its taken child agreed and the others
+  // contradicted.  Provisional ids: drafter nodes their index, n-gram nodes
+  // ND + the item that makes them.
+  auto path_tok = [&](int c, int k) -> int32_t {  // token k (1-based) of chain c's path
+    return k <= c ? s_tok[1 + (k - 1) * Kc] : s_itok[c * Lg + (k - c - 1)];
+  };
+  // e^s of every drafter candidate for each of its three cases (plain,
+  // agreed, contradicted) and of an n-gram node, clamped to [-80, 80]: one
+  // exponential per thread, item w = 3 (v - 1) + case, then the n-gram node's
+  const double adj = (double)s_adj;
+  auto ex = [](double x) { return exp(x > 80.0 ? 80.0 : (x < -80.0 ? -80.0 : x)); };
+  auto exps = [&](int w0, int step) {
+    for (int w = w0; w <= 3 * (ND - 1); w += step) {
       if (w == 3 * (ND - 1)) {
         s_eng = ex((double)s_ngs);
         continue;
@@ -248,6 +177,114 @@ __global__ void __launch_bounds__(TB_THREADS) build_tree_kernel(TreeParams p) {
       else
         s_ec[v] = ex(sv - adj);
     }
+  };
+  if (NC <= 32 && warp < TB_MERGE_WARPS) {
+    // up to 32 chains: all steps at once by the first 8 warps (their own
+    // barrier), from two tables -- the depth at which each chain's path leaves
+    // the picks, and the common-prefix length of every pair of chains (c' < c,
+    // pair c (c - 1) / 2 + c') -- while the other warps form the exponentials
+    constexpr int MT = 32 * TB_MERGE_WARPS;
+    int32_t* const s_leave = s_bpar;  // [NC]
+    int32_t* const s_lcp = s_bucket;  // [NC (NC - 1) / 2]
+    const int kmax = NC + Lg;         // no path is longer
+    if (j < NC) s_leave[j] = j + s_len[j] + 1;  // past the last step: never leaves
+    for (int i = j; i < NC * NC; i += MT) {
+      const int c = i / NC, c2 = i - c * NC;
+      if (c2 < c) s_lcp[c * (c - 1) / 2 + c2] = min(c2 + s_len[c2], c + s_len[c]);
+    }
+    merge_bar();
+    for (int i = j; i < nct; i += MT) {
+      const int c = i / Lg, t = i - c * Lg, d = c + t + 1;
+      if (t < s_len[c] && (d > P || s_itok[i] != s_tok[1 + (d - 1) * Kc])) atomicMin(&s_leave[c], d);
+    }
+    for (int i = j; i < NC * NC * kmax; i += MT) {
+      const int k = 1 + i % kmax, cc = i / kmax, c = cc / NC, c2 = cc - c * NC;
+      // the paths of c2 < c agree on their first c2 tokens (both picks)
+      if (c2 < c && k > c2 && k <= min(c2 + s_len[c2], c + s_len[c]) && path_tok(c2, k) != path_tok(c, k))
+        atomicMin(&s_lcp[c * (c - 1) / 2 + c2], k - 1);
+    }
+    merge_bar();
+    for (int i = j; i < nct; i += MT) {
+      const int c = i / Lg, t = i - c * Lg;
+      if (t >= s_len[c]) continue;
+      const int d = c + t + 1, leave = s_leave[c];
+      auto node_at = [&](int dd) -> int32_t {
+        if (dd < leave) return 1 + (dd - 1) * Kc;  // the pick at depth dd
+        if (dd == leave && dd <= P) {
+          const int32_t x = path_tok(c, dd);
+          for (int k = 1; k < Kc; ++k)
+            if (s_tok[1 + (dd - 1) * Kc + k] == x) return 1 + (dd - 1) * Kc + k;  // a sibling
+        }
+        int first = c;
+        for (int c2 = 0; c2 < c; ++c2)
+          if (s_lcp[c * (c - 1) / 2 + c2] >= dd) {
+            first = c2;
+            break;
+          }
+        return ND + first * Lg + (dd - first - 1);
+      };
+      const int32_t node = node_at(d);
+      const int32_t par = t == 0 ? (c == 0 ? 0 : 1 + (c - 1) * Kc) : node_at(d - 1);
+      s_node[i] = node;
+      s_ipar[i] = par;
+      const int32_t c0 = par < ND ? s_dk[par] : -1;
+      if (c0 >= 0) {
+        for (int32_t k = 0; k < Kc; ++k)
+          if (c0 + k != node) s_contra[c0 + k] = 1;
+        if (node < ND) s_agree[node] = 1;
+      }
+    }
+  } else if (NC <= 32) {
+    exps(j - 32 * TB_MERGE_WARPS, TB_THREADS - 32 * TB_MERGE_WARPS);
+  } else if (warp == 0) {
+    // more than 32 chains: depth by depth by warp 0, 32 chains a round (lane
+    // = chain), the first chain with the same (parent, token) at a depth the
+    // lowest lane of its __match_any_sync group or an earlier round's chain
+    const int levels = s_levels;
+    for (int d = 1; d <= levels; ++d) {
+      for (int cb = 0; cb < NC; cb += 32) {
+        const int c = cb + lane, t = d - c - 1;
+        const bool active = c < NC && t >= 0 && t < s_len[c];
+        const int jj = c * Lg + t;
+        int32_t par = -1, xt = 0, node = -1;
+        if (active) {
+          par = t == 0 ? (c == 0 ? 0 : 1 + (c - 1) * Kc) : s_node[jj - 1];
+          xt = s_itok[jj];
+          const int32_t c0 = par < ND ? s_dk[par] : -1;
+          if (c0 >= 0) {
+            node = child_with(s_tok, c0, Kc, xt);
+            for (int32_t k = 0; k < Kc; ++k)
+              if (c0 + k != node) s_contra[c0 + k] = 1;
+            if (node >= 0) s_agree[node] = 1;
+          }
+        }
+        const bool need = active && node < 0;
+        const unsigned mask = __ballot_sync(0xFFFFFFFFu, need);
+        if (need) {
+          const unsigned long long key = ((unsigned long long)(uint32_t)par << 32) | (uint32_t)xt;
+          const unsigned grp = __match_any_sync(mask, key);
+          const int c1 = cb + __ffs(grp) - 1;
+          node = ND + c1 * Lg + (d - c1 - 1);
+          // chains of earlier rounds come first in chain order
+          for (int c2 = 0; c2 < cb; ++c2) {
+            const int t2 = d - c2 - 1;
+            if (t2 < 0 || t2 >= s_len[c2]) continue;
+            const int j2 = c2 * Lg + t2;
+            if (s_itok[j2] == xt && s_ipar[j2] == par) {
+              node = ND + j2;
+              break;
+            }
+          }
+        }
+        if (active) {
+          s_node[jj] = node;
+          s_ipar[jj] = par;
+        }
+        __syncwarp();
+      }
+    }
+  } else {
+    exps(j - 32, TB_THREADS - 32);  // meanwhile, by the other warps
   }
   __syncthreads();
   // the n-gram nodes in the order the sequential merge makes them: a step that
