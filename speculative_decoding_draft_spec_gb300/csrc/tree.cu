@@ -93,7 +93,6 @@ __global__ void __launch_bounds__(TB_THREADS) build_tree_kernel(TreeParams p) {
   int32_t* const s_before = s_ipar;
   __shared__ int32_t s_bucket[TB_THREADS], s_bpar[TB_THREADS], s_dcnt[TB_THREADS + 1], s_doff[TB_THREADS + 1];
   __shared__ int32_t s_N, s_maxd, s_levels, s_len[TB_THREADS], s_wcnt[TB_THREADS / 32];
-  __shared__ float s_ngs, s_adj;
   __shared__ double s_eng;
   const int r = blockIdx.x, j = threadIdx.x;
   const int lane = j & 31, warp = j >> 5;
@@ -106,8 +105,6 @@ __global__ void __launch_bounds__(TB_THREADS) build_tree_kernel(TreeParams p) {
       s_tok[0] = p.anchor[r];
       s_par[0] = -1;
       s_depth[0] = 0;
-      s_ngs = p.ng_score[r];
-      s_adj = p.ng_adj[r];
       s_dk[0] = P > 0 ? 1 : -1;
     } else {
       const int i = (j - 1) / Kc, k = (j - 1) - i * Kc;
@@ -141,9 +138,17 @@ __global__ void __launch_bounds__(TB_THREADS) build_tree_kernel(TreeParams p) {
     }
     s_len[j] = my_gl;
   }
-  __syncthreads();  // s_levels is zero from here on
-  if (j < NC) atomicMax(&s_levels, j + my_gl);  // chain c's steps sit at depths c+1 .. c+gl
-  __syncthreads();
+  if (NC > 32) {
+    __syncthreads();  // s_levels is zero from here on
+    if (j < NC) atomicMax(&s_levels, j + my_gl);  // chain c's steps sit at depths c+1 .. c+gl
+    __syncthreads();
+  } else if (warp >= TB_MERGE_WARPS) {
+    // the exponential warps signal that their part of the set-up is written
+    // and go on without waiting (they read nothing the others write)
+    asm volatile("bar.arrive 2, %0;" ::"n"(TB_THREADS) : "memory");
+  } else {
+    asm volatile("bar.sync 2, %0;" ::"n"(TB_THREADS) : "memory");
+  }
   // the node of every chain step.  A step's node depends only on its token
   // path from the anchor (chain c's path: pick_0 .. pick_{c-1}, then its own
   // tokens): while the path follows the picks it is the next pick; at the first
@@ -160,12 +165,12 @@ __global__ void __launch_bounds__(TB_THREADS) build_tree_kernel(TreeParams p) {
   // e^s of every drafter candidate for each of its three cases (plain,
   // agreed, contradicted) and of an n-gram node, clamped to [-80, 80]: one
   // exponential per thread, item w = 3 (v - 1) + case, then the n-gram node's
-  const double adj = (double)s_adj;
+  const double adj = (double)p.ng_adj[r];
   auto ex = [](double x) { return exp(x > 80.0 ? 80.0 : (x < -80.0 ? -80.0 : x)); };
   auto exps = [&](int w0, int step) {
     for (int w = w0; w <= 3 * (ND - 1); w += step) {
       if (w == 3 * (ND - 1)) {
-        s_eng = ex((double)s_ngs);
+        s_eng = ex((double)p.ng_score[r]);
         continue;
       }
       const int v = 1 + w / 3, cs = w - 3 * (v - 1);
