@@ -16,24 +16,25 @@
 //   s: the given drafter score + adj if agreed, else - adj if contradicted; or
 //     the n-gram score; clamped to [-80, 80];
 //   q_j = e^{s_j} / (1 + sum over the children c of parent(j) of e^{s_c})
-//     (children summed in index order), Q_j = Q_parent(j) q_j, in fp64;
+//     (children summed in index order), Q_j = the product of q along the path
+//     from the anchor, in fp64;
 //   order: Q descending, ties to the lower index; the tree: the anchor and the
 //     first width-1 candidates, depth-first with children in index order.
 //
 // GB300 layout: one CTA per request, one thread per candidate (at most 512),
-// everything in shared memory.  Warp 0 merges the chains depth by depth, one
-// lane per chain and a warp barrier per depth: a step's node depends only on
-// its token path from the anchor, so the steps at one depth resolve together
-// (against their parents' nodes and the other chains' steps at that depth);
-// meanwhile the other warps form e^s of every drafter candidate for its three
-// cases (fp64 runs on a narrow pipe on this part).  The new n-gram nodes are
-// numbered by a block-wide count in the order a sequential merge would make
-// them.  A node's children are a known index range of drafter candidates plus
-// a list of n-gram nodes in index order, so the per-parent sums and the
-// depth-first offsets cost O(children) per node; the rank of every candidate
-// is a count over all candidates, the subtree sizes come from shared-memory
-// atomics along each path, and Q is formed level by level from the anchor by
-// warp 0 over depth buckets.
+// everything in shared memory.  A step's node depends only on its token path
+// from the anchor; with up to 32 chains, eight warps find every step's node at
+// once from two tables (where each chain's path leaves the picks, and the
+// common-prefix length of every pair of chains), while the other eight warps
+// form e^s of every drafter candidate for its three cases (fp64 runs on a
+// narrow pipe on this part).  More chains: warp 0 merges depth by depth.  The
+// new n-gram nodes are numbered by a block-wide count in the order a
+// sequential merge would make them.  A node's children are a known index range
+// of drafter candidates plus a list of n-gram nodes in index order, so the
+// per-parent sums and the depth-first offsets cost O(children) per node; Q is
+// formed by pointer jumping along the parent links, the rank of every
+// candidate is a count over all candidates, and the subtree sizes come from
+// shared-memory atomics along each path.
 #include "common.cuh"
 
 namespace spec {
@@ -91,7 +92,8 @@ __global__ void __launch_bounds__(TB_THREADS) build_tree_kernel(TreeParams p) {
   // the selection and the sibling offsets reuse the chain steps' tokens and parents
   int32_t* const s_sel = s_itok;
   int32_t* const s_before = s_ipar;
-  __shared__ int32_t s_bucket[TB_THREADS], s_bpar[TB_THREADS], s_dcnt[TB_THREADS + 1], s_doff[TB_THREADS + 1];
+  // scratch: the merge's path tables, then the Q pointers
+  __shared__ int32_t s_bucket[TB_THREADS], s_bpar[TB_THREADS];
   __shared__ int32_t s_N, s_maxd, s_levels, s_len[TB_THREADS], s_wcnt[TB_THREADS / 32];
   __shared__ double s_eng;
   const int r = blockIdx.x, j = threadIdx.x;
@@ -120,11 +122,9 @@ __global__ void __launch_bounds__(TB_THREADS) build_tree_kernel(TreeParams p) {
   s_ngfirst[j] = 0x7FFFFFFF;
   s_ngnext[j] = -1;
   s_size[j] = 0;
-  s_dcnt[j] = 0;
   if (j == 0) {
     s_maxd = 0;
     s_levels = 0;
-    s_dcnt[TB_THREADS] = 0;
   }
   // chain item j = c Lg + t: the t-th step of chain c
   const int nct = NC * Lg;
@@ -322,14 +322,8 @@ __global__ void __launch_bounds__(TB_THREADS) build_tree_kernel(TreeParams p) {
     s_depth[v] = my_c + my_t + 1;
     atomicMin(&s_ngfirst[pv], v);
   }
-  if (j < ND) {
-    atomicMax(&s_maxd, s_depth[j]);
-    atomicAdd(&s_dcnt[s_depth[j]], 1);
-  }
-  if (makes) {
-    atomicMax(&s_maxd, my_c + my_t + 1);
-    atomicAdd(&s_dcnt[my_c + my_t + 1], 1);
-  }
+  if (j < ND) atomicMax(&s_maxd, s_depth[j]);
+  if (makes) atomicMax(&s_maxd, my_c + my_t + 1);
   __syncthreads();
   // each n-gram node's next sibling: the smallest larger index among the nodes
   // made at its depth with its parent; e^s of every candidate
@@ -355,28 +349,9 @@ __global__ void __launch_bounds__(TB_THREADS) build_tree_kernel(TreeParams p) {
       s_e[j] = s_eng;
   }
   const int32_t maxd = s_maxd;
-  if (warp == 0) {  // offsets of the depth buckets
-    int32_t run = 0;
-    for (int32_t d0 = 0; d0 <= maxd; d0 += 32) {
-      const int32_t d = d0 + lane;
-      const int32_t v = d <= maxd ? s_dcnt[d] : 0;
-      int32_t x = v;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int32_t y = __shfl_up_sync(0xFFFFFFFFu, x, o);
-        if (lane >= o) x += y;
-      }
-      if (d <= maxd) {
-        s_doff[d] = run + x - v;
-        s_dcnt[d] = run + x - v;  // the bucket's fill cursor
-      }
-      run += __shfl_sync(0xFFFFFFFFu, x, 31);
-    }
-    if (lane == 0) s_doff[maxd + 1] = run;
-  }
-  __syncthreads();
+  __syncthreads();  // every candidate's e^s is chosen
   // Eq. (6) denominators: thread j sums its own children in index order, the
-  // drafter range first; and the depth buckets are filled
+  // drafter range first
   if (j < N) {
     double den = 1.0;
     const int32_t c0 = j < ND ? s_dk[j] : -1;
@@ -384,27 +359,35 @@ __global__ void __launch_bounds__(TB_THREADS) build_tree_kernel(TreeParams p) {
       for (int32_t k = 0; k < Kc; ++k) den += s_e[c0 + k];
     for (int32_t g = s_ngfirst[j]; g >= 0; g = s_ngnext[g]) den += s_e[g];
     s_den[j] = den;
-    const int32_t b = atomicAdd(&s_dcnt[s_depth[j]], 1);
-    s_bucket[b] = j;
-    s_bpar[b] = s_par[j];
   }
   __syncthreads();
-  // q_j = e^{s_j} / den(parent); Q_j = Q_parent(j) q_j level by level from the
-  // anchor down (the order of the definition's products), by warp 0
-  if (j > 0 && j < N) s_Q[j] = s_e[j] / s_den[s_par[j]];  // q until its level turns it into Q
+  // q_j = e^{s_j} / den(parent), then Q_j, the product of q along the path
+  // from the anchor, by pointer jumping: after round k a node holds the
+  // product of the last 2^k factors of its path and the node 2^k steps up (the
+  // anchor holds 1 and points to itself), so max depth d needs ceil(log2 d)
+  // rounds.  The products associate differently from the left-to-right
+  // definition, which moves Q by a few units in the last place.
+  int32_t* const s_up = s_bucket;
+  if (j < N) {
+    s_Q[j] = j > 0 ? s_e[j] / s_den[s_par[j]] : 1.0;
+    s_up[j] = j > 0 ? s_par[j] : 0;
+  }
   __syncthreads();
-  if (warp == 0) {
-    if (lane == 0) s_Q[0] = 1.0;
-    __syncwarp();
-    for (int32_t d = 1; d <= maxd; ++d) {
-      for (int32_t b = s_doff[d] + lane; b < s_doff[d + 1]; b += 32) {
-        const int32_t v = s_bucket[b];
-        s_Q[v] = s_Q[s_bpar[b]] * s_Q[v];
-      }
-      __syncwarp();
+  for (int32_t covered = 1; covered < maxd; covered <<= 1) {
+    double qa = 1.0;
+    int32_t ua = 0;
+    if (j < N) {
+      const int32_t u = s_up[j];
+      qa = s_Q[u];
+      ua = s_up[u];
     }
+    __syncthreads();
+    if (j < N) {
+      s_Q[j] = qa * s_Q[j];
+      s_up[j] = ua;
+    }
+    __syncthreads();
   }
-  __syncthreads();
   // best-first rank (Q descending, ties to the lower index) and selection
   if (j < N) {
     bool sel = (j == 0);
