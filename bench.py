@@ -8,12 +8,14 @@ batch-128 mixed editing / chat configuration (context 4096, budget 256,
 V = 151936 bf16 logits, T = 0); its logits are synthetic, laid out exactly as
 the allocation asks (the target forward itself is not part of the path).
 
-Timing: each input set's two launches are captured as two CUDA graphs; W
-warm-up steps, then K steps of graph replays between a barrier and a device
-synchronisation, with CUDA events on the launching stream before, between and
-after the two graphs (replays keep the device queue ahead of the host, so the
-events time the kernels, not host launch gaps); three input sets rotate so
-that every step reads logits that are not in L2 (3 x 117 MB > 129 MB).
+Timing: one CUDA graph holds a pass over the input sets (one round per set,
+the launches in order on one stream) and each set's round is also a graph of
+its own; W warm-up steps, then K steps of graph replays (passes, then single
+rounds for the remainder) between a barrier and a device synchronisation,
+with CUDA events on the launching stream around them (replays keep the device
+queue ahead of the host, so the events time the kernels, not host launch
+gaps); three input sets rotate so that every step reads logits that are not
+in L2 (3 x 117 MB > 129 MB).
 `value` = verified draft tokens per second (sum of verify_len per step);
 rows/s, per-kernel times, the verify kernel's HBM roofline fraction, an
 end-to-end figure through host buffers, the oracle's CPU time and the SM
@@ -318,10 +320,14 @@ def timed_parts(torch, sets, names, steps, warmup, barrier=lambda: None, sampler
     """`sets` holds, per input set, one function per component of a step (in
     step order), each taking the stream to launch on.
 
-    The timed region: every set's whole step is captured as one CUDA graph; W
-    untimed steps, then `steps` timed steps between a barrier and a device
-    synchronisation, step i replaying set i % len(sets)'s graph; CUDA events
-    on the launching stream around the region.
+    The timed region: one CUDA graph holds a whole pass over the sets (step
+    i on set i % len(sets), each step's launches in order on one stream, so
+    consecutive steps run back to back as they would inside a captured decode
+    step, without a graph launch between them), and every set's single step is
+    a graph of its own.  W untimed steps, then `steps` timed steps between a
+    barrier and a device synchronisation: steps // len(sets) replays of the
+    pass graph, then the remaining steps' single graphs; CUDA events on the
+    launching stream around the region.
 
     Per-component times: for each component, one graph of `launches`
     back-to-back launches of it, cycling over the sets, replayed after the
@@ -336,16 +342,22 @@ def timed_parts(torch, sets, names, steps, warmup, barrier=lambda: None, sampler
     stream = torch.cuda.current_stream()
     nset = len(sets)
     steps_g = [capture(torch, lambda st, fns=fns: [f(st) for f in fns]) for fns in sets]
-    for i in range(warmup):
-        steps_g[i % nset].replay()
+    pass_g = capture(torch, lambda st: [f(st) for fns in sets for f in fns])
+
+    def run(n):
+        for _ in range(n // nset):
+            pass_g.replay()
+        for i in range(n % nset):
+            steps_g[i].replay()
+
+    run(warmup)
     torch.cuda.synchronize()
     barrier()
     torch.cuda.synchronize()
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with (sampler if sampler is not None else contextlib.nullcontext()):
         t_start.record(stream)
-        for i in range(steps):
-            steps_g[i % nset].replay()
+        run(steps)
         t_end.record(stream)
         torch.cuda.synchronize()
     barrier()
@@ -384,8 +396,9 @@ def round_parts(S, torch, cfg, rnd):
 
 
 def timed_rounds(S, torch, cfg, rounds, steps, warmup, barrier=lambda: None, sampler=None):
-    """The chain round (draft + price, verify) timed over per-round graphs, one
-    per input set; returns the elapsed ms and the mean per-kernel us."""
+    """The chain round (draft + price, verify) timed over graph replays of
+    whole passes over the input sets (timed_parts); returns the elapsed ms and
+    the mean per-kernel us."""
     sets = [round_parts(S, torch, cfg, rnd) for rnd in rounds]
     return timed_parts(torch, sets, ["draft_price", "verify"], steps, warmup, barrier, sampler)
 
