@@ -8,10 +8,10 @@ batch-128 mixed editing / chat configuration (context 4096, budget 256,
 V = 151936 bf16 logits, T = 0); its logits are synthetic, laid out exactly as
 the allocation asks (the target forward itself is not part of the path).
 
-Timing: one CUDA graph holds a pass over the input sets (one round per set,
-the launches in order on one stream) and each set's round is also a graph of
-its own; W warm-up steps, then K steps of graph replays (passes, then single
-rounds for the remainder) between a barrier and a device synchronisation,
+Timing: one CUDA graph holds a pass of 30 rounds rotating over the input
+sets (the launches in order on one stream) and each set's round is also a
+graph of its own; W warm-up steps, then K steps of graph replays (passes,
+then single rounds for the remainder) between a barrier and a device synchronisation,
 with CUDA events on the launching stream around them (replays keep the device
 queue ahead of the host, so the events time the kernels, not host launch
 gaps); three input sets rotate so that every step reads logits that are not
@@ -302,6 +302,9 @@ def make_rounds(S, torch, W, cfg, nbuf):
     return rounds, n_rows, n_tok, logits
 
 
+PASS_STEPS = 30  # steps per replay of a pass graph
+
+
 def capture(torch, fn):
     """fn(stream) captured into a CUDA graph, after one run on a side stream."""
     s = torch.cuda.Stream()
@@ -320,14 +323,14 @@ def timed_parts(torch, sets, names, steps, warmup, barrier=lambda: None, sampler
     """`sets` holds, per input set, one function per component of a step (in
     step order), each taking the stream to launch on.
 
-    The timed region: one CUDA graph holds a whole pass over the sets (step
-    i on set i % len(sets), each step's launches in order on one stream, so
-    consecutive steps run back to back as they would inside a captured decode
-    step, without a graph launch between them), and every set's single step is
-    a graph of its own.  W untimed steps, then `steps` timed steps between a
-    barrier and a device synchronisation: steps // len(sets) replays of the
-    pass graph, then the remaining steps' single graphs; CUDA events on the
-    launching stream around the region.
+    The timed region: one CUDA graph holds a pass of about PASS_STEPS steps
+    (a whole number of rotations over the sets, step i on set i % len(sets),
+    each step's launches in order on one stream, so consecutive steps run back
+    to back as they would inside a captured decode step, without a graph
+    launch between them), and every set's single step is a graph of its own.
+    W untimed steps, then `steps` timed steps between a barrier and a device
+    synchronisation: whole passes, then the remaining steps' single graphs;
+    CUDA events on the launching stream around the region.
 
     Per-component times: for each component, one graph of `launches`
     back-to-back launches of it, cycling over the sets, replayed after the
@@ -342,13 +345,14 @@ def timed_parts(torch, sets, names, steps, warmup, barrier=lambda: None, sampler
     stream = torch.cuda.current_stream()
     nset = len(sets)
     steps_g = [capture(torch, lambda st, fns=fns: [f(st) for f in fns]) for fns in sets]
-    pass_g = capture(torch, lambda st: [f(st) for fns in sets for f in fns])
+    per = nset * max(1, PASS_STEPS // nset)
+    pass_g = capture(torch, lambda st: [f(st) for i in range(per) for f in sets[i % nset]])
 
     def run(n):
-        for _ in range(n // nset):
+        for _ in range(n // per):
             pass_g.replay()
-        for i in range(n % nset):
-            steps_g[i].replay()
+        for i in range(n % per):
+            steps_g[i % nset].replay()
 
     run(warmup)
     torch.cuda.synchronize()
