@@ -109,6 +109,17 @@ __global__ void __launch_bounds__(SPEC_CTA_THREADS, 1) ngram_kernel(NgramParams 
       s_ps.c[tid] = p.c[(int64_t)r * p.cx.K + tid];
     }
   }
+  // the Eq. (1) table is read once per request after the scan, at a row the scan
+  // picks: every CTA brings its share of the table's lines into L2 now, while
+  // the history copies are in flight, so that read hits L2
+  if (PRICE && !p.cx.tab_const && tid < 32) {
+    const int64_t n_h = (int64_t)p.cx.L * (SPEC_TAB_N * 2 + 2 * (p.cx.m_cap + 1));  // table floats
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(p.cx.table) & ~(uintptr_t)127;
+    const uintptr_t a1 = reinterpret_cast<uintptr_t>(p.cx.table + n_h);
+    const uintptr_t step = (uintptr_t)gridDim.x * 32u * 128u;  // one 128-byte line per lane
+    for (uintptr_t a = a0 + ((uintptr_t)blockIdx.x * 32u + (uintptr_t)tid) * 128u; a < a1; a += step)
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
+  }
   const int32_t nc = valid && T >= 2 ? T - 1 : 0;  // candidate end positions 0..T-2
   const int32_t per = (nc + C - 1) / C;
   const int32_t j0 = min(nc, rank * per);
