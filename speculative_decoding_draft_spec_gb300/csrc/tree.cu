@@ -191,22 +191,49 @@ __global__ void __launch_bounds__(TB_THREADS) build_tree_kernel(TreeParams p) {
     constexpr int MT = 32 * TB_MERGE_WARPS;
     int32_t* const s_leave = s_bpar;  // [NC]
     int32_t* const s_lcp = s_bucket;  // [NC (NC - 1) / 2]
-    const int kmax = NC + Lg;         // no path is longer
-    if (j < NC) s_leave[j] = j + s_len[j] + 1;  // past the last step: never leaves
-    for (int i = j; i < NC * NC; i += MT) {
-      const int c = i / NC, c2 = i - c * NC;
-      if (c2 < c) s_lcp[c * (c - 1) / 2 + c2] = min(c2 + s_len[c2], c + s_len[c]);
+    // warp w takes chains w, w + 8, ...: the depth at which the chain's path
+    // leaves the picks, 32 steps per ballot
+    for (int c = warp; c < NC; c += TB_MERGE_WARPS) {
+      const int len = s_len[c];
+      int leave = c + len + 1;  // past the last step: never leaves
+      for (int t0 = 0; t0 < len; t0 += 32) {
+        const int t = t0 + lane, d = c + t + 1;
+        const bool off = t < len && (d > P || s_itok[c * Lg + t] != s_tok[1 + (d - 1) * Kc]);
+        const unsigned m = __ballot_sync(0xFFFFFFFFu, off);
+        if (m != 0u) {
+          leave = c + t0 + __ffs(m);
+          break;
+        }
+      }
+      if (lane == 0) s_leave[c] = leave;
     }
     merge_bar();
-    for (int i = j; i < nct; i += MT) {
-      const int c = i / Lg, t = i - c * Lg, d = c + t + 1;
-      if (t < s_len[c] && (d > P || s_itok[i] != s_tok[1 + (d - 1) * Kc])) atomicMin(&s_leave[c], d);
-    }
-    for (int i = j; i < NC * NC * kmax; i += MT) {
-      const int k = 1 + i % kmax, cc = i / kmax, c = cc / NC, c2 = cc - c * NC;
-      // the paths of c2 < c agree on their first c2 tokens (both picks)
-      if (c2 < c && k > c2 && k <= min(c2 + s_len[c2], c + s_len[c]) && path_tok(c2, k) != path_tok(c, k))
-        atomicMin(&s_lcp[c * (c - 1) / 2 + c2], k - 1);
+    // pairs c2 < c (pair c (c - 1) / 2 + c2; warp w takes pairs w, w + 8, ...):
+    // both paths follow the picks through depth c2, and chain c's through depth
+    // c, so the paths part where chain c2 leaves the picks if that is at or
+    // before depth c; otherwise they agree through depth c and part at the
+    // first difference of the two chains' own tokens
+    const int NP = NC * (NC - 1) / 2;
+    for (int pi = warp; pi < NP; pi += TB_MERGE_WARPS) {
+      int c = (int)((1.0f + sqrtf(1.0f + 8.0f * (float)pi)) * 0.5f);
+      while (c * (c - 1) / 2 > pi) --c;
+      while ((c + 1) * c / 2 <= pi) ++c;
+      const int c2 = pi - c * (c - 1) / 2;
+      const int lim = min(c2 + s_len[c2], c + s_len[c]);
+      const int lv = s_leave[c2];
+      int lcp = lv <= c ? min(lv - 1, lim) : lim;
+      if (lv > c) {
+        for (int k0 = c + 1; k0 <= lim; k0 += 32) {
+          const int k = k0 + lane;
+          const unsigned m = __ballot_sync(
+              0xFFFFFFFFu, k <= lim && s_itok[c2 * Lg + (k - c2 - 1)] != s_itok[c * Lg + (k - c - 1)]);
+          if (m != 0u) {
+            lcp = k0 + __ffs(m) - 2;
+            break;
+          }
+        }
+      }
+      if (lane == 0) s_lcp[pi] = lcp;
     }
     merge_bar();
     for (int i = j; i < nct; i += MT) {
