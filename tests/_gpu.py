@@ -202,3 +202,14 @@ def assert_tree_equal(g, o, rel=1e-12):
         cut = min(Q[list(sel_o)]) if sel_o else 1.0
         assert all(abs(Q[c] - cut) <= rel * cut for c in diff), (r, sorted(diff))
         assert abs(sum(Q[list(sel_g)]) - sum(Q[list(sel_o)])) <= rel * max(1.0, sum(Q[list(sel_o)])), r
+        # the GPU's rows still form a depth-first layout, and a candidate that
+        # both select has the same token under the same parent candidate
+        gc, gp, gt = g["cand_id"][r], g["parent"][r], g["tok"][r]
+        assert int(gc[0]) == 0 and int(gp[0]) == -1, r
+        assert all(0 <= int(gp[i]) < i for i in range(1, n)), r
+        o_tok = {int(o.cand_id[r, i]): int(o.tok[r, i]) for i in range(n)}
+        o_par = {int(o.cand_id[r, i]): int(o.cand_id[r, int(o.parent[r, i])]) for i in range(1, n)}
+        for i in range(1, n):
+            c = int(gc[i])
+            if c in o_par:
+                assert int(gt[i]) == o_tok[c] and int(gc[int(gp[i])]) == o_par[c], (r, c)

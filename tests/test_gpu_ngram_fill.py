@@ -128,7 +128,10 @@ def _random_chain_blocks(seed, B, P, Kc, Lg):
 
 
 @pytest.mark.parametrize("P,Kc,Lg,width", [(8, 4, 12, 16), (8, 4, 32, 64), (3, 2, 6, 256), (12, 3, 30, 200),
-                                           (1, 1, 5, 4), (0, 2, 9, 8)])
+                                           (1, 1, 5, 4), (0, 2, 9, 8),
+                                           # 21 and 32 chains: the parallel merge at its widest (496 chain
+                                           # pairs); 41 chains: the depth-by-depth merge
+                                           (20, 3, 12, 64), (31, 4, 8, 128), (40, 2, 8, 32)])
 def test_builder_parity_with_chains_from_every_pick(S, P, Kc, Lg, width):
     c = _random_chain_blocks(P * 100 + Lg, 40, P, Kc, Lg)
     args = (c["anchor"], c["cand_tok"], c["cand_score"], c["ng_tok"], c["ng_len"], c["ng_score"], c["ng_adj"])
