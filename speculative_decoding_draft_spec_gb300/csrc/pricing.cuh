@@ -81,8 +81,10 @@ struct PriceStage {
 // this warp before a __syncwarp.  Lane j stages h_{j+1}; then every lane runs
 // the same left-to-right recurrence over the staged rows, one correctly
 // rounded fp32 operation at a time, and keeps the values of position j+1,
-// which it writes.  The loops stay rolled: this code runs once per request and
-// its latency, not its throughput, is on the critical path of the round.
+// which it writes.  The loops are unrolled by four, so that the staged values
+// of four positions are loaded together ahead of the dependent products: this
+// code runs once per request, and its latency is on the critical path of the
+// round.
 __device__ __forceinline__ void price_request_warp(const PriceCtx& cx, int r, int lane, PriceStage& ps,
                                                    int32_t gl, int32_t n, int32_t a, int32_t m, int32_t dl,
                                                    uint32_t& st) {
@@ -107,7 +109,7 @@ __device__ __forceinline__ void price_request_warp(const PriceCtx& cx, int r, in
   float run_g = 1.0f, run_d = 1.0f, vg = 0.0f, vd = 0.0f, my_g = 0.0f, my_d = 0.0f;
   bool d_prefix = dl >= 1 && gl > dl;  // d is a proper prefix of g (contains rule)
   const int32_t jn = gl > dl ? gl : dl;
-#pragma unroll 1
+#pragma unroll 4
   for (int j = 0; j < jn; ++j) {
     if (j < gl) {
       run_g = __fmul_rn(run_g, ps.h[j]);
@@ -166,7 +168,7 @@ __device__ __forceinline__ void price_request_warp(const PriceCtx& cx, int r, in
       pm = contains ? (uint8_t)1 : model_pm;
     }
     float prev = __shfl_sync(0xFFFFFFFFu, sv, dl - 1);  // dl >= 1 on this branch
-#pragma unroll 1
+#pragma unroll 4
     for (int j = dl; j < gl; ++j) {
       prev = __fmul_rn(prev, ps.h[j]);
       if (j == lane) {
