@@ -394,26 +394,30 @@ __global__ void __launch_bounds__(TB_THREADS) build_tree_kernel(TreeParams p) {
   // anchor holds 1 and points to itself), so max depth d needs ceil(log2 d)
   // rounds.  The products associate differently from the left-to-right
   // definition, which moves Q by a few units in the last place.
-  int32_t* const s_up = s_bucket;
+  // two buffers each for Q and the jump pointers (the denominators and the
+  // merge's table are free by now), so a round needs one barrier
+  double* qa = s_Q;
+  double* qb = s_den;
+  int32_t* ua = s_bucket;
+  int32_t* ub = s_bpar;
   if (j < N) {
-    s_Q[j] = j > 0 ? s_e[j] / s_den[s_par[j]] : 1.0;
-    s_up[j] = j > 0 ? s_par[j] : 0;
+    qa[j] = j > 0 ? s_e[j] / s_den[s_par[j]] : 1.0;
+    ua[j] = j > 0 ? s_par[j] : 0;
   }
   __syncthreads();
   for (int32_t covered = 1; covered < maxd; covered <<= 1) {
-    double qa = 1.0;
-    int32_t ua = 0;
     if (j < N) {
-      const int32_t u = s_up[j];
-      qa = s_Q[u];
-      ua = s_up[u];
+      const int32_t u = ua[j];
+      qb[j] = qa[u] * qa[j];
+      ub[j] = ua[u];
     }
     __syncthreads();
-    if (j < N) {
-      s_Q[j] = qa * s_Q[j];
-      s_up[j] = ua;
-    }
-    __syncthreads();
+    double* const tq = qa;
+    qa = qb;
+    qb = tq;
+    int32_t* const tu = ua;
+    ua = ub;
+    ub = tu;
   }
   // best-first rank (Q descending, ties to the lower index) and selection
   if (j < N) {
@@ -421,11 +425,11 @@ __global__ void __launch_bounds__(TB_THREADS) build_tree_kernel(TreeParams p) {
     if (j > 0) {
       // Q >= 0, so its bit pattern orders like its value: integer compares
       // (fp64 compares run on the narrow FP64 pipe)
-      const unsigned long long kj = (unsigned long long)__double_as_longlong(s_Q[j]);
+      const unsigned long long kj = (unsigned long long)__double_as_longlong(qa[j]);
       int32_t rank = 0;
 #pragma unroll 8
       for (int32_t i = 1; i < N; ++i) {
-        const unsigned long long ki = (unsigned long long)__double_as_longlong(s_Q[i]);
+        const unsigned long long ki = (unsigned long long)__double_as_longlong(qa[i]);
         rank += (ki > kj || (ki == kj && i < j)) ? 1 : 0;
       }
       sel = rank < p.width - 1;
