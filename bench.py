@@ -305,6 +305,14 @@ def make_rounds(S, torch, W, cfg, nbuf):
 PASS_STEPS = 30  # steps per replay of a pass graph
 
 
+def step_plan(n, nset, per):
+    """How n steps run: (replays of the pass graph, sets of the single-step
+    graphs after them).  A pass holds `per` steps (a multiple of nset) on sets
+    0, 1, .., so step i runs on set i % nset either way."""
+    assert per % nset == 0
+    return n // per, [i % nset for i in range(n % per)]
+
+
 def capture(torch, fn):
     """fn(stream) captured into a CUDA graph, after one run on a side stream."""
     s = torch.cuda.Stream()
@@ -349,10 +357,11 @@ def timed_parts(torch, sets, names, steps, warmup, barrier=lambda: None, sampler
     pass_g = capture(torch, lambda st: [f(st) for i in range(per) for f in sets[i % nset]])
 
     def run(n):
-        for _ in range(n // per):
+        passes, singles = step_plan(n, nset, per)
+        for _ in range(passes):
             pass_g.replay()
-        for i in range(n % per):
-            steps_g[i % nset].replay()
+        for i in singles:
+            steps_g[i].replay()
 
     run(warmup)
     torch.cuda.synchronize()

@@ -1,6 +1,7 @@
-"""Host logic of bench.py's clock record: a timed region shorter than the
+"""Host logic of bench.py: the clock record (a timed region shorter than the
 sampling interval is still bracketed by samples, and the throttle reasons are
-read from nvidia-smi's columns.  nvidia-smi is faked by a script on PATH."""
+read from nvidia-smi's columns; nvidia-smi is faked by a script on PATH), and
+the plan of graph replays that runs exactly K steps in input-set rotation."""
 import os
 import stat
 import time
@@ -50,3 +51,14 @@ def test_missing_tool_gives_an_empty_record(tmp_path, monkeypatch):
     with clk:
         pass
     assert clk.summary() == {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+
+
+def test_step_plan_runs_exactly_n_steps_in_set_rotation():
+    # the timed region replays passes of `per` steps and then single steps;
+    # expanded, step i must run on set i % nset and there must be n of them
+    for nset in (1, 2, 3, 10):
+        per = nset * max(1, bench.PASS_STEPS // nset)
+        for n in (0, 1, 3, per - 1, per, per + 1, 2 * per + 7, 20000):
+            passes, singles = bench.step_plan(n, nset, per)
+            steps = [i % nset for i in range(per)] * passes + singles
+            assert steps == [i % nset for i in range(n)]
