@@ -745,6 +745,41 @@ def run_gpu(args):
     print(json.dumps(line), flush=True)
 
 
+def run_once():
+    """One launch each of the tree n-gram fill and the tree builder (the
+    filled-tree workload: 32 requests, 4096-token texts, chains from the anchor
+    and 8 picks, trees of 16 rows) and of draft sampling (batch-4 code editing,
+    4 x 7 bf16 draft rows, T = 1), for a profiler."""
+    import torch
+
+    import speculative_decoding_draft_spec_gb300 as S
+    import workloads as W
+
+    S.build()
+    i32 = dict(dtype=torch.int32, device="cuda")
+    dev = lambda a: torch.as_tensor(np.ascontiguousarray(a)).cuda()
+    c = W.tree_fill_bs32(width=16)
+    B, P, Lg = c["B"], c["cand_tok"].shape[1], c["Lg"]
+    ws = S.Workspace(B, 1, 1, 1)
+    tok, ev = (torch.empty((B, P + 1, Lg), **i32) for _ in range(2))
+    ln = torch.empty((B, P + 1), **i32)
+    S.spec_ngram_fill(dev(c["hist"]), dev(c["hist_len"]), dev(c["cand_tok"]), c["n_min"], c["copy_cap"],
+                      c["max_depth"], tok, ln, ev, ws)
+    blk = [dev(c[k]) for k in ("anchor", "cand_tok", "cand_score")] + [tok, ln] + \
+          [dev(c[k]) for k in ("ng_score", "ng_adj")]
+    tt, tp, tc = (torch.empty((B, 16), **i32) for _ in range(3))
+    nr = torch.empty(B, **i32)
+    S.spec_build_tree(*blk, 16, tt, tp, tc, nr, ws)
+    e = W.edit_bs4(temperature=1.0, probabilistic=True)
+    dl = torch.from_numpy(e["draft_logits"].view(np.int16)).view(torch.bfloat16).cuda()
+    ws2 = S.Workspace(e["B"], e["B"] * (e["L"] + 1), e["K"], e["V"])
+    y = torch.empty((e["B"], e["K"]), **i32)
+    S.spec_sample_drafts(dl, 1.0, y, ws2, seed=0, step=0)
+    torch.cuda.synchronize()
+    ok = int(ws.status()) == 0 and int(ws2.status()) == 0
+    print(json.dumps({"legs": "once", "tree_rows": int(nr.sum()), "status_clean": ok}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -752,13 +787,16 @@ def main():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--legs", default="all", choices=["all", "timed"],
-                    help="timed: only the warm-up and timed loop (for profiling)")
+    ap.add_argument("--legs", default="all", choices=["all", "timed", "once"],
+                    help="timed: only the warm-up and timed loop; once: one launch each of the tree "
+                         "fill, tree builder and draft sampling kernels (both for profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.legs == "once":
+        run_once()
     else:
         run_gpu(args)
 
