@@ -91,9 +91,8 @@ typedef enum {
 #define SPEC_DEV_BAD_VALUE 0x10u /* a confidence outside [0,1] (clamped), a feature
                                     outside the estimator table (h = 0)             */
 #define SPEC_DEV_TIMEOUT 0x20u   /* a bounded wait on an asynchronous copy ran out  */
-#define SPEC_DEV_OVERFLOW 0x40u  /* a fixed on-chip table was too small: the n-gram
-                                    fill met more than 2048 distinct followers of
-                                    one three-token context (that chain stops)     */
+#define SPEC_DEV_OVERFLOW 0x40u  /* reserved: no call sets it (the n-gram fill
+                                    counts any number of followers exactly)        */
 
 /* limits */
 #define SPEC_MAX_L 31            /* longest chain (L) and n-gram proposal           */
@@ -287,9 +286,9 @@ spec_status spec_draft_and_price(
  * [batch x (P+1)], ng_ev [batch x (P+1) x Lg] (each token's evidence: the
  * length of the copy it continues, capped at copy_cap, for steps 1-2; minus
  * the follower's count for step 3; 0 past the chain).
- * hist_len[r] outside [0, hist_stride] sets SPEC_DEV_BAD_LENGTH (no chains);
- * more than 2048 distinct followers of one context set SPEC_DEV_OVERFLOW and
- * stop that chain.  Limits: P >= 0, Kc >= 1, 1 <= n_min <= copy_cap,
+ * hist_len[r] outside [0, hist_stride] sets SPEC_DEV_BAD_LENGTH (no chains).
+ * Any number of distinct followers is counted exactly (a context with more
+ * than 2048 takes extra passes over the text).  Limits: P >= 0, Kc >= 1, 1 <= n_min <= copy_cap,
  * max_depth >= 0, Lg >= 0, P + Lg <= 4096, batch <= 65535.  The workspace
  * serves only its status word.
  * ------------------------------------------------------------------------ */
@@ -406,14 +405,20 @@ spec_status spec_size_budget(int32_t batch, int32_t L, const float* S, const int
  * Scratch: a fixed array of (64 + SPEC_STATIC_PRICE_MAX_BATCH * SPEC_MAX_L)
  * 32-bit words (32,000 bytes) in this library's device memory; this call and
  * its kernel allocate nothing.
- * Set-up: the first call on each device looks up that array's device address
- * (cudaGetSymbolAddress, with the device current) and keeps it; make that
- * first call before the stream is captured into a graph.
+ * Set-up: the first call in each context looks up that array's device
+ * address (cudaGetSymbolAddress, with the device current) and keeps it with
+ * the context's process-unique id (cuCtxGetId); a call from another context
+ * -- after cudaDeviceReset, or from a driver-API context on the same device --
+ * looks it up again, so no kept address outlives its context.  Make the first
+ * call in a context before the stream is captured into a graph.
  * Limits: batch <= SPEC_STATIC_PRICE_MAX_BATCH, else SPEC_ERR_UNSUPPORTED
  * before any device work; the other limits of spec_price_and_allocate.
  * Zero state: the array's arrival counter must be zero when a call's kernel
  * starts; it is zero when the library's device code loads into a context, and
- * every call leaves it at zero.  The allocation keys need no initial value.
+ * every call whose kernel runs to completion leaves it at zero.  A kernel cut
+ * off part way (a sticky CUDA error) leaves the context unusable; the context
+ * that replaces it starts from a zeroed array.  The allocation keys need no
+ * initial value.
  * Concurrency: every call on one device shares the one array, so calls whose
  * kernels may overlap on the device (different streams without an order
  * between them, or several host threads) race; keep them in one stream order.

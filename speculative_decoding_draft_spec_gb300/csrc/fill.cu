@@ -26,7 +26,9 @@
 // block-wide pass over the text (each thread tests its end positions four at
 // a time, extends the matches it finds, and the block takes the max of
 // (l << 32 | j)), a follower step one pass that counts followers in a
-// shared-memory hash table (atomics) and one max over it.  Reading on along a
+// shared-memory hash table (atomics) and one max over it (more passes, over
+// halves of the follower value range, where a context has more distinct
+// followers than the table holds).  Reading on along a
 // passage needs no lookup, so a whole run of such steps is one parallel copy.
 // All threads carry the same chain state, so every branch is block-uniform.
 #include "common.cuh"
@@ -36,6 +38,7 @@ namespace spec {
 #define FL_THREADS 256
 #define FL_HASH 2048  // follower table entries (a power of two)
 #define FL_STAGE_MAX 16384  // longest text staged in shared memory (64 KB)
+#define FL_RANGES 40        // follower ranges pending at once (21 splits deep at most)
 
 struct FillParams {
   const int32_t* hist;
@@ -73,6 +76,9 @@ __global__ void __launch_bounds__(FL_THREADS) ngram_fill_kernel(FillParams p) {
   __shared__ int32_t s_cnt[FL_HASH], s_last[FL_HASH];
   __shared__ unsigned long long s_red[FL_THREADS / 32];
   __shared__ int32_t s_overflow;
+  // the follower value ranges still to count, [s_rlo, s_rhi) (a stack)
+  __shared__ unsigned long long s_rlo[FL_RANGES], s_rhi[FL_RANGES];
+  __shared__ int32_t s_sp;
   const int tid = threadIdx.x;
   const int c = blockIdx.x, r = blockIdx.y;
   const int C = p.P + 1;
@@ -160,43 +166,76 @@ __global__ void __launch_bounds__(FL_THREADS) ngram_fill_kernel(FillParams p) {
         e = run;
         found = true;
       } else if (len >= 3) {
-        // the most frequent follower of the last three tokens
+        // the most frequent follower of the last three tokens, counted in a
+        // shared-memory hash table.  When a pass meets more distinct followers
+        // than the table holds, the follower value range of that pass is split
+        // in halves and each half is counted by a pass of its own; a range of
+        // at most FL_HASH values always fits, so the count is exact for any
+        // text (at most 21 levels of splitting).  Each follower lives in one
+        // range, so the best (count, last position) over the ranges is the
+        // best overall.
         const int32_t a = ctx(len - 3), b = ctx(len - 2), d = last;
-        for (int h = tid; h < FL_HASH; h += FL_THREADS) {
-          s_key[h] = 0ull;
-          s_cnt[h] = 0;
-          s_last[h] = -1;
-        }
-        __syncthreads();
-        for (int64_t j = 2 + tid; j <= (int64_t)T - 2; j += FL_THREADS) {
-          if (xs[j] != d || xs[j - 1] != b || xs[j - 2] != a) continue;
-          const int32_t f = xs[j + 1];
-          const unsigned long long key = (1ull << 32) | (unsigned long long)(uint32_t)f;
-          uint32_t h = ((uint32_t)f * 2654435761u) >> (32 - 11);
-          bool placed = false;
-          for (int probe = 0; probe < FL_HASH && !placed; ++probe) {
-            const unsigned long long prev = atomicCAS(&s_key[h], 0ull, key);
-            if (prev == 0ull || prev == key) {
-              atomicAdd(&s_cnt[h], 1);
-              atomicMax(&s_last[h], (int32_t)j);
-              placed = true;
-            }
-            h = (h + 1) & (FL_HASH - 1);
-          }
-          if (!placed) s_overflow = 1;
-        }
-        __syncthreads();
         unsigned long long top = 0;
-        for (int h = tid; h < FL_HASH; h += FL_THREADS)
-          if (s_key[h] != 0ull) {
-            const unsigned long long k = ((unsigned long long)s_cnt[h] << 32) | (unsigned long long)s_last[h];
-            top = k > top ? k : top;
+        if (tid == 0) {
+          s_rlo[0] = 0ull;
+          s_rhi[0] = 1ull << 32;
+          s_sp = 1;
+        }
+        __syncthreads();
+        while (s_sp > 0) {  // block-uniform: s_sp changes only between barriers
+          const unsigned long long lo = s_rlo[s_sp - 1], hi = s_rhi[s_sp - 1];
+          for (int h = tid; h < FL_HASH; h += FL_THREADS) {
+            s_key[h] = 0ull;
+            s_cnt[h] = 0;
+            s_last[h] = -1;
           }
-        top = block_max_u64(top, s_red);
-        if (s_overflow) {
-          // more distinct followers than the table holds: the chain stops here
-          if (tid == 0) set_status(p.status, SPEC_DEV_OVERFLOW);
-        } else if (top != 0ull) {
+          if (tid == 0) s_overflow = 0;
+          __syncthreads();
+          for (int64_t j = 2 + tid; j <= (int64_t)T - 2; j += FL_THREADS) {
+            if (xs[j] != d || xs[j - 1] != b || xs[j - 2] != a) continue;
+            const int32_t f = xs[j + 1];
+            if ((unsigned long long)(uint32_t)f < lo || (unsigned long long)(uint32_t)f >= hi) continue;
+            const unsigned long long key = (1ull << 32) | (unsigned long long)(uint32_t)f;
+            uint32_t h = ((uint32_t)f * 2654435761u) >> (32 - 11);
+            bool placed = false;
+            for (int probe = 0; probe < FL_HASH && !placed; ++probe) {
+              const unsigned long long prev = atomicCAS(&s_key[h], 0ull, key);
+              if (prev == 0ull || prev == key) {
+                atomicAdd(&s_cnt[h], 1);
+                atomicMax(&s_last[h], (int32_t)j);
+                placed = true;
+              }
+              h = (h + 1) & (FL_HASH - 1);
+            }
+            if (!placed) s_overflow = 1;
+          }
+          __syncthreads();
+          if (s_overflow) {
+            __syncthreads();  // every thread has read s_overflow and the range
+            if (tid == 0) {   // replace the range by its halves, the lower on top
+              const unsigned long long mid = lo + (hi - lo) / 2;
+              s_rlo[s_sp - 1] = mid;
+              s_rhi[s_sp - 1] = hi;
+              s_rlo[s_sp] = lo;
+              s_rhi[s_sp] = mid;
+              ++s_sp;
+            }
+            __syncthreads();
+            continue;
+          }
+          unsigned long long best_here = 0;
+          for (int h = tid; h < FL_HASH; h += FL_THREADS)
+            if (s_key[h] != 0ull) {
+              const unsigned long long k = ((unsigned long long)s_cnt[h] << 32) | (unsigned long long)s_last[h];
+              best_here = k > best_here ? k : best_here;
+            }
+          best_here = block_max_u64(best_here, s_red);
+          top = best_here > top ? best_here : top;
+          __syncthreads();  // every thread has read s_sp and s_red
+          if (tid == 0) --s_sp;
+          __syncthreads();
+        }
+        if (top != 0ull) {
           y = xs[(int64_t)(uint32_t)top + 1];
           e = -(int32_t)(top >> 32);
           q = -1;

@@ -22,6 +22,9 @@
 // row offsets.
 #include "pricing.cuh"
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include <mutex>
 
 namespace spec {
@@ -236,24 +239,65 @@ static __device__ __align__(256) uint32_t
 namespace {
 constexpr int kMaxDevices = 256;
 std::mutex g_static_mu;
-uint32_t* g_static_addr[kMaxDevices] = {};
+// per device: the id of the context the address was looked up in, and the address
+struct StaticAddr {
+  unsigned long long ctx_id;
+  uint32_t* addr;
+};
+StaticAddr g_static_addr[kMaxDevices] = {};
+PFN_cuCtxGetCurrent_v4000 g_ctx_current = nullptr;
+PFN_cuCtxGetId_v12000 g_ctx_id = nullptr;
+bool g_ctx_fns = false;
+
+// Process-unique id of the calling thread's current context (the driver never
+// hands an id out twice in one process, unlike a context handle, whose value
+// can come back after the context is destroyed); 0 when there is none.
+unsigned long long current_context_id() {
+  if (!g_ctx_fns) {
+    g_ctx_fns = true;
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_ctx_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(f);
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_ctx_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(f);
+  }
+  if (!g_ctx_current || !g_ctx_id) return 0;
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (g_ctx_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+  if (g_ctx_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
 }  // namespace
 
-// Device address of the fixed scratch array on the current device, looked up
-// once per device.  (Internal: not exported from the library.)
+// Device address of the fixed scratch array in the current device's current
+// context.  It is looked up (cudaGetSymbolAddress, with that device current)
+// the first time a context calls, and kept with the context's id: a call from
+// another context -- after cudaDeviceReset, or from a driver-API context on the
+// same device -- looks it up again, so no address outlives its context.
+// (Internal: not exported from the library.)
 __attribute__((visibility("hidden"))) cudaError_t spec_static_price_scratch(uint32_t** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(g_static_mu);
-  if (!g_static_addr[dev]) {
-    void* addr = nullptr;
-    e = cudaGetSymbolAddress(&addr, spec::g_static_price_scratch);
-    if (e != cudaSuccess) return e;
-    g_static_addr[dev] = static_cast<uint32_t*>(addr);
+  const unsigned long long id = current_context_id();
+  StaticAddr& slot = g_static_addr[dev];
+  if (id != 0 && slot.addr != nullptr && slot.ctx_id == id) {
+    *out = slot.addr;
+    return cudaSuccess;
   }
-  *out = g_static_addr[dev];
+  void* addr = nullptr;
+  e = cudaGetSymbolAddress(&addr, spec::g_static_price_scratch);
+  if (e != cudaSuccess) return e;
+  // the lookup makes the device's primary context current when none was
+  slot.ctx_id = id != 0 ? id : current_context_id();
+  slot.addr = static_cast<uint32_t*>(addr);
+  *out = slot.addr;
   return cudaSuccess;
 }
 

@@ -91,16 +91,21 @@ def test_fill_flags_a_bad_length(S):
     assert o.len[1].tolist() == [0, 0, 0]
 
 
-def test_fill_follower_table_overflow_stops_the_chain(S):
-    # "1 2 3" followed by 2100 distinct tokens, then a context whose 4-token
-    # suffix is new: more followers than the on-chip table holds
-    body = np.stack([np.ones(2100), 2 * np.ones(2100), 3 * np.ones(2100), 1000 + np.arange(2100)], 1).ravel()
-    hist = np.concatenate([body, [99, 1, 2, 3]]).astype(np.int32)[None]
-    ws = S.Workspace(1, 1, 1, 1)
-    g = gpu_ngram_fill(S, ws, hist, np.array([hist.shape[1]], np.int32), np.zeros((1, 0, 1), np.int32), 4, 256,
-                       32, 8)
-    assert ws.status() == S.DEV_BITS["overflow"]
-    assert g["len"].tolist() == [[0]]
+@pytest.mark.parametrize("n_fol,reps,extra", [(2100, 1, (1700,)), (2049, 1, ()), (5000, 1, (4321, 17)),
+                                               (3000, 2, (2999, 5, 2999)), (16000, 1, (9, 15999))])
+def test_fill_counts_more_followers_than_the_table_exactly(S, n_fol, reps, extra):
+    """"1 2 3" followed by n_fol distinct tokens (each `reps` times), some of
+    them once more, then a context whose 4-token suffix is new: more distinct
+    followers than the 2048-entry on-chip table holds.  The chains equal the
+    oracle's, which counts every follower, and no status bit is set; the
+    16,000-follower text (64,004 tokens) is too long to stage on chip."""
+    body = np.stack([np.ones(n_fol), 2 * np.ones(n_fol), 3 * np.ones(n_fol), 1000 + np.arange(n_fol)], 1).ravel()
+    parts = [body] * reps + [np.array([1, 2, 3, 1000 + k]) for k in extra] + [np.array([99, 1, 2, 3])]
+    hist = np.concatenate(parts).astype(np.int32)[None]
+    o = _check(S, hist, np.array([hist.shape[1]], np.int32), np.zeros((1, 0, 1), np.int32), 4, 256, 32, 8)
+    assert o.len[0, 0] > 0
+    want = 1000 + (extra[-1] if extra else n_fol - 1)  # most frequent, then most recent
+    assert o.tok[0, 0, 0] == want
 
 
 # ------------------------------------------------------------------ the builder with chains from every pick

@@ -4,8 +4,11 @@ spec_price_and_allocate on the same inputs.
 
 Its outputs must equal the workspace call's bit for bit (the two run the same
 kernel), on two calls in a row: the second call only gets them right if the
-first left the fixed array's arrival counter at zero.  This file is collected
-last and passes alone or after the other tests."""
+first left the fixed array's arrival counter at zero.  The largest batch and
+chain the array holds (256 requests of 31 slots) are exercised on the device,
+and neither torch's allocator nor the device's free memory moves across
+calls.  This file is collected last and passes alone or after the other
+tests."""
 import ctypes as C
 
 import numpy as np
@@ -102,3 +105,70 @@ def test_static_pricing_reports_device_errors_in_the_callers_word(S):
     common = (0.1, 5, 15, "model_only", True)
     _equal(_run(S, True, est, arrays, *common, status=status), _run(S, False, est, arrays, *common, ws=ws))
     assert int(status.item()) & S.DEV_BITS["bad_value"]
+
+
+def _random_inputs(rng, B, K, L):
+    d = rng.integers(0, 20, (B, K)).astype(np.int32)
+    g = np.full((B, L), -1, np.int32)
+    g_len = rng.integers(0, L + 1, B).astype(np.int32)
+    for r in range(B):
+        g[r, :g_len[r]] = rng.integers(0, 20, g_len[r])
+        if rng.random() < 0.3 and g_len[r] > K:  # the n-gram chain contains the model chain
+            g[r, :K] = d[r]
+    conf = rng.choice([0.5, 0.9, 0.95, 1.0, 0.7], (B, K)).astype(np.float32)
+    n = rng.integers(0, 17, B).astype(np.int32)
+    n[rng.random(B) < 0.3] = 15
+    a = rng.integers(0, 2, B).astype(np.int32)
+    m = np.maximum(n, rng.integers(0, 400, B)).astype(np.int32)
+    return [d, conf, rng.integers(0, K + 1, B).astype(np.int32), g, g_len, n, a, m]
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("coef", ["table5", "constant"])
+def test_static_pricing_at_the_arrays_full_size(S, coef):
+    """256 requests x 31 slots (every word of the key area), budgets near the
+    slot count, twice in a row against the workspace call."""
+    rng = np.random.default_rng(256)
+    B, K, L = 256, 7, 31
+    arrays = _random_inputs(rng, B, K, L)
+    est = S.EstimatorTable(W.table5_coef() if coef == "table5" else W.constant_coef(0.9), L)
+    ws = S.Workspace(B, 1, K, 1)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for budget in (B * L - 3, B * L, B * L + 7):
+        common = (0.04, budget, L, "proposed", True)
+        ref = _run(S, False, est, arrays, *common, ws=ws)
+        for _ in range(2):
+            _equal(_run(S, True, est, arrays, *common, status=status), ref)
+    assert int(status.item()) == 0 and ws.status() == 0
+
+
+@pytest.mark.gpu
+def test_static_pricing_allocates_nothing(S):
+    """After a warm-up call, further calls change neither torch's allocated
+    bytes nor the device's free memory."""
+    c = W.mixed_bs128()
+    arrays = [torch.as_tensor(np.ascontiguousarray(x)).cuda() for x in _inputs(c)]
+    d, conf, d_len, g, g_len, n, a, m = arrays
+    B, L = g.shape
+    est = S.EstimatorTable(c["coef"], c["L"])
+    i32 = dict(dtype=torch.int32, device="cuda")
+    outs = (torch.empty((B, L), **i32), torch.empty((B, L), device="cuda"), torch.empty(B, **i32),
+            torch.empty(B, **i32), torch.empty(B, **i32), torch.empty(B + 1, **i32),
+            torch.empty((B, L), dtype=torch.uint8, device="cuda"))
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+
+    def call():
+        S.spec_price_and_allocate_static(d, conf, d_len, g, g_len, n, a, m, est, c["lam"], c["budget"],
+                                         c["max_verify_len"], c["policy"], c["draft_greedy"], *outs,
+                                         status_word=status)
+
+    for _ in range(2):
+        call()
+    torch.cuda.synchronize()
+    alloc0, free0 = torch.cuda.memory_allocated(), torch.cuda.mem_get_info()[0]
+    for _ in range(8):
+        call()
+    torch.cuda.synchronize()
+    assert torch.cuda.memory_allocated() == alloc0
+    assert torch.cuda.mem_get_info()[0] == free0
+    assert int(status.item()) == 0
