@@ -232,6 +232,24 @@ def oracle_layout(cfg):
                                 cfg["policy"], cfg["draft_greedy"])
 
 
+def host_cpu():
+    """The host the oracle runs on: its architecture, CPU model (lscpu) and the
+    number of cores the process may use."""
+    import platform
+
+    info = {"arch": platform.machine(), "cores_available": len(os.sched_getaffinity(0))
+            if hasattr(os, "sched_getaffinity") else os.cpu_count(), "cpu_count": os.cpu_count()}
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            k, _, v = ln.partition(":")
+            if k.strip() in ("Model name", "Vendor ID", "Socket(s)", "Core(s) per socket"):
+                info[k.strip().lower().replace(" ", "_").replace("(s)", "s")] = v.strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return info
+
+
 def cpu_baseline(cfg, lay, logits, seconds=10.0):
     tokens, t0, n = 0, time.perf_counter(), 0
     while time.perf_counter() - t0 < seconds:
@@ -239,7 +257,8 @@ def cpu_baseline(cfg, lay, logits, seconds=10.0):
         n += 1
     dt = time.perf_counter() - t0
     return {"value": tokens / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{n} full oracle rounds of the {WORKLOAD} batch ({dt:.1f} s, single-threaded C)"}
+            "sample": f"{n} full oracle rounds of the {WORKLOAD} batch ({dt:.1f} s, single-threaded C)",
+            "host": host_cpu()}
 
 
 def run_reference(args):
@@ -270,7 +289,8 @@ def run_reference(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": config_json(cfg, {"sample_requests_per_step": s}),
             "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
-                             "sample": f"{s} of {cfg['B']} requests per step (lookup + verify), batch pricing"},
+                             "sample": f"{s} of {cfg['B']} requests per step (lookup + verify), batch pricing",
+                             "host": host_cpu()},
             "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -416,74 +436,95 @@ def timed_rounds(S, torch, cfg, rounds, steps, warmup, barrier=lambda: None, sam
     return timed_parts(torch, sets, ["draft_price", "verify"], steps, warmup, barrier, sampler)
 
 
-def measure_bs4(S, torch, W, steps, warmup, hbm):
-    """The batch-4 code-editing configuration (T = 0): same round, same timing;
-    ten rotating input sets (10 x 19.5 MB of logits > L2)."""
-    cfg = W.edit_bs4()
-    rounds, n_rows, n_tok, _ = make_rounds(S, torch, W, cfg, 10)
-    ms, comp = timed_rounds(S, torch, cfg, rounds, steps, warmup)
-    achieved = n_rows * cfg["V"] * 2 / (comp["verify"] * 1e-6) / 1e9
-    return {"workload": "edit_bs4: B=4, V=151936, history 2048, budget 64, lambda 0.04, T=0, bf16 logits",
-            "value": n_tok * steps / (ms * 1e-3), "unit": UNIT, "rows_per_s": n_rows * steps / (ms * 1e-3),
-            "ms_per_step": ms / steps, "steps": steps, "verified_tokens_per_step": n_tok,
-            "verify_rows_per_step": n_rows, "components_us": {k: round(v, 3) for k, v in comp.items()},
-            "verify_roofline_frac": round(achieved / hbm, 4),
-            "l2": "10 rotating input sets (10 x 19.5 MB > L2)"}
+EDIT_RATES = (0.0, 0.15, 0.30, 0.45, 0.60, 0.70)
+BS4_SETS = 10  # rotating input sets: 10 x (19.5 MB of target rows (+ 8.5 MB of draft rows)) > L2
 
 
-def measure_bs4_probabilistic(S, torch, W, steps, warmup, hbm):
-    """Batch-4 code editing at T = 1 with probabilistic drafting (extension
-    policy): the drafter's 7 tokens sampled on the device from its bf16 rows
-    (spec_sample_drafts), draft + price, then sampled verification against
-    the draft rows; ten rotating input sets (10 x (19.5 + 8.5) MB > L2).  The
-    sampling step counter is held fixed so that every round has the same
-    layout; the work does not depend on the drawn values."""
+def measure_bs4(S, torch, W, steps, warmup, hbm, rate, probabilistic=False):
+    """The batch-4 code-editing configuration with all four requests at one edit
+    rate: draft + price, then chain verification of the allocated rows.
+
+    T = 0: greedy drafts (proposed policy).  T = 1 with probabilistic drafting
+    (extension policy): the drafter's 7 tokens are sampled on the device from
+    its bf16 rows (spec_sample_drafts) before draft + price, and the sampled
+    verification reads the draft rows too; the sampling step counter is held
+    fixed so that every round has the same layout (the work does not depend on
+    the drawn values), and verification's Philox step is the input set's
+    index.  Same timing as the batch-128 round, over ten rotating input sets.
+    Also reports the accepted drafts per round (summed over the batch, mean
+    over the sets) and the share of requests whose chain is the n-gram one."""
     from speculative_decoding_draft_spec_gb300.round import ChainRound
 
-    cfg = W.edit_bs4(temperature=1.0, probabilistic=True)
+    T = 1.0 if probabilistic else 0.0
+    cfg = W.edit_bs4(temperature=T, probabilistic=probabilistic, edit_rates=[rate] * 4)
     B, K, L, V = cfg["B"], cfg["K"], cfg["L"], cfg["V"]
-    max_rows = B * (L + 1)
-    dl = torch.from_numpy(cfg["draft_logits"].view(np.int16)).view(torch.bfloat16).to("cuda")
+    greedy = not probabilistic
+    dl = None
+    if probabilistic:
+        dl = torch.from_numpy(cfg["draft_logits"].view(np.int16)).view(torch.bfloat16).to("cuda")
     rounds = []
-    for _ in range(10):
-        rnd = ChainRound(B, cfg["hist"].shape[1], K, L, V, torch.bfloat16, max_rows, cfg["coef"], cfg["n_min"],
-                         cfg["n_max"], cfg["copy_cap"], with_draft=True)
+    for _ in range(BS4_SETS):
+        rnd = ChainRound(B, cfg["hist"].shape[1], K, L, V, torch.bfloat16, B * (L + 1), cfg["coef"], cfg["n_min"],
+                         cfg["n_max"], cfg["copy_cap"], with_draft=probabilistic)
         rnd.load(cfg["hist"], cfg["hist_len"], cfg["d"], cfg["c"], cfg["d_len"])
-        rnd.draft_logits.copy_(dl)
+        if probabilistic:
+            rnd.draft_logits.copy_(dl)
         rounds.append(rnd)
-    stream = torch.cuda.current_stream()
 
-    def sample(rnd):
-        S.spec_sample_drafts(rnd.draft_logits, 1.0, rnd.d, rnd.ws, seed=0, step=0, stream=stream)
+    def sample(rnd, st):
+        S.spec_sample_drafts(rnd.draft_logits, 1.0, rnd.d, rnd.ws, seed=0, step=0, stream=st)
 
-    sample(rounds[0])
-    rounds[0].draft_and_price(cfg["lam"], cfg["budget"], cfg["max_verify_len"], cfg["policy"], False, stream)
+    first = rounds[0]
+    if probabilistic:
+        sample(first, None)
+    first.draft_and_price(cfg["lam"], cfg["budget"], cfg["max_verify_len"], cfg["policy"], greedy)
     torch.cuda.synchronize()
-    row_off = rounds[0].row_off.cpu().numpy()
-    vlen = rounds[0].verify_len.cpu().numpy()
+    row_off = first.row_off.cpu().numpy()
+    vlen = first.verify_len.cpu().numpy()
+    source = first.source.cpu().numpy()
     n_rows, n_tok = int(row_off[-1]), int(vlen.sum())
     lt = torch.from_numpy(W.compact_logits(cfg, row_off, vlen).view(np.int16)).view(torch.bfloat16).to("cuda")
     for rnd in rounds:
         rnd.logits[:n_rows].copy_(lt)
+    sets = []
+    for k, rnd in enumerate(rounds):
+        parts = [lambda st, rnd=rnd: sample(rnd, st)] if probabilistic else []
+        parts += [lambda st, rnd=rnd: rnd.draft_and_price(cfg["lam"], cfg["budget"], cfg["max_verify_len"],
+                                                          cfg["policy"], greedy, st),
+                  lambda st, rnd=rnd, k=k: rnd.verify(temperature=T, seed=0, step=k, stream=st)]
+        sets.append(parts)
+    names = (["sample_drafts"] if probabilistic else []) + ["draft_price", "verify"]
+    ms, comp = timed_parts(torch, sets, names, steps, warmup)
+    torch.cuda.synchronize()
+    accepted = statistics.mean(int(r.n_accepted.sum().item()) for r in rounds)
+    rd_bytes = n_rows * V * 2
+    q_rows = 0
+    if probabilistic:  # draft rows verification reads: sampled (not point-mass) positions within verify_len
+        pm = first.point_mass.cpu().numpy()
+        q_rows = int(sum(int((pm[r, :min(int(vlen[r]), K)] == 0).sum()) for r in range(B)))
+    ver_bytes = (n_rows + q_rows) * V * 2
+    out = {"edit_rate": rate, "value": n_tok * steps / (ms * 1e-3), "unit": UNIT,
+           "rows_per_s": n_rows * steps / (ms * 1e-3), "us_per_round": 1e3 * ms / steps, "steps": steps,
+           "verified_tokens_per_step": n_tok, "verify_rows_per_step": n_rows, "draft_rows_read": q_rows,
+           "accepted_per_step": accepted, "ngram_chain_share": float(np.isin(source, (1, 2)).mean()),
+           "components_us": {k: round(v, 3) for k, v in comp.items()},
+           "verify_roofline_frac": round(ver_bytes / (comp["verify"] * 1e-6) / 1e9 / hbm, 4),
+           "status_clean": all(int(r.ws.status()) == 0 for r in rounds)}
+    if probabilistic:
+        out["extension_tail_share"] = float(((source == 3) & (first.chain_len.cpu().numpy() > K)).mean())
+        out["sample_drafts_roofline_frac"] = round(B * K * V * 2 / (comp["sample_drafts"] * 1e-6) / 1e9 / hbm, 4)
+    del rounds
+    return out
 
-    # one graph per component and input set; the verification's Philox step is
-    # the set's index (the work does not depend on the uniforms' values)
-    sets = [[lambda st, rnd=rnd: S.spec_sample_drafts(rnd.draft_logits, 1.0, rnd.d, rnd.ws, seed=0, step=0,
-                                                      stream=st),
-             lambda st, rnd=rnd: rnd.draft_and_price(cfg["lam"], cfg["budget"], cfg["max_verify_len"], cfg["policy"],
-                                                     False, st),
-             lambda st, rnd=rnd, k=k: rnd.verify(temperature=1.0, seed=0, step=k, stream=st)]
-            for k, rnd in enumerate(rounds)]
-    ms, comp = timed_parts(torch, sets, ["sample_drafts", "draft_price", "verify"], steps, warmup)
-    draft_bytes = B * K * V * 2
-    return {"workload": "edit_bs4 probabilistic: B=4, T=1, drafts sampled on the device, extension policy, "
-                        "bf16 V=151936",
-            "value": n_tok * steps / (ms * 1e-3), "unit": UNIT, "ms_per_step": ms / steps, "steps": steps,
-            "verified_tokens_per_step": n_tok, "verify_rows_per_step": n_rows,
-            "components_us": {k: round(v, 3) for k, v in comp.items()},
-            "sample_drafts_roofline_frac": round(draft_bytes / (comp["sample_drafts"] * 1e-6) / 1e9 / hbm, 4),
-            "status_clean": all(int(r.ws.status()) == 0 for r in rounds),
-            "l2": "10 rotating input sets (10 x 28 MB > L2)"}
+
+def measure_bs4_sweep(S, torch, W, steps, warmup, hbm, probabilistic=False):
+    """measure_bs4 at each edit rate of the configuration's sweep."""
+    per = [measure_bs4(S, torch, W, steps, warmup, hbm, r, probabilistic) for r in EDIT_RATES]
+    T = 1 if probabilistic else 0
+    what = ("drafts sampled on the device, extension policy" if probabilistic else "greedy drafts, proposed policy")
+    return {"workload": f"edit_bs4: B=4, V=151936 bf16, history 2048, budget 64, lambda 0.04, T={T}, {what}; "
+                        "edit rate swept over {0,15,30,45,60,70}% (all four requests at one rate)",
+            "by_edit_rate": per, "l2": f"{BS4_SETS} rotating input sets per rate (> L2)"}
 
 
 def measure_long_sampled(S, torch, W, steps, warmup, hbm):
@@ -527,12 +568,14 @@ def measure_long_sampled(S, torch, W, steps, warmup, hbm):
             "l2": "2 rotating input sets (2 x 622 MB > L2)"}
 
 
-def measure_tree(S, torch, W, steps, warmup, hbm):
-    """The tree round, batch 32 trees of 16 rows (bf16 V = 151936): the candidate
-    tree built on the device from the drafter's block and the n-gram chain
-    (spec_build_tree), then greedy tree verification (spec_verify_tree); two
-    logit sets (2 x 156 MB > L2)."""
-    cfg = W.tree_bs32(width=16)
+def measure_tree(S, torch, W, steps, warmup, hbm, width=16):
+    """The tree round, batch 32 trees of `width` rows (bf16 V = 151936): the
+    candidate tree built on the device from the drafter's block and the n-gram
+    chain (spec_build_tree), then greedy tree verification (spec_verify_tree)
+    of logits that plant a true path of mean accept length 3 (capped by the
+    tree); enough rotating logit sets to hold over 300 MB (two at width 16,
+    eight at width 4), so no step reads rows still in L2."""
+    cfg = W.tree_bs32(width=width)
     B, V, n = cfg["B"], cfg["V"], cfg["width"]
     dev = lambda a, dt=None: torch.as_tensor(np.ascontiguousarray(a)).to("cuda") if dt is None else \
         torch.as_tensor(np.ascontiguousarray(a)).to("cuda", dt)
@@ -547,7 +590,8 @@ def measure_tree(S, torch, W, steps, warmup, hbm):
     rows = int(node_off_h[-1])
     logits, _ = W.tree_logits(node_off_h, tok_h, par_h, V)
     lt = torch.from_numpy(logits.view(np.int16)).view(torch.bfloat16).to("cuda")
-    sets = [lt, lt.clone()]
+    nset = max(2, -(-300_000_000 // (rows * V * 2)))
+    sets = [lt] + [lt.clone() for _ in range(nset - 1)]
     node_off = dev(node_off_h)
     # the verify reads the builder's rows in place: [B x n] with every tree full
     assert np.all(nrow.cpu().numpy() == n)
@@ -561,14 +605,23 @@ def measure_tree(S, torch, W, steps, warmup, hbm):
             for lg in sets]
     ms, comp = timed_parts(torch, sets, ["build", "verify"], steps, warmup)
     accepted = int(acc.sum().item())
-    return {"workload": "tree_bs32: B=32, block of 8 picks with top-4 candidates plus a 15-token n-gram chain, "
-                        "trees of 16 rows, bf16 V=151936",
+    return {"width": n,
+            "workload": f"tree_bs32: B=32, block of 8 picks with top-4 candidates plus a 15-token n-gram chain, "
+                        f"trees of {n} rows, bf16 V=151936, planted mean accept length 3 (capped by the tree)",
             "tree_rows_per_s": rows * steps / (ms * 1e-3), "accepted_tokens_per_s": accepted * steps / (ms * 1e-3),
             "ms_per_step": ms / steps, "steps": steps, "rows_per_step": rows, "accepted_per_step": accepted,
             "components_us": {k: round(v, 3) for k, v in comp.items()},
             "verify_roofline_frac": round(rows * V * 2 / (comp["verify"] * 1e-6) / 1e9 / hbm, 4),
             "status_clean": int(ws.status()) == 0 and int(ws_b.status()) == 0,
-            "l2": "2 rotating logit sets (2 x 156 MB > L2)"}
+            "l2": f"{nset} rotating logit sets ({nset} x {rows * V * 2 / 1e6:.1f} MB > L2)"}
+
+
+def measure_tree_widths(S, torch, W, steps, warmup, hbm):
+    """measure_tree at each tree width of the configuration (4, 8, 12, 16 rows)."""
+    per = [measure_tree(S, torch, W, steps, warmup, hbm, w) for w in (4, 8, 12, 16)]
+    top = dict(per[-1])
+    top["by_width"] = per
+    return top
 
 
 def measure_tree_fill(S, torch, W, steps, warmup, hbm):
@@ -705,10 +758,10 @@ def run_gpu(args):
               "C0": 256.0, "p": 1.0, "b_star": int(b_out.item()), "lambda": float(l_out.item())}
 
     hbm, peak_kind = peaks()
-    bs4 = measure_bs4(S, torch, W, min(args.steps, 5000), args.warmup, hbm)
-    bs4_prob = measure_bs4_probabilistic(S, torch, W, min(args.steps, 3000), args.warmup, hbm)
+    bs4 = measure_bs4_sweep(S, torch, W, min(args.steps, 3000), args.warmup, hbm)
+    bs4_prob = measure_bs4_sweep(S, torch, W, min(args.steps, 2000), args.warmup, hbm, probabilistic=True)
     long_sampled = measure_long_sampled(S, torch, W, min(args.steps, 1000), args.warmup, hbm)
-    tree = measure_tree(S, torch, W, min(args.steps, 2000), args.warmup, hbm)
+    tree = measure_tree_widths(S, torch, W, min(args.steps, 2000), args.warmup, hbm)
     tree_fill = measure_tree_fill(S, torch, W, min(args.steps, 2000), args.warmup, hbm)
     if rank != 0:
         return
@@ -749,7 +802,8 @@ def run_once():
     """One launch each of the tree n-gram fill and the tree builder (the
     filled-tree workload: 32 requests, 4096-token texts, chains from the anchor
     and 8 picks, trees of 16 rows) and of draft sampling (batch-4 code editing,
-    4 x 7 bf16 draft rows, T = 1), for a profiler."""
+    4 x 7 bf16 draft rows, T = 1), then the chain verifications of
+    once_verify_launches, for a profiler."""
     import torch
 
     import speculative_decoding_draft_spec_gb300 as S
@@ -777,7 +831,56 @@ def run_once():
     S.spec_sample_drafts(dl, 1.0, y, ws2, seed=0, step=0)
     torch.cuda.synchronize()
     ok = int(ws.status()) == 0 and int(ws2.status()) == 0
-    print(json.dumps({"legs": "once", "tree_rows": int(nr.sum()), "status_clean": ok}), flush=True)
+    rows = once_verify_launches(S, torch, W)
+    print(json.dumps({"legs": "once", "tree_rows": int(nr.sum()), "verify_rows": rows, "status_clean": ok}),
+          flush=True)
+
+
+def once_verify_launches(S, torch, W):
+    """One chain verification each, after its round's draft + price: batch-4 code
+    editing at T = 0 (40 bf16 rows), batch-4 code editing at T = 1 with drafts
+    sampled on the device (bf16 target and draft rows; the sampled kernel and
+    the max(0, p - q) draw), and the batch-64 long-context workload at T = 0.7
+    (fp32, 16 rows per request), for a profiler.  Returns the verify rows of each."""
+    from speculative_decoding_draft_spec_gb300.round import ChainRound
+
+    out = {}
+    c = W.edit_bs4()
+    rnd = ChainRound(c["B"], c["hist"].shape[1], c["K"], c["L"], c["V"], torch.bfloat16, c["B"] * (c["L"] + 1),
+                     c["coef"], c["n_min"], c["n_max"], c["copy_cap"])
+    rnd.load(c["hist"], c["hist_len"], c["d"], c["c"], c["d_len"])
+    rnd.draft_and_price(c["lam"], c["budget"], c["max_verify_len"], c["policy"], True)
+    ro, vl = rnd.row_off.cpu().numpy(), rnd.verify_len.cpu().numpy()
+    n = int(ro[-1])
+    rnd.logits[:n].copy_(torch.from_numpy(W.compact_logits(c, ro, vl).view(np.int16)).view(torch.bfloat16))
+    rnd.verify(temperature=0.0)
+    torch.cuda.synchronize()
+    out["edit_bs4"] = n
+    c = W.edit_bs4(temperature=1.0, probabilistic=True)
+    rnd = ChainRound(c["B"], c["hist"].shape[1], c["K"], c["L"], c["V"], torch.bfloat16, c["B"] * (c["L"] + 1),
+                     c["coef"], c["n_min"], c["n_max"], c["copy_cap"], with_draft=True)
+    rnd.load(c["hist"], c["hist_len"], c["d"], c["c"], c["d_len"])
+    rnd.draft_logits.copy_(torch.from_numpy(c["draft_logits"].view(np.int16)).view(torch.bfloat16))
+    S.spec_sample_drafts(rnd.draft_logits, 1.0, rnd.d, rnd.ws, seed=0, step=0)
+    rnd.draft_and_price(c["lam"], c["budget"], c["max_verify_len"], c["policy"], False)
+    ro, vl = rnd.row_off.cpu().numpy(), rnd.verify_len.cpu().numpy()
+    n = int(ro[-1])
+    rnd.logits[:n].copy_(torch.from_numpy(W.compact_logits(c, ro, vl).view(np.int16)).view(torch.bfloat16))
+    rnd.verify(temperature=1.0, seed=0, step=0)
+    torch.cuda.synchronize()
+    out["edit_bs4_probabilistic"] = n
+    c = W.long_bs64()
+    rows = c["rows_per_request"]
+    rnd = ChainRound(c["B"], c["hist"].shape[1], c["K"], c["L"], c["V"], torch.float32, c["B"] * rows, c["coef"],
+                     c["n_min"], c["n_max"], c["copy_cap"])
+    rnd.load(c["hist"], c["hist_len"], c["d"], c["c"], c["d_len"])
+    rnd.logits.copy_(torch.from_numpy(W.materialised_logits(c)))
+    rnd.draft_and_price(c["lam"], c["budget"], c["max_verify_len"], c["policy"], True)
+    rnd.verify(temperature=c["temperature"], seed=0, step=0,
+               row_off=torch.as_tensor(c["row_off_materialised"]).cuda())
+    torch.cuda.synchronize()
+    out["long_bs64"] = int((rnd.verify_len.cpu().numpy() + 1).sum())
+    return out
 
 
 def main():
@@ -789,7 +892,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--legs", default="all", choices=["all", "timed", "once"],
                     help="timed: only the warm-up and timed loop; once: one launch each of the tree "
-                         "fill, tree builder and draft sampling kernels (both for profiling)")
+                         "fill, tree builder and draft sampling kernels and of the batch-4 greedy, batch-4 "
+                         "sampled and long-context sampled verifications (both for profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

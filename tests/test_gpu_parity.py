@@ -276,25 +276,46 @@ def test_chain_tiny_materialised_rows(S, T, prob):
     assert ws.status() == 0
 
 
-@pytest.mark.parametrize("T,prob", [(0.0, False), (1.0, False), (1.0, True)])
-def test_chain_edit_bs4_full_vocab(S, T, prob):
-    c = W.edit_bs4(temperature=T, probabilistic=prob)
+def _chain_edit_vs_oracle(S, c, T):
     lay = _layout(S, c)
     logits = W.compact_logits(c, lay.row_off, lay.verify_len)
     draft = c["draft_logits"]
     ws = _ws(S, c["B"], int(lay.row_off[-1]), c["K"], c["V"])
     lt = logits_dev(logits)
     dt = None if draft is None else logits_dev(draft)
-    stats = []
     for step in range(8 if T > 0 else 1):
         g = gpu_chain(S, ws, None, lay.row_off, lay.chain, lay.verify_len, lay.point_mass, draft, T,
                       seed=0, step=step, logits_t=lt, draft_t=dt)
         o = O.verify_chain(logits, lay.row_off, lay.chain, lay.verify_len, lay.point_mass, draft, T, 0, step)
         if T == 0:
             assert np.array_equal(g["out"], o.out_tokens) and np.array_equal(g["na"], o.n_accepted)
+            assert np.array_equal(g["ne"], o.n_emitted)
         else:
-            stats.append(compare_sampled(g, o, logits, lay.row_off, lay.chain, lay.verify_len, lay.point_mass,
-                                         draft, T))
+            compare_sampled(g, o, logits, lay.row_off, lay.chain, lay.verify_len, lay.point_mass, draft, T)
+    assert ws.status() == 0
+    return lay
+
+
+@pytest.mark.parametrize("T,prob", [(0.0, False), (1.0, False), (1.0, True)])
+def test_chain_edit_bs4_full_vocab(S, T, prob):
+    _chain_edit_vs_oracle(S, W.edit_bs4(temperature=T, probabilistic=prob), T)
+
+
+# the code-editing configuration swept over its edit rates, all four requests at one rate
+EDIT_RATES = [0.0, 0.15, 0.30, 0.45, 0.60, 0.70]
+
+
+@pytest.mark.parametrize("rate", EDIT_RATES)
+@pytest.mark.parametrize("T,prob", [(0.0, False), (1.0, False), (1.0, True)])
+def test_chain_edit_bs4_by_edit_rate(S, rate, T, prob):
+    _chain_edit_vs_oracle(S, W.edit_bs4(temperature=T, probabilistic=prob, edit_rates=[rate] * 4), T)
+
+
+@pytest.mark.parametrize("rate", EDIT_RATES)
+@pytest.mark.parametrize("prob", [False, True])
+def test_fused_draft_and_price_by_edit_rate(S, rate, prob):
+    c = W.edit_bs4(temperature=1.0 if prob else 0.0, probabilistic=prob, edit_rates=[rate] * 4)
+    got, o, ws = _fused_vs_oracle(S, c)
     assert ws.status() == 0
 
 

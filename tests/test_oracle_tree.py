@@ -109,6 +109,38 @@ def test_planted_paths_of_the_tree_workload_are_recovered(orc, width):
         assert tv.accept_len[r] == len(path) - 1
 
 
+@pytest.mark.parametrize("width", [8, 12, 16])
+def test_tree_workload_realises_mean_accept_length_3(orc, width):
+    """The 32-request tree workload plants paths whose accept lengths average 3
+    (the configuration's expected accept length), within 0.5."""
+    cfg = W.tree_bs32(width=width)
+    tb = orc.build_tree(cfg["anchor"], cfg["cand_tok"], cfg["cand_score"], cfg["ng_tok"], cfg["ng_len"],
+                        cfg["ng_score"], cfg["ng_adj"], width)
+    node_off, tok, parent = W.flatten_trees(tb.tok, tb.parent, tb.n_rows)
+    logits, planted = W.tree_logits(node_off, tok, parent, cfg["V"])
+    tv = orc.verify_tree(logits, node_off, tok, parent, cfg["max_nodes"])
+    assert [len(p) - 1 for p in planted] == tv.accept_len.tolist()
+    assert abs(tv.accept_len.mean() - 3.0) <= 0.5, tv.accept_len.mean()
+
+
+def test_filled_tree_workload_realises_mean_accept_length_3(orc):
+    c = W.tree_fill_bs32(width=16)
+    fo = orc.ngram_fill(c["hist"], c["hist_len"], c["cand_tok"], c["n_min"], c["copy_cap"], c["max_depth"], c["Lg"])
+    tb = orc.build_tree(c["anchor"], c["cand_tok"], c["cand_score"], fo.tok, fo.len, c["ng_score"], c["ng_adj"], 16)
+    node_off, tok, parent = W.flatten_trees(tb.tok, tb.parent, tb.n_rows)
+    logits, _ = W.tree_logits(node_off, tok, parent, c["V"])
+    tv = orc.verify_tree(logits, node_off, tok, parent, 16)
+    assert abs(tv.accept_len.mean() - 3.0) <= 0.5, tv.accept_len.mean()
+
+
+@pytest.mark.parametrize("depth", [1, 2, 3, 4, 6, 9, 20])
+def test_capped_geometric_rate_gives_mean_3_or_the_depth(depth):
+    a = W._capped_geometric_rate(depth, 3.0)
+    assert 0.0 < a <= 1.0
+    mean = sum(a ** k for k in range(1, depth + 1))  # E[min(A, d)] = sum_k P(A >= k)
+    assert abs(mean - min(3.0, depth)) < 1e-9
+
+
 def test_invalid_trees_are_flagged(orc):
     rows = np.zeros((3, 5), np.float32)
     tv = orc.verify_tree(rows, np.array([0, 3], np.int32), np.array([0, 1, 2], np.int32),

@@ -458,31 +458,66 @@ def flatten_trees(tok, parent, n_rows):
     return node_off, t, p
 
 
-def tree_logits(node_off, tok, parent, V, seed=1005, dtype="bf16", margin=8.0):
+def _capped_geometric_rate(depth, mean):
+    """alpha in [0, 1] with sum_{k=1..depth} alpha^k = min(mean, depth): the
+    acceptance rate whose geometric accept length, capped at `depth`, has that
+    mean (bisection; alpha = 1 when the cap is at or below the mean)."""
+    if depth <= mean:
+        return 1.0
+    lo, hi = 0.0, 1.0
+    for _ in range(60):
+        a = 0.5 * (lo + hi)
+        if sum(a ** k for k in range(1, depth + 1)) < mean:
+            lo = a
+        else:
+            hi = a
+    return 0.5 * (lo + hi)
+
+
+def tree_logits(node_off, tok, parent, V, seed=1005, dtype="bf16", margin=8.0, mean_accept=3.0):
     """bf16 (or fp32) logits N(0, 1) for the rows of given trees, with a planted
-    true path per request: from the anchor, a geometric number of steps (mean 3)
-    each to a uniformly chosen child, the target's argmax at a row being the
-    token of the next path node (margin +margin); at the path's last node the
-    argmax is a token that matches none of its children.  Returns (logits,
-    planted paths as row indices)."""
+    true path per request whose accept length has mean `mean_accept` (3),
+    capped by the tree.
+
+    Request r's accept length A is geometric on 0..d, d the depth of its tree
+    (P(A >= k) = alpha^k for k <= d), with alpha chosen so that E[A] =
+    min(3, d); the draws are stratified over the batch (request r takes the
+    quantile at (pi(r) + v) / B for a seeded permutation pi and v ~ U[0, 1)),
+    so that the batch's mean is close to the law's.  The path walks A steps
+    from the anchor, each to a uniformly chosen child whose subtree is deep
+    enough for the steps left (the spine of picks or an n-gram chain; siblings
+    are leaves).  At each path node but the last the target's argmax is the
+    token of the next path node (margin +margin); at the last node it is a
+    token that matches none of its children.  Returns (logits, planted paths
+    as row indices)."""
     rng = np.random.default_rng(seed)
     N = int(node_off[-1])
+    B = len(node_off) - 1
     row_truth = np.full(N, -1, np.int32)
     planted = []
-    for r in range(len(node_off) - 1):
+    strata = (rng.permutation(B) + rng.random(B)) / max(B, 1)
+    for r in range(B):
         base, n = int(node_off[r]), int(node_off[r + 1] - node_off[r])
-        A = int(rng.geometric(0.25)) - 1
+        kids_of = [[] for _ in range(n)]
+        for j in range(1, n):
+            kids_of[int(parent[base + j])].append(j)
+        height = [0] * n  # parents precede children: one backward pass
+        for j in range(n - 1, 0, -1):
+            pj = int(parent[base + j])
+            height[pj] = max(height[pj], height[j] + 1)
+        d = height[0]
+        alpha = _capped_geometric_rate(d, mean_accept)
+        u = float(strata[r])
+        A = d if alpha >= 1.0 else min(d, int(np.floor(np.log1p(-u) / np.log(alpha))))
         cur, depth, path = 0, 0, [0]
         while depth < A:
-            kids = [j for j in range(n) if parent[base + j] == cur]
-            if not kids:
-                break
-            nxt = kids[int(rng.integers(0, len(kids)))]
+            pool = [j for j in kids_of[cur] if height[j] >= A - depth - 1]
+            nxt = pool[int(rng.integers(0, len(pool)))]
             row_truth[base + cur] = tok[base + nxt]
             cur = nxt
             path.append(cur)
             depth += 1
-        kid_toks = {int(tok[base + j]) for j in range(n) if parent[base + j] == cur}
+        kid_toks = {int(tok[base + j]) for j in kids_of[cur]}
         t = int(rng.integers(0, V))
         while t in kid_toks:
             t = (t + 1) % V
