@@ -101,6 +101,7 @@ typedef enum {
 #define SPEC_MAX_TREE_NODES 256
 #define SPEC_MAX_TREE_CANDIDATES 512 /* the builder's 1 + P Kc + n_chains Lg      */
 #define SPEC_MAX_COPY_CAP 4096
+#define SPEC_MAX_VOCAB 524288    /* largest vocabulary of a workspace / logit row    */
 
 const char* spec_status_string(spec_status s);
 int32_t spec_version(void);
@@ -127,8 +128,12 @@ typedef struct {
   size_t off_counter2;   /* uint32 [max_batch]: second-phase counters        */
   size_t off_record;     /* 64 B [max_batch]: resample records              */
   size_t off_rowkey;     /* uint64 [max_rows]: packed row argmax             */
-  size_t off_partial;    /* float2 [(max_rows + max_batch K) x units]        */
-  size_t off_partial2;   /* double [max_batch x units]                       */
+  size_t off_partial;    /* float2 [(max_rows + max_batch K) x pstride]: per
+                            chunk (max, sum) of a row, then the logit at its
+                            draft token; pstride = units + 1 rounded up to
+                            even                                             */
+  size_t off_partial2;   /* float [max_batch x pstride]: per chunk residual
+                            mass of a rejected position                    */
   size_t off_keys;       /* uint32 [SPEC_MAX_PRICE_BATCH x SPEC_MAX_L]:
                             allocation keys of the pricing step            */
   size_t off_counter3;   /* uint32 [max_batch x max(K, 1)]: per draft-row
@@ -351,11 +356,11 @@ spec_status spec_build_tree(int32_t batch, int32_t P, int32_t Kc, const int32_t*
  * spec_verify_chain's.  The positions are drawn independently from the given
  * rows (a drafter whose row depends on the previous token produces its rows
  * inside its own network).  dbg_u / dbg_q [batch x K] (may be NULL): the
- * uniform and q of the drawn token.  The per-unit (max, sum) of every row are
- * left in the workspace slots that spec_verify_chain uses for q rows.
+ * uniform and q of the drawn token.  The rows' per-chunk (max, sum) are left
+ * in workspace slots apart from the target rows'.
  * T must be > 0.  A row holding NaN or +Inf sets SPEC_DEV_NONFINITE.
- * Limits: batch <= the workspace's max_batch, 1 <= K <= its K, vocab <= its
- * vocab.
+ * Limits: batch <= the workspace's max_batch and <= 2048, 1 <= K <= its K,
+ * vocab <= its vocab.
  * ------------------------------------------------------------------------ */
 spec_status spec_sample_drafts(int32_t batch, int32_t K, int32_t vocab, spec_dtype dtype,
                                const void* draft_logits, float temperature, uint64_t seed, uint64_t step,
@@ -470,7 +475,9 @@ spec_status spec_price_and_allocate_static(
  * Invalid request (layout, verify_len > L): SPEC_DEV_BAD_LENGTH,
  * n_accepted = n_emitted = 0 and no tokens.  A draft id outside [0, vocab)
  * sets SPEC_DEV_BAD_TOKEN and is rejected.
- * Limits: L <= SPEC_MAX_L, vocab >= 1, batch <= 65535.
+ * Limits: L <= SPEC_MAX_L, 1 <= vocab <= SPEC_MAX_VOCAB, batch <= 2048,
+ * (max_rows + batch K) x ceil(vocab / chunk) < 2^31 with chunk = 4096 (bf16)
+ * or 2048 (fp32) entries; else SPEC_ERR_UNSUPPORTED.
  * ------------------------------------------------------------------------ */
 spec_status spec_verify_chain(
     int32_t batch, int32_t vocab, spec_dtype dtype, const void* target_logits,
@@ -494,7 +501,8 @@ spec_status spec_verify_chain(
  * the accepted nodes, then the argmax at the last one, then -1).
  * A malformed tree sets SPEC_DEV_BAD_TREE (n outside [1, max_nodes]:
  * SPEC_DEV_BAD_LENGTH) and gives accept_len = -1 with no tokens.
- * Limits: max_nodes <= SPEC_MAX_TREE_NODES, node_off[batch] <= max_rows.
+ * Limits: max_nodes <= SPEC_MAX_TREE_NODES, node_off[batch] <= max_rows,
+ * 1 <= vocab <= SPEC_MAX_VOCAB, batch <= 2048.
  * ------------------------------------------------------------------------ */
 spec_status spec_verify_tree(int32_t batch, int32_t vocab, spec_dtype dtype, const void* logits,
                              const int32_t* node_off, int32_t max_rows, const int32_t* tok,

@@ -66,6 +66,7 @@ cudaError_t spec_launch_verify_chain(int32_t batch, int32_t vocab, int32_t dtype
                                      int32_t* n_emitted, float* dbg_ratio, float* dbg_u,
                                      float* dbg_resid, const spec_workspace* ws, int num_sms,
                                      cudaStream_t stream);
+int spec_verify_limits_ok(int32_t vocab, int32_t dtype, int64_t rows, int num_sms);
 cudaError_t spec_launch_verify_tree(int32_t batch, int32_t vocab, int32_t dtype, const void* logits,
                                     const int32_t* node_off, const int32_t* tok,
                                     const int32_t* parent, int32_t max_nodes, int32_t* path,
@@ -95,7 +96,7 @@ spec_status from_cuda(cudaError_t e) { return e == cudaSuccess ? SPEC_OK : SPEC_
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 bool layout(int32_t max_batch, int32_t max_rows, int32_t K, int32_t vocab, spec_workspace* w) {
-  if (max_batch < 0 || max_rows < 0 || K < 0 || vocab < 1 || K > SPEC_MAX_L) return false;
+  if (max_batch < 0 || max_rows < 0 || K < 0 || vocab < 1 || K > SPEC_MAX_L || vocab > SPEC_MAX_VOCAB) return false;
   const int64_t units = ((int64_t)vocab + SPEC_UNIT - 1) / SPEC_UNIT;
   size_t off = 256;  // status word + padding
   w->off_counter = off;
@@ -106,10 +107,11 @@ bool layout(int32_t max_batch, int32_t max_rows, int32_t K, int32_t vocab, spec_
   off = align256(off + 64 * (size_t)max_batch);
   w->off_rowkey = off;
   off = align256(off + sizeof(unsigned long long) * (size_t)max_rows);
+  const size_t pstride = (size_t)spec_partial_stride((int)units);
   w->off_partial = off;
-  off = align256(off + sizeof(float2) * (size_t)units * ((size_t)max_rows + (size_t)max_batch * K));
+  off = align256(off + sizeof(float2) * pstride * ((size_t)max_rows + (size_t)max_batch * K));
   w->off_partial2 = off;
-  off = align256(off + sizeof(double) * (size_t)units * (size_t)max_batch);
+  off = align256(off + sizeof(float) * pstride * (size_t)max_batch);
   w->off_keys = off;  // sized for the largest pricing batch, whatever max_batch is
   off = align256(off + sizeof(uint32_t) * (size_t)SPEC_MAX_PRICE_BATCH * SPEC_MAX_L);
   w->off_counter3 = off;
@@ -332,6 +334,7 @@ spec_status spec_sample_drafts(int32_t batch, int32_t K, int32_t vocab, spec_dty
   if (batch == 0) return SPEC_OK;
   const int sms = device_sms();
   if (sms <= 0) return SPEC_ERR_CUDA;
+  if (!spec_verify_limits_ok(vocab, (int32_t)dtype, (int64_t)batch * K, sms)) return SPEC_ERR_UNSUPPORTED;
   return from_cuda(spec_launch_sample_drafts(batch, K, vocab, (int32_t)dtype, draft_logits, temperature, seed, step,
                                              y, dbg_u, dbg_q, ws, sms, stream));
 }
@@ -396,6 +399,8 @@ spec_status spec_verify_chain(int32_t batch, int32_t vocab, spec_dtype dtype, co
   if (batch == 0) return SPEC_OK;
   const int sms = device_sms();
   if (sms <= 0) return SPEC_ERR_CUDA;
+  if (!spec_verify_limits_ok(vocab, (int32_t)dtype, (int64_t)max_rows + (int64_t)batch * K, sms))
+    return SPEC_ERR_UNSUPPORTED;
   spec_workspace w = *ws;
   w.max_rows = max_rows;  // partial slots of q rows follow the call's own row bound
   return from_cuda(spec_launch_verify_chain(batch, vocab, (int32_t)dtype, target_logits, row_off,
@@ -420,6 +425,7 @@ spec_status spec_verify_tree(int32_t batch, int32_t vocab, spec_dtype dtype, con
   if (batch == 0) return SPEC_OK;
   const int sms = device_sms();
   if (sms <= 0) return SPEC_ERR_CUDA;
+  if (!spec_verify_limits_ok(vocab, (int32_t)dtype, (int64_t)max_rows, sms)) return SPEC_ERR_UNSUPPORTED;
   spec_workspace w = *ws;
   w.max_rows = max_rows;
   return from_cuda(spec_launch_verify_tree(batch, vocab, (int32_t)dtype, logits, node_off, tok, parent,

@@ -10,6 +10,12 @@
 #define SPEC_CTA_THREADS (32 * SPEC_WARPS_PER_CTA)
 #define SPEC_UNIT 2048  // vocabulary entries per work unit (one warp)
 
+// float2 entries between two rows of the workspace's chunk partials: one per
+// chunk of the finest chunking (2048 fp32 entries), then a spare entry (the
+// logit at the row's draft token), rounded up to an even count so that every
+// row starts on a 16-byte boundary
+static inline __host__ __device__ int spec_partial_stride(int units) { return (units + 2) & ~1; }
+
 namespace spec {
 
 __device__ __forceinline__ void set_status(uint32_t* status, uint32_t bits) {
@@ -170,6 +176,10 @@ __device__ __forceinline__ uint32_t atomic_add_acq_rel(uint32_t* p, uint32_t v) 
   return old;
 }
 
+// order this thread's earlier generic-proxy accesses (and the acquire that
+// preceded them) before its later bulk copies, which read through the async proxy
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async;" ::: "memory"); }
+
 // workspace view used by device code
 struct WsView {
   uint32_t* status;
@@ -178,9 +188,9 @@ struct WsView {
   uint32_t* counter3;  // per draft-row arrival counters (probabilistic drafting)
   unsigned char* record;
   unsigned long long* rowkey;
-  float2* partial;
-  double* partial2;
-  int32_t units;  // stride of the partial arrays
+  float2* partial;   // per chunk (max, sum) of each row, spec_partial_stride(units) entries per row
+  float* partial2;   // per chunk residual mass of each request's rejected position
+  int32_t units;     // ceil(vocab / 2048)
   int32_t max_rows;
   int32_t max_batch;
   int32_t K;

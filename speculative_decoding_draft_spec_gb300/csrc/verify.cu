@@ -1,5 +1,6 @@
 // verify.cu -- steps 3 and 4 of the round: chain verification and greedy tree
-// verification over full-vocabulary logit rows.
+// verification over full-vocabulary logit rows, and the drafter's
+// probabilistic tokens (a draw per draft row).
 //
 // Chain (Hybrid Spark sec. 2, App. H; the fixed-cost parallel drafter page's
 // verification rule): accept y_i iff u_i < min(1, p_i(y_i)/q_i(y_i)), q a
@@ -9,45 +10,50 @@
 // Tree (AdaSpark sec. 2.2): a node is accepted iff its token equals the argmax
 // at its parent's row and its parent is accepted; commit the path and the
 // argmax after it.
+// Drafting (Hybrid Spark sec. 4.5, App. H): y_k ~ softmax(z_k / T) for each
+// draft row, by inverse CDF at a Philox uniform.
 //
-// GB300 layout.  The HBM-bound part is one pass over every verify row.  One
-// CTA per SM, 12 warps each; the work is the sequence of 8 KB chunks of the
-// rows (4096 bf16 / 2048 fp32 entries) in (request, row, chunk) order, and
-// every warp takes an equal contiguous range of it.  Each warp streams its
-// range through its own 8 KB shared-memory stage filled by one-dimensional
-// bulk async copies (completion on an mbarrier, bounded wait): it moves a
-// landed chunk into registers and refills the stage at once, so its next
-// copy is in flight while it computes.  One 8 KB copy per warp (96 KB per
-// SM, 15 MB over the GPU) keeps HBM busy; deeper rings measured slower, as
-// longer memory queues widen the spread of the warps' finish times.  Per
-// chunk a warp
-// produces
-//   greedy rows:  a packed 64-bit (ordered value, ~index) key; keys of one
-//                 row fold in registers and reach the row's workspace key with
-//                 one atomicMax per run of the row (largest value, lowest
+// GB300 layout.  The HBM-bound part is one pass over every row.  One CTA per
+// SM, 12 warps each; the work is the sequence of 8 KB chunks of the rows (4096
+// bf16 / 2048 fp32 entries) in (request, row, chunk) order, and every warp
+// takes an equal contiguous range of it.  Each warp streams its range through
+// its own 8 KB shared-memory stage, filled by one-dimensional bulk async
+// copies (completion on an mbarrier, bounded wait): it moves a landed chunk
+// into registers and refills the stage at once, so one copy per warp is in
+// flight (longer memory queues widen the spread of the warps' finish times).
+// Per chunk a warp produces
+//   greedy / tree rows: a packed 64-bit (ordered value, ~index) key; keys of
+//                 one row fold in registers and reach the row's workspace key
+//                 with one atomicMax per run of the row (largest value, lowest
 //                 index);
-//   sampled rows: (max, sum of 2^((z - max) log2e / T)) per 2048-entry unit
-//                 in the workspace.
-// Each request has an arrival counter; the warp that completes a request's
-// last chunk (acquire-release atomic, no waiting) finalizes it: argmax
-// compare or Philox accept tests, and for a draw the inverse CDF in
-// vocabulary order located first over the units' sums and then inside the
-// one unit that holds the crossing (a second read of 4-8 KB, not of the row).
-// A draw from max(0, p - q) needs both normalisers first; those requests are
-// finished by a second, small kernel over the rejected (p, q) row pairs.
+//   sampled rows: the chunk's (max, sum of 2^((z - max) log2e / T)) in the
+//                 workspace, and the logit at the row's draft token when the
+//                 chunk holds it.
+// Each request (each draft row, when drafting) has an arrival counter; the
+// warp that completes its last chunk (acquire-release atomic, no waiting)
+// finalizes it in an 8 KB scratch of its own beside its stage: the request's
+// partial rows arrive there by one bulk copy each, so merging the row
+// normalisers, reading p(y) and q(y) and locating a draw's chunk take one
+// memory round trip, and a draw's chunk is then walked in shared memory.  A
+// draw from max(0, p - q) needs a second pass over two rows once both
+// normalisers are known; those requests are finished by resample_kernel, one
+// CTA per (request, chunk).
 #include <cuda_bf16.h>
 
 #include "common.cuh"
 
 namespace spec {
 
-enum { MODE_CHAIN_GREEDY = 0, MODE_CHAIN_SAMPLE = 1, MODE_TREE = 2 };
+enum { MODE_CHAIN_GREEDY = 0, MODE_CHAIN_SAMPLE = 1, MODE_TREE = 2, MODE_DRAFT = 3 };
 
-// streaming kernel: 12 warps per CTA, one CTA per SM, each warp with its own
-// 8 KB stage (96 KB of shared memory in flight per SM)
 #define VR_WARPS 12
 #define VR_THREADS (32 * VR_WARPS)
-enum { KIND_POINT = 0, KIND_BONUS = 1, KIND_Q = 2 };
+#define VR_STAGE 8192            // bytes per stage: one chunk (one copy in flight per warp)
+#define VR_BARS 2                // per warp: the stage's, and the finalizer scratch's
+// shared memory of one warp: its stage, then (sampled modes) the finalizer's scratch
+#define VR_WBUF(MODE) (VR_STAGE * ((MODE) == ::spec::MODE_CHAIN_SAMPLE || (MODE) == ::spec::MODE_DRAFT ? 2 : 1))
+#define RS_THREADS 256           // resample_kernel: one CTA per (request, chunk)
+#define SPEC_WAIT_POLLS (1u << 22)
 
 struct VerifyParams {
   int32_t batch, vocab;
@@ -74,8 +80,10 @@ struct VerifyParams {
   int32_t max_nodes;
   int32_t* path;
   int32_t* accept_len;
-  int32_t units;   // ceil(vocab / SPEC_UNIT)
-  int32_t vec_ok;  // every row starts on a 16-byte boundary
+  int32_t nch;      // chunks per row: ceil(vocab / entries per chunk)
+  int32_t rowf;     // float2 entries of a staged partial row: nch + 1 (the spare), rounded up to even
+  int32_t pstride;  // float2 entries between partial rows in the workspace (>= rowf)
+  int32_t vec_ok;   // every row starts on a 16-byte boundary
   WsView ws;
 };
 
@@ -88,6 +96,19 @@ struct __align__(16) Record {
   int32_t pad[7];
 };
 
+__device__ __forceinline__ float2* partial_row(const VerifyParams& p, int slot) {
+  return p.ws.partial + (int64_t)slot * p.pstride;
+}
+// the draft row (request r, 1-based position i) that carries q_i: its workspace slot
+__device__ __forceinline__ int q_slot_of(const VerifyParams& p, int r, int i) {
+  return p.max_rows + r * p.K + (i - 1);
+}
+// index of the n-th (0-based) set bit of m
+__device__ __forceinline__ int nth_bit(uint32_t m, int n) {
+  for (int t = 0; t < n; ++t) m &= m - 1u;
+  return __ffs(m) - 1;
+}
+
 // ------------------------------------------------------------------ loading
 // strided layout: lane-interleaved 16-byte vectors (coalesced); element j of
 // a lane sits at unit offset idx_strided<DT>(lane, j)
@@ -98,113 +119,22 @@ __device__ __forceinline__ int idx_strided(int lane, int j, bool vec) {
   return 4 * (lane + 32 * (j >> 2)) + (j & 3);
 }
 
-// 64 values of one unit, fp32, missing entries = -inf
+// 64 values of one 2048-entry unit in scalar loads (element j of a lane at
+// offset lane + 32 j), missing entries = -inf; for rows that are not 16-byte
+// aligned
 template <int DT>
-__device__ __forceinline__ void load_unit(const void* row, int e0, int n_el, bool vec, int lane,
-                                          float v[64]) {
-  if (vec) {
-    if (DT == 1) {
-      const uint16_t* rp = static_cast<const uint16_t*>(row) + e0;
-      uint4 w[8];
+__device__ __forceinline__ void load_unit(const void* row, int e0, int n_el, bool vec, int lane, float v[64]) {
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const int vv = lane + 32 * k;
-        if (8 * vv < n_el)
-          w[k] = ldg_stream(rp + 8 * vv);
-        else
-          w[k] = make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);
-      }
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        v[8 * k + 0] = bf16_lo(w[k].x);
-        v[8 * k + 1] = bf16_hi(w[k].x);
-        v[8 * k + 2] = bf16_lo(w[k].y);
-        v[8 * k + 3] = bf16_hi(w[k].y);
-        v[8 * k + 4] = bf16_lo(w[k].z);
-        v[8 * k + 5] = bf16_hi(w[k].z);
-        v[8 * k + 6] = bf16_lo(w[k].w);
-        v[8 * k + 7] = bf16_hi(w[k].w);
-      }
-    } else {
-      const float* rp = static_cast<const float*>(row) + e0;
-      uint4 w[16];
-#pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        const int vv = lane + 32 * k;
-        if (4 * vv < n_el)
-          w[k] = ldg_stream(rp + 4 * vv);
-        else
-          w[k] = make_uint4(0xFF800000u, 0xFF800000u, 0xFF800000u, 0xFF800000u);
-      }
-#pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        v[4 * k + 0] = __uint_as_float(w[k].x);
-        v[4 * k + 1] = __uint_as_float(w[k].y);
-        v[4 * k + 2] = __uint_as_float(w[k].z);
-        v[4 * k + 3] = __uint_as_float(w[k].w);
-      }
+  for (int j = 0; j < 64; ++j) {
+    const int i = lane + 32 * j;
+    float x = -INFINITY;
+    if (i < n_el) {
+      if (DT == 1)
+        x = __uint_as_float((uint32_t)__ldg(static_cast<const uint16_t*>(row) + e0 + i) << 16);
+      else
+        x = __ldg(static_cast<const float*>(row) + e0 + i);
     }
-  } else {
-#pragma unroll
-    for (int j = 0; j < 64; ++j) {
-      const int i = lane + 32 * j;
-      float x = -INFINITY;
-      if (i < n_el) {
-        if (DT == 1)
-          x = __uint_as_float((uint32_t)__ldg(static_cast<const uint16_t*>(row) + e0 + i) << 16);
-        else
-          x = __ldg(static_cast<const float*>(row) + e0 + i);
-      }
-      v[j] = x;
-    }
-  }
-}
-
-// contiguous layout for the sampling rescan: lane l holds unit offsets
-// [64 l, 64 l + 64) in order; missing entries = -inf
-template <int DT>
-__device__ __forceinline__ void load_unit_contig(const void* row, int e0, int n_el, bool vec,
-                                                 int lane, float v[64]) {
-  const int b = 64 * lane;
-  if (vec && b + 64 <= n_el) {
-    if (DT == 1) {
-      const uint4* rp = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(row) + e0 + b);
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const uint4 w = __ldcg(rp + k);
-        v[8 * k + 0] = bf16_lo(w.x);
-        v[8 * k + 1] = bf16_hi(w.x);
-        v[8 * k + 2] = bf16_lo(w.y);
-        v[8 * k + 3] = bf16_hi(w.y);
-        v[8 * k + 4] = bf16_lo(w.z);
-        v[8 * k + 5] = bf16_hi(w.z);
-        v[8 * k + 6] = bf16_lo(w.w);
-        v[8 * k + 7] = bf16_hi(w.w);
-      }
-    } else {
-      const uint4* rp = reinterpret_cast<const uint4*>(static_cast<const float*>(row) + e0 + b);
-#pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        const uint4 w = __ldcg(rp + k);
-        v[4 * k + 0] = __uint_as_float(w.x);
-        v[4 * k + 1] = __uint_as_float(w.y);
-        v[4 * k + 2] = __uint_as_float(w.z);
-        v[4 * k + 3] = __uint_as_float(w.w);
-      }
-    }
-  } else {
-#pragma unroll
-    for (int j = 0; j < 64; ++j) {
-      const int i = b + j;
-      float x = -INFINITY;
-      if (i < n_el) {
-        if (DT == 1)
-          x = __uint_as_float((uint32_t)__ldcg(static_cast<const unsigned short*>(row) + e0 + i) << 16);
-        else
-          x = __ldcg(static_cast<const float*>(row) + e0 + i);
-      }
-      v[j] = x;
-    }
+    v[j] = x;
   }
 }
 
@@ -224,8 +154,7 @@ struct Vec {
   static constexpr int NV = 16;                // vectors per lane per chunk
   static constexpr int PER = DT == 1 ? 8 : 4;  // entries per vector
   static constexpr int CH = 32 * NV * PER;     // entries per chunk: 4096 bf16 / 2048 fp32
-  static constexpr int BYTES = 8192;           // bytes per chunk (one pipeline stage)
-  static constexpr int STAGES = 1;  // copies in flight per warp
+  static constexpr int BYTES = VR_STAGE;       // bytes per chunk (one stage)
   static constexpr int SUB = CH / SPEC_UNIT;   // 2048-entry units per chunk
   static constexpr uint32_t NEG = DT == 1 ? 0xFF80FF80u : 0xFF800000u;
 };
@@ -532,354 +461,247 @@ __device__ __forceinline__ void merge_ms(float& m, float& s, float m2, float s2,
   m = nm;
 }
 
-// (max, sum) of R rows from their unit partials, by the whole warp at once.
-// Row k (its partials at slot_of(k); none when negative) is merged by G lanes,
-// G the largest power of two with R G <= 32: each lane takes every G-th unit
-// in batches of MB independent loads (one memory round trip per batch, with an
-// online rescale), then the G lanes combine by shuffles.  More than 32 rows
-// take several rounds.  Lane l receives row want_a(l)'s result in *a and row
-// want_b(l)'s in *b (negative: none, (-inf, 0)).
-template <typename SlotFn>
-__device__ __forceinline__ void merge_rows_warp(const VerifyParams& p, int R, SlotFn slot_of, int lane, int want_a,
-                                                float2* a, int want_b, float2* b) {
-  constexpr int MB = 20;
-  int G = 1;
-  while (G < 32 && R * 2 * G <= 32) G <<= 1;
-  const int rpr = 32 / G, sub = lane & (G - 1);
-  *a = make_float2(-INFINITY, 0.0f);
-  *b = make_float2(-INFINITY, 0.0f);
-  for (int k0 = 0; k0 < R; k0 += rpr) {
-    const int k = k0 + lane / G;
-    const int slot = k < R ? slot_of(k) : -1;
-    float m = -INFINITY, s = 0.0f;
-    if (slot >= 0) {
-      const float2* pr = &p.ws.partial[(int64_t)slot * p.ws.units];
-      for (int u0 = sub; u0 < p.units; u0 += MB * G) {
-        float2 t[MB];
-#pragma unroll
-        for (int q = 0; q < MB; ++q) {
-          const int u = u0 + q * G;
-          t[q] = u < p.units ? __ldcg(&pr[u]) : make_float2(-INFINITY, 0.0f);
-        }
-        float bm = -INFINITY;
-#pragma unroll
-        for (int q = 0; q < MB; ++q) bm = fmaxf(bm, t[q].x);
-        if (bm == -INFINITY) continue;
-        const float nm = fmaxf(m, bm);
-        float acc = (m == -INFINITY) ? 0.0f : s * ex2((m - nm) * p.c);
-#pragma unroll
-        for (int q = 0; q < MB; ++q)
-          if (t[q].x != -INFINITY) acc += t[q].y * ex2((t[q].x - nm) * p.c);
-        m = nm;
-        s = acc;
-      }
-    }
-    for (int o = G >> 1; o >= 1; o >>= 1) {
-      const float m2 = __shfl_xor_sync(0xFFFFFFFFu, m, o), s2 = __shfl_xor_sync(0xFFFFFFFFu, s, o);
-      merge_ms(m, s, m2, s2, p.c);
-    }
-    // rows k0 .. k0 + rpr - 1 sit at lanes (k - k0) G
-    const bool in_a = want_a >= k0 && want_a < k0 + rpr, in_b = want_b >= k0 && want_b < k0 + rpr;
-    const float ma = __shfl_sync(0xFFFFFFFFu, m, in_a ? (want_a - k0) * G : 0);
-    const float sa = __shfl_sync(0xFFFFFFFFu, s, in_a ? (want_a - k0) * G : 0);
-    const float mb = __shfl_sync(0xFFFFFFFFu, m, in_b ? (want_b - k0) * G : 0);
-    const float sb = __shfl_sync(0xFFFFFFFFu, s, in_b ? (want_b - k0) * G : 0);
-    if (in_a) *a = make_float2(ma, sa);
-    if (in_b) *b = make_float2(mb, sb);
-  }
-}
 
-// Inverse CDF over unit weights w_u (unit order), at the fraction u of their
-// total: returns the unit holding the crossing of t = u * total, the weight
-// before it, the total and t.  Each lane owns `per` consecutive units, so lane
-// order is unit order; a lane keeps its first four weights in registers for
-// the walk that locates the crossing.  The sums run in fp32 (the weights are
-// fp32 products, and fp64 work runs on a narrow pipe on this part).
+// ------------------------------------------------------------------ draws
+// Inverse CDF over chunk weights (chunk order) at the fraction u of their
+// total: the chunk holding the crossing of t = u * total, the weight before
+// it, the total and t.  Lane l holds the weights of chunks [per l, per l +
+// per) in wl (per <= 8), so lane order is chunk order; the sums run in fp32.
 struct Crossing {
-  int unit;
-  float before;  // weight of the units before `unit`; -1: t at or above the total
+  int unit;      // the crossing chunk
+  float before;  // weight of the chunks before it; -1: t at or above the total (take the last entry)
   float total;
   float t;
 };
 
-template <typename WFn>
-__device__ __forceinline__ Crossing find_unit(int units, float u, int lane, WFn wfn) {
-  const int per = (units + 31) / 32;
-  const int u0 = lane * per;
-  float w4[4];
-#pragma unroll
-  for (int q = 0; q < 4; ++q) w4[q] = (q < per && u0 + q < units) ? wfn(u0 + q) : 0.0f;
+__device__ __forceinline__ Crossing find_chunk(const float (&wl)[8], int per, float u, int lane) {
   float lsum = 0.0f;
-  int last_pos = -1;
+  int last_q = -1;
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    lsum += w4[q];
-    if (w4[q] > 0.0f) last_pos = u0 + q;
-  }
-  for (int q = 4; q < per; ++q) {
-    const int uu = u0 + q;
-    if (uu < units) {
-      const float w = wfn(uu);
-      lsum += w;
-      if (w > 0.0f) last_pos = uu;
+  for (int q = 0; q < 8; ++q)
+    if (q < per) {
+      lsum += wl[q];
+      if (wl[q] > 0.0f) last_q = q;
     }
-  }
   const float incl = warp_incl_scan(lsum);
   const float excl = incl - lsum;
   Crossing c;
   c.total = __shfl_sync(0xFFFFFFFFu, incl, 31);
   c.t = u * c.total;
-  const float t = c.t;
-  const unsigned hit = __ballot_sync(0xFFFFFFFFu, incl > t && lsum > 0.0f);
+  const unsigned hit = __ballot_sync(0xFFFFFFFFu, incl > c.t && lsum > 0.0f);
   if (hit) {
     const int src = __ffs(hit) - 1;
     int unit = -1;
-    float before = 0.0f;
-    if (lane == src) {
-      float run = excl;
+    float before = 0.0f, run = excl, wlast = 0.0f;
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float w = w4[q];
-        if (unit < 0 && q < per && u0 + q < units) {
-          if (run + w > t && w > 0.0f) {
-            unit = u0 + q;
-            before = run;
-          }
-          run += w;
-        }
-      }
-      for (int q = 4; q < per && unit < 0; ++q) {
-        const int uu = u0 + q;
-        if (uu >= units) break;
-        const float w = wfn(uu);
-        if (run + w > t && w > 0.0f) {
-          unit = uu;
+    for (int q = 0; q < 8; ++q)
+      if (q < per) {
+        if (unit < 0 && wl[q] > 0.0f && run + wl[q] > c.t) {
+          unit = per * lane + q;
           before = run;
         }
-        run += w;
+        run += wl[q];
+        if (q == last_q) wlast = wl[q];
       }
-      if (unit < 0) {  // rounding inside the lane: its last unit with mass
-        unit = last_pos;
-        float wl = 0.0f;
-        if (last_pos >= 0) {
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
-            if (u0 + q == last_pos) wl = w4[q];
-          if (last_pos >= u0 + 4) wl = wfn(last_pos);
-        }
-        before = incl - wl;
-      }
+    if (unit < 0) {  // rounding inside the lane: its last chunk with weight
+      unit = per * lane + last_q;
+      before = incl - wlast;
     }
     c.unit = __shfl_sync(0xFFFFFFFFu, unit, src);
     c.before = __shfl_sync(0xFFFFFFFFu, before, src);
-  } else {
-    // t at or above the total (rounding): the last unit with mass
-    const unsigned has = __ballot_sync(0xFFFFFFFFu, last_pos >= 0);
+  } else {  // t at or above the total (rounding): the last chunk with weight
+    const unsigned has = __ballot_sync(0xFFFFFFFFu, last_q >= 0);
     const int src = has ? 31 - __clz(has) : 0;
-    const int lp = __shfl_sync(0xFFFFFFFFu, last_pos, src);
-    c.unit = lp < 0 ? 0 : lp;
-    c.before = -1.0f;  // marker: take the last positive entry of the unit
+    const int lp = __shfl_sync(0xFFFFFFFFu, per * lane + last_q, src);
+    c.unit = has ? lp : 0;
+    c.before = -1.0f;
   }
   return c;
 }
 
-// inside one unit: the smallest index whose running sum (from `before`)
-// exceeds t, over residual values r[64] in contiguous lane layout.  Returns
-// (index within the unit, r at that index); falls back to the last positive.
-// The sums inside the unit run from the unit's start, against t - before.
-__device__ __forceinline__ int find_in_unit(const float r[64], float before, float t, int lane, float* r_at) {
-  float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
-#pragma unroll
-  for (int j = 0; j < 64; j += 4) {
-    a0 += r[j];
-    a1 += r[j + 1];
-    a2 += r[j + 2];
-    a3 += r[j + 3];
+// the weight 2^(z c - mc) of a logit z (0 for -inf: 2^-inf = +0) and 0 for
+// entry `skip`; computed unconditionally and then selected, so that a run of
+// weights compiles to straight-line code whose exponentials overlap
+struct SoftW {
+  float c, mc;
+  int skip;
+  __device__ __forceinline__ float operator()(int e, float x) const {
+    const float w = ex2(fmaf(x, c, -mc));
+    return e == skip ? 0.0f : w;
   }
-  const float lsum = (a0 + a1) + (a2 + a3);
-  const float incl = warp_incl_scan(lsum);
-  const float excl = incl - lsum;
-  const float tr = t - before;
-  int pick = -1;
-  float rv = 0.0f;
-  const bool last_mode = before < 0.0f;
-  const unsigned hit = last_mode ? 0u : __ballot_sync(0xFFFFFFFFu, incl > tr && lsum > 0.0f);
-  if (hit) {
-    const int src = __ffs(hit) - 1;
-    if (lane == src) {
-      // unrolled without an early exit, so r[] stays in registers
-      float run = excl, lastv = 0.0f;
-      int lastp = -1;
-#pragma unroll
-      for (int j = 0; j < 64; ++j) {
-        const float x = r[j];
-        if (x > 0.0f) {
-          lastp = j;
-          lastv = x;
-        }
-        run += x;
-        if (pick < 0 && run > tr && x > 0.0f) {
-          pick = 64 * lane + j;
-          rv = x;
-        }
-      }
-      if (pick < 0 && lastp >= 0) {
-        pick = 64 * lane + lastp;
-        rv = lastv;
-      }
-    }
-    pick = __shfl_sync(0xFFFFFFFFu, pick, src);
-    rv = __shfl_sync(0xFFFFFFFFu, rv, src);
-  } else {
-    int lastp = -1;
-    for (int j = 0; j < 64; ++j)
-      if (r[j] > 0.0f) lastp = j;
-    const unsigned has = __ballot_sync(0xFFFFFFFFu, lastp >= 0);
-    if (has) {
-      const int src = 31 - __clz(has);
-      pick = __shfl_sync(0xFFFFFFFFu, 64 * lane + lastp, src);
-      float mine = 0.0f;
-#pragma unroll
-      for (int j = 0; j < 64; ++j)
-        if (j == lastp) mine = r[j];
-      rv = __shfl_sync(0xFFFFFFFFu, mine, src);
-    } else {
-      pick = 0;
-      rv = 0.0f;
-    }
-  }
-  *r_at = rv;
-  return pick;
-}
-
-
-// ---- one unit's weights for a draw, in compact code.  A draw runs once per
-// request, from cold instruction caches, so these loops stay rolled: lane l
-// owns the unit's entries [64 l, 64 l + 64), read through L1 in 16-byte
-// vectors (one memory round trip for the first pass; the rest hit L1).  The
-// weight of entry z is 2^(z c - mc), 0 for -inf and for the excluded index.
-template <int DT>
-__device__ __forceinline__ void unpack_vec(const uint4& w, float (&x)[DT == 1 ? 8 : 4]) {
-  if (DT == 1) {
-    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      x[2 * q] = bf16_lo(ws[q]);
-      x[2 * q + 1] = bf16_hi(ws[q]);
-    }
-  } else {
-    x[0] = __uint_as_float(w.x);
-    x[1] = __uint_as_float(w.y);
-    x[2] = __uint_as_float(w.z);
-    x[3] = __uint_as_float(w.w);
-  }
-}
+};
 
 template <int DT>
-__device__ __forceinline__ float entry_l1(const void* row, int64_t i) {
-  if (DT == 1) return __uint_as_float((uint32_t)__ldca(static_cast<const unsigned short*>(row) + i) << 16);
-  return __ldca(static_cast<const float*>(row) + i);
+__device__ __forceinline__ float word_entry(uint32_t word, int h) {
+  if (DT == 1) return h ? bf16_hi(word) : bf16_lo(word);
+  return __uint_as_float(word);
 }
 
-// the lane's entries in order, from running sum `run`, with weight wf(k, x)
-// of unit entry k with logit x: mode 0 returns their total; mode 1 stops at
-// the first entry whose running sum exceeds t (its unit index in *pick,
-// weight in *w_at), else gives the last entry with positive weight (-1 if none)
-template <int DT, int MODE, typename WF>
-__device__ __forceinline__ float unit_lane_pass(const void* row, int e0, int n_el, bool vec, int lane, float run,
-                                                float t, int* pick, float* w_at, WF wf) {
-  constexpr int PER = DT == 1 ? 8 : 4;
-  constexpr size_t ESZ = DT == 1 ? 2 : 4;
-  const int b = 64 * lane;
-  const int cnt = min(64, n_el - b);
-  float sum = 0.0f, lastw = 0.0f;
-  int last = -1;
-  if (MODE == 1) *pick = -1;
-  if (cnt <= 0) return 0.0f;
-  auto take = [&](int k, float w) -> bool {  // true: crossing found
-    if (MODE == 0) {
-      sum += w;
-    } else if (w > 0.0f) {
-      run += w;
-      last = k;
-      lastw = w;
-      if (run > t) {
-        *pick = k;
-        *w_at = w;
-        return true;
-      }
-    }
-    return false;
-  };
-  if (vec && cnt == 64) {
-    const uint4* rp = reinterpret_cast<const uint4*>(static_cast<const char*>(row) + (size_t)(e0 + b) * ESZ);
-    if (DT != 1)  // the lane's 256 bytes span two 128-byte lines: ask for both at once
-      asm volatile("prefetch.global.L1 [%0];" ::"l"(rp + 8));
-#pragma unroll 2
-    for (int i = 0; i < 64 / PER; ++i) {
-      float x[PER];
-      unpack_vec<DT>(__ldca(rp + i), x);
-#pragma unroll
-      for (int e = 0; e < PER; ++e) {
-        const int k = b + i * PER + e;
-        if (take(k, wf(k, x[e]))) return 0.0f;
-      }
-    }
-  } else {
-    for (int j = 0; j < cnt; ++j) {
-      const int k = b + j;
-      const float x = entry_l1<DT>(row, (int64_t)e0 + k);
-      if (take(k, wf(k, x))) return 0.0f;
-    }
-  }
-  if (MODE == 1) {
-    *pick = last;
-    *w_at = lastw;
-  }
-  return sum;
-}
-
-// inverse CDF inside one unit: the first entry (in index order) whose running
-// sum from `before` exceeds t; the last entry with positive weight when
-// rounding leaves none (before < 0: always the last).  Returns the unit index
-// and *w_at its weight.
+// A chunk staged in shared memory, lane l owning entries [E l, E l + E)
+// (E = entries per chunk / 32).  chunk_lane_sum: the lane's total weight.  The
+// lane's 32-bit words are read in an order rotated by the lane (the warp's
+// reads fall in distinct banks), eight words at a time, and their weights are
+// independent terms summed by a tree: one warp alone on its scheduler runs
+// this, so its dependency chains are what the time is.
 template <int DT, typename WF>
-__device__ __forceinline__ int unit_draw(const void* row, int e0, int n_el, bool vec, int lane, float before, float t,
-                                         float* w_at, WF wf) {
-  int pk;
-  float wa;
-  const float lsum = unit_lane_pass<DT, 0>(row, e0, n_el, vec, lane, 0.0f, 0.0f, &pk, &wa, wf);
+__device__ __forceinline__ float chunk_lane_sum(const uint32_t* wbuf, int n_el, int lane, WF wf) {
+  constexpr int EW = DT == 1 ? 2 : 1;  // entries per word
+  constexpr int E = Vec<DT>::CH / 32;  // entries per lane
+  constexpr int WPL = E / EW;          // words per lane (64)
+  constexpr int BW = 8;                // words per batch
+  float s = 0.0f;
+  for (int j0 = 0; j0 < WPL; j0 += BW) {
+    uint32_t word[BW];
+#pragma unroll
+    for (int b = 0; b < BW; ++b) word[b] = wbuf[lane * WPL + ((j0 + b + lane) & (WPL - 1))];
+    float t[BW * EW];
+#pragma unroll
+    for (int b = 0; b < BW; ++b)
+#pragma unroll
+      for (int h = 0; h < EW; ++h) {
+        const int e = E * lane + EW * ((j0 + b + lane) & (WPL - 1)) + h;
+        const float w = wf(e, word_entry<DT>(word[b], h));  // past n_el: stale words, selected away
+        t[b * EW + h] = e < n_el ? w : 0.0f;
+      }
+#pragma unroll
+    for (int h = BW * EW / 2; h > 0; h >>= 1)
+#pragma unroll
+      for (int k = 0; k < h; ++k) t[k] += t[k + h];
+    s += t[0];
+  }
+  return s;
+}
+
+// Inverse CDF inside a staged chunk: the first entry whose running sum from
+// `before` exceeds t (before < 0: the last entry with weight), from the lane
+// sums (pass 1) and then the crossing lane's entries spread over the warp
+// (pass 2).  Returns the entry and *w_at its weight.
+template <int DT, typename WF>
+__device__ int chunk_draw(const unsigned char* buf, int n_el, int lane, float before, float t, float* w_at, WF wf) {
+  constexpr int EW = DT == 1 ? 2 : 1;
+  constexpr int E = Vec<DT>::CH / 32;
+  constexpr int F = E / 32;  // the crossing lane's entries per lane in pass 2 (4 / 2)
+  const uint32_t* wbuf = reinterpret_cast<const uint32_t*>(buf);
+  const float lsum = chunk_lane_sum<DT>(wbuf, n_el, lane, wf);
   const float incl = warp_incl_scan(lsum);
   const float tr = t - before;
   const unsigned hit = before < 0.0f ? 0u : __ballot_sync(0xFFFFFFFFu, incl > tr && lsum > 0.0f);
   const unsigned has = __ballot_sync(0xFFFFFFFFu, lsum > 0.0f);
   int src;
-  float run, tt;
+  float tl;
   if (hit) {
     src = __ffs(hit) - 1;
-    run = incl - lsum;
-    tt = tr;
+    tl = tr - __shfl_sync(0xFFFFFFFFu, incl - lsum, src);
   } else {
     src = has ? 31 - __clz(has) : 0;
-    run = 0.0f;
-    tt = INFINITY;  // no crossing: the lane's last positive entry
+    tl = INFINITY;  // no crossing: the last entry with weight
   }
-  int pick = -1;
-  float w = 0.0f;
-  if (lane == src) unit_lane_pass<DT, 1>(row, e0, n_el, vec, lane, run, tt, &pick, &w, wf);
-  pick = __shfl_sync(0xFFFFFFFFu, pick, src);
-  *w_at = __shfl_sync(0xFFFFFFFFu, w, src);
+  float wv[F], s2 = 0.0f;
+#pragma unroll
+  for (int f = 0; f < F; ++f) {
+    const int e = E * src + F * lane + f;
+    const float w = wf(e, word_entry<DT>(wbuf[e / EW], e % EW));  // e < 4096: inside the stage
+    wv[f] = e < n_el ? w : 0.0f;
+    s2 += w;
+  }
+  const float inc2 = warp_incl_scan(s2);
+  const unsigned hit2 = __ballot_sync(0xFFFFFFFFu, inc2 > tl && s2 > 0.0f);
+  int pick = -1, lp = -1;
+  float wp = 0.0f, lw = 0.0f, run = inc2 - s2;
+#pragma unroll
+  for (int f = 0; f < F; ++f)
+    if (wv[f] > 0.0f) {
+      run += wv[f];
+      if (pick < 0 && run > tl) {
+        pick = E * src + F * lane + f;
+        wp = wv[f];
+      }
+      lp = E * src + F * lane + f;
+      lw = wv[f];
+    }
+  int lane2;
+  if (hit2) {
+    lane2 = __ffs(hit2) - 1;
+    if (pick < 0) {  // rounding inside the lane: its last entry with weight
+      pick = lp;
+      wp = lw;
+    }
+  } else {
+    const unsigned h2 = __ballot_sync(0xFFFFFFFFu, lp >= 0);
+    lane2 = h2 ? 31 - __clz(h2) : 0;
+    pick = lp;
+    wp = lw;
+  }
+  pick = __shfl_sync(0xFFFFFFFFu, pick, lane2);
+  *w_at = __shfl_sync(0xFFFFFFFFu, wp, lane2);
   return pick < 0 ? 0 : pick;
 }
 
-// the weight 2^(z c - mc) of a logit z (0 for -inf and for entry `skip`)
-struct SoftW {
-  float c, mc;
-  int skip;
-  __device__ __forceinline__ float operator()(int k, float x) const {
-    return (k == skip || x == -INFINITY) ? 0.0f : ex2(fmaf(x, c, -mc));
-  }
+// ------------------------------------------------------------------ finalizer scratch
+// 8 KB of a warp's shared memory beside its stage, filled by bulk copies that
+// complete on the warp's second mbarrier.
+struct Scratch {
+  unsigned char* buf;
+  uint64_t* bar;
+  uint32_t phase;
+  int dead;  // a copy did not land in time: the scratch is not used again
 };
+
+// wait for the scratch's copies; false (SPEC_DEV_TIMEOUT set) when the bound ran out
+__device__ __forceinline__ bool scratch_wait(Scratch& sc, uint32_t* status, int lane) {
+  const bool ok = mbar_wait_bounded(sc.bar, sc.phase, SPEC_WAIT_POLLS);
+  sc.phase ^= 1u;
+  if (__all_sync(0xFFFFFFFFu, ok)) return true;
+  if (lane == 0) set_status(status, SPEC_DEV_TIMEOUT);
+  sc.dead = 1;
+  return false;
+}
+
+// n <= 32 partial rows into the scratch (row j from slot slot_of(j), rowf
+// float2 each), one bulk copy per lane; stage_rows_issue returns at once
+// (scratch_wait completes it), stage_rows waits
+template <typename SlotFn>
+__device__ __forceinline__ void stage_rows_issue(const VerifyParams& p, Scratch& sc, int n, SlotFn slot_of,
+                                                 int lane) {
+  const uint32_t rb = (uint32_t)p.rowf * 8u;
+  fence_proxy_async();
+  if (lane == 0) mbar_arrive_expect_tx(sc.bar, rb * (uint32_t)n);
+  __syncwarp();
+  if (lane < n) bulk_g2s(sc.buf + (size_t)lane * rb, partial_row(p, slot_of(lane)), rb, sc.bar);
+}
+template <typename SlotFn>
+__device__ __forceinline__ bool stage_rows(const VerifyParams& p, Scratch& sc, int n, SlotFn slot_of, int lane) {
+  stage_rows_issue(p, sc, n, slot_of, lane);
+  return scratch_wait(sc, p.ws.status, lane);
+}
+
+// the n_el entries of a row from entry e0 into the scratch (one chunk)
+template <int DT>
+__device__ __forceinline__ bool stage_chunk(const VerifyParams& p, Scratch& sc, const void* row, int e0, int n_el,
+                                            int lane) {
+  constexpr int ESZ = DT == 1 ? 2 : 4;
+  if (p.vec_ok) {
+    if (lane == 0) {
+      mbar_arrive_expect_tx(sc.bar, (uint32_t)(n_el * ESZ));
+      bulk_g2s(sc.buf, static_cast<const char*>(row) + (size_t)e0 * ESZ, (uint32_t)(n_el * ESZ), sc.bar);
+    }
+    return scratch_wait(sc, p.ws.status, lane);
+  }
+  // rows off a 16-byte boundary: plain loads
+  if (DT == 1) {
+    const uint16_t* src = static_cast<const uint16_t*>(row) + e0;
+    uint16_t* dst = reinterpret_cast<uint16_t*>(sc.buf);
+#pragma unroll 8
+    for (int i = lane; i < n_el; i += 32) dst[i] = __ldcg(src + i);
+  } else {
+    const float* src = static_cast<const float*>(row) + e0;
+    float* dst = reinterpret_cast<float*>(sc.buf);
+#pragma unroll 8
+    for (int i = lane; i < n_el; i += 32) dst[i] = __ldcg(src + i);
+  }
+  __syncwarp();
+  return true;
+}
 
 // ------------------------------------------------------------------ finalize
 __device__ __forceinline__ void write_invalid_chain(const VerifyParams& p, int r, int lane) {
@@ -893,10 +715,6 @@ __device__ __forceinline__ void write_invalid_chain(const VerifyParams& p, int r
     p.n_emitted[r] = 0;
     if (p.dbg_resid) p.dbg_resid[r] = -1.0f;
   }
-}
-
-__device__ __forceinline__ int q_slot_of(const VerifyParams& p, int r, int i /*1-based*/) {
-  return p.max_rows + r * p.K + (i - 1);
 }
 
 template <int DT>
@@ -933,94 +751,124 @@ __device__ void finalize_chain_greedy(const VerifyParams& p, int r, int base, in
   }
 }
 
+// Sampled chain verification of request r: rows 0..ell at slots base + k (p),
+// then one draft row per set bit i of qmask (q of position i + 1).
 template <int DT>
-__device__ void finalize_chain_sample(const VerifyParams& p, int r, int base, int ell, int lane) {
-  const int32_t* y = p.chain + (int64_t)r * p.L;
-  const uint8_t* pmr = p.pm ? p.pm + (int64_t)r * p.L : nullptr;
-  // lane i-1 tests position i: its token's logits are loaded first, so that
-  // those loads overlap the merges below
+__device__ void finalize_chain_sample(const VerifyParams& p, int r, int base, int ell, uint32_t qmask, int lane,
+                                      Scratch& sc) {
+  if (sc.dead) return;
+  constexpr int CH = Vec<DT>::CH;
+  constexpr size_t ESZ = DT == 1 ? 2 : 4;
   const bool tested = lane < ell;
-  int use_q_lane = 0, yi = -1;
+  const int R = ell + 1 + __popc(qmask);
+  const int rows_fit = min(32, VR_STAGE / (p.rowf * 8));  // rows per staging round (one copy per lane)
+  const bool has_q = tested && ((qmask >> lane) & 1u);
+  const int kq = has_q ? ell + 1 + __popc(qmask & ((1u << lane) - 1u)) : -1;  // lane's q row
+  auto slot_of = [&](int k) -> int {
+    return k <= ell ? base + k : q_slot_of(p, r, nth_bit(qmask, k - ell - 1) + 1);
+  };
+  // the first rows' copies go out first; the draft tokens' loads and the
+  // uniforms (lane i tests position i + 1, lane ell holds the bonus's) overlap them
+  stage_rows_issue(p, sc, min(R, rows_fit), slot_of, lane);
+  const int yi = tested ? __ldcg(p.chain + (int64_t)r * p.L + lane) : -1;
+  float u = -1.0f, u2 = 0.0f;
+  if (lane <= ell) round_uniforms(p.seed, p.step, (uint32_t)r, (uint32_t)(lane + 1), &u, &u2);
+  // (max, sum) of every row from its chunk partials: the rows staged a batch at
+  // a time (one batch at the shapes of the configurations), G lanes per row
+  float2 msp = make_float2(-INFINITY, 0.0f), msq = msp;
   float zp = 0.0f, zq = 0.0f;
-  if (tested) {
-    yi = y[lane];
-    use_q_lane = (p.use_q && pmr && pmr[lane] == 0 && lane + 1 <= p.K) ? 1 : 0;
-    if (yi >= 0 && yi < p.vocab) {
-      zp = load_one<DT>(p.logits, (int64_t)(base + lane) * p.vocab + yi);
-      if (use_q_lane) zq = load_one<DT>(p.draft, ((int64_t)r * p.K + lane) * p.vocab + yi);
+  int k_lo = 0, k_hi = 0;  // the rows of the last batch
+  for (int k0 = 0; k0 < R; k0 += rows_fit) {
+    const int k1 = min(R, k0 + rows_fit), nr = k1 - k0;
+    if (k0 > 0) stage_rows_issue(p, sc, nr, [&](int j) { return slot_of(k0 + j); }, lane);
+    if (!scratch_wait(sc, p.ws.status, lane)) return;
+    k_lo = k0;
+    k_hi = k1;
+    int G = 1;
+    while (G < 32 && nr * 2 * G <= 32) G <<= 1;
+    const int rr = lane / G;
+    // the lane's chunks: their max first, then the rescaled sums as
+    // independent terms (four accumulators), so no chain runs through the chunks
+    float m = -INFINITY, s = 0.0f;
+    if (rr < nr) {
+      const float2* P = reinterpret_cast<const float2*>(sc.buf + (size_t)rr * p.rowf * 8);
+      const int c0 = lane & (G - 1);
+#pragma unroll 4
+      for (int cc = c0; cc < p.nch; cc += G) m = fmaxf(m, P[cc].x);
+      if (m != -INFINITY) {
+        auto term = [&](int cc) -> float {  // an empty chunk (-inf, 0) weighs 0
+          const float2 t = P[cc < p.nch ? cc : 0];
+          const float w = t.y * ex2((t.x - m) * p.c);
+          return cc < p.nch ? w : 0.0f;
+        };
+        float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
+        for (int cc = c0; cc < p.nch; cc += 4 * G) {
+          a0 += term(cc);
+          a1 += term(cc + G);
+          a2 += term(cc + 2 * G);
+          a3 += term(cc + 3 * G);
+        }
+        s = (a0 + a1) + (a2 + a3);
+      }
+    }
+    for (int o = G >> 1; o >= 1; o >>= 1) {
+      const float m2 = __shfl_xor_sync(0xFFFFFFFFu, m, o), s2 = __shfl_xor_sync(0xFFFFFFFFu, s, o);
+      merge_ms(m, s, m2, s2, p.c);
+    }
+    // lane i takes its p row (k = i) and its q row (k = kq), each merged at lane (k - k0) G;
+    // a row's spare entry holds the logit at its draft token
+    const bool inp = lane <= ell && lane >= k0 && lane < k1, inq = kq >= k0 && kq < k1;
+    const int sp_ = inp ? (lane - k0) * G : 0, sq_ = inq ? (kq - k0) * G : 0;
+    const float a0 = __shfl_sync(0xFFFFFFFFu, m, sp_), a1 = __shfl_sync(0xFFFFFFFFu, s, sp_);
+    const float b0 = __shfl_sync(0xFFFFFFFFu, m, sq_), b1 = __shfl_sync(0xFFFFFFFFu, s, sq_);
+    if (inp) {
+      msp = make_float2(a0, a1);
+      zp = reinterpret_cast<const float2*>(sc.buf + (size_t)(lane - k0) * p.rowf * 8)[p.nch].x;
+    }
+    if (inq) {
+      msq = make_float2(b0, b1);
+      zq = reinterpret_cast<const float2*>(sc.buf + (size_t)(kq - k0) * p.rowf * 8)[p.nch].x;
     }
   }
-  // (max, sum) of the p rows 0 .. ell (row k = lane k) and of the q rows of
-  // the positions that carry one (row ell + 1 + j = the j-th such position),
-  // merged by the whole warp at once
-  const unsigned qmask = __ballot_sync(0xFFFFFFFFu, use_q_lane);
-  const int R = ell + 1 + __popc(qmask);
-  auto slot_of = [&](int k) -> int {
-    if (k <= ell) return base + k;
-    unsigned mm = qmask;
-    int i = 0;
-    for (int t = 0; t <= k - ell - 1; ++t) {
-      i = __ffs(mm) - 1;
-      mm &= mm - 1u;
-    }
-    return q_slot_of(p, r, i + 1);
-  };
-  float2 prow, qrow;
-  merge_rows_warp(p, R, slot_of, lane, lane <= ell ? lane : -1, &prow,
-                  use_q_lane ? ell + 1 + __popc(qmask & ((1u << lane) - 1u)) : -1, &qrow);
-  const float mrow = prow.x, srow = prow.y, mq = qrow.x, sq = qrow.y;
   // accept tests
-  float ratio = -1.0f, u = -1.0f, u2 = 0.0f;
+  float ratio = -1.0f;
   bool acc = false;
   if (tested) {
-    round_uniforms(p.seed, p.step, (uint32_t)r, (uint32_t)(lane + 1), &u, &u2);
     if (yi < 0 || yi >= p.vocab) {
       set_status(p.ws.status, SPEC_DEV_BAD_TOKEN);
       ratio = 0.0f;
     } else {
-      const float py = ex2((zp - mrow) * p.c) / srow;
-      if (use_q_lane) {
-        const float qy = ex2((zq - mq) * p.c) / sq;
-        ratio = py / qy;
-      } else {
-        ratio = py;
-      }
+      // p(y) / q(y) = 2^((zp - mp) c) sq / (2^((zq - mq) c) sp); the quotient of
+      // a fast divide (a few ulp) is far inside the 1e-5 band of the decision
+      const float ep = ex2((zp - msp.x) * p.c);
+      ratio = has_q ? __fdividef(ep * msq.y, ex2((zq - msq.x) * p.c) * msp.y) : __fdividef(ep, msp.y);
     }
     acc = (ratio >= 1.0f) || (u < ratio);
   }
   const unsigned fail = __ballot_sync(0xFFFFFFFFu, tested && !acc);
-  const int stop = fail ? __ffs(fail) - 1 : ell;  // 0-based row that is sampled
+  const int stop = fail ? __ffs(fail) - 1 : ell;  // 0-based row that is drawn from
+  if (!tested) u = -1.0f;
   const int n_acc = stop;
-  // dbg and accepted tokens
   for (int j = lane; j < p.L; j += 32) {
     const bool tj = j <= stop && j < ell;
     if (p.dbg_ratio) p.dbg_ratio[(int64_t)r * p.L + j] = tj ? ratio : -1.0f;
     if (p.dbg_u) p.dbg_u[(int64_t)r * p.L + j] = tj ? u : -1.0f;
   }
   for (int j = lane; j <= p.L; j += 32)
-    if (j != n_acc) p.out_tokens[(int64_t)r * (p.L + 1) + j] = j < n_acc ? (j == lane ? yi : y[j]) : -1;
+    if (j != n_acc) p.out_tokens[(int64_t)r * (p.L + 1) + j] = j < n_acc ? yi : -1;  // lane j holds y[j]
   if (lane == 0) {
     p.n_accepted[r] = n_acc;
     p.n_emitted[r] = n_acc + 1;
   }
   // the draw
-  float u2_stop;
-  {
-    float ua, ub;
-    round_uniforms(p.seed, p.step, (uint32_t)r, (uint32_t)(stop + 1), &ua, &ub);
-    u2_stop = ub;
-  }
-  const float m = __shfl_sync(0xFFFFFFFFu, mrow, stop);
-  const float s = __shfl_sync(0xFFFFFFFFu, srow, stop);
+  const float u2s = __shfl_sync(0xFFFFFFFFu, u2, stop);
+  const float m = __shfl_sync(0xFFFFFFFFu, msp.x, stop), s = __shfl_sync(0xFFFFFFFFu, msp.y, stop);
   const bool rejected = stop < ell;
-  const int y_stop = rejected ? __shfl_sync(0xFFFFFFFFu, yi, stop) : -1;
-  const int q_stop = rejected ? __shfl_sync(0xFFFFFFFFu, use_q_lane, stop) : 0;
-  if (q_stop) {
-    // needs both normalisers: finished by resample_kernel
-    const float mqs = __shfl_sync(0xFFFFFFFFu, mq, stop);
-    const float sqs = __shfl_sync(0xFFFFFFFFu, sq, stop);
+  const int y_stop = __shfl_sync(0xFFFFFFFFu, yi, stop);
+  if (rejected && ((qmask >> stop) & 1u)) {
+    // max(0, p - q) needs both normalisers and a second pass: resample_kernel
+    const float mqs = __shfl_sync(0xFFFFFFFFu, msq.x, stop), sqs = __shfl_sync(0xFFFFFFFFu, msq.y, stop);
     if (lane == 0) {
-      Record* rec = reinterpret_cast<Record*>(p.ws.record) + r;
       Record t;
       t.flag = 1;
       t.pos = stop + 1;
@@ -1030,52 +878,127 @@ __device__ void finalize_chain_sample(const VerifyParams& p, int r, int base, in
       t.sp = s;
       t.mq = mqs;
       t.sq = sqs;
-      t.u2 = u2_stop;
-      *rec = t;
+      t.u2 = u2s;
+      *(reinterpret_cast<Record*>(p.ws.record) + r) = t;
     }
     return;
   }
+  // from p (all accepted: the bonus) or p without a rejected point mass y
   const int slot = base + stop;
-  const void* row = static_cast<const char*>(p.logits) + (int64_t)slot * p.vocab * (DT == 1 ? 2 : 4);
-  const int yv = (y_stop >= 0 && y_stop < p.vocab) ? y_stop : -1;  // point mass to remove
-  const int u_y = yv >= 0 ? yv / SPEC_UNIT : -1;
-  const bool vec = p.vec_ok != 0;
-  const float zy = __shfl_sync(0xFFFFFFFFu, zp, stop);  // y's logit, loaded for its test
-  auto w_plain = [&](int uu) -> float {
-    const float2 t = __ldcg(&p.ws.partial[(int64_t)slot * p.ws.units + uu]);
-    if (t.x == -INFINITY) return 0.0f;
-    return t.y * ex2((t.x - m) * p.c);
-  };
-  // The unit holding y, with y removed: first its partial less y's own term
-  // (no rescan).  Where the residual mass is under 1/16 of the row's, that
-  // difference can lose the precision the draw needs, and the unit is
-  // rescanned instead.
-  const float w_self = yv >= 0 ? ex2(fmaf(zy, p.c, -m * p.c)) : 0.0f;
-  auto w_fast = [&](int uu) -> float {
-    const float w = w_plain(uu);
-    return uu == u_y ? fmaxf(w - w_self, 0.0f) : w;
-  };
-  Crossing cr = find_unit(p.units, u2_stop, lane, w_fast);
-  const float mc = m * p.c;
-  if (yv >= 0 && !(cr.total >= 0.0625f * s)) {
-    const int ey = u_y * SPEC_UNIT;
-    int pk;
-    float wa;
-    const float w_y = warp_sum(unit_lane_pass<DT, 0>(row, ey, min(SPEC_UNIT, p.vocab - ey), vec, lane, 0.0f, 0.0f,
-                                                     &pk, &wa, SoftW{p.c, mc, yv - ey}));
-    cr = find_unit(p.units, u2_stop, lane, [&](int uu) -> float { return uu == u_y ? w_y : w_plain(uu); });
+  const char* row = static_cast<const char*>(p.logits) + (int64_t)slot * p.vocab * ESZ;
+  const int yv = (rejected && y_stop >= 0 && y_stop < p.vocab) ? y_stop : -1;
+  const int cy = yv >= 0 ? yv / CH : -1;
+  const float zy = __shfl_sync(0xFFFFFFFFu, zp, stop);  // y's logit, read for its test
+  const float2* P;
+  if (stop >= k_lo && stop < k_hi) {
+    P = reinterpret_cast<const float2*>(sc.buf + (size_t)(stop - k_lo) * p.rowf * 8);
+  } else {
+    if (!stage_rows(p, sc, 1, [&](int) { return slot; }, lane)) return;
+    P = reinterpret_cast<const float2*>(sc.buf);
   }
-  // the draw removes y when the residual mass (unnormalised) exceeds 1e-30
-  // of the row's mass, else it falls back to p itself
+  const float mc = m * p.c;
+  const int per = (p.nch + 31) / 32;
+  float wl[8];
+  float w_cy = 0.0f;  // y's chunk without the removal
+  const float w_self = yv >= 0 ? ex2(fmaf(zy, p.c, -mc)) : 0.0f;
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const int cc = per * lane + q;
+    float w = 0.0f;
+    if (q < per && cc < p.nch) {
+      const float2 t = P[cc];
+      w = t.y * ex2((t.x - m) * p.c);  // an empty chunk (-inf, 0) weighs 0
+    }
+    if (cc == cy) {
+      w_cy = w;
+      w = fmaxf(w - w_self, 0.0f);  // y's chunk less y's own term
+    }
+    wl[q] = w;
+  }
+  Crossing cr = find_chunk(wl, per, u2s, lane);
+  int staged = -1;  // the chunk the scratch holds
+  if (yv >= 0 && !(cr.total >= 0.0625f * s)) {
+    // the residual mass is under 1/16 of the row's: y's chunk less y, summed
+    // exactly instead of by the difference
+    const int e0 = cy * CH, n_el = min(CH, p.vocab - e0);
+    if (!stage_chunk<DT>(p, sc, row, e0, n_el, lane)) return;
+    staged = cy;
+    const float w_y = warp_sum(chunk_lane_sum<DT>(reinterpret_cast<const uint32_t*>(sc.buf), n_el, lane,
+                                                  SoftW{p.c, mc, yv - e0}));
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      if (per * lane + q == cy) wl[q] = w_y;
+    cr = find_chunk(wl, per, u2s, lane);
+  }
+  // the draw removes y when the residual mass exceeds 1e-30 of the row's,
+  // else it falls back to p itself
   const bool remove = yv >= 0 && cr.total > 1e-30f * s;
-  if (yv >= 0 && !remove) cr = find_unit(p.units, u2_stop, lane, w_plain);
-  const int e0 = cr.unit * SPEC_UNIT;
-  float r_at;
-  const int pick = unit_draw<DT>(row, e0, min(SPEC_UNIT, p.vocab - e0), vec, lane, cr.before, cr.t, &r_at,
-                                 SoftW{p.c, mc, remove ? yv - e0 : -1});
+  if (yv >= 0 && !remove) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      if (per * lane + q == cy) wl[q] = w_cy;
+    cr = find_chunk(wl, per, u2s, lane);
+  }
+  const int e0 = cr.unit * CH, n_el = min(CH, p.vocab - e0);
+  if (staged != cr.unit && !stage_chunk<DT>(p, sc, row, e0, n_el, lane)) return;
+  float w_at;
+  const int pick = chunk_draw<DT>(sc.buf, n_el, lane, cr.before, cr.t, &w_at, SoftW{p.c, mc, remove ? yv - e0 : -1});
   if (lane == 0) {
     p.out_tokens[(int64_t)r * (p.L + 1) + n_acc] = e0 + pick;
-    if (p.dbg_resid) p.dbg_resid[r] = r_at / cr.total;
+    if (p.dbg_resid) p.dbg_resid[r] = w_at / cr.total;
+  }
+}
+
+// The drafter's probabilistic token of draft row `row` (request r, position
+// k + 1): y ~ softmax(z / T) by inverse CDF at word 0 of Philox counter
+// (r, 0x40000000 + k + 1, lo32(step), hi32(step)), a counter domain apart from
+// verification's; q(y) in dbg_resid.
+template <int DT>
+__device__ void finalize_draft(const VerifyParams& p, int row, int lane, Scratch& sc) {
+  if (sc.dead) return;
+  constexpr int CH = Vec<DT>::CH;
+  constexpr size_t ESZ = DT == 1 ? 2 : 4;
+  const int r = row / p.K, k = row - r * p.K;
+  const int slot = q_slot_of(p, r, k + 1);
+  if (!stage_rows(p, sc, 1, [&](int) { return slot; }, lane)) return;
+  const float2* P = reinterpret_cast<const float2*>(sc.buf);
+  const int per = (p.nch + 31) / 32;
+  float lm = -INFINITY;
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const int cc = per * lane + q;
+    if (q < per && cc < p.nch) lm = fmaxf(lm, P[cc].x);
+  }
+  const float m = warp_max(lm);
+  uint32_t o[4];
+  philox4x32_10((uint32_t)r, 0x40000000u + (uint32_t)(k + 1), (uint32_t)p.step, (uint32_t)(p.step >> 32),
+                (uint32_t)p.seed, (uint32_t)(p.seed >> 32), o);
+  const float u = (float)(o[0] >> 8) * (1.0f / 16777216.0f);
+  int y = 0;
+  float q_at = 0.0f, total = 0.0f;
+  if (m != -INFINITY) {
+    float wl[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int cc = per * lane + q;
+      float w = 0.0f;
+      if (q < per && cc < p.nch) {
+        const float2 t = P[cc];
+        w = t.y * ex2((t.x - m) * p.c);  // an empty chunk (-inf, 0) weighs 0
+      }
+      wl[q] = w;
+    }
+    const Crossing cr = find_chunk(wl, per, u, lane);
+    total = cr.total;
+    const int e0 = cr.unit * CH, n_el = min(CH, p.vocab - e0);
+    const char* base = static_cast<const char*>(p.draft) + (int64_t)row * p.vocab * ESZ;
+    if (!stage_chunk<DT>(p, sc, base, e0, n_el, lane)) return;
+    y = e0 + chunk_draw<DT>(sc.buf, n_el, lane, cr.before, cr.t, &q_at, SoftW{p.c, m * p.c, -1});
+  }
+  if (lane == 0) {
+    p.out_tokens[row] = y;
+    if (p.dbg_u) p.dbg_u[row] = u;
+    if (p.dbg_resid) p.dbg_resid[row] = total > 0.0f ? q_at / total : 0.0f;
   }
 }
 
@@ -1156,199 +1079,239 @@ __device__ void finalize_tree(const VerifyParams& p, int r, int base, int n, int
 // ------------------------------------------------------------------ main kernel
 // A cursor walks work rows in increasing order and locates each row's data.
 struct Cursor {
-  int r, item, slot;
+  int r, item, slot, pos;  // pos: the row's 1-based position (draft rows: their position)
   const char* row;
 };
 
 template <int MODE>
 __device__ __forceinline__ void locate(const VerifyParams& p, const int32_t* s_pre, const int32_t* s_base,
-                                       const int32_t* s_len, int item, size_t esz, Cursor& c) {
+                                       const int32_t* s_len, const uint32_t* s_qm, int item, size_t esz,
+                                       Cursor& c) {
   if (item == c.item) return;
-  while (s_pre[c.r + 1] <= item) ++c.r;
   c.item = item;
+  if constexpr (MODE == MODE_DRAFT) {  // item = draft row (request item / K, position item % K + 1)
+    const int r = item / p.K, k = item - r * p.K;
+    c.r = item;
+    c.pos = k + 1;
+    c.slot = q_slot_of(p, r, k + 1);
+    c.row = static_cast<const char*>(p.draft) + (int64_t)item * p.vocab * esz;
+    return;
+  } else {
+  while (s_pre[c.r + 1] <= item) ++c.r;
   const int li = item - s_pre[c.r];
   const int len = s_len[c.r];
   if (MODE == MODE_TREE || li <= len) {
     c.slot = s_base[c.r] + li;
+    c.pos = li + 1;
     c.row = static_cast<const char*>(p.logits) + (int64_t)c.slot * p.vocab * esz;
-  } else {
-    // the (li - len)-th position (1-based) that carries a draft distribution
-    int want = li - len, pos = 1;
-    const uint8_t* pmr = p.pm + (int64_t)c.r * p.L;
-    for (int i = 1; i <= len && i <= p.K; ++i)
-      if (pmr[i - 1] == 0 && --want == 0) {
-        pos = i;
-        break;
-      }
+  } else {  // the (li - len)-th position that carries a draft distribution
+    const int pos = nth_bit(s_qm[c.r], li - len - 1) + 1;
     c.slot = q_slot_of(p, c.r, pos);
+    c.pos = pos;
     c.row = static_cast<const char*>(p.draft) + ((int64_t)c.r * p.K + pos - 1) * p.vocab * esz;
+  }
   }
 }
 
 template <int DT, int MODE>
 __global__ void __launch_bounds__(VR_THREADS, 1) verify_rows_kernel(VerifyParams p) {
-  constexpr int ST = Vec<DT>::STAGES, UB = Vec<DT>::BYTES;
   constexpr size_t esz = DT == 1 ? 2 : 4;
+  constexpr int CH = Vec<DT>::CH;
+  constexpr bool SAMPLED = MODE == MODE_CHAIN_SAMPLE || MODE == MODE_DRAFT;
   extern __shared__ __align__(128) unsigned char smem[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  unsigned char* stage = smem + (size_t)warp * ST * UB;  // this warp's ring of unit buffers
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)VR_WARPS * ST * UB) + warp * ST;
-  int32_t* s_pre = reinterpret_cast<int32_t*>(smem + (size_t)VR_WARPS * ST * (UB + 8));
+  constexpr size_t WB = VR_WBUF(MODE);
+  unsigned char* wbuf = smem + (size_t)warp * WB;  // this warp's stage (and scratch)
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)VR_WARPS * WB) + warp * VR_BARS;
+  int32_t* s_pre = reinterpret_cast<int32_t*>(smem + (size_t)VR_WARPS * (WB + 8 * VR_BARS));
   int32_t* s_base = s_pre + p.batch + 1;
   int32_t* s_len = s_base + p.batch;
+  uint32_t* s_qm = reinterpret_cast<uint32_t*>(s_len + p.batch);
   __shared__ int32_t s_part[VR_WARPS];
 
   const int B = p.batch;
-  // ---- per-request work rows (every CTA builds the same table)
-  const int per_t = (B + VR_THREADS - 1) / VR_THREADS;
-  int32_t my_sum = 0;
-  const int32_t tot_rows = p.row_off[B];
-  for (int q = 0; q < per_t; ++q) {
-    const int r = tid * per_t + q;
-    if (r >= B) break;
-    const int32_t b0 = p.row_off[r], b1 = p.row_off[r + 1];
-    int32_t cnt = 0, len = 0;
-    bool valid;
-    if (MODE == MODE_TREE) {
-      len = b1 - b0;
-      valid = b0 >= 0 && len >= 1 && len <= p.max_nodes && b1 <= tot_rows && tot_rows <= p.max_rows;
-      cnt = valid ? len : 0;
-    } else {
-      len = p.verify_len[r];
-      valid = len >= 0 && len <= p.L && b0 >= 0 && (int64_t)b0 + len < b1 && b1 <= tot_rows &&
-              tot_rows <= p.max_rows;
-      cnt = valid ? len + 1 : 0;
-      if (valid && MODE == MODE_CHAIN_SAMPLE && p.use_q && p.pm) {
-        const uint8_t* pmr = p.pm + (int64_t)r * p.L;
-        for (int i = 1; i <= len; ++i)
-          if (pmr[i - 1] == 0) {
-            if (i <= p.K)
-              ++cnt;
-            else if (blockIdx.x == 0)
-              set_status(p.ws.status, SPEC_DEV_BAD_LENGTH);
-          }
-      }
-    }
-    if (!valid && blockIdx.x == 0) set_status(p.ws.status, SPEC_DEV_BAD_LENGTH);
-    s_base[r] = b0;
-    s_len[r] = valid ? len : -1;
-    s_pre[r] = cnt;
-    my_sum += cnt;
-  }
-  // block exclusive scan of the per-thread sums: warp shuffles, then the warp totals
-  {
-    int32_t x = my_sum;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int32_t t = __shfl_up_sync(0xFFFFFFFFu, x, o);
-      if (lane >= o) x += t;
-    }
-    if (lane == 31) s_part[warp] = x;
-    __syncthreads();
-    int32_t before = 0, all = 0;
-#pragma unroll
-    for (int q = 0; q < VR_WARPS; ++q) {
-      const int32_t t = s_part[q];
-      if (q < warp) before += t;
-      all += t;
-    }
-    int32_t run = before + x - my_sum;
+  uint32_t n_items;
+  if (MODE == MODE_DRAFT) {
+    n_items = (uint32_t)B * (uint32_t)p.K;
+  } else {
+    // ---- per-request work rows (every CTA builds the same table)
+    const int per_t = (B + VR_THREADS - 1) / VR_THREADS;
+    int32_t my_sum = 0;
+    const int32_t tot_rows = p.row_off[B];
     for (int q = 0; q < per_t; ++q) {
       const int r = tid * per_t + q;
       if (r >= B) break;
-      const int32_t cnt = s_pre[r];
-      s_pre[r] = run;
-      run += cnt;
-    }
-    if (tid == 0) s_pre[B] = all;
-  }
-  __syncthreads();
-
-  // ---- outputs of invalid requests (CTA 0 only)
-  if (blockIdx.x == 0) {
-    for (int r = warp; r < B; r += VR_WARPS) {
-      if (s_len[r] >= 0) continue;
+      const int32_t b0 = p.row_off[r], b1 = p.row_off[r + 1];
+      int32_t cnt = 0, len = 0;
+      uint32_t qm = 0;
+      bool valid;
+      // the draft-distribution flags of the request's L positions, loaded
+      // together with its offsets (they do not depend on its length)
+      uint8_t f[SPEC_MAX_L];
+      if (MODE == MODE_CHAIN_SAMPLE && p.use_q && p.pm) {
+        const uint8_t* pmr = p.pm + (int64_t)r * p.L;
+#pragma unroll
+        for (int i = 0; i < SPEC_MAX_L; ++i) f[i] = i < p.L ? pmr[i] : (uint8_t)1;
+      }
       if (MODE == MODE_TREE) {
-        for (int j = lane; j < p.max_nodes; j += 32) {
-          p.path[(int64_t)r * p.max_nodes + j] = -1;
-          p.out_tokens[(int64_t)r * p.max_nodes + j] = -1;
-        }
-        if (lane == 0) p.accept_len[r] = -1;
+        len = b1 - b0;
+        valid = b0 >= 0 && len >= 1 && len <= p.max_nodes && b1 <= tot_rows && tot_rows <= p.max_rows;
+        cnt = valid ? len : 0;
       } else {
-        write_invalid_chain(p, r, lane);
+        len = p.verify_len[r];
+        valid = len >= 0 && len <= p.L && b0 >= 0 && (int64_t)b0 + len < b1 && b1 <= tot_rows &&
+                tot_rows <= p.max_rows;
+        cnt = valid ? len + 1 : 0;
+        if (valid && MODE == MODE_CHAIN_SAMPLE && p.use_q && p.pm) {
+          // the positions that carry a draft distribution
+          bool beyond = false;
+#pragma unroll
+          for (int i = 0; i < SPEC_MAX_L; ++i)
+            if (i < len && f[i] == 0) {
+              if (i < p.K)
+                qm |= 1u << i;
+              else
+                beyond = true;
+            }
+          if (beyond && blockIdx.x == 0) set_status(p.ws.status, SPEC_DEV_BAD_LENGTH);
+          cnt += __popc(qm);
+        }
+      }
+      if (!valid && blockIdx.x == 0) set_status(p.ws.status, SPEC_DEV_BAD_LENGTH);
+      s_base[r] = b0;
+      s_len[r] = valid ? len : -1;
+      s_qm[r] = qm;
+      s_pre[r] = cnt;
+      my_sum += cnt;
+    }
+    // block exclusive scan of the per-thread sums: warp shuffles, then the warp totals
+    {
+      int32_t x = my_sum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int32_t t = __shfl_up_sync(0xFFFFFFFFu, x, o);
+        if (lane >= o) x += t;
+      }
+      if (lane == 31) s_part[warp] = x;
+      __syncthreads();
+      int32_t before = 0, all = 0;
+#pragma unroll
+      for (int q = 0; q < VR_WARPS; ++q) {
+        const int32_t t = s_part[q];
+        if (q < warp) before += t;
+        all += t;
+      }
+      int32_t run = before + x - my_sum;
+      for (int q = 0; q < per_t; ++q) {
+        const int r = tid * per_t + q;
+        if (r >= B) break;
+        const int32_t cnt = s_pre[r];
+        s_pre[r] = run;
+        run += cnt;
+      }
+      if (tid == 0) s_pre[B] = all;
+    }
+    __syncthreads();
+    n_items = (uint32_t)s_pre[B];
+
+    // ---- outputs of invalid requests (CTA 0 only)
+    if (blockIdx.x == 0) {
+      for (int r = warp; r < B; r += VR_WARPS) {
+        if (s_len[r] >= 0) continue;
+        if (MODE == MODE_TREE) {
+          for (int j = lane; j < p.max_nodes; j += 32) {
+            p.path[(int64_t)r * p.max_nodes + j] = -1;
+            p.out_tokens[(int64_t)r * p.max_nodes + j] = -1;
+          }
+          if (lane == 0) p.accept_len[r] = -1;
+        } else {
+          write_invalid_chain(p, r, lane);
+        }
       }
     }
   }
 
-  // ---- this warp's contiguous range of chunks (8 KB of one row each)
-  constexpr int CH = Vec<DT>::CH;
-  const int units = (p.vocab + CH - 1) / CH;  // chunks per row
-  const int64_t total = (int64_t)s_pre[B] * units;
-  const int64_t nw = (int64_t)gridDim.x * VR_WARPS;
-  const int64_t gw = (int64_t)blockIdx.x * VR_WARPS + warp;
-  const int64_t lo = gw * total / nw, hi = (gw + 1) * total / nw;
+  // ---- this warp's contiguous range [lo, hi) of chunks (8 KB of one row each):
+  // floor(gw total / nw) .. floor((gw + 1) total / nw) in 32-bit arithmetic
+  // (the host bounds total below 2^31 and nw^2 below 2^31)
+  const uint32_t nch = (uint32_t)p.nch;
+  const uint32_t total = n_items * nch;
+  const uint32_t nw = gridDim.x * VR_WARPS, gw = blockIdx.x * VR_WARPS + warp;
+  const uint32_t qq = total / nw, rem = total - qq * nw;
+  const uint32_t lo = gw * qq + (gw * rem) / nw, hi = (gw + 1) * qq + ((gw + 1) * rem) / nw;
   if (lo >= hi) return;
   const bool vec = p.vec_ok != 0;
-
   Cursor ic, cc;  // issue and consume cursors
   {
-    const int first = (int)(lo / units);
-    int a = 0, b = B - 1;  // last r with s_pre[r] <= first
-    while (a < b) {
-      const int mid = (a + b + 1) >> 1;
-      if (s_pre[mid] <= first)
-        a = mid;
-      else
-        b = mid - 1;
+    const int first = (int)(lo / nch);
+    int a = 0;
+    if (MODE != MODE_DRAFT) {  // last r with s_pre[r] <= first
+      int b = B - 1;
+      while (a < b) {
+        const int mid = (a + b + 1) >> 1;
+        if (s_pre[mid] <= first)
+          a = mid;
+        else
+          b = mid - 1;
+      }
     }
     ic.r = cc.r = a;
     ic.item = cc.item = -1;
   }
   // the issue cursor walks (item, chunk) incrementally from lo; it locates a
   // row only when it enters it and then advances its source pointer
-  int is_item = (int)(lo / units), is_u = (int)(lo - (int64_t)is_item * units);
+  int is_item = (int)(lo / nch), is_u = (int)(lo - (uint32_t)is_item * nch);
   const char* is_src = nullptr;
   auto issue = [&](int s) {
     if (is_src == nullptr) {
-      locate<MODE>(p, s_pre, s_base, s_len, is_item, esz, ic);
+      locate<MODE>(p, s_pre, s_base, s_len, s_qm, is_item, esz, ic);
       is_src = ic.row + (size_t)is_u * CH * esz;
     }
-    const uint32_t bytes = (is_u + 1 < units) ? (uint32_t)UB : (uint32_t)((p.vocab - is_u * CH) * esz);
+    const uint32_t bytes = (is_u + 1 < (int)nch) ? (uint32_t)VR_STAGE : (uint32_t)((p.vocab - is_u * CH) * esz);
     mbar_arrive_expect_tx(&bars[s], bytes);
-    bulk_g2s(stage + (size_t)s * UB, is_src, bytes, &bars[s]);
-    is_src += UB;
-    if (++is_u == units) {
+    bulk_g2s(wbuf + (size_t)s * VR_STAGE, is_src, bytes, &bars[s]);
+    is_src += VR_STAGE;
+    if (++is_u == (int)nch) {
       is_u = 0;
       ++is_item;
       is_src = nullptr;
     }
   };
-  if (vec) {
-    if (lane == 0) {
-      for (int s = 0; s < ST; ++s) mbar_init(&bars[s], 1);
-      fence_mbar_init();
-      for (int s = 0; s < ST && lo + s < hi; ++s) issue(s);
-    }
-    __syncwarp();
+  if (lane == 0) {
+    for (int s = 0; s < VR_BARS; ++s) mbar_init(&bars[s], 1);
+    fence_mbar_init();
+    if (vec)
+      issue(0);
   }
+  __syncwarp();
 
-  int run_r = -1, run_slot = -1;
+  int run_r = -1, run_slot = -1, run_y = -1;
+  constexpr int s = 0;  // the stage
   uint32_t run_units = 0;
   unsigned long long run_key = 0ull;
   int bad = 0, aborted = 0;
-  int64_t w = lo;
+  uint32_t w = lo;
+  uint32_t ph = 0;
+  Scratch sc;
+  if (SAMPLED) {
+    sc.buf = wbuf + VR_STAGE;
+    sc.bar = &bars[1];
+    sc.phase = 0;
+    sc.dead = 0;
+  }
 
   auto flush_row = [&]() {
-    if (MODE != MODE_CHAIN_SAMPLE && run_slot >= 0 && run_key != 0ull && lane == 0)
+    if ((MODE == MODE_CHAIN_GREEDY || MODE == MODE_TREE) && run_slot >= 0 && run_key != 0ull && lane == 0)
       atomicMax(&p.ws.rowkey[run_slot], run_key);
   };
   auto flush_request = [&]() {
     if (run_r < 0) return;
+    uint32_t* ctr = MODE == MODE_DRAFT ? &p.ws.counter3[run_r] : &p.ws.counter[run_r];
     int last = 0;
     if (lane == 0) {
       // release this warp's partials / row keys, acquire everyone else's
-      const uint32_t need = (uint32_t)((s_pre[run_r + 1] - s_pre[run_r]) * units);
-      const uint32_t old = atomic_add_acq_rel(&p.ws.counter[run_r], run_units);
+      const uint32_t need = MODE == MODE_DRAFT ? nch : (uint32_t)(s_pre[run_r + 1] - s_pre[run_r]) * nch;
+      const uint32_t old = atomic_add_acq_rel(ctr, run_units);
       last = (old + run_units == need);
     }
     last = __shfl_sync(0xFFFFFFFFu, last, 0);
@@ -1358,21 +1321,23 @@ __global__ void __launch_bounds__(VR_THREADS, 1) verify_rows_kernel(VerifyParams
         finalize_tree(p, run_r, s_base[run_r], s_len[run_r], lane);
       else if (MODE == MODE_CHAIN_GREEDY)
         finalize_chain_greedy<DT>(p, run_r, s_base[run_r], s_len[run_r], lane);
+      else if (MODE == MODE_CHAIN_SAMPLE)
+        finalize_chain_sample<DT>(p, run_r, s_base[run_r], s_len[run_r], s_qm[run_r], lane, sc);
       else
-        finalize_chain_sample<DT>(p, run_r, s_base[run_r], s_len[run_r], lane);
-      if (lane == 0) p.ws.counter[run_r] = 0u;
+        finalize_draft<DT>(p, run_r, lane, sc);
+      if (lane == 0) *ctr = 0u;
     }
   };
 
-  int item = (int)(lo / units), u = (int)(lo - (int64_t)item * units);
-  int s = 0;
-  uint32_t ph = 0;
+  int item = (int)(lo / nch), u = (int)(lo - (uint32_t)item * nch);
   for (; w < hi; ++w) {
-    locate<MODE>(p, s_pre, s_base, s_len, item, esz, cc);
+    locate<MODE>(p, s_pre, s_base, s_len, s_qm, item, esz, cc);
     if (cc.slot != run_slot) {
       flush_row();
       run_slot = cc.slot;
       run_key = 0ull;
+      if (MODE == MODE_CHAIN_SAMPLE)  // the row's draft token (none on the bonus row)
+        run_y = cc.pos <= s_len[cc.r] ? __ldcg(p.chain + (int64_t)cc.r * p.L + cc.pos - 1) : -1;
     }
     if (cc.r != run_r) {
       flush_request();
@@ -1381,44 +1346,43 @@ __global__ void __launch_bounds__(VR_THREADS, 1) verify_rows_kernel(VerifyParams
     }
     const int e0 = u * CH;
     const int n_el = min(CH, p.vocab - e0);
+    const bool has_y = MODE == MODE_CHAIN_SAMPLE && run_y >= e0 && run_y < e0 + n_el;
+    float zy = 0.0f;
     unsigned long long key = 0ull;
-    float2 ms[Vec<DT>::SUB];
+    float2 ms = make_float2(-INFINITY, 0.0f);
     if (vec) {
-      const bool landed = mbar_wait_bounded(&bars[s], ph, 1u << 22);
+      const bool landed = mbar_wait_bounded(&bars[s], ph, SPEC_WAIT_POLLS);
       if (!__all_sync(0xFFFFFFFFu, landed)) {  // warp-uniform decision
         aborted = 1;
         break;
       }
-      // copy the chunk to registers and refill the stage at once, so that the
-      // next copy is in flight while the warp computes
+      // copy the chunk to registers (and the draft token's logit) and refill
+      // the stage at once, so that the next copy is in flight while the warp computes
       uint4 v[Vec<DT>::NV];
-      vec_load_smem<DT>(stage + (size_t)s * UB, n_el, lane, v);
+      const unsigned char* st = wbuf + (size_t)s * VR_STAGE;
+      vec_load_smem<DT>(st, n_el, lane, v);
+      if (has_y)
+        zy = DT == 1 ? __uint_as_float((uint32_t) reinterpret_cast<const uint16_t*>(st)[run_y - e0] << 16)
+                     : reinterpret_cast<const float*>(st)[run_y - e0];
       __syncwarp();
-      if (lane == 0 && w + ST < hi) issue(s);
-      if (MODE == MODE_CHAIN_SAMPLE) {
-        if (DT == 1) {
-          ms[0] = unit_softmax_vec<DT, 0, 8>(v, p.c, bad);
-          if (Vec<DT>::SUB > 1) ms[Vec<DT>::SUB - 1] = unit_softmax_vec<DT, 8, 8>(v, p.c, bad);
-        } else {
-          ms[0] = unit_softmax_vec<DT, 0, 16>(v, p.c, bad);
-        }
-      } else if (DT == 1) {
+      if (lane == 0 && w + 1 < hi) issue(s);
+      if (SAMPLED)
+        ms = unit_softmax_vec<DT, 0, Vec<DT>::NV>(v, p.c, bad);
+      else if (DT == 1)
         key = chunk_argmax_bf16(v, n_el, lane, bad);
-      } else {
+      else
         key = unit_argmax_vec<DT>(v, n_el, lane, bad);
-      }
     } else {
+      if (has_y) zy = load_one<DT>(cc.row, run_y);
 #pragma unroll
       for (int j = 0; j < Vec<DT>::SUB; ++j) {
         const int e1 = e0 + j * SPEC_UNIT;
         const int n1 = min(SPEC_UNIT, p.vocab - e1);
-        if (n1 <= 0) {
-          ms[j] = make_float2(-INFINITY, 0.0f);
-          continue;
-        }
+        if (n1 <= 0) continue;
         const void* unit = cc.row + (size_t)e1 * esz;
-        if (MODE == MODE_CHAIN_SAMPLE) {
-          ms[j] = unit_softmax_scalar<DT>(unit, n1, lane, p.c, bad);
+        if (SAMPLED) {
+          const float2 t = unit_softmax_scalar<DT>(unit, n1, lane, p.c, bad);
+          merge_ms(ms.x, ms.y, t.x, t.y, p.c);
         } else {
           unsigned long long k1 = unit_argmax_scalar<DT>(unit, n1, lane, bad);
           if (k1 != 0ull) {  // rebase to the chunk offset
@@ -1429,13 +1393,11 @@ __global__ void __launch_bounds__(VR_THREADS, 1) verify_rows_kernel(VerifyParams
         }
       }
     }
-    if (MODE == MODE_CHAIN_SAMPLE) {
+    if (SAMPLED) {
       if (lane == 0) {
-#pragma unroll
-        for (int j = 0; j < Vec<DT>::SUB; ++j) {
-          const int uu = u * Vec<DT>::SUB + j;
-          if (uu * SPEC_UNIT < p.vocab) __stcg(&p.ws.partial[(int64_t)cc.slot * p.ws.units + uu], ms[j]);
-        }
+        float2* pr = partial_row(p, cc.slot);
+        __stcg(&pr[u], ms);
+        if (has_y) __stcg(&pr[p.nch], make_float2(zy, 0.0f));
       }
     } else if (key != 0ull) {
       // rebase the chunk offset to the row index; keys of one row fold by max
@@ -1445,229 +1407,205 @@ __global__ void __launch_bounds__(VR_THREADS, 1) verify_rows_kernel(VerifyParams
       if (kk > run_key) run_key = kk;
     }
     ++run_units;
-    if (++u == units) {
+    if (++u == (int)nch) {
       u = 0;
       ++item;
     }
-    if (++s == ST) {
-      s = 0;
-      ph ^= 1u;
-    }
+    ph ^= 1u;
   }
   if (aborted) {
-    // a copy did not land in time: record it, wait (bounded) for every copy this
-    // warp still has in flight, and stop without finalizing
+    // a copy did not land in time: record it, wait (bounded) once more for
+    // the copy this warp has in flight, and stop without finalizing
     if (lane == 0) {
       set_status(p.ws.status, SPEC_DEV_TIMEOUT);
-      for (int64_t x = w; x < hi && x < w + ST; ++x) {
-        const int s = (int)((x - lo) % ST);
-        mbar_wait_bounded(&bars[s], (uint32_t)(((x - lo) / ST) & 1), 1u << 22);
-      }
+      mbar_wait_bounded(&bars[0], ph, SPEC_WAIT_POLLS);
     }
     __syncwarp();
     return;
   }
   flush_row();
   flush_request();
+  if (SAMPLED && sc.dead && lane == 0) mbar_wait_bounded(sc.bar, sc.phase ^ 1u, SPEC_WAIT_POLLS);  // the copy given up on
   if (bad && lane == 0) set_status(p.ws.status, SPEC_DEV_NONFINITE);
 }
 
 // ------------------------------------------------------------------ draw from max(0, p - q)
-template <int DT>
-__global__ void __launch_bounds__(SPEC_CTA_THREADS) resample_kernel(VerifyParams p) {
+// Block-wide helpers of resample_kernel (RS_THREADS threads).
+// inclusive prefix over the block's threads in thread order; *total = the sum
+__device__ __forceinline__ float block_incl_scan(float v, float* s_w, float* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int units = p.units;
-  const int64_t total = (int64_t)p.batch * units;
-  const int64_t nwarps = (int64_t)gridDim.x * SPEC_WARPS_PER_CTA;
-  const size_t esz = DT == 1 ? 2 : 4;
-  const bool vec = p.vec_ok != 0;
-  for (int64_t w = (int64_t)blockIdx.x * SPEC_WARPS_PER_CTA + warp; w < total; w += nwarps) {
-    const int r = (int)(w / units);
-    const int u = (int)(w - (int64_t)r * units);
-    // the whole record in one round trip (four 16-byte loads)
-    Record rec;
-    {
-      const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const Record*>(p.ws.record) + r);
-      uint4* dst = reinterpret_cast<uint4*>(&rec);
+  const float wi = warp_incl_scan(v);
+  if (lane == 31) s_w[warp] = wi;
+  __syncthreads();
+  float before = 0.0f, all = 0.0f;
 #pragma unroll
-      for (int q = 0; q < 4; ++q) dst[q] = __ldcg(src + q);
-    }
-    if (!rec.flag) continue;
-    const void* prow = static_cast<const char*>(p.logits) + (int64_t)rec.prow * p.vocab * esz;
-    const void* qrow = static_cast<const char*>(p.draft) +
-                       ((int64_t)r * p.K + rec.pos - 1) * p.vocab * esz;
-    const float ip = 1.0f / rec.sp, iq = 1.0f / rec.sq;
-    const float mpc = rec.mp * p.c, mqc = rec.mq * p.c;
-    auto resid = [&](const float* vp, const float* vq, int j) -> float {
-      const float a = vp[j] == -INFINITY ? 0.0f : ex2(fmaf(vp[j], p.c, -mpc)) * ip;
-      const float b = vq[j] == -INFINITY ? 0.0f : ex2(fmaf(vq[j], p.c, -mqc)) * iq;
-      return a > b ? a - b : 0.0f;
-    };
-    {
-      const int e0 = u * SPEC_UNIT, n_el = min(SPEC_UNIT, p.vocab - e0);
-      float vp[64], vq[64];
-      load_unit_contig<DT>(prow, e0, n_el, vec, lane, vp);
-      load_unit_contig<DT>(qrow, e0, n_el, vec, lane, vq);
-      float a0 = 0.0f, a1 = 0.0f;
+  for (int q = 0; q < RS_THREADS / 32; ++q) {
+    const float t = s_w[q];
+    if (q < warp) before += t;
+    all += t;
+  }
+  __syncthreads();  // s_w free again
+  *total = all;
+  return before + wi;
+}
+// the first (last) thread whose predicate holds, or -1
+__device__ __forceinline__ int block_first(bool pred, int* s_i, bool last) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const unsigned b = __ballot_sync(0xFFFFFFFFu, pred);
+  if (lane == 0) s_i[warp] = b ? 32 * warp + (last ? 31 - __clz(b) : __ffs(b) - 1) : -1;
+  __syncthreads();
+  int m = -1;
 #pragma unroll
-      for (int j = 0; j < 64; j += 2) {
-        a0 += resid(vp, vq, j);
-        a1 += resid(vp, vq, j + 1);
+  for (int q = 0; q < RS_THREADS / 32; ++q) {
+    const int t = s_i[q];
+    if (t >= 0 && (m < 0 || (last ? t > m : t < m))) m = t;
+  }
+  __syncthreads();
+  return m;
+}
+// N consecutive entries of a row from entry e (fp32; -inf past the row's end)
+template <int DT, int N>
+__device__ __forceinline__ void load_entries(const void* row, int e, int vocab, bool vec, float (&x)[N]) {
+  if (vec) {
+    constexpr int PV = DT == 1 ? 8 : 4;  // entries per 16-byte vector
+    uint4 w[N / PV];
+#pragma unroll
+    for (int k = 0; k < N / PV; ++k)
+      w[k] = e + PV * k < vocab ? __ldcg(reinterpret_cast<const uint4*>(static_cast<const char*>(row) +
+                                                                         (size_t)(e + PV * k) * (DT == 1 ? 2 : 4)))
+                                : make_uint4(Vec<DT>::NEG, Vec<DT>::NEG, Vec<DT>::NEG, Vec<DT>::NEG);
+#pragma unroll
+    for (int k = 0; k < N / PV; ++k) {
+      const uint32_t q4[4] = {w[k].x, w[k].y, w[k].z, w[k].w};
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        if (DT == 1) {
+          x[PV * k + 2 * h] = bf16_lo(q4[h]);
+          x[PV * k + 2 * h + 1] = bf16_hi(q4[h]);
+        } else {
+          x[PV * k + h] = __uint_as_float(q4[h]);
+        }
       }
-      const float ws = warp_sum(a0 + a1);
-      if (lane == 0) __stcg(&p.ws.partial2[(int64_t)r * p.ws.units + u], (double)ws);
     }
-    int last = 0;
-    if (lane == 0) {
-      __threadfence();
-      const uint32_t old = atomicAdd(&p.ws.counter2[r], 1u);
-      last = (old + 1u == (uint32_t)units);
-    }
-    last = __shfl_sync(0xFFFFFFFFu, last, 0);
-    if (!last) continue;
-    __threadfence();
-    // the residual mass; at or below 1e-30 the draw falls back to p
-    const int pslot = rec.prow;
-    auto w_res = [&](int uu) -> float { return (float)__ldcg(&p.ws.partial2[(int64_t)r * p.ws.units + uu]); };
-    auto w_p = [&](int uu) -> float {
-      const float2 t = __ldcg(&p.ws.partial[(int64_t)pslot * p.ws.units + uu]);
-      if (t.x == -INFINITY) return 0.0f;
-      return t.y * ex2((t.x - rec.mp) * p.c) * ip;
-    };
-    Crossing cr = find_unit(units, rec.u2, lane, w_res);
-    const bool fallback = !(cr.total > 1e-30f);
-    if (fallback) cr = find_unit(units, rec.u2, lane, w_p);
-    const int e0 = cr.unit * SPEC_UNIT, n_el = min(SPEC_UNIT, p.vocab - e0);
-    float vp[64], vq[64], rr[64];
-    load_unit_contig<DT>(prow, e0, n_el, vec, lane, vp);
-    load_unit_contig<DT>(qrow, e0, n_el, vec, lane, vq);
+  } else {
 #pragma unroll
-    for (int j = 0; j < 64; ++j)
-      rr[j] = fallback ? (vp[j] == -INFINITY ? 0.0f : ex2(fmaf(vp[j], p.c, -mpc)) * ip) : resid(vp, vq, j);
-    float r_at;
-    const int pick = find_in_unit(rr, cr.before, cr.t, lane, &r_at);
-    if (lane == 0) {
-      p.out_tokens[(int64_t)r * (p.L + 1) + rec.pos - 1] = e0 + pick;
-      if (p.dbg_resid) p.dbg_resid[r] = r_at / cr.total;
-      Record* wr = reinterpret_cast<Record*>(p.ws.record) + r;
-      wr->flag = 0;
-      p.ws.counter2[r] = 0u;
-    }
+    for (int j = 0; j < N; ++j) x[j] = e + j < vocab ? load_one<DT>(row, e + j) : -INFINITY;
   }
 }
 
-// ------------------------------------------------------------------ probabilistic drafting
-// y_k ~ softmax(z_k / T) for the drafter's rows (Hybrid Spark sec. 4.5, App. H).
-// One pass over each row: per 8 KB chunk, (max, sum of 2^((z - max) log2e / T))
-// per 2048-entry unit into the workspace partials -- the slots the verification
-// kernel uses for the same q rows -- and the warp that completes a row draws
-// from it: the crossing unit from the units' weights, then the crossing entry
-// inside that unit (a second read of one 4-8 KB unit).  The uniform is word 0
-// of Philox counter (r, 0x40000000 + k, lo32(step), hi32(step)), key
-// (lo32(seed), hi32(seed)), a counter domain apart from verification's.
+// One CTA per (chunk c, request r) with a record: the chunk's mass of
+// max(0, p - q) at the rejected position, summed over the block; the last
+// CTA of the request (arrival counter) locates the crossing chunk over those
+// masses at u' of their total (p itself when the mass is at most 1e-30), then
+// the crossing entry inside it, each thread holding PER consecutive entries.
 template <int DT>
-__device__ void draw_draft(const VerifyParams& p, int row, int r, int k, int slot, int lane) {
-  // the row's unit partials, lane l holding units [per l, per l + per) (the
-  // layout find_unit walks), loaded once for the row max and the weights
-  const int per = (p.units + 31) / 32, u0 = lane * per;
-  const float2* pr = &p.ws.partial[(int64_t)slot * p.ws.units];
-  float2 t4[4];
-#pragma unroll
-  for (int q = 0; q < 4; ++q)
-    t4[q] = (q < per && u0 + q < p.units) ? __ldcg(&pr[u0 + q]) : make_float2(-INFINITY, 0.0f);
-  float lm = fmaxf(fmaxf(t4[0].x, t4[1].x), fmaxf(t4[2].x, t4[3].x));
-  for (int q = 4; q < per; ++q)
-    if (u0 + q < p.units) lm = fmaxf(lm, __ldcg(&pr[u0 + q]).x);
-  const float m = warp_max(lm);
-  uint32_t o[4];
-  philox4x32_10((uint32_t)r, 0x40000000u + (uint32_t)(k + 1), (uint32_t)p.step, (uint32_t)(p.step >> 32),
-                (uint32_t)p.seed, (uint32_t)(p.seed >> 32), o);
-  const float u = (float)(o[0] >> 8) * (1.0f / 16777216.0f);
-  const char* base = static_cast<const char*>(p.draft) + (int64_t)row * p.vocab * (DT == 1 ? 2 : 4);
-  int y = 0;
-  float q_at = 0.0f;
-  float total = 0.0f;
-  if (m != -INFINITY) {
-    auto w_plain = [&](int uu) -> float {
-      const int q = uu - u0;
-      const float2 t = q == 0 ? t4[0] : q == 1 ? t4[1] : q == 2 ? t4[2] : q == 3 ? t4[3] : __ldcg(&pr[uu]);
-      if (t.x == -INFINITY) return 0.0f;
-      return t.y * ex2((t.x - m) * p.c);
-    };
-    const Crossing cr = find_unit(p.units, u, lane, w_plain);
-    total = cr.total;
-    float v[64];
-    const int e0 = cr.unit * SPEC_UNIT;
-    const int n_el = min(SPEC_UNIT, p.vocab - e0);
-    load_unit_contig<DT>(base, e0, n_el, p.vec_ok != 0, lane, v);
-    const float mc = m * p.c;
-#pragma unroll
-    for (int j = 0; j < 64; ++j) v[j] = (v[j] == -INFINITY) ? 0.0f : ex2(fmaf(v[j], p.c, -mc));
-    const int pick = find_in_unit(v, cr.before, cr.t, lane, &q_at);
-    y = e0 + pick;
-  }
-  if (lane == 0) {
-    p.out_tokens[row] = y;
-    if (p.dbg_u) p.dbg_u[row] = u;
-    if (p.dbg_resid) p.dbg_resid[row] = total > 0.0f ? q_at / total : 0.0f;
-  }
-}
-
-template <int DT>
-__global__ void __launch_bounds__(SPEC_CTA_THREADS) sample_drafts_kernel(VerifyParams p) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  constexpr int CH = Vec<DT>::CH, SUB = Vec<DT>::SUB;
-  const int chunks = (p.vocab + CH - 1) / CH;
-  const int rows = p.batch * p.K;
-  const int64_t total = (int64_t)rows * chunks;
-  const int64_t nwarps = (int64_t)gridDim.x * SPEC_WARPS_PER_CTA;
-  const size_t esz = DT == 1 ? 2 : 4;
+__global__ void __launch_bounds__(RS_THREADS) resample_kernel(VerifyParams p) {
+  constexpr int CH = Vec<DT>::CH, PER = CH / RS_THREADS;  // 16 bf16 / 8 fp32 entries per thread
+  constexpr size_t ESZ = DT == 1 ? 2 : 4;
+  __shared__ __align__(16) Record s_rec;
+  __shared__ float s_w[RS_THREADS / 32];
+  __shared__ int s_i[RS_THREADS / 32];
+  __shared__ int s_last;
+  __shared__ float s_f[2];
+  const int tid = threadIdx.x;
+  const int c = blockIdx.x, r = blockIdx.y;
+  if (tid < 4)
+    reinterpret_cast<uint4*>(&s_rec)[tid] =
+        __ldcg(reinterpret_cast<const uint4*>(reinterpret_cast<const Record*>(p.ws.record) + r) + tid);
+  __syncthreads();
+  if (!s_rec.flag) return;
+  const Record rec = s_rec;
   const bool vec = p.vec_ok != 0;
-  int bad = 0;
-  for (int64_t w = (int64_t)blockIdx.x * SPEC_WARPS_PER_CTA + warp; w < total; w += nwarps) {
-    const int row = (int)(w / chunks), ch = (int)(w - (int64_t)row * chunks);
-    const int r = row / p.K, k = row - r * p.K;  // position k + 1
-    const int slot = q_slot_of(p, r, k + 1);
-    const char* base = static_cast<const char*>(p.draft) + (int64_t)row * p.vocab * esz;
-    const int e0 = ch * CH, n_el = min(CH, p.vocab - e0);
-    float2 ms[SUB];
-    if (vec) {
-      uint4 v[Vec<DT>::NV];
-      vec_load_global<DT>(base + (size_t)e0 * esz, n_el, lane, v);
-      if (DT == 1) {
-        ms[0] = unit_softmax_vec<DT, 0, 8>(v, p.c, bad);
-        if (SUB > 1) ms[SUB - 1] = unit_softmax_vec<DT, 8, 8>(v, p.c, bad);
-      } else {
-        ms[0] = unit_softmax_vec<DT, 0, 16>(v, p.c, bad);
-      }
-    } else {
+  const char* prow = static_cast<const char*>(p.logits) + (int64_t)rec.prow * p.vocab * ESZ;
+  const char* qrow = static_cast<const char*>(p.draft) + ((int64_t)r * p.K + rec.pos - 1) * p.vocab * ESZ;
+  const float ip = 1.0f / rec.sp, iq = 1.0f / rec.sq;
+  const float mpc = rec.mp * p.c, mqc = rec.mq * p.c;
+  // weights of logits (2^-inf = +0 covers the empty entries)
+  auto pw = [&](float z) -> float { return ex2(fmaf(z, p.c, -mpc)) * ip; };
+  auto resid = [&](float zp, float zq) -> float {
+    const float a = pw(zp);
+    const float b = ex2(fmaf(zq, p.c, -mqc)) * iq;
+    return fmaxf(a - b, 0.0f);
+  };
+  float* masses = reinterpret_cast<float*>(p.ws.partial2) + (int64_t)r * p.pstride;
+  {
+    float zp[PER], zq[PER];
+    load_entries<DT, PER>(prow, c * CH + PER * tid, p.vocab, vec, zp);
+    load_entries<DT, PER>(qrow, c * CH + PER * tid, p.vocab, vec, zq);
+    float sum = 0.0f;
 #pragma unroll
-      for (int j = 0; j < SUB; ++j) {
-        const int e1 = e0 + j * SPEC_UNIT;
-        const int n1 = min(SPEC_UNIT, p.vocab - e1);
-        ms[j] = n1 <= 0 ? make_float2(-INFINITY, 0.0f)
-                        : unit_softmax_scalar<DT>(base + (size_t)e1 * esz, n1, lane, p.c, bad);
-      }
+    for (int j = 0; j < PER; ++j) sum += resid(zp[j], zq[j]);
+    float tot;
+    block_incl_scan(sum, s_w, &tot);
+    if (tid == 0) {
+      __stcg(&masses[c], tot);
+      // release this chunk's mass, acquire the others'
+      s_last = atomic_add_acq_rel(&p.ws.counter2[r], 1u) + 1u == (uint32_t)p.nch;
     }
-    int last = 0;
-    if (lane == 0) {
+    __syncthreads();
+    if (!s_last) return;
+  }
+  // ---- the last CTA of request r draws
+  float w = tid < p.nch ? __ldcg(&masses[tid]) : 0.0f;
+  float total;
+  float incl = block_incl_scan(w, s_w, &total);
+  const bool fallback = !(total > 1e-30f);
+  if (fallback) {  // no residual mass: the draw falls back to p
+    w = 0.0f;
+    if (tid < p.nch) {
+      const float2 t = __ldcg(&partial_row(p, rec.prow)[tid]);
+      w = t.y * ex2((t.x - rec.mp) * p.c) * ip;
+    }
+    incl = block_incl_scan(w, s_w, &total);
+  }
+  const float t = rec.u2 * total;
+  int cx = block_first(incl > t && w > 0.0f, s_i, false);
+  const bool last_mode = cx < 0;  // t at or above the total (rounding): the last entry with mass
+  if (last_mode) cx = block_first(w > 0.0f, s_i, true);
+  if (cx < 0) cx = 0;
+  if (tid == cx) s_f[0] = incl - w;
+  __syncthreads();
+  const float tt = last_mode ? INFINITY : t - s_f[0];
+  // the crossing chunk's entries
+  float wv[PER], sum = 0.0f;
+  {
+    float zp[PER], zq[PER];
+    load_entries<DT, PER>(prow, cx * CH + PER * tid, p.vocab, vec, zp);
+    if (!fallback) load_entries<DT, PER>(qrow, cx * CH + PER * tid, p.vocab, vec, zq);
 #pragma unroll
-      for (int j = 0; j < SUB; ++j) {
-        const int uu = ch * SUB + j;
-        if (uu * SPEC_UNIT < p.vocab) __stcg(&p.ws.partial[(int64_t)slot * p.ws.units + uu], ms[j]);
-      }
-      // release this chunk's partials, acquire the row's others
-      const uint32_t old = atomic_add_acq_rel(&p.ws.counter3[row], 1u);
-      last = (old + 1u == (uint32_t)chunks);
-    }
-    last = __shfl_sync(0xFFFFFFFFu, last, 0);
-    if (last) {
-      __syncwarp();  // orders every lane after lane 0's acquire
-      if (lane == 0) p.ws.counter3[row] = 0u;
-      draw_draft<DT>(p, row, r, k, slot, lane);
+    for (int j = 0; j < PER; ++j) {
+      wv[j] = fallback ? pw(zp[j]) : resid(zp[j], zq[j]);
+      sum += wv[j];
     }
   }
-  if (bad && lane == 0) set_status(p.ws.status, SPEC_DEV_NONFINITE);
+  float all;
+  const float inc2 = block_incl_scan(sum, s_w, &all);
+  int th = block_first(inc2 > tt && sum > 0.0f, s_i, false);
+  const bool none = th < 0;
+  if (none) th = block_first(sum > 0.0f, s_i, true);
+  if (tid == (th < 0 ? 0 : th)) {
+    int pick = -1, lp = -1;
+    float wp = 0.0f, lw = 0.0f, run = inc2 - sum;
+#pragma unroll
+    for (int j = 0; j < PER; ++j)
+      if (wv[j] > 0.0f) {
+        run += wv[j];
+        if (pick < 0 && !none && run > tt) {
+          pick = j;
+          wp = wv[j];
+        }
+        lp = j;
+        lw = wv[j];
+      }
+    if (pick < 0) {  // rounding, or no crossing: the last entry with mass
+      pick = lp < 0 ? 0 : lp;
+      wp = lw;
+    }
+    p.out_tokens[(int64_t)r * (p.L + 1) + rec.pos - 1] = cx * CH + PER * tid + pick;
+    if (p.dbg_resid) p.dbg_resid[r] = wp / total;
+    reinterpret_cast<Record*>(p.ws.record)[r].flag = 0;
+    p.ws.counter2[r] = 0u;
+  }
 }
 
 }  // namespace spec
@@ -1677,37 +1615,15 @@ __global__ void __launch_bounds__(SPEC_CTA_THREADS) sample_drafts_kernel(VerifyP
 // ---------------------------------------------------------------------------
 namespace {
 
-template <typename Kern>
-int grid_for(Kern k, size_t smem, int num_sms) {
-  int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, SPEC_CTA_THREADS, smem) != cudaSuccess ||
-      per_sm < 1)
-    per_sm = 1;
-  return per_sm * num_sms;
-}
-
 template <int DT, int MODE>
 cudaError_t launch_rows(const spec::VerifyParams& p, int num_sms, cudaStream_t stream) {
-  using V = spec::Vec<DT>;
-  const size_t smem = (size_t)VR_WARPS * V::STAGES * (V::BYTES + 8) +
-                      (size_t)(3 * p.batch + 1) * sizeof(int32_t);
+  const size_t table = MODE == spec::MODE_DRAFT ? 0 : (size_t)(4 * p.batch + 1) * sizeof(int32_t);
+  const size_t smem = (size_t)VR_WARPS * (VR_WBUF(MODE) + 8 * VR_BARS) + table;
   auto k = spec::verify_rows_kernel<DT, MODE>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  // one CTA per SM: the shared-memory rings hold the bytes in flight
+  // one CTA per SM: the shared-memory stages hold the bytes in flight
   k<<<num_sms, VR_THREADS, smem, stream>>>(p);
-  return cudaGetLastError();
-}
-
-template <int DT>
-cudaError_t launch_resample(const spec::VerifyParams& p, int num_sms, cudaStream_t stream) {
-  auto k = spec::resample_kernel<DT>;
-  static int cached_grid = 0;
-  if (cached_grid == 0) cached_grid = grid_for(k, 0, num_sms);
-  int64_t need = ((int64_t)p.batch * p.units + SPEC_WARPS_PER_CTA - 1) / SPEC_WARPS_PER_CTA;
-  int grid = (int)(need < cached_grid ? need : cached_grid);
-  if (grid < 1) grid = 1;
-  k<<<grid, SPEC_CTA_THREADS, 0, stream>>>(p);
   return cudaGetLastError();
 }
 
@@ -1721,7 +1637,7 @@ spec::WsView ws_view(const spec_workspace* ws) {
   v.record = reinterpret_cast<unsigned char*>(b + ws->off_record);
   v.rowkey = reinterpret_cast<unsigned long long*>(b + ws->off_rowkey);
   v.partial = reinterpret_cast<float2*>(b + ws->off_partial);
-  v.partial2 = reinterpret_cast<double*>(b + ws->off_partial2);
+  v.partial2 = reinterpret_cast<float*>(b + ws->off_partial2);
   v.units = ws->units;
   v.max_rows = ws->max_rows;
   v.max_batch = ws->max_batch;
@@ -1729,7 +1645,26 @@ spec::WsView ws_view(const spec_workspace* ws) {
   return v;
 }
 
+// the chunk geometry of a call: chunks per row, the staged partial row and the
+// workspace's partial row stride
+void set_chunks(spec::VerifyParams& p, int dtype, const spec_workspace* ws) {
+  const int ch = dtype == SPEC_BF16 ? spec::Vec<1>::CH : spec::Vec<0>::CH;
+  p.nch = (p.vocab + ch - 1) / ch;
+  p.rowf = (p.nch + 2) & ~1;
+  p.pstride = spec_partial_stride(ws->units);
+}
+
 }  // namespace
+
+// The largest vocabulary (a row's chunk weights fit 8 per lane, and the draw
+// kernel gives each chunk one thread) and the bound on a launch's chunks
+// (32-bit work split).
+extern "C" int spec_verify_limits_ok(int32_t vocab, int32_t dtype, int64_t rows, int num_sms) {
+  const int ch = dtype == SPEC_BF16 ? spec::Vec<1>::CH : spec::Vec<0>::CH;
+  const int64_t nch = ((int64_t)vocab + ch - 1) / ch;
+  const int64_t nw = (int64_t)num_sms * VR_WARPS;
+  return vocab <= SPEC_MAX_VOCAB && rows * nch < ((int64_t)1 << 31) && nw * nw < ((int64_t)1 << 31);
+}
 
 extern "C" cudaError_t spec_launch_verify_chain(
     int32_t batch, int32_t vocab, int32_t dtype, const void* logits, const int32_t* row_off,
@@ -1760,7 +1695,7 @@ extern "C" cudaError_t spec_launch_verify_chain(
   p.dbg_ratio = dbg_ratio;
   p.dbg_u = dbg_u;
   p.dbg_resid = dbg_resid;
-  p.units = (vocab + SPEC_UNIT - 1) / SPEC_UNIT;
+  set_chunks(p, dtype, ws);
   const size_t esz = dtype == SPEC_BF16 ? 2 : 4;
   p.vec_ok = (((size_t)vocab * esz) % 16 == 0 && (reinterpret_cast<uintptr_t>(logits) & 15u) == 0 &&
               (draft == nullptr || (reinterpret_cast<uintptr_t>(draft) & 15u) == 0))
@@ -1776,7 +1711,12 @@ extern "C" cudaError_t spec_launch_verify_chain(
     e = greedy ? launch_rows<0, spec::MODE_CHAIN_GREEDY>(p, num_sms, stream)
                : launch_rows<0, spec::MODE_CHAIN_SAMPLE>(p, num_sms, stream);
   if (e != cudaSuccess || !p.use_q) return e;
-  return dtype == SPEC_BF16 ? launch_resample<1>(p, num_sms, stream) : launch_resample<0>(p, num_sms, stream);
+  const dim3 grid((unsigned)p.nch, (unsigned)batch);
+  if (dtype == SPEC_BF16)
+    spec::resample_kernel<1><<<grid, RS_THREADS, 0, stream>>>(p);
+  else
+    spec::resample_kernel<0><<<grid, RS_THREADS, 0, stream>>>(p);
+  return cudaGetLastError();
 }
 
 extern "C" cudaError_t spec_launch_verify_tree(int32_t batch, int32_t vocab, int32_t dtype,
@@ -1797,7 +1737,7 @@ extern "C" cudaError_t spec_launch_verify_tree(int32_t batch, int32_t vocab, int
   p.path = path;
   p.accept_len = accept_len;
   p.out_tokens = out_tokens;
-  p.units = (vocab + SPEC_UNIT - 1) / SPEC_UNIT;
+  set_chunks(p, dtype, ws);
   const size_t esz = dtype == SPEC_BF16 ? 2 : 4;
   p.vec_ok = (((size_t)vocab * esz) % 16 == 0 && (reinterpret_cast<uintptr_t>(logits) & 15u) == 0) ? 1 : 0;
   p.ws = ws_view(ws);
@@ -1822,18 +1762,11 @@ extern "C" cudaError_t spec_launch_sample_drafts(int32_t batch, int32_t K, int32
   p.out_tokens = y;
   p.dbg_u = dbg_u;
   p.dbg_resid = dbg_q;
-  p.units = (vocab + SPEC_UNIT - 1) / SPEC_UNIT;
+  set_chunks(p, dtype, ws);
   const size_t esz = dtype == SPEC_BF16 ? 2 : 4;
   p.vec_ok = (((size_t)vocab * esz) % 16 == 0 && (reinterpret_cast<uintptr_t>(draft_logits) & 15u) == 0) ? 1 : 0;
   p.ws = ws_view(ws);
   if (batch == 0) return cudaSuccess;
-  const int ch = dtype == SPEC_BF16 ? spec::Vec<1>::CH : spec::Vec<0>::CH;
-  const int64_t chunks = (int64_t)batch * K * ((vocab + ch - 1) / ch);
-  const int64_t want = (chunks + SPEC_WARPS_PER_CTA - 1) / SPEC_WARPS_PER_CTA;
-  const int grid = (int)(want < (int64_t)num_sms * 8 ? want : (int64_t)num_sms * 8);
-  if (dtype == SPEC_BF16)
-    spec::sample_drafts_kernel<1><<<grid, SPEC_CTA_THREADS, 0, stream>>>(p);
-  else
-    spec::sample_drafts_kernel<0><<<grid, SPEC_CTA_THREADS, 0, stream>>>(p);
-  return cudaGetLastError();
+  return dtype == SPEC_BF16 ? launch_rows<1, spec::MODE_DRAFT>(p, num_sms, stream)
+                            : launch_rows<0, spec::MODE_DRAFT>(p, num_sms, stream);
 }

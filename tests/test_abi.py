@@ -79,6 +79,8 @@ def test_workspace_bytes(spec):
     assert lib.spec_workspace_bytes(-1, 1, 1, 1) == 0
     assert lib.spec_workspace_bytes(1, 1, 1, 0) == 0
     assert lib.spec_workspace_bytes(1, 1, 99, 10) == 0
+    assert lib.spec_workspace_bytes(1, 1, 1, 524288) > 0  # SPEC_MAX_VOCAB
+    assert lib.spec_workspace_bytes(1, 1, 1, 524289) == 0
 
 
 def test_estimator_table_bytes(spec):
