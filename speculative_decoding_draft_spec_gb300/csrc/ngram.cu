@@ -95,6 +95,15 @@ __global__ void __launch_bounds__(SPEC_CTA_THREADS, 1) ngram_kernel(NgramParams 
   const int r = blockIdx.x / C;
   const int tid = threadIdx.x;
   const int32_t* x = p.hist + (int64_t)r * p.stride;
+  // one CTA per request (rows of at most 8192 tokens): the whole row is copied
+  // at once, before its length is read, so the copy and that load overlap
+  const bool whole_row = !CLUSTER && p.use_bulk;
+  if (whole_row && tid == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+    mbar_arrive_expect_tx(&bar, (uint32_t)p.stride * 4u);
+    bulk_g2s(smem_tok, x, (uint32_t)p.stride * 4u, &bar);
+  }
 
   const int32_t T = p.hist_len[r];
   const bool valid = (T >= 0) && ((int64_t)T <= p.stride);
@@ -126,19 +135,28 @@ __global__ void __launch_bounds__(SPEC_CTA_THREADS, 1) ngram_kernel(NgramParams 
   const int32_t j1 = min(nc, j0 + per);
   const bool work = j0 < j1;
 
-  // staged ranges, rounded to 4-token (16-byte) boundaries
-  const int32_t w0 = max(0, j0 - p.cap + 1) & ~3;
-  const int32_t w1 = (j1 + 3) & ~3;
-  const int32_t s0 = max(0, T - p.cap) & ~3;
-  const int32_t s1 = (T + 3) & ~3;
-  int32_t* win = smem_tok;               // x[w0 .. w1)
-  int32_t* suf = smem_tok + p.win_cap;   // x[s0 .. s1)
+  // staged ranges, rounded to 4-token (16-byte) boundaries (the whole row: both are it)
+  const int32_t w0 = whole_row ? 0 : max(0, j0 - p.cap + 1) & ~3;
+  const int32_t w1 = whole_row ? (int32_t)p.stride : (j1 + 3) & ~3;
+  const int32_t s0 = whole_row ? 0 : max(0, T - p.cap) & ~3;
+  const int32_t s1 = whole_row ? (int32_t)p.stride : (T + 3) & ~3;
+  int32_t* win = smem_tok;                                   // x[w0 .. w1)
+  int32_t* suf = whole_row ? smem_tok : smem_tok + p.win_cap;  // x[s0 .. s1)
 
   __shared__ int32_t s_q[SPEC_WARPS_PER_CTA][NG_QCAP];  // queued long candidates per warp
   __shared__ int32_t s_qn[SPEC_WARPS_PER_CTA];
   if (tid == 0) s_flag = 0;
   if (tid < SPEC_WARPS_PER_CTA) s_qn[tid] = 0;
-  if (work) {
+  if (whole_row) {
+    __syncthreads();  // the barrier's initialisation and s_flag are visible
+    if (!mbar_wait_bounded(&bar, 0, 1u << 22)) {
+      // the copy has not landed: record it, wait (bounded) for it to finish
+      // writing this CTA's shared memory, and skip the scan
+      if (tid == 0) set_status(p.status, SPEC_DEV_TIMEOUT);
+      atomicOr(&s_flag, 1);
+      mbar_wait_bounded(&bar, 0, 1u << 22);
+    }
+  } else if (work) {
     if (p.use_bulk) {
       if (tid == 0) {
         mbar_init(&bar, 1);
@@ -357,7 +375,7 @@ __global__ void __launch_bounds__(SPEC_CTA_THREADS, 1) ngram_kernel(NgramParams 
         }
       }
       __syncthreads();
-      if (s_last) select_budget_cta(p.sc, suf + p.suf_cap);
+      if (s_last) select_budget_cta(p.sc, smem_tok + p.win_cap + p.suf_cap);
     }
   }
   if (CLUSTER) cluster.sync();  // peers keep their shared memory until rank 0 has read it

@@ -658,7 +658,9 @@ __device__ __forceinline__ bool scratch_wait(Scratch& sc, uint32_t* status, int 
 }
 
 // n <= 32 partial rows into the scratch (row j from slot slot_of(j), rowf
-// float2 each), one bulk copy per lane; stage_rows_issue returns at once
+// float2 each): one bulk copy per run of rows whose slots are consecutive (a
+// request's target rows are one run, its draft rows runs of consecutive
+// positions), issued by the run's first lane; stage_rows_issue returns at once
 // (scratch_wait completes it), stage_rows waits
 template <typename SlotFn>
 __device__ __forceinline__ void stage_rows_issue(const VerifyParams& p, Scratch& sc, int n, SlotFn slot_of,
@@ -667,7 +669,15 @@ __device__ __forceinline__ void stage_rows_issue(const VerifyParams& p, Scratch&
   fence_proxy_async();
   if (lane == 0) mbar_arrive_expect_tx(sc.bar, rb * (uint32_t)n);
   __syncwarp();
-  if (lane < n) bulk_g2s(sc.buf + (size_t)lane * rb, partial_row(p, slot_of(lane)), rb, sc.bar);
+  const int sl = lane < n ? slot_of(lane) : 0;
+  const int prev = __shfl_up_sync(0xFFFFFFFFu, sl, 1);
+  const bool start = lane < n && (lane == 0 || sl != prev + 1);
+  const unsigned starts = __ballot_sync(0xFFFFFFFFu, start);
+  if (start) {
+    const unsigned later = lane < 31 ? starts & ~((2u << lane) - 1u) : 0u;
+    const int end = later ? __ffs(later) - 1 : n;
+    bulk_g2s(sc.buf + (size_t)lane * rb, partial_row(p, sl), rb * (uint32_t)(end - lane), sc.bar);
+  }
 }
 template <typename SlotFn>
 __device__ __forceinline__ bool stage_rows(const VerifyParams& p, Scratch& sc, int n, SlotFn slot_of, int lane) {
@@ -1147,11 +1157,15 @@ __global__ void __launch_bounds__(VR_THREADS, 1) verify_rows_kernel(VerifyParams
       bool valid;
       // the draft-distribution flags of the request's L positions, loaded
       // together with its offsets (they do not depend on its length)
-      uint8_t f[SPEC_MAX_L];
+      uint32_t zf = 0;  // bit i: position i + 1 carries a draft distribution (flag 0)
       if (MODE == MODE_CHAIN_SAMPLE && p.use_q && p.pm) {
         const uint8_t* pmr = p.pm + (int64_t)r * p.L;
+        uint8_t f[SPEC_MAX_L];
 #pragma unroll
         for (int i = 0; i < SPEC_MAX_L; ++i) f[i] = i < p.L ? pmr[i] : (uint8_t)1;
+#pragma unroll
+        for (int i = 0; i < SPEC_MAX_L; ++i) zf |= (f[i] == 0 ? 1u : 0u) << i;
+        asm volatile("" ::"r"(zf));  // keeps these loads beside the offsets' (not sunk past their use)
       }
       if (MODE == MODE_TREE) {
         len = b1 - b0;
@@ -1164,15 +1178,10 @@ __global__ void __launch_bounds__(VR_THREADS, 1) verify_rows_kernel(VerifyParams
         cnt = valid ? len + 1 : 0;
         if (valid && MODE == MODE_CHAIN_SAMPLE && p.use_q && p.pm) {
           // the positions that carry a draft distribution
-          bool beyond = false;
-#pragma unroll
-          for (int i = 0; i < SPEC_MAX_L; ++i)
-            if (i < len && f[i] == 0) {
-              if (i < p.K)
-                qm |= 1u << i;
-              else
-                beyond = true;
-            }
+          const uint32_t within = len >= 32 ? 0xFFFFFFFFu : (1u << len) - 1u;
+          const uint32_t kmask = p.K >= 32 ? 0xFFFFFFFFu : (1u << p.K) - 1u;
+          qm = zf & within & kmask;
+          const bool beyond = (zf & within & ~kmask) != 0u;
           if (beyond && blockIdx.x == 0) set_status(p.ws.status, SPEC_DEV_BAD_LENGTH);
           cnt += __popc(qm);
         }
@@ -1651,7 +1660,10 @@ void set_chunks(spec::VerifyParams& p, int dtype, const spec_workspace* ws) {
   const int ch = dtype == SPEC_BF16 ? spec::Vec<1>::CH : spec::Vec<0>::CH;
   p.nch = (p.vocab + ch - 1) / ch;
   p.rowf = (p.nch + 2) & ~1;
-  p.pstride = spec_partial_stride(ws->units);
+  // the call's rows lie rowf apart (<= the workspace's stride for the finest
+  // chunking), so consecutive slots are one contiguous block
+  p.pstride = p.rowf;
+  (void)ws;
 }
 
 }  // namespace
