@@ -78,7 +78,8 @@ def source_hash(paths):
 
 def measured_traffic(kernel, workload):
     """DRAM bytes per launch of `kernel` on `workload` from the committed ncu summary
-    (profiles/traffic.json), or None when the kernel's sources changed since."""
+    (profiles/traffic.json), or None when the kernel's sources changed since (or
+    no capture of that launch exists)."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
@@ -510,9 +511,15 @@ def measure_bs4(S, torch, W, steps, warmup, hbm, rate, probabilistic=False):
            "components_us": {k: round(v, 3) for k, v in comp.items()},
            "verify_roofline_frac": round(ver_bytes / (comp["verify"] * 1e-6) / 1e9 / hbm, 4),
            "status_clean": all(int(r.ws.status()) == 0 for r in rounds)}
+    wl = f"edit_bs4 {'probabilistic ' if probabilistic else ''}rate {rate:.2f}"
+    out["verify_traffic"] = measured_traffic(
+        "verify_rows_kernel<bf16, sampled>" if probabilistic else "verify_rows_kernel<bf16, greedy>", wl)
+    out["verify_algorithmic_bytes"] = ver_bytes
     if probabilistic:
         out["extension_tail_share"] = float(((source == 3) & (first.chain_len.cpu().numpy() > K)).mean())
         out["sample_drafts_roofline_frac"] = round(B * K * V * 2 / (comp["sample_drafts"] * 1e-6) / 1e9 / hbm, 4)
+        out["sample_drafts_traffic"] = measured_traffic("verify_rows_kernel<bf16, drafting>", wl)
+        out["resample_traffic"] = measured_traffic("resample_kernel<bf16>", wl)
     del rounds
     return out
 
@@ -564,6 +571,8 @@ def measure_long_sampled(S, torch, W, steps, warmup, hbm):
             "ms_per_step": ms / steps, "steps": steps, "verified_tokens_per_step": n_tok,
             "verify_rows_per_step": n_rows, "components_us": {k: round(v, 3) for k, v in comp.items()},
             "verify_roofline_frac": round(achieved / hbm, 4),
+            "verify_algorithmic_bytes": n_rows * V * 4,
+            "verify_traffic": measured_traffic("verify_rows_kernel<fp32, sampled>", "long_bs64"),
             "status_clean": all(int(r.ws.status()) == 0 for r in rounds),
             "l2": "2 rotating input sets (2 x 622 MB > L2)"}
 
@@ -838,14 +847,15 @@ def run_once():
 
 def once_verify_launches(S, torch, W):
     """One chain verification each, after its round's draft + price: batch-4 code
-    editing at T = 0 (40 bf16 rows), batch-4 code editing at T = 1 with drafts
-    sampled on the device (bf16 target and draft rows; the sampled kernel and
-    the max(0, p - q) draw), and the batch-64 long-context workload at T = 0.7
-    (fp32, 16 rows per request), for a profiler.  Returns the verify rows of each."""
+    editing at the 30 % edit rate at T = 0 (bf16 rows), the same at T = 1 with
+    drafts sampled on the device (bf16 target and draft rows; the sampled
+    kernel and the max(0, p - q) draw), and the batch-64 long-context workload
+    at T = 0.7 (fp32, 16 rows per request), for a profiler.  Returns the verify
+    rows of each."""
     from speculative_decoding_draft_spec_gb300.round import ChainRound
 
     out = {}
-    c = W.edit_bs4()
+    c = W.edit_bs4(edit_rates=[0.3] * 4)
     rnd = ChainRound(c["B"], c["hist"].shape[1], c["K"], c["L"], c["V"], torch.bfloat16, c["B"] * (c["L"] + 1),
                      c["coef"], c["n_min"], c["n_max"], c["copy_cap"])
     rnd.load(c["hist"], c["hist_len"], c["d"], c["c"], c["d_len"])
@@ -855,8 +865,8 @@ def once_verify_launches(S, torch, W):
     rnd.logits[:n].copy_(torch.from_numpy(W.compact_logits(c, ro, vl).view(np.int16)).view(torch.bfloat16))
     rnd.verify(temperature=0.0)
     torch.cuda.synchronize()
-    out["edit_bs4"] = n
-    c = W.edit_bs4(temperature=1.0, probabilistic=True)
+    out["edit_bs4 rate 0.30"] = n
+    c = W.edit_bs4(temperature=1.0, probabilistic=True, edit_rates=[0.3] * 4)
     rnd = ChainRound(c["B"], c["hist"].shape[1], c["K"], c["L"], c["V"], torch.bfloat16, c["B"] * (c["L"] + 1),
                      c["coef"], c["n_min"], c["n_max"], c["copy_cap"], with_draft=True)
     rnd.load(c["hist"], c["hist_len"], c["d"], c["c"], c["d_len"])
@@ -868,7 +878,7 @@ def once_verify_launches(S, torch, W):
     rnd.logits[:n].copy_(torch.from_numpy(W.compact_logits(c, ro, vl).view(np.int16)).view(torch.bfloat16))
     rnd.verify(temperature=1.0, seed=0, step=0)
     torch.cuda.synchronize()
-    out["edit_bs4_probabilistic"] = n
+    out["edit_bs4 probabilistic rate 0.30"] = n
     c = W.long_bs64()
     rows = c["rows_per_request"]
     rnd = ChainRound(c["B"], c["hist"].shape[1], c["K"], c["L"], c["V"], torch.float32, c["B"] * rows, c["coef"],

@@ -1313,32 +1313,41 @@ __global__ void __launch_bounds__(VR_THREADS, 1) verify_rows_kernel(VerifyParams
     if ((MODE == MODE_CHAIN_GREEDY || MODE == MODE_TREE) && run_slot >= 0 && run_key != 0ull && lane == 0)
       atomicMax(&p.ws.rowkey[run_slot], run_key);
   };
-  auto flush_request = [&]() {
-    if (run_r < 0) return;
-    uint32_t* ctr = MODE == MODE_DRAFT ? &p.ws.counter3[run_r] : &p.ws.counter[run_r];
+  // a request's arrival: true for the warp that completes it
+  auto arrive = [&]() -> bool {
     int last = 0;
     if (lane == 0) {
       // release this warp's partials / row keys, acquire everyone else's
+      uint32_t* ctr = MODE == MODE_DRAFT ? &p.ws.counter3[run_r] : &p.ws.counter[run_r];
       const uint32_t need = MODE == MODE_DRAFT ? nch : (uint32_t)(s_pre[run_r + 1] - s_pre[run_r]) * nch;
       const uint32_t old = atomic_add_acq_rel(ctr, run_units);
       last = (old + run_units == need);
     }
     last = __shfl_sync(0xFFFFFFFFu, last, 0);
-    if (last) {
-      __syncwarp();  // orders every lane after lane 0's acquire
-      if (MODE == MODE_TREE)
-        finalize_tree(p, run_r, s_base[run_r], s_len[run_r], lane);
-      else if (MODE == MODE_CHAIN_GREEDY)
-        finalize_chain_greedy<DT>(p, run_r, s_base[run_r], s_len[run_r], lane);
-      else if (MODE == MODE_CHAIN_SAMPLE)
-        finalize_chain_sample<DT>(p, run_r, s_base[run_r], s_len[run_r], s_qm[run_r], lane, sc);
-      else
-        finalize_draft<DT>(p, run_r, lane, sc);
-      if (lane == 0) *ctr = 0u;
-    }
+    if (last) __syncwarp();  // orders every lane after lane 0's acquire
+    return last != 0;
+  };
+  auto finalize = [&](int r) {
+    if (MODE == MODE_TREE)
+      finalize_tree(p, r, s_base[r], s_len[r], lane);
+    else if (MODE == MODE_CHAIN_GREEDY)
+      finalize_chain_greedy<DT>(p, r, s_base[r], s_len[r], lane);
+    else if (MODE == MODE_CHAIN_SAMPLE)
+      finalize_chain_sample<DT>(p, r, s_base[r], s_len[r], s_qm[r], lane, sc);
+    else
+      finalize_draft<DT>(p, r, lane, sc);
+    if (lane == 0) *(MODE == MODE_DRAFT ? &p.ws.counter3[r] : &p.ws.counter[r]) = 0u;
   };
 
+  // The stream runs in an inner loop; a request this warp completes in the
+  // middle of its range leaves that loop and is finalized between two chunks,
+  // so the finalizer's code lies outside the loop body and the loop's own code
+  // stays contiguous (a finalizer inlined inside the loop body measured as
+  // instruction-cache misses on every warp of small launches).
   int item = (int)(lo / nch), u = (int)(lo - (uint32_t)item * nch);
+  int pend = -1;  // a request completed by this warp, to finalize
+  bool ended = false;
+  while (!ended) {
   for (; w < hi; ++w) {
     locate<MODE>(p, s_pre, s_base, s_len, s_qm, item, esz, cc);
     if (cc.slot != run_slot) {
@@ -1349,9 +1358,14 @@ __global__ void __launch_bounds__(VR_THREADS, 1) verify_rows_kernel(VerifyParams
         run_y = cc.pos <= s_len[cc.r] ? __ldcg(p.chain + (int64_t)cc.r * p.L + cc.pos - 1) : -1;
     }
     if (cc.r != run_r) {
-      flush_request();
+      const bool last = run_r >= 0 && arrive();
+      const int done_r = run_r;
       run_r = cc.r;
       run_units = 0;
+      if (last) {
+        pend = done_r;
+        break;
+      }
     }
     const int e0 = u * CH;
     const int n_el = min(CH, p.vocab - e0);
@@ -1422,6 +1436,17 @@ __global__ void __launch_bounds__(VR_THREADS, 1) verify_rows_kernel(VerifyParams
     }
     ph ^= 1u;
   }
+  if (aborted) break;
+  if (pend < 0) {  // the range is done: the last request's arrival
+    flush_row();
+    if (run_r >= 0 && arrive()) pend = run_r;
+    ended = true;
+  }
+  if (pend >= 0) {
+    finalize(pend);
+    pend = -1;
+  }
+  }
   if (aborted) {
     // a copy did not land in time: record it, wait (bounded) once more for
     // the copy this warp has in flight, and stop without finalizing
@@ -1432,46 +1457,11 @@ __global__ void __launch_bounds__(VR_THREADS, 1) verify_rows_kernel(VerifyParams
     __syncwarp();
     return;
   }
-  flush_row();
-  flush_request();
   if (SAMPLED && sc.dead && lane == 0) mbar_wait_bounded(sc.bar, sc.phase ^ 1u, SPEC_WAIT_POLLS);  // the copy given up on
   if (bad && lane == 0) set_status(p.ws.status, SPEC_DEV_NONFINITE);
 }
 
 // ------------------------------------------------------------------ draw from max(0, p - q)
-// Block-wide helpers of resample_kernel (RS_THREADS threads).
-// inclusive prefix over the block's threads in thread order; *total = the sum
-__device__ __forceinline__ float block_incl_scan(float v, float* s_w, float* total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const float wi = warp_incl_scan(v);
-  if (lane == 31) s_w[warp] = wi;
-  __syncthreads();
-  float before = 0.0f, all = 0.0f;
-#pragma unroll
-  for (int q = 0; q < RS_THREADS / 32; ++q) {
-    const float t = s_w[q];
-    if (q < warp) before += t;
-    all += t;
-  }
-  __syncthreads();  // s_w free again
-  *total = all;
-  return before + wi;
-}
-// the first (last) thread whose predicate holds, or -1
-__device__ __forceinline__ int block_first(bool pred, int* s_i, bool last) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const unsigned b = __ballot_sync(0xFFFFFFFFu, pred);
-  if (lane == 0) s_i[warp] = b ? 32 * warp + (last ? 31 - __clz(b) : __ffs(b) - 1) : -1;
-  __syncthreads();
-  int m = -1;
-#pragma unroll
-  for (int q = 0; q < RS_THREADS / 32; ++q) {
-    const int t = s_i[q];
-    if (t >= 0 && (m < 0 || (last ? t > m : t < m))) m = t;
-  }
-  __syncthreads();
-  return m;
-}
 // N consecutive entries of a row from entry e (fp32; -inf past the row's end)
 template <int DT, int N>
 __device__ __forceinline__ void load_entries(const void* row, int e, int vocab, bool vec, float (&x)[N]) {
@@ -1503,20 +1493,23 @@ __device__ __forceinline__ void load_entries(const void* row, int e, int vocab, 
 }
 
 // One CTA per (chunk c, request r) with a record: the chunk's mass of
-// max(0, p - q) at the rejected position, summed over the block; the last
-// CTA of the request (arrival counter) locates the crossing chunk over those
-// masses at u' of their total (p itself when the mass is at most 1e-30), then
-// the crossing entry inside it, each thread holding PER consecutive entries.
+// max(0, p - q) at the rejected position (warp sums, then one exchange); the
+// last CTA of the request (arrival counter) draws: warp 0 locates the crossing
+// chunk over the chunks' masses at u' of their total (p itself when that mass
+// is at most 1e-30), then every thread takes PER consecutive entries of that
+// chunk, and the one thread whose running range holds the crossing (or, when
+// rounding leaves none, holds the last entry with mass) walks its entries and
+// writes the token.  Every step but the walk is warp-wide: six CTA barriers.
 template <int DT>
 __global__ void __launch_bounds__(RS_THREADS) resample_kernel(VerifyParams p) {
   constexpr int CH = Vec<DT>::CH, PER = CH / RS_THREADS;  // 16 bf16 / 8 fp32 entries per thread
+  constexpr int NW = RS_THREADS / 32;
   constexpr size_t ESZ = DT == 1 ? 2 : 4;
   __shared__ __align__(16) Record s_rec;
-  __shared__ float s_w[RS_THREADS / 32];
-  __shared__ int s_i[RS_THREADS / 32];
-  __shared__ int s_last;
-  __shared__ float s_f[2];
-  const int tid = threadIdx.x;
+  __shared__ float s_w[NW];
+  __shared__ int s_last, s_cx;
+  __shared__ float s_t[3];  // the crossing chunk's weight before it (-1: last mode), the total, t
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int c = blockIdx.x, r = blockIdx.y;
   if (tid < 4)
     reinterpret_cast<uint4*>(&s_rec)[tid] =
@@ -1544,9 +1537,13 @@ __global__ void __launch_bounds__(RS_THREADS) resample_kernel(VerifyParams p) {
     float sum = 0.0f;
 #pragma unroll
     for (int j = 0; j < PER; ++j) sum += resid(zp[j], zq[j]);
-    float tot;
-    block_incl_scan(sum, s_w, &tot);
+    sum = warp_sum(sum);
+    if (lane == 0) s_w[warp] = sum;
+    __syncthreads();
     if (tid == 0) {
+      float tot = 0.0f;
+#pragma unroll
+      for (int q = 0; q < NW; ++q) tot += s_w[q];
       __stcg(&masses[c], tot);
       // release this chunk's mass, acquire the others'
       s_last = atomic_add_acq_rel(&p.ws.counter2[r], 1u) + 1u == (uint32_t)p.nch;
@@ -1554,28 +1551,45 @@ __global__ void __launch_bounds__(RS_THREADS) resample_kernel(VerifyParams p) {
     __syncthreads();
     if (!s_last) return;
   }
-  // ---- the last CTA of request r draws
-  float w = tid < p.nch ? __ldcg(&masses[tid]) : 0.0f;
-  float total;
-  float incl = block_incl_scan(w, s_w, &total);
-  const bool fallback = !(total > 1e-30f);
-  if (fallback) {  // no residual mass: the draw falls back to p
-    w = 0.0f;
-    if (tid < p.nch) {
-      const float2 t = __ldcg(&partial_row(p, rec.prow)[tid]);
-      w = t.y * ex2((t.x - rec.mp) * p.c) * ip;
+  // ---- the last CTA of request r draws.  Warp 0: the crossing chunk over the
+  // masses (8 per lane at most; p's chunk weights when the residual is empty)
+  if (warp == 0) {
+    const int per = (p.nch + 31) / 32;
+    float wl[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int cc = per * lane + q;
+      wl[q] = (q < per && cc < p.nch) ? __ldcg(&masses[cc]) : 0.0f;
     }
-    incl = block_incl_scan(w, s_w, &total);
+    Crossing cr = find_chunk(wl, per, rec.u2, lane);
+    const int fallback = !(cr.total > 1e-30f);
+    if (fallback) {  // no residual mass: the draw falls back to p
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const int cc = per * lane + q;
+        float w = 0.0f;
+        if (q < per && cc < p.nch) {
+          const float2 t = __ldcg(&partial_row(p, rec.prow)[cc]);
+          w = t.y * ex2((t.x - rec.mp) * p.c) * ip;
+        }
+        wl[q] = w;
+      }
+      cr = find_chunk(wl, per, rec.u2, lane);
+    }
+    if (lane == 0) {
+      s_cx = cr.unit | (fallback << 30);
+      s_t[0] = cr.before;
+      s_t[1] = cr.total;
+      s_t[2] = cr.t;
+    }
   }
-  const float t = rec.u2 * total;
-  int cx = block_first(incl > t && w > 0.0f, s_i, false);
-  const bool last_mode = cx < 0;  // t at or above the total (rounding): the last entry with mass
-  if (last_mode) cx = block_first(w > 0.0f, s_i, true);
-  if (cx < 0) cx = 0;
-  if (tid == cx) s_f[0] = incl - w;
   __syncthreads();
-  const float tt = last_mode ? INFINITY : t - s_f[0];
-  // the crossing chunk's entries
+  const int cx = s_cx & 0x3FFFFFFF;
+  const bool fallback = (s_cx >> 30) != 0;
+  const float before = s_t[0], total = s_t[1];
+  const bool last_mode = before < 0.0f;  // t at or above the total: the last entry with mass
+  const float tt = last_mode ? INFINITY : s_t[2] - before;
+  // ---- the crossing chunk's entries, PER consecutive ones per thread
   float wv[PER], sum = 0.0f;
   {
     float zp[PER], zq[PER];
@@ -1587,31 +1601,56 @@ __global__ void __launch_bounds__(RS_THREADS) resample_kernel(VerifyParams p) {
       sum += wv[j];
     }
   }
-  float all;
-  const float inc2 = block_incl_scan(sum, s_w, &all);
-  int th = block_first(inc2 > tt && sum > 0.0f, s_i, false);
-  const bool none = th < 0;
-  if (none) th = block_first(sum > 0.0f, s_i, true);
-  if (tid == (th < 0 ? 0 : th)) {
+  // this thread's running weight over the chunk, in thread order: excl is
+  // the previous thread's incl bit for bit (a shuffle within the warp, the same
+  // sums across warps), so the ranges [excl, incl) tile [0, ctot) exactly
+  const float winc = warp_incl_scan(sum);
+  const float wprev = __shfl_up_sync(0xFFFFFFFFu, winc, 1);
+  if (lane == 31) s_w[warp] = winc;
+  if (tid == 0) s_last = -1;  // (read again below as the writer's key)
+  __syncthreads();
+  float wbefore = 0.0f, ctot = 0.0f;
+#pragma unroll
+  for (int q = 0; q < NW; ++q) {
+    const float t = s_w[q];
+    if (q < warp) wbefore += t;
+    ctot += t;
+  }
+  const float incl = wbefore + winc, excl = lane == 0 ? wbefore : wbefore + wprev;
+  // the writer: the thread whose range holds the crossing (one at most), else
+  // the last thread with mass; a key picks exactly one (rounding could leave
+  // several threads at the total)
+  const float tc = fmaxf(tt, 0.0f);
+  const bool cross = !last_mode && sum > 0.0f && excl <= tc && tc < incl;
+  const bool lastpos = sum > 0.0f && incl == ctot && (last_mode || !(tc < ctot));
+  if (cross || lastpos) atomicMax(&s_last, cross ? RS_THREADS + tid : tid);
+  __syncthreads();
+  const int key = s_last;
+  if (key >= 0 && tid == (key & (RS_THREADS - 1))) {
     int pick = -1, lp = -1;
-    float wp = 0.0f, lw = 0.0f, run = inc2 - sum;
+    float wp = 0.0f, lw = 0.0f, run = excl;
 #pragma unroll
     for (int j = 0; j < PER; ++j)
       if (wv[j] > 0.0f) {
         run += wv[j];
-        if (pick < 0 && !none && run > tt) {
+        if (pick < 0 && key >= RS_THREADS && run > tc) {
           pick = j;
           wp = wv[j];
         }
         lp = j;
         lw = wv[j];
       }
-    if (pick < 0) {  // rounding, or no crossing: the last entry with mass
-      pick = lp < 0 ? 0 : lp;
+    if (pick < 0) {  // rounding inside the thread, or the last entry with mass
+      pick = lp;
       wp = lw;
     }
     p.out_tokens[(int64_t)r * (p.L + 1) + rec.pos - 1] = cx * CH + PER * tid + pick;
     if (p.dbg_resid) p.dbg_resid[r] = wp / total;
+  } else if (key < 0 && tid == 0) {  // no entry of the chunk has mass (not reached in exact arithmetic)
+    p.out_tokens[(int64_t)r * (p.L + 1) + rec.pos - 1] = cx * CH;
+    if (p.dbg_resid) p.dbg_resid[r] = 0.0f;
+  }
+  if (tid == 0) {
     reinterpret_cast<Record*>(p.ws.record)[r].flag = 0;
     p.ws.counter2[r] = 0u;
   }
