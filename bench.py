@@ -9,9 +9,10 @@ V = 151936 bf16 logits, T = 0); its logits are synthetic, laid out exactly as
 the allocation asks (the target forward itself is not part of the path).
 
 Timing: one CUDA graph holds a pass of 30 rounds rotating over the input
-sets (the launches in order on one stream) and each set's round is also a
-graph of its own; W warm-up steps, then K steps of graph replays (passes,
-then single rounds for the remainder) between a barrier and a device synchronisation,
+sets (the launches in order on one stream) and one more holds the rounds of K
+past the last whole pass (all K when K < 30); each graph runs once untimed,
+then W warm-up steps, then K steps of graph replays (passes, then the tail)
+between a barrier and a device synchronisation,
 with CUDA events on the launching stream around them (replays keep the device
 queue ahead of the host, so the events time the kernels, not host launch
 gaps); three input sets rotate so that every step reads logits that are not
@@ -356,9 +357,10 @@ def timed_parts(torch, sets, names, steps, warmup, barrier=lambda: None, sampler
     (a whole number of rotations over the sets, step i on set i % len(sets),
     each step's launches in order on one stream, so consecutive steps run back
     to back as they would inside a captured decode step, without a graph
-    launch between them), and every set's single step is a graph of its own.
-    W untimed steps, then `steps` timed steps between a barrier and a device
-    synchronisation: whole passes, then the remaining steps' single graphs;
+    launch between them), and one more graph holds the steps of `steps` past
+    the last whole pass (for steps < PASS_STEPS, all of them).  Each graph
+    runs once untimed, then W untimed steps, then `steps` timed steps between
+    a barrier and a device synchronisation: whole passes, then the tail graph;
     CUDA events on the launching stream around the region.
 
     Per-component times: for each component, one graph of `launches`
@@ -376,14 +378,24 @@ def timed_parts(torch, sets, names, steps, warmup, barrier=lambda: None, sampler
     steps_g = [capture(torch, lambda st, fns=fns: [f(st) for f in fns]) for fns in sets]
     per = nset * max(1, PASS_STEPS // nset)
     pass_g = capture(torch, lambda st: [f(st) for i in range(per) for f in sets[i % nset]])
+    _, tail = step_plan(steps, nset, per)
+    tail_g = capture(torch, lambda st: [f(st) for i in tail for f in sets[i]]) if tail else None
 
-    def run(n):
+    def run(n, tail_graph=None):
         passes, singles = step_plan(n, nset, per)
         for _ in range(passes):
             pass_g.replay()
-        for i in singles:
-            steps_g[i].replay()
+        if tail_graph is not None:
+            tail_graph.replay()
+        else:
+            for i in singles:
+                steps_g[i].replay()
 
+    # warm-up: every graph the timed region replays runs once first (so no
+    # graph upload falls inside it), then the W warm-up steps
+    pass_g.replay()
+    if tail_g is not None:
+        tail_g.replay()
     run(warmup)
     torch.cuda.synchronize()
     barrier()
@@ -391,7 +403,7 @@ def timed_parts(torch, sets, names, steps, warmup, barrier=lambda: None, sampler
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with (sampler if sampler is not None else contextlib.nullcontext()):
         t_start.record(stream)
-        run(steps)
+        run(steps, tail_g)
         t_end.record(stream)
         torch.cuda.synchronize()
     barrier()
