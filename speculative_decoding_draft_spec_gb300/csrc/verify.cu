@@ -519,122 +519,140 @@ __device__ __forceinline__ Crossing find_chunk(const float (&wl)[8], int per, fl
   return c;
 }
 
-// the weight 2^(z c - mc) of a logit z (0 for -inf: 2^-inf = +0) and 0 for
-// entry `skip`; computed unconditionally and then selected, so that a run of
-// weights compiles to straight-line code whose exponentials overlap
-struct SoftW {
-  float c, mc;
-  int skip;
-  __device__ __forceinline__ float operator()(int e, float x) const {
-    const float w = ex2(fmaf(x, c, -mc));
-    return e == skip ? 0.0f : w;
-  }
-};
+// A chunk staged in shared memory, seen as 16 steps of 32 x PER consecutive
+// entries (32 vectors of 16 bytes each).  Lanes 2k and 2k + 1 sum the two
+// halves of step k, 16 vectors each, in a rolled loop whose reads are rotated
+// by k (odd lanes by k + 4) so that each quarter-warp's 16-byte reads fall in
+// distinct banks; one pair shuffle then gives the step totals, and the
+// crossing step is read once more as vector `lane` of that step.  Entries that
+// take no part hold -inf in the stage (a chunk's tail past the row, an entry
+// left out), so no entry carries a test.  The finalizing warp runs this once,
+// alone on its scheduler: compact code (a rolled loop, few cold instruction
+// lines) with overlapping exponentials inside an iteration is what counts.
 
+// entry i (< PER) of a vector
 template <int DT>
-__device__ __forceinline__ float word_entry(uint32_t word, int h) {
-  if (DT == 1) return h ? bf16_hi(word) : bf16_lo(word);
-  return __uint_as_float(word);
+__device__ __forceinline__ float vec_entry(const uint4& x, int i) {
+  constexpr int EW = DT == 1 ? 2 : 1;  // entries per word
+  const int q = i / EW;
+  const uint32_t w = q == 0 ? x.x : q == 1 ? x.y : q == 2 ? x.z : x.w;
+  return DT == 1 ? ((i & 1) ? bf16_hi(w) : bf16_lo(w)) : __uint_as_float(w);
 }
 
-// A chunk staged in shared memory, lane l owning entries [E l, E l + E)
-// (E = entries per chunk / 32).  chunk_lane_sum: the lane's total weight.  The
-// lane's 32-bit words are read in an order rotated by the lane (the warp's
-// reads fall in distinct banks), eight words at a time, and their weights are
-// independent terms summed by a tree: one warp alone on its scheduler runs
-// this, so its dependency chains are what the time is.
-template <int DT, typename WF>
-__device__ __forceinline__ float chunk_lane_sum(const uint32_t* wbuf, int n_el, int lane, WF wf) {
-  constexpr int EW = DT == 1 ? 2 : 1;  // entries per word
-  constexpr int E = Vec<DT>::CH / 32;  // entries per lane
-  constexpr int WPL = E / EW;          // words per lane (64)
-  constexpr int BW = 8;                // words per batch
-  float s = 0.0f;
-  for (int j0 = 0; j0 < WPL; j0 += BW) {
-    uint32_t word[BW];
+// the weights 2^(z c - mc) of a vector, summed as a tree
+template <int DT>
+__device__ __forceinline__ float vec_weight(const uint4& x, float mc, float c) {
+  constexpr int PER = Vec<DT>::PER;
+  float t[PER];
 #pragma unroll
-    for (int b = 0; b < BW; ++b) word[b] = wbuf[lane * WPL + ((j0 + b + lane) & (WPL - 1))];
-    float t[BW * EW];
+  for (int i = 0; i < PER; ++i) t[i] = ex2(fmaf(vec_entry<DT>(x, i), c, -mc));  // 2^-inf = +0
 #pragma unroll
-    for (int b = 0; b < BW; ++b)
+  for (int h = PER / 2; h > 0; h >>= 1)
 #pragma unroll
-      for (int h = 0; h < EW; ++h) {
-        const int e = E * lane + EW * ((j0 + b + lane) & (WPL - 1)) + h;
-        const float w = wf(e, word_entry<DT>(word[b], h));  // past n_el: stale words, selected away
-        t[b * EW + h] = e < n_el ? w : 0.0f;
-      }
-#pragma unroll
-    for (int h = BW * EW / 2; h > 0; h >>= 1)
-#pragma unroll
-      for (int k = 0; k < h; ++k) t[k] += t[k + h];
-    s += t[0];
+    for (int i = 0; i < h; ++i) t[i] += t[i + h];
+  return t[0];
+}
+
+// the lane's half-step sum (lane 2k + h: half h of step k)
+template <int DT>
+__device__ __forceinline__ float half_step_sum(const unsigned char* buf, float mc, float c, int lane) {
+  const int k = lane >> 1, h = lane & 1;
+  const uint4* base = reinterpret_cast<const uint4*>(buf) + 32 * k + 16 * h;
+  const int rot = k + 4 * h;
+  float s0 = 0.0f, s1 = 0.0f;
+#pragma unroll 2
+  for (int j = 0; j < 16; j += 2) {
+    s0 += vec_weight<DT>(base[(j + rot) & 15], mc, c);
+    s1 += vec_weight<DT>(base[(j + 1 + rot) & 15], mc, c);
   }
-  return s;
+  return s0 + s1;
+}
+
+// the warp total of a staged chunk's weights
+template <int DT>
+__device__ __forceinline__ float chunk_sum(const unsigned char* buf, float mc, float c, int lane) {
+  return warp_sum(half_step_sum<DT>(buf, mc, c, lane));
 }
 
 // Inverse CDF inside a staged chunk: the first entry whose running sum from
-// `before` exceeds t (before < 0: the last entry with weight), from the lane
-// sums (pass 1) and then the crossing lane's entries spread over the warp
-// (pass 2).  Returns the entry and *w_at its weight.
-template <int DT, typename WF>
-__device__ int chunk_draw(const unsigned char* buf, int n_el, int lane, float before, float t, float* w_at, WF wf) {
-  constexpr int EW = DT == 1 ? 2 : 1;
-  constexpr int E = Vec<DT>::CH / 32;
-  constexpr int F = E / 32;  // the crossing lane's entries per lane in pass 2 (4 / 2)
-  const uint32_t* wbuf = reinterpret_cast<const uint32_t*>(buf);
-  const float lsum = chunk_lane_sum<DT>(wbuf, n_el, lane, wf);
-  const float incl = warp_incl_scan(lsum);
-  const float tr = t - before;
-  const unsigned hit = before < 0.0f ? 0u : __ballot_sync(0xFFFFFFFFu, incl > tr && lsum > 0.0f);
-  const unsigned has = __ballot_sync(0xFFFFFFFFu, lsum > 0.0f);
-  int src;
-  float tl;
+// `before` exceeds t (before < 0, or no crossing after rounding: the last
+// entry with weight), by the step whose running total crosses it and then the
+// entry inside that step.  Weights 2^(z c - mc).  Returns the entry and *w_at
+// its weight.
+template <int DT>
+__device__ int chunk_draw(const unsigned char* buf, int lane, float before, float t, float* w_at, float mc, float c) {
+  constexpr int PER = Vec<DT>::PER;
+  const float hs = half_step_sum<DT>(buf, mc, c, lane);
+  const float stot = hs + __shfl_xor_sync(0xFFFFFFFFu, hs, 1);
+  const float st = __shfl_sync(0xFFFFFFFFu, stot, (2 * lane) & 31);
+  const float sk = lane < 16 ? st : 0.0f;  // lane k: step k's total
+  const float incl = warp_incl_scan(sk);
+  const float tl = before < 0.0f ? INFINITY : t - before;
+  const unsigned has = __ballot_sync(0xFFFFFFFFu, sk > 0.0f);
+  const unsigned hit = __ballot_sync(0xFFFFFFFFu, incl > tl && sk > 0.0f);  // none for tl = INFINITY
+  int ks;
+  float t2;
   if (hit) {
-    src = __ffs(hit) - 1;
-    tl = tr - __shfl_sync(0xFFFFFFFFu, incl - lsum, src);
+    ks = __ffs(hit) - 1;
+    t2 = tl - __shfl_sync(0xFFFFFFFFu, incl - sk, ks);
   } else {
-    src = has ? 31 - __clz(has) : 0;
-    tl = INFINITY;  // no crossing: the last entry with weight
+    ks = has ? 31 - __clz(has) : 0;
+    t2 = INFINITY;
   }
-  float wv[F], s2 = 0.0f;
+  const uint4 x = reinterpret_cast<const uint4*>(buf)[32 * ks + lane];
+  const int e = PER * (32 * ks + lane);
+  float wv[PER], ls = 0.0f;
 #pragma unroll
-  for (int f = 0; f < F; ++f) {
-    const int e = E * src + F * lane + f;
-    const float w = wf(e, word_entry<DT>(wbuf[e / EW], e % EW));  // e < 4096: inside the stage
-    wv[f] = e < n_el ? w : 0.0f;
-    s2 += w;
+  for (int i = 0; i < PER; ++i) {
+    wv[i] = ex2(fmaf(vec_entry<DT>(x, i), c, -mc));
+    ls += wv[i];
   }
-  const float inc2 = warp_incl_scan(s2);
-  const unsigned hit2 = __ballot_sync(0xFFFFFFFFu, inc2 > tl && s2 > 0.0f);
+  const float inc2 = warp_incl_scan(ls);
+  const unsigned hit2 = __ballot_sync(0xFFFFFFFFu, inc2 > t2 && ls > 0.0f);
   int pick = -1, lp = -1;
-  float wp = 0.0f, lw = 0.0f, run = inc2 - s2;
+  float wp = 0.0f, lw = 0.0f, run = inc2 - ls;
 #pragma unroll
-  for (int f = 0; f < F; ++f)
-    if (wv[f] > 0.0f) {
-      run += wv[f];
-      if (pick < 0 && run > tl) {
-        pick = E * src + F * lane + f;
-        wp = wv[f];
+  for (int i = 0; i < PER; ++i)
+    if (wv[i] > 0.0f) {
+      run += wv[i];
+      if (pick < 0 && run > t2) {
+        pick = e + i;
+        wp = wv[i];
       }
-      lp = E * src + F * lane + f;
-      lw = wv[f];
+      lp = e + i;
+      lw = wv[i];
     }
-  int lane2;
+  int src;
   if (hit2) {
-    lane2 = __ffs(hit2) - 1;
+    src = __ffs(hit2) - 1;
     if (pick < 0) {  // rounding inside the lane: its last entry with weight
       pick = lp;
       wp = lw;
     }
   } else {
     const unsigned h2 = __ballot_sync(0xFFFFFFFFu, lp >= 0);
-    lane2 = h2 ? 31 - __clz(h2) : 0;
+    src = h2 ? 31 - __clz(h2) : 0;
     pick = lp;
     wp = lw;
   }
-  pick = __shfl_sync(0xFFFFFFFFu, pick, lane2);
-  *w_at = __shfl_sync(0xFFFFFFFFu, wp, lane2);
+  pick = __shfl_sync(0xFFFFFFFFu, pick, src);
+  *w_at = __shfl_sync(0xFFFFFFFFu, wp, src);
   return pick < 0 ? 0 : pick;
+}
+
+// entry i of a staged chunk set to -inf (returns its bits) or back to `bits`
+template <int DT>
+__device__ __forceinline__ uint32_t stage_entry_swap(unsigned char* buf, int i, uint32_t bits) {
+  if (DT == 1) {
+    uint16_t* q = reinterpret_cast<uint16_t*>(buf) + i;
+    const uint32_t old = *q;
+    *q = (uint16_t)bits;
+    return old;
+  }
+  uint32_t* q = reinterpret_cast<uint32_t*>(buf) + i;
+  const uint32_t old = *q;
+  *q = bits;
+  return old;
 }
 
 // ------------------------------------------------------------------ finalizer scratch
@@ -690,24 +708,31 @@ template <int DT>
 __device__ __forceinline__ bool stage_chunk(const VerifyParams& p, Scratch& sc, const void* row, int e0, int n_el,
                                             int lane) {
   constexpr int ESZ = DT == 1 ? 2 : 4;
+  constexpr int CH = Vec<DT>::CH;
   if (p.vec_ok) {
     if (lane == 0) {
       mbar_arrive_expect_tx(sc.bar, (uint32_t)(n_el * ESZ));
       bulk_g2s(sc.buf, static_cast<const char*>(row) + (size_t)e0 * ESZ, (uint32_t)(n_el * ESZ), sc.bar);
     }
-    return scratch_wait(sc, p.ws.status, lane);
+    // the entries past the row hold -inf (bytes the copy does not write)
+    if (DT == 1) {
+      for (int i = n_el + lane; i < CH; i += 32) reinterpret_cast<uint16_t*>(sc.buf)[i] = (uint16_t)Vec<DT>::NEG;
+    } else {
+      for (int i = n_el + lane; i < CH; i += 32) reinterpret_cast<uint32_t*>(sc.buf)[i] = Vec<DT>::NEG;
+    }
+    return scratch_wait(sc, p.ws.status, lane);  // (a warp-wide vote: the stores above are ordered too)
   }
-  // rows off a 16-byte boundary: plain loads
+  // rows off a 16-byte boundary: plain loads, -inf past the row
   if (DT == 1) {
     const uint16_t* src = static_cast<const uint16_t*>(row) + e0;
     uint16_t* dst = reinterpret_cast<uint16_t*>(sc.buf);
 #pragma unroll 8
-    for (int i = lane; i < n_el; i += 32) dst[i] = __ldcg(src + i);
+    for (int i = lane; i < CH; i += 32) dst[i] = i < n_el ? __ldcg(src + i) : (uint16_t)Vec<DT>::NEG;
   } else {
-    const float* src = static_cast<const float*>(row) + e0;
-    float* dst = reinterpret_cast<float*>(sc.buf);
+    const uint32_t* src = reinterpret_cast<const uint32_t*>(static_cast<const float*>(row) + e0);
+    uint32_t* dst = reinterpret_cast<uint32_t*>(sc.buf);
 #pragma unroll 8
-    for (int i = lane; i < n_el; i += 32) dst[i] = __ldcg(src + i);
+    for (int i = lane; i < CH; i += 32) dst[i] = i < n_el ? __ldcg(src + i) : Vec<DT>::NEG;
   }
   __syncwarp();
   return true;
@@ -926,15 +951,19 @@ __device__ void finalize_chain_sample(const VerifyParams& p, int r, int base, in
     wl[q] = w;
   }
   Crossing cr = find_chunk(wl, per, u2s, lane);
-  int staged = -1;  // the chunk the scratch holds
+  int staged = -1;       // the chunk the scratch holds
+  bool y_out = false;    // y's entry of the staged chunk is -inf (its bits in lane 0's y_bits)
+  uint32_t y_bits = 0u;
   if (yv >= 0 && !(cr.total >= 0.0625f * s)) {
     // the residual mass is under 1/16 of the row's: y's chunk less y, summed
     // exactly instead of by the difference
     const int e0 = cy * CH, n_el = min(CH, p.vocab - e0);
     if (!stage_chunk<DT>(p, sc, row, e0, n_el, lane)) return;
     staged = cy;
-    const float w_y = warp_sum(chunk_lane_sum<DT>(reinterpret_cast<const uint32_t*>(sc.buf), n_el, lane,
-                                                  SoftW{p.c, mc, yv - e0}));
+    if (lane == 0) y_bits = stage_entry_swap<DT>(sc.buf, yv - e0, Vec<DT>::NEG);  // y left out
+    __syncwarp();
+    y_out = true;
+    const float w_y = chunk_sum<DT>(sc.buf, mc, p.c, lane);
 #pragma unroll
     for (int q = 0; q < 8; ++q)
       if (per * lane + q == cy) wl[q] = w_y;
@@ -950,9 +979,17 @@ __device__ void finalize_chain_sample(const VerifyParams& p, int r, int base, in
     cr = find_chunk(wl, per, u2s, lane);
   }
   const int e0 = cr.unit * CH, n_el = min(CH, p.vocab - e0);
-  if (staged != cr.unit && !stage_chunk<DT>(p, sc, row, e0, n_el, lane)) return;
+  if (staged != cr.unit) {
+    if (!stage_chunk<DT>(p, sc, row, e0, n_el, lane)) return;
+    y_out = false;
+  }
+  const bool want_out = remove && cr.unit == cy;  // the draw leaves y out
+  if (want_out != y_out) {
+    if (lane == 0) y_bits = stage_entry_swap<DT>(sc.buf, yv - e0, want_out ? Vec<DT>::NEG : y_bits);
+    __syncwarp();
+  }
   float w_at;
-  const int pick = chunk_draw<DT>(sc.buf, n_el, lane, cr.before, cr.t, &w_at, SoftW{p.c, mc, remove ? yv - e0 : -1});
+  const int pick = chunk_draw<DT>(sc.buf, lane, cr.before, cr.t, &w_at, mc, p.c);
   if (lane == 0) {
     p.out_tokens[(int64_t)r * (p.L + 1) + n_acc] = e0 + pick;
     if (p.dbg_resid) p.dbg_resid[r] = w_at / cr.total;
@@ -1003,7 +1040,7 @@ __device__ void finalize_draft(const VerifyParams& p, int row, int lane, Scratch
     const int e0 = cr.unit * CH, n_el = min(CH, p.vocab - e0);
     const char* base = static_cast<const char*>(p.draft) + (int64_t)row * p.vocab * ESZ;
     if (!stage_chunk<DT>(p, sc, base, e0, n_el, lane)) return;
-    y = e0 + chunk_draw<DT>(sc.buf, n_el, lane, cr.before, cr.t, &q_at, SoftW{p.c, m * p.c, -1});
+    y = e0 + chunk_draw<DT>(sc.buf, lane, cr.before, cr.t, &q_at, m * p.c, p.c);
   }
   if (lane == 0) {
     p.out_tokens[row] = y;
