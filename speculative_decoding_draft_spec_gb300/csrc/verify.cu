@@ -84,6 +84,8 @@ struct VerifyParams {
   int32_t rowf;     // float2 entries of a staged partial row: nch + 1 (the spare), rounded up to even
   int32_t pstride;  // float2 entries between partial rows in the workspace (>= rowf)
   int32_t vec_ok;   // every row starts on a 16-byte boundary
+  uint64_t m_nw;    // floor(2^32 / d) + 1 for d = the grid's warps (division by a multiply-high)
+  uint64_t m_nch;   // the same for d = nch
   WsView ws;
 };
 
@@ -100,6 +102,14 @@ __device__ __forceinline__ float2* partial_row(const VerifyParams& p, int slot) 
   return p.ws.partial + (int64_t)slot * p.pstride;
 }
 // the draft row (request r, 1-based position i) that carries q_i: its workspace slot
+// n / d for n < 2^31 from m = floor(2^32 / d) + 1: m d exceeds 2^32 by at
+// most d, so the multiply-high is the quotient or one more (n < 2^31 keeps the
+// excess below 1/2), and one test corrects it
+__device__ __forceinline__ uint32_t udiv(uint32_t n, uint32_t d, uint64_t m) {
+  const uint32_t q = (uint32_t)(((uint64_t)n * m) >> 32);
+  return q * d > n ? q - 1u : q;
+}
+
 __device__ __forceinline__ int q_slot_of(const VerifyParams& p, int r, int i) {
   return p.max_rows + r * p.K + (i - 1);
 }
@@ -1189,11 +1199,12 @@ __global__ void __launch_bounds__(VR_THREADS, 1) verify_rows_kernel(VerifyParams
       const int r = tid * per_t + q;
       if (r >= B) break;
       const int32_t b0 = p.row_off[r], b1 = p.row_off[r + 1];
+      const int32_t vl = MODE == MODE_TREE ? 0 : p.verify_len[r];  // issued with the offsets
       int32_t cnt = 0, len = 0;
       uint32_t qm = 0;
       bool valid;
       // the draft-distribution flags of the request's L positions, loaded
-      // together with its offsets (they do not depend on its length)
+      // together with its offsets and length (they do not depend on them)
       uint32_t zf = 0;  // bit i: position i + 1 carries a draft distribution (flag 0)
       if (MODE == MODE_CHAIN_SAMPLE && p.use_q && p.pm) {
         const uint8_t* pmr = p.pm + (int64_t)r * p.L;
@@ -1209,7 +1220,7 @@ __global__ void __launch_bounds__(VR_THREADS, 1) verify_rows_kernel(VerifyParams
         valid = b0 >= 0 && len >= 1 && len <= p.max_nodes && b1 <= tot_rows && tot_rows <= p.max_rows;
         cnt = valid ? len : 0;
       } else {
-        len = p.verify_len[r];
+        len = vl;
         valid = len >= 0 && len <= p.L && b0 >= 0 && (int64_t)b0 + len < b1 && b1 <= tot_rows &&
                 tot_rows <= p.max_rows;
         cnt = valid ? len + 1 : 0;
@@ -1283,22 +1294,24 @@ __global__ void __launch_bounds__(VR_THREADS, 1) verify_rows_kernel(VerifyParams
   const uint32_t nch = (uint32_t)p.nch;
   const uint32_t total = n_items * nch;
   const uint32_t nw = gridDim.x * VR_WARPS, gw = blockIdx.x * VR_WARPS + warp;
-  const uint32_t qq = total / nw, rem = total - qq * nw;
-  const uint32_t lo = gw * qq + (gw * rem) / nw, hi = (gw + 1) * qq + ((gw + 1) * rem) / nw;
+  const uint32_t qq = udiv(total, nw, p.m_nw), rem = total - qq * nw;
+  const uint32_t lo = gw * qq + udiv(gw * rem, nw, p.m_nw), hi = (gw + 1) * qq + udiv((gw + 1) * rem, nw, p.m_nw);
   if (lo >= hi) return;
   const bool vec = p.vec_ok != 0;
+  const int first = (int)udiv(lo, nch, p.m_nch);  // the item of chunk lo
   Cursor ic, cc;  // issue and consume cursors
   {
-    const int first = (int)(lo / nch);
     int a = 0;
-    if (MODE != MODE_DRAFT) {  // last r with s_pre[r] <= first
-      int b = B - 1;
-      while (a < b) {
-        const int mid = (a + b + 1) >> 1;
-        if (s_pre[mid] <= first)
-          a = mid;
-        else
-          b = mid - 1;
+    if (MODE != MODE_DRAFT) {
+      // the last r with s_pre[r] <= first (s_pre[0] = 0): the warp tests 32
+      // evenly spaced candidates of [a, end) per round
+      int end = B;
+      while (end - a > 1) {
+        const int step = (end - a + 31) >> 5;
+        const int cand = a + step * lane;
+        const unsigned ok = __ballot_sync(0xFFFFFFFFu, cand < end && s_pre[cand] <= first);
+        a += step * (31 - __clz(ok));  // bit 0 is set: s_pre[a] <= first
+        end = min(end, a + step);
       }
     }
     ic.r = cc.r = a;
@@ -1306,7 +1319,7 @@ __global__ void __launch_bounds__(VR_THREADS, 1) verify_rows_kernel(VerifyParams
   }
   // the issue cursor walks (item, chunk) incrementally from lo; it locates a
   // row only when it enters it and then advances its source pointer
-  int is_item = (int)(lo / nch), is_u = (int)(lo - (uint32_t)is_item * nch);
+  int is_item = first, is_u = (int)(lo - (uint32_t)first * nch);
   const char* is_src = nullptr;
   auto issue = [&](int s) {
     if (is_src == nullptr) {
@@ -1381,7 +1394,7 @@ __global__ void __launch_bounds__(VR_THREADS, 1) verify_rows_kernel(VerifyParams
   // so the finalizer's code lies outside the loop body and the loop's own code
   // stays contiguous (a finalizer inlined inside the loop body measured as
   // instruction-cache misses on every warp of small launches).
-  int item = (int)(lo / nch), u = (int)(lo - (uint32_t)item * nch);
+  int item = first, u = (int)(lo - (uint32_t)first * nch);
   int pend = -1;  // a request completed by this warp, to finalize
   bool ended = false;
   while (!ended) {
@@ -1701,7 +1714,10 @@ __global__ void __launch_bounds__(RS_THREADS) resample_kernel(VerifyParams p) {
 namespace {
 
 template <int DT, int MODE>
-cudaError_t launch_rows(const spec::VerifyParams& p, int num_sms, cudaStream_t stream) {
+cudaError_t launch_rows(const spec::VerifyParams& p0, int num_sms, cudaStream_t stream) {
+  spec::VerifyParams p = p0;
+  p.m_nw = ((uint64_t)1 << 32) / (uint64_t)(num_sms * VR_WARPS) + 1;
+  p.m_nch = ((uint64_t)1 << 32) / (uint64_t)p.nch + 1;
   const size_t table = MODE == spec::MODE_DRAFT ? 0 : (size_t)(4 * p.batch + 1) * sizeof(int32_t);
   const size_t smem = (size_t)VR_WARPS * (VR_WBUF(MODE) + 8 * VR_BARS) + table;
   auto k = spec::verify_rows_kernel<DT, MODE>;
