@@ -50,6 +50,10 @@ struct NgramParams {
   PriceCtx cx;
   SelectCtx sc;
   uint32_t* arrive;  // request arrival counter (zero between calls)
+  // the Eq. (1) table staged in the pricing CTA's shared memory: its offset in
+  // 4-byte words (16-byte aligned), -1 when it is read from global memory
+  int32_t tab_off;
+  uint32_t tab_bytes;
 };
 
 // top-2 of a set of distinct keys held as (b1 >= b2) per lane, merged across the warp
@@ -98,11 +102,23 @@ __global__ void __launch_bounds__(SPEC_CTA_THREADS, 1) ngram_kernel(NgramParams 
   // one CTA per request (rows of at most 8192 tokens): the whole row is copied
   // at once, before its length is read, so the copy and that load overlap
   const bool whole_row = !CLUSTER && p.use_bulk;
-  if (whole_row && tid == 0) {
-    mbar_init(&bar, 1);
+  // fused pricing: the CTA that prices (rank 0) copies the Eq. (1) table into
+  // its shared memory behind the history, so the row the scan picks is an
+  // on-chip read when the pricing needs it
+  __shared__ __align__(8) uint64_t tbar;
+  const bool tab_smem = PRICE && rank == 0 && p.tab_off >= 0;
+  if (tid == 0 && (whole_row || tab_smem)) {
+    if (whole_row) mbar_init(&bar, 1);
+    if (tab_smem) mbar_init(&tbar, 1);
     fence_mbar_init();
-    mbar_arrive_expect_tx(&bar, (uint32_t)p.stride * 4u);
-    bulk_g2s(smem_tok, x, (uint32_t)p.stride * 4u, &bar);
+    if (whole_row) {
+      mbar_arrive_expect_tx(&bar, (uint32_t)p.stride * 4u);
+      bulk_g2s(smem_tok, x, (uint32_t)p.stride * 4u, &bar);
+    }
+    if (tab_smem) {
+      mbar_arrive_expect_tx(&tbar, p.tab_bytes);
+      bulk_g2s(smem_tok + p.tab_off, p.cx.table, p.tab_bytes, &tbar);
+    }
   }
 
   const int32_t T = p.hist_len[r];
@@ -121,7 +137,7 @@ __global__ void __launch_bounds__(SPEC_CTA_THREADS, 1) ngram_kernel(NgramParams 
   // the Eq. (1) table is read once per request after the scan, at a row the scan
   // picks: every CTA brings its share of the table's lines into L2 now, while
   // the history copies are in flight, so that read hits L2
-  if (PRICE && !p.cx.tab_const && tid < 32) {
+  if (PRICE && !p.cx.tab_const && p.tab_off < 0 && tid < 32) {
     const int64_t n_h = (int64_t)p.cx.L * (SPEC_TAB_N * 2 + 2 * (p.cx.m_cap + 1));  // table floats
     const uintptr_t a0 = reinterpret_cast<uintptr_t>(p.cx.table) & ~(uintptr_t)127;
     const uintptr_t a1 = reinterpret_cast<uintptr_t>(p.cx.table + n_h);
@@ -364,8 +380,17 @@ __global__ void __launch_bounds__(SPEC_CTA_THREADS, 1) ngram_kernel(NgramParams 
       if (tid < 32) {
         uint32_t st = 0;
         if (tid < p.L) s_ps.g[tid] = tid < len ? tok_at(jb + 1 + tid) : -1;
+        const float* stab = nullptr;  // the staged table, once its copy has landed
+        if (tab_smem) {
+          if (mbar_wait_bounded(&tbar, 0, 1u << 22)) {
+            stab = reinterpret_cast<const float*>(smem_tok + p.tab_off);
+          } else {  // record it, wait (bounded) for the copy to finish, price from global memory
+            st |= SPEC_DEV_TIMEOUT;
+            mbar_wait_bounded(&tbar, 0, 1u << 22);
+          }
+        }
         __syncwarp();
-        price_request_warp(p.cx, r, tid, s_ps, len, n_out, a_out, m_out, s_dl, st);
+        price_request_warp(p.cx, r, tid, s_ps, len, n_out, a_out, m_out, s_dl, st, stab);
         if (st) set_status(p.status, st);
         __syncwarp();
         if (tid == 0) {
@@ -531,6 +556,20 @@ extern "C" cudaError_t spec_launch_draft_price(
   if (!ngram_geometry(stride < 1 ? 1 : stride, cap, spec::select_scratch_ints(batch, L), &C, &p, &smem)) {
     *unsupported = 1;
     return cudaSuccess;
+  }
+  // the Eq. (1) table into the pricing CTA's shared memory when it is whole
+  // 16-byte pieces, 16-byte aligned and at most SPEC_TAB_SMEM_MAX bytes
+  p.tab_off = -1;
+  p.tab_bytes = 0;
+  if (!est->use_constant_h) {
+    const size_t tb = sizeof(float) * (size_t)L * (SPEC_TAB_N * 2 + 2 * ((size_t)est->m_cap + 1));
+    const size_t off = (smem + 15) & ~(size_t)15;
+    if (tb % 16 == 0 && tb <= SPEC_TAB_SMEM_MAX && (reinterpret_cast<uintptr_t>(table) & 15u) == 0 &&
+        off + tb <= 200 * 1024) {
+      p.tab_off = (int32_t)(off / sizeof(int32_t));
+      p.tab_bytes = (uint32_t)tb;
+      smem = off + tb;
+    }
   }
   return launch_ngram_kernel<true>(p, C, smem, batch, stream);
 }

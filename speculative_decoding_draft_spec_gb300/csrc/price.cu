@@ -127,7 +127,7 @@ __global__ void __launch_bounds__(PR_THREADS, 1) price_kernel(PriceParams p) {
         ps.c[lane] = p.c[(int64_t)r * K + lane];
       }
       __syncwarp();
-      price_request_warp(p.cx, r, lane, ps, gl, n, a, m, dl, st);
+      price_request_warp(p.cx, r, lane, ps, gl, n, a, m, dl, st, nullptr);
     }
     if (st) set_status(p.status, st);
   }

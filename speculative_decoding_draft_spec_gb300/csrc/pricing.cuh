@@ -17,6 +17,7 @@
 #include "common.cuh"
 
 #define SPEC_TAB_N 33  // n in [0, SPEC_MAX_N]
+#define SPEC_TAB_SMEM_MAX (48 * 1024)  // the largest Eq. (1) table fused pricing stages in shared memory
 
 namespace spec {
 
@@ -55,14 +56,14 @@ __device__ __forceinline__ float clamp_conf(float ck, uint32_t& st) {
 
 // The Eq. (1) table row of features (n, a, m): h_1..h_L contiguous, or null
 // when n lies outside the table (h = 0, flagged).
-__device__ __forceinline__ const float* table_row(const PriceCtx& cx, int32_t n, int32_t a, int32_t m,
-                                                  int32_t gl, uint32_t& st) {
-  if (cx.tab_const) return cx.table;
+__device__ __forceinline__ const float* table_row(const PriceCtx& cx, const float* table, int32_t n, int32_t a,
+                                                  int32_t m, int32_t gl, uint32_t& st) {
+  if (cx.tab_const) return table;
   if (n == cx.n_full) {
     m = m < 0 ? 0 : (m > cx.m_cap ? cx.m_cap : m);
-    return cx.table + (int64_t)cx.L * SPEC_TAB_N * 2 + (int64_t)(a * (cx.m_cap + 1) + m) * cx.L;
+    return table + (int64_t)cx.L * SPEC_TAB_N * 2 + (int64_t)(a * (cx.m_cap + 1) + m) * cx.L;
   }
-  if (n >= 0 && n <= SPEC_MAX_N) return cx.table + (int64_t)(n * 2 + a) * cx.L;
+  if (n >= 0 && n <= SPEC_MAX_N) return table + (int64_t)(n * 2 + a) * cx.L;
   if (gl > 0) st |= SPEC_DEV_BAD_VALUE;
   return nullptr;
 }
@@ -85,9 +86,11 @@ struct PriceStage {
 // of four positions are loaded together ahead of the dependent products: this
 // code runs once per request, and its latency is on the critical path of the
 // round.
+// stab: a copy of the Eq. (1) table in this CTA's shared memory, or null to
+// read the table in global memory.
 __device__ __forceinline__ void price_request_warp(const PriceCtx& cx, int r, int lane, PriceStage& ps,
                                                    int32_t gl, int32_t n, int32_t a, int32_t m, int32_t dl,
-                                                   uint32_t& st) {
+                                                   uint32_t& st, const float* stab) {
   const int32_t K = cx.K, L = cx.L;
   if (dl < 0 || dl > K) {
     st |= SPEC_DEV_BAD_LENGTH;
@@ -101,8 +104,11 @@ __device__ __forceinline__ void price_request_warp(const PriceCtx& cx, int r, in
     st |= SPEC_DEV_BAD_VALUE;
     a = 1;
   }
-  const float* hrow = table_row(cx, n, a, m, gl, st);
-  if (lane < gl) ps.h[lane] = hrow ? __ldg(hrow + (cx.tab_const ? 0 : lane)) : 0.0f;
+  const float* hrow = table_row(cx, stab ? stab : cx.table, n, a, m, gl, st);
+  if (lane < gl) {
+    const float* hp = hrow + (cx.tab_const ? 0 : lane);
+    ps.h[lane] = hrow ? (stab ? *hp : __ldg(hp)) : 0.0f;
+  }
   if (lane < dl) ps.c[lane] = clamp_conf(ps.c[lane], st);
   __syncwarp();
   // S^g_k, S^d_k and the chain values, k = 1, 2, ... in order
