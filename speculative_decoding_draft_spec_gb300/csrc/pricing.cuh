@@ -269,6 +269,7 @@ static __device__ __forceinline__ void select_budget_cta(const SelectCtx& sc, in
   int32_t* bc = red + 64;                                           // [2][4] + candidate count
   int parity = 0;
   for (int i = tid; i < 2 * NB; i += nt) s_hist[i] = 0;
+  for (int i = tid; i < NCAND; i += nt) s_cand[i] = 0u;  // the ranking reads whole groups of four
   if (tid == 0) bc[8] = 0;
   // keys: batches of 8 slots per thread, every load issued before any is used
   int32_t my_valid = 0;
@@ -363,13 +364,16 @@ static __device__ __forceinline__ void select_budget_cta(const SelectCtx& sc, in
       __syncthreads();
       int32_t* b = bc + 4 * 2;  // words 8..11: [8] count (done), [9] theta, [10] need
       if (tid < cnt) {
+        // the candidates four at a time (the zeroes past cnt count in neither
+        // sum: the key sought is at least 1)
         const uint32_t v = s_cand[tid];
+        const uint4* c4 = reinterpret_cast<const uint4*>(s_cand);
         int32_t gt = 0, ge = 0;
 #pragma unroll 4
-        for (int i = 0; i < cnt; ++i) {
-          const uint32_t u = s_cand[i];
-          gt += u > v;
-          ge += u >= v;
+        for (int i = 0; i < ((cnt + 3) >> 2); ++i) {
+          const uint4 u = c4[i];
+          gt += (int32_t)(u.x > v) + (int32_t)(u.y > v) + (int32_t)(u.z > v) + (int32_t)(u.w > v);
+          ge += (int32_t)(u.x >= v) + (int32_t)(u.y >= v) + (int32_t)(u.z >= v) + (int32_t)(u.w >= v);
         }
         if (gt < rem && rem <= ge) {  // every copy of v writes the same values
           b[1] = (int32_t)v;
@@ -386,7 +390,7 @@ static __device__ __forceinline__ void select_budget_cta(const SelectCtx& sc, in
   // 1024 x 31 slots, so neither field overflows
   const int rp = (B + nt - 1) / nt;
   const int r_lo = min(B, tid * rp), r_hi = min(B, r_lo + rp);
-  int32_t mine = 0;
+  int32_t mine = 0, above0 = 0, eq0 = 0;  // (above, eq) of request r_lo, kept for the second pass
   for (int r = r_lo; r < r_hi; ++r) {
     int32_t above = 0, eq = 0;
 #pragma unroll 4
@@ -395,18 +399,26 @@ static __device__ __forceinline__ void select_budget_cta(const SelectCtx& sc, in
       above += w > theta;
       eq += w == theta;
     }
+    if (r == r_lo) {
+      above0 = above;
+      eq0 = eq;
+    }
     mine += (above << 16) | eq;
   }
   int32_t tot;
   const int32_t incl = cta_incl_scan(mine, red, parity, &tot);
   int32_t A = (incl - mine) >> 16, E = (incl - mine) & 0xFFFF;
   for (int r = r_lo; r < r_hi; ++r) {
-    int32_t above = 0, eq = 0;
+    int32_t above = above0, eq = eq0;
+    if (r != r_lo) {
+      above = 0;
+      eq = 0;
 #pragma unroll 4
-    for (int k = 0; k < L; ++k) {
-      const uint32_t w = s_key[r * L + k];
-      above += w > theta;
-      eq += w == theta;
+      for (int k = 0; k < L; ++k) {
+        const uint32_t w = s_key[r * L + k];
+        above += w > theta;
+        eq += w == theta;
+      }
     }
     const int32_t take = min(eq, max(0, need - E));
     sc.verify_len[r] = above + take;
