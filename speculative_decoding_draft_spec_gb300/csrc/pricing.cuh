@@ -205,10 +205,11 @@ __device__ __forceinline__ void price_request_warp(const PriceCtx& cx, int r, in
 // lies among the first `need` such slots in slot order; theta and need follow
 // from the budget: none (theta = ~0), every valid slot (budget >= number of
 // valid slots: theta = 0), else theta = the key of the budget-th slot in the
-// order (key desc, slot asc).  That key is found from the top bits down: a
-// 1024-bin shared-memory histogram of bits 29..20 (then 19..10, 9..0 while the
-// chosen bin still holds more than 256 keys) locates it, and the keys of the
-// chosen bin are then ranked against each other directly.  Survivals fall
+// order (key desc, slot asc).  A 1024-bin shared-memory histogram of the
+// survival value (linear bins) locates it (then of key bits 29..20, 19..10,
+// 9..0 among that bin's keys while the chosen bin still holds more than 256
+// keys), and the keys of the chosen bin are then ranked against each other
+// directly.  Survivals fall
 // along a chain (products of factors in [0, 1]) and ties go to the lower
 // position, so every request takes a prefix:
 // ell_r = above_r + min(eq_r, max(0, need - E_r)) with E_r the ties of the
@@ -298,17 +299,30 @@ static __device__ __forceinline__ void select_budget_cta(const SelectCtx& sc, in
     theta = 0u;
     need = 0;
   } else {
-    uint32_t prefix = 0u;  // key bits at and above `hi` fixed so far
+    // Level 0 bins the survival value linearly (a valid key is the value's
+    // bits + 1, and value x 1024 is exact, so the bins keep the keys' order):
+    // keys close in value spread over many bins, and few share the chosen one.
+    // Only when that bin still holds more than NCAND keys do the next levels
+    // fix the key's bits ten at a time among the bin's keys.
+    auto vbin = [](uint32_t w) -> int { return min(NB - 1, (int)(__uint_as_float(w - 1u) * (float)NB)); };
+    int vb = -1;           // the chosen value bin
+    uint32_t prefix = 0u;  // key bits at and above `hi` fixed so far (levels 1..3)
     int hi = 30;           // keys are below 2^30
-    int32_t rem = budget;  // slots still to take among the keys matching the prefix
+    int32_t rem = budget;  // slots still to take among the keys of the bin and prefix
     int32_t cnt = nslots;
+    auto member = [&](uint32_t w) -> bool { return w != 0u && vbin(w) == vb && (w >> hi) == (prefix >> hi); };
 #pragma unroll 1
-    for (int level = 0; level < 3; ++level) {
+    for (int level = 0; level < 4; ++level) {
       const int shift = hi - 10;
       int32_t* hist = s_hist + (level & 1) * NB;
+#pragma unroll 4
       for (int q = tid; q < nslots; q += nt) {
         const uint32_t w = s_key[q];
-        if ((w >> hi) == (prefix >> hi)) atomicAdd(&hist[(w >> shift) & (NB - 1)], 1);
+        if (level == 0) {
+          if (w != 0u) atomicAdd(&hist[vbin(w)], 1);
+        } else if (member(w)) {
+          atomicAdd(&hist[(w >> shift) & (NB - 1)], 1);
+        }
       }
       __syncthreads();
       // thread t owns bins 1023 - 4t .. 1020 - 4t (descending) and zeroes them
@@ -344,10 +358,14 @@ static __device__ __forceinline__ void select_budget_cta(const SelectCtx& sc, in
         b[2] = c;
       }
       __syncthreads();
-      prefix |= (uint32_t)b[0] << shift;
+      if (level == 0) {
+        vb = b[0];
+      } else {
+        prefix |= (uint32_t)b[0] << shift;
+        hi = shift;
+      }
       rem = b[1];
       cnt = b[2];
-      hi = shift;
       if (cnt <= NCAND || hi == 0) break;
     }
     if (hi == 0) {
@@ -357,9 +375,10 @@ static __device__ __forceinline__ void select_budget_cta(const SelectCtx& sc, in
     } else {
       // the chosen bin's keys, ranked directly: theta is the value v with
       // #(keys > v) < rem <= #(keys >= v)
+#pragma unroll 4
       for (int q = tid; q < nslots; q += nt) {
         const uint32_t w = s_key[q];
-        if ((w >> hi) == (prefix >> hi)) s_cand[atomicAdd(&bc[8], 1)] = w;
+        if (member(w)) s_cand[atomicAdd(&bc[8], 1)] = w;
       }
       __syncthreads();
       int32_t* b = bc + 4 * 2;  // words 8..11: [8] count (done), [9] theta, [10] need
