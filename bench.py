@@ -460,7 +460,8 @@ def measure_bs4(S, torch, W, steps, warmup, hbm, rate, probabilistic=False):
     T = 0: greedy drafts (proposed policy).  T = 1 with probabilistic drafting
     (extension policy): the drafter's 7 tokens are sampled on the device from
     its bf16 rows (spec_sample_drafts) before draft + price, and the sampled
-    verification reads the draft rows too; the sampling step counter is held
+    verification (spec_verify_chain_drafted) takes the draft rows' statistics
+    from that call instead of reading them again; the sampling step counter is held
     fixed so that every round has the same layout (the work does not depend on
     the drawn values), and verification's Philox step is the input set's
     index.  Same timing as the batch-128 round, over ten rotating input sets.
@@ -504,21 +505,21 @@ def measure_bs4(S, torch, W, steps, warmup, hbm, rate, probabilistic=False):
         parts = [lambda st, rnd=rnd: sample(rnd, st)] if probabilistic else []
         parts += [lambda st, rnd=rnd: rnd.draft_and_price(cfg["lam"], cfg["budget"], cfg["max_verify_len"],
                                                           cfg["policy"], greedy, st),
-                  lambda st, rnd=rnd, k=k: rnd.verify(temperature=T, seed=0, step=k, stream=st)]
+                  lambda st, rnd=rnd, k=k: rnd.verify(temperature=T, seed=0, step=k, stream=st,
+                                                      drafted=probabilistic)]
         sets.append(parts)
     names = (["sample_drafts"] if probabilistic else []) + ["draft_price", "verify"]
     ms, comp = timed_parts(torch, sets, names, steps, warmup)
     torch.cuda.synchronize()
     accepted = statistics.mean(int(r.n_accepted.sum().item()) for r in rounds)
-    rd_bytes = n_rows * V * 2
     q_rows = 0
-    if probabilistic:  # draft rows verification reads: sampled (not point-mass) positions within verify_len
+    if probabilistic:  # draft rows whose statistics verification reuses: sampled positions within verify_len
         pm = first.point_mass.cpu().numpy()
         q_rows = int(sum(int((pm[r, :min(int(vlen[r]), K)] == 0).sum()) for r in range(B)))
-    ver_bytes = (n_rows + q_rows) * V * 2
+    ver_bytes = n_rows * V * 2  # verification streams the target rows only
     out = {"edit_rate": rate, "value": n_tok * steps / (ms * 1e-3), "unit": UNIT,
            "rows_per_s": n_rows * steps / (ms * 1e-3), "us_per_round": 1e3 * ms / steps, "steps": steps,
-           "verified_tokens_per_step": n_tok, "verify_rows_per_step": n_rows, "draft_rows_read": q_rows,
+           "verified_tokens_per_step": n_tok, "verify_rows_per_step": n_rows, "draft_rows_reused": q_rows,
            "accepted_per_step": accepted, "ngram_chain_share": float(np.isin(source, (1, 2)).mean()),
            "components_us": {k: round(v, 3) for k, v in comp.items()},
            "verify_roofline_frac": round(ver_bytes / (comp["verify"] * 1e-6) / 1e9 / hbm, 4),
@@ -860,8 +861,9 @@ def run_once():
 def once_verify_launches(S, torch, W):
     """One chain verification each, after its round's draft + price: batch-4 code
     editing at the 30 % edit rate at T = 0 (bf16 rows), the same at T = 1 with
-    drafts sampled on the device (bf16 target and draft rows; the sampled
-    kernel and the max(0, p - q) draw), and the batch-64 long-context workload
+    drafts sampled on the device (bf16 target rows, the draft rows' statistics
+    from the drafting call; the sampled kernel and the max(0, p - q) draw, which
+    reads the draft row), and the batch-64 long-context workload
     at T = 0.7 (fp32, 16 rows per request), for a profiler.  Returns the verify
     rows of each."""
     from speculative_decoding_draft_spec_gb300.round import ChainRound
@@ -888,7 +890,7 @@ def once_verify_launches(S, torch, W):
     ro, vl = rnd.row_off.cpu().numpy(), rnd.verify_len.cpu().numpy()
     n = int(ro[-1])
     rnd.logits[:n].copy_(torch.from_numpy(W.compact_logits(c, ro, vl).view(np.int16)).view(torch.bfloat16))
-    rnd.verify(temperature=1.0, seed=0, step=0)
+    rnd.verify(temperature=1.0, seed=0, step=0, drafted=True)
     torch.cuda.synchronize()
     out["edit_bs4 probabilistic rate 0.30"] = n
     c = W.long_bs64()

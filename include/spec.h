@@ -488,6 +488,31 @@ spec_status spec_verify_chain(
     const spec_workspace* ws, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------
+ * spec_verify_chain_drafted: spec_verify_chain, with the same arguments and
+ * the same results, when the draft distributions come from
+ * spec_sample_drafts on the same workspace.  That call left each draft row's
+ * per-chunk (max, sum) statistics and the logit at its drawn token in the
+ * workspace; this one uses them instead of reading the draft rows again, so
+ * it streams only the target rows (the draft rows are still read, from L2,
+ * by the max(0, p - q) draw at a rejection).
+ * Requires: draft_logits, K, vocab, dtype and temperature equal to that
+ * spec_sample_drafts call's; for every position with point_mass == 0, the
+ * chain holds the token that call drew (as spec_draft_and_price places it);
+ * no call that writes draft-row statistics (spec_sample_drafts or
+ * spec_verify_chain with draft_logits) on the same workspace in between.
+ * draft_logits, point_mass and temperature > 0 are required
+ * (SPEC_ERR_INVALID_ARG).  A temperature other than the drafting call's sets
+ * SPEC_DEV_BAD_VALUE.
+ * ------------------------------------------------------------------------ */
+spec_status spec_verify_chain_drafted(
+    int32_t batch, int32_t vocab, spec_dtype dtype, const void* target_logits,
+    const int32_t* row_off, int32_t max_rows, const void* draft_logits, int32_t K,
+    const int32_t* chain, int32_t L, const int32_t* verify_len, const uint8_t* point_mass,
+    float temperature, uint64_t seed, uint64_t step, int32_t* out_tokens, int32_t* n_accepted,
+    int32_t* n_emitted, float* dbg_ratio, float* dbg_u, float* dbg_resid,
+    const spec_workspace* ws, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
  * Step 4: greedy tree verification ([AS] sec. 2.2, sec. 3.5).
  *
  * Request r's tree has n = node_off[r+1] - node_off[r] nodes (1 <= n <=

@@ -24,7 +24,7 @@ from ._build import build
 
 __all__ = [
     "build", "load", "Workspace", "EstimatorTable", "SpecError", "spec_ngram_propose",
-    "spec_price_and_allocate", "spec_price_and_allocate_static", "spec_draft_and_price", "spec_verify_chain", "spec_verify_tree", "spec_build_tree", "spec_ngram_fill", "spec_size_budget", "spec_sample_drafts", "POLICY",
+    "spec_price_and_allocate", "spec_price_and_allocate_static", "spec_draft_and_price", "spec_verify_chain", "spec_verify_chain_drafted", "spec_verify_tree", "spec_build_tree", "spec_ngram_fill", "spec_size_budget", "spec_sample_drafts", "POLICY",
     "DEV_BITS",
 ]
 
@@ -89,6 +89,8 @@ SIGNATURES = {
                               _vp, _vp, _vp, _vp, _WSP, _vp], _i32),
     "spec_verify_chain": ([_i32, _i32, _i32, _vp, _vp, _i32, _vp, _i32, _vp, _i32, _vp, _vp, _f32,
                            _u64, _u64, _vp, _vp, _vp, _vp, _vp, _vp, _WSP, _vp], _i32),
+    "spec_verify_chain_drafted": ([_i32, _i32, _i32, _vp, _vp, _i32, _vp, _i32, _vp, _i32, _vp, _vp, _f32,
+                                   _u64, _u64, _vp, _vp, _vp, _vp, _vp, _vp, _WSP, _vp], _i32),
     "spec_build_tree": ([_i32, _i32, _i32, _vp, _vp, _vp, _vp, _i32, _i32, _vp, _vp, _vp, _i32, _vp, _vp, _vp,
                          _vp, _WSP, _vp], _i32),
     "spec_ngram_fill": ([_vp, _i64, _vp, _i32, _i32, _i32, _vp, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _WSP, _vp],
@@ -264,17 +266,25 @@ def spec_draft_and_price(hist, hist_len, n_min, n_max, copy_cap, g, g_len, match
 
 def spec_verify_chain(target_logits, row_off, max_rows, chain, verify_len, out_tokens, n_accepted,
                       n_emitted, ws: Workspace, draft_logits=None, point_mass=None, temperature=0.0,
-                      seed=0, step=0, dbg_ratio=None, dbg_u=None, dbg_resid=None, stream=None):
+                      seed=0, step=0, dbg_ratio=None, dbg_u=None, dbg_resid=None, stream=None, drafted=False):
+    """drafted=True calls spec_verify_chain_drafted (the draft rows' statistics
+    from the preceding spec_sample_drafts on this workspace)."""
     B, L = chain.shape
     V = target_logits.shape[-1]
     K = 0 if draft_logits is None else draft_logits.shape[1]
     if draft_logits is not None and draft_logits.dtype != target_logits.dtype:
         raise TypeError("draft and target logits must share a dtype")
-    _check("spec_verify_chain", load().spec_verify_chain(
+    name = "spec_verify_chain_drafted" if drafted else "spec_verify_chain"
+    _check(name, getattr(load(), name)(
         B, V, _dtype_code(target_logits), _ptr(target_logits), _ptr(row_off), int(max_rows),
         _ptr(draft_logits), K, _ptr(chain), L, _ptr(verify_len), _ptr(point_mass), float(temperature),
         int(seed), int(step), _ptr(out_tokens), _ptr(n_accepted), _ptr(n_emitted), _ptr(dbg_ratio),
         _ptr(dbg_u), _ptr(dbg_resid), ws.ref, _stream(stream)))
+
+
+def spec_verify_chain_drafted(*args, **kw):
+    """spec_verify_chain with the draft rows' statistics from spec_sample_drafts."""
+    return spec_verify_chain(*args, drafted=True, **kw)
 
 
 def spec_verify_tree(logits, node_off, max_rows, tok, parent, max_nodes, path, accept_len, out_tokens,

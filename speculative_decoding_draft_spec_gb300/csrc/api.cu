@@ -64,8 +64,8 @@ cudaError_t spec_launch_verify_chain(int32_t batch, int32_t vocab, int32_t dtype
                                      const uint8_t* pm, float temperature, uint64_t seed,
                                      uint64_t step, int32_t* out_tokens, int32_t* n_accepted,
                                      int32_t* n_emitted, float* dbg_ratio, float* dbg_u,
-                                     float* dbg_resid, const spec_workspace* ws, int num_sms,
-                                     cudaStream_t stream);
+                                     float* dbg_resid, int32_t q_reuse_base, const spec_workspace* ws,
+                                     int num_sms, cudaStream_t stream);
 int spec_verify_limits_ok(int32_t vocab, int32_t dtype, int64_t rows, int num_sms);
 cudaError_t spec_launch_verify_tree(int32_t batch, int32_t vocab, int32_t dtype, const void* logits,
                                     const int32_t* node_off, const int32_t* tok,
@@ -377,15 +377,20 @@ spec_status spec_draft_and_price(
   return from_cuda(e);
 }
 
-spec_status spec_verify_chain(int32_t batch, int32_t vocab, spec_dtype dtype, const void* target_logits,
-                              const int32_t* row_off, int32_t max_rows, const void* draft_logits,
-                              int32_t K, const int32_t* chain, int32_t L, const int32_t* verify_len,
-                              const uint8_t* point_mass, float temperature, uint64_t seed,
-                              uint64_t step, int32_t* out_tokens, int32_t* n_accepted,
-                              int32_t* n_emitted, float* dbg_ratio, float* dbg_u, float* dbg_resid,
-                              const spec_workspace* ws, cudaStream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// spec_verify_chain (reuse 0) and spec_verify_chain_drafted (reuse 1)
+spec_status verify_chain(int32_t batch, int32_t vocab, spec_dtype dtype, const void* target_logits,
+                         const int32_t* row_off, int32_t max_rows, const void* draft_logits, int32_t K,
+                         const int32_t* chain, int32_t L, const int32_t* verify_len, const uint8_t* point_mass,
+                         float temperature, uint64_t seed, uint64_t step, int32_t* out_tokens,
+                         int32_t* n_accepted, int32_t* n_emitted, float* dbg_ratio, float* dbg_u,
+                         float* dbg_resid, int reuse, const spec_workspace* ws, cudaStream_t stream) {
   if (batch < 0 || vocab < 1 || L < 1 || K < 0 || max_rows < 0 || !(temperature == temperature))
     return SPEC_ERR_INVALID_ARG;
+  if (reuse && (!draft_logits || !point_mass || !(temperature > 0.0f))) return SPEC_ERR_INVALID_ARG;
   if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_INVALID_ARG;
   if (L > SPEC_MAX_L || K > SPEC_MAX_L || batch > kMaxVerifyBatch) return SPEC_ERR_UNSUPPORTED;
   if (!row_off) return SPEC_ERR_INVALID_ARG;
@@ -402,11 +407,42 @@ spec_status spec_verify_chain(int32_t batch, int32_t vocab, spec_dtype dtype, co
   if (!spec_verify_limits_ok(vocab, (int32_t)dtype, (int64_t)max_rows + (int64_t)batch * K, sms))
     return SPEC_ERR_UNSUPPORTED;
   spec_workspace w = *ws;
-  w.max_rows = max_rows;  // partial slots of q rows follow the call's own row bound
+  w.max_rows = max_rows;  // the call's row bound; partial slots of draft rows follow it, except when
+                          // they are reused: they sit where spec_sample_drafts put them, after the
+                          // workspace's row capacity
   return from_cuda(spec_launch_verify_chain(batch, vocab, (int32_t)dtype, target_logits, row_off,
                                             draft_logits, K, chain, L, verify_len, point_mass,
                                             temperature, seed, step, out_tokens, n_accepted,
-                                            n_emitted, dbg_ratio, dbg_u, dbg_resid, &w, sms, stream));
+                                            n_emitted, dbg_ratio, dbg_u, dbg_resid, reuse ? ws->max_rows : -1,
+                                            &w, sms, stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+spec_status spec_verify_chain(int32_t batch, int32_t vocab, spec_dtype dtype, const void* target_logits,
+                              const int32_t* row_off, int32_t max_rows, const void* draft_logits,
+                              int32_t K, const int32_t* chain, int32_t L, const int32_t* verify_len,
+                              const uint8_t* point_mass, float temperature, uint64_t seed,
+                              uint64_t step, int32_t* out_tokens, int32_t* n_accepted,
+                              int32_t* n_emitted, float* dbg_ratio, float* dbg_u, float* dbg_resid,
+                              const spec_workspace* ws, cudaStream_t stream) {
+  return verify_chain(batch, vocab, dtype, target_logits, row_off, max_rows, draft_logits, K, chain, L,
+                      verify_len, point_mass, temperature, seed, step, out_tokens, n_accepted, n_emitted,
+                      dbg_ratio, dbg_u, dbg_resid, 0, ws, stream);
+}
+
+spec_status spec_verify_chain_drafted(int32_t batch, int32_t vocab, spec_dtype dtype, const void* target_logits,
+                                      const int32_t* row_off, int32_t max_rows, const void* draft_logits,
+                                      int32_t K, const int32_t* chain, int32_t L, const int32_t* verify_len,
+                                      const uint8_t* point_mass, float temperature, uint64_t seed,
+                                      uint64_t step, int32_t* out_tokens, int32_t* n_accepted,
+                                      int32_t* n_emitted, float* dbg_ratio, float* dbg_u, float* dbg_resid,
+                                      const spec_workspace* ws, cudaStream_t stream) {
+  return verify_chain(batch, vocab, dtype, target_logits, row_off, max_rows, draft_logits, K, chain, L,
+                      verify_len, point_mass, temperature, seed, step, out_tokens, n_accepted, n_emitted,
+                      dbg_ratio, dbg_u, dbg_resid, 1, ws, stream);
 }
 
 spec_status spec_verify_tree(int32_t batch, int32_t vocab, spec_dtype dtype, const void* logits,

@@ -60,6 +60,7 @@ struct VerifyParams {
   const void* logits;      // target logits (chain) or tree logits
   const int32_t* row_off;  // chain: row_off [batch+1]; tree: node_off [batch+1]
   int32_t max_rows;
+  int32_t qbase;  // partial slot of draft row (r, i) = qbase + r K + i - 1
   const void* draft;  // [batch x K x vocab] or null
   int32_t K;
   const int32_t* chain;
@@ -67,6 +68,7 @@ struct VerifyParams {
   const int32_t* verify_len;
   const uint8_t* pm;
   int32_t use_q;  // draft logits present and T > 0
+  int32_t reuse_q;  // the draft rows' partials and spare entries come from the drafting call: not streamed
   float c;        // log2(e) / T
   uint64_t seed, step;
   int32_t* out_tokens;
@@ -111,7 +113,7 @@ __device__ __forceinline__ uint32_t udiv(uint32_t n, uint32_t d, uint64_t m) {
 }
 
 __device__ __forceinline__ int q_slot_of(const VerifyParams& p, int r, int i) {
-  return p.max_rows + r * p.K + (i - 1);
+  return p.qbase + r * p.K + (i - 1);
 }
 // index of the n-th (0-based) set bit of m
 __device__ __forceinline__ int nth_bit(uint32_t m, int n) {
@@ -806,6 +808,10 @@ __device__ void finalize_chain_sample(const VerifyParams& p, int r, int base, in
   constexpr size_t ESZ = DT == 1 ? 2 : 4;
   const bool tested = lane < ell;
   const int R = ell + 1 + __popc(qmask);
+  // reused draft-row partials: the drafting call recorded its log2(e) / T in
+  // header word 3; another temperature is flagged (the partials stand)
+  if (p.reuse_q && qmask && lane == 0 && __ldcg(p.ws.status + 3) != __float_as_uint(p.c))
+    set_status(p.ws.status, SPEC_DEV_BAD_VALUE);
   const int rows_fit = min(32, VR_STAGE / (p.rowf * 8));  // rows per staging round (one copy per lane)
   const bool has_q = tested && ((qmask >> lane) & 1u);
   const int kq = has_q ? ell + 1 + __popc(qmask & ((1u << lane) - 1u)) : -1;  // lane's q row
@@ -1032,7 +1038,7 @@ __device__ void finalize_draft(const VerifyParams& p, int row, int lane, Scratch
                 (uint32_t)p.seed, (uint32_t)(p.seed >> 32), o);
   const float u = (float)(o[0] >> 8) * (1.0f / 16777216.0f);
   int y = 0;
-  float q_at = 0.0f, total = 0.0f;
+  float q_at = 0.0f, total = 0.0f, zy = -INFINITY;
   if (m != -INFINITY) {
     float wl[8];
 #pragma unroll
@@ -1050,9 +1056,18 @@ __device__ void finalize_draft(const VerifyParams& p, int row, int lane, Scratch
     const int e0 = cr.unit * CH, n_el = min(CH, p.vocab - e0);
     const char* base = static_cast<const char*>(p.draft) + (int64_t)row * p.vocab * ESZ;
     if (!stage_chunk<DT>(p, sc, base, e0, n_el, lane)) return;
-    y = e0 + chunk_draw<DT>(sc.buf, lane, cr.before, cr.t, &q_at, m * p.c, p.c);
+    const int pick = chunk_draw<DT>(sc.buf, lane, cr.before, cr.t, &q_at, m * p.c, p.c);
+    y = e0 + pick;
+    zy = DT == 1 ? __uint_as_float((uint32_t) reinterpret_cast<const uint16_t*>(sc.buf)[pick] << 16)
+                 : reinterpret_cast<const float*>(sc.buf)[pick];
   }
   if (lane == 0) {
+    // the spare entry of the row's partials: the logit at the drawn token, as
+    // verification's stream would record it, so verification can reuse the
+    // row's partials instead of reading the row again (and the temperature
+    // they were made at)
+    __stcg(&partial_row(p, slot)[p.nch], make_float2(zy, 0.0f));
+    p.ws.status[3] = __float_as_uint(p.c);
     p.out_tokens[row] = y;
     if (p.dbg_u) p.dbg_u[row] = u;
     if (p.dbg_resid) p.dbg_resid[row] = total > 0.0f ? q_at / total : 0.0f;
@@ -1231,7 +1246,7 @@ __global__ void __launch_bounds__(VR_THREADS, 1) verify_rows_kernel(VerifyParams
           qm = zf & within & kmask;
           const bool beyond = (zf & within & ~kmask) != 0u;
           if (beyond && blockIdx.x == 0) set_status(p.ws.status, SPEC_DEV_BAD_LENGTH);
-          cnt += __popc(qm);
+          if (!p.reuse_q) cnt += __popc(qm);  // reused draft rows are not streamed
         }
       }
       if (!valid && blockIdx.x == 0) set_status(p.ws.status, SPEC_DEV_BAD_LENGTH);
@@ -1775,13 +1790,14 @@ extern "C" cudaError_t spec_launch_verify_chain(
     const void* draft, int32_t K, const int32_t* chain, int32_t L, const int32_t* verify_len,
     const uint8_t* pm, float temperature, uint64_t seed, uint64_t step, int32_t* out_tokens,
     int32_t* n_accepted, int32_t* n_emitted, float* dbg_ratio, float* dbg_u, float* dbg_resid,
-    const spec_workspace* ws, int num_sms, cudaStream_t stream) {
+    int32_t q_reuse_base, const spec_workspace* ws, int num_sms, cudaStream_t stream) {
   spec::VerifyParams p = {};
   p.batch = batch;
   p.vocab = vocab;
   p.logits = logits;
   p.row_off = row_off;
   p.max_rows = ws->max_rows;
+  p.qbase = ws->max_rows;
   p.draft = draft;
   p.K = draft ? K : 0;
   p.chain = chain;
@@ -1790,6 +1806,9 @@ extern "C" cudaError_t spec_launch_verify_chain(
   p.pm = pm;
   const bool greedy = !(temperature > 0.0f);
   p.use_q = (!greedy && draft != nullptr && pm != nullptr) ? 1 : 0;
+  // reused draft rows: their partials where the drafting call wrote them
+  p.reuse_q = p.use_q && q_reuse_base >= 0 ? 1 : 0;
+  if (p.reuse_q) p.qbase = q_reuse_base;
   p.c = greedy ? 0.0f : (float)(1.4426950408889634 / (double)temperature);
   p.seed = seed;
   p.step = step;
@@ -1835,6 +1854,7 @@ extern "C" cudaError_t spec_launch_verify_tree(int32_t batch, int32_t vocab, int
   p.logits = logits;
   p.row_off = node_off;
   p.max_rows = ws->max_rows;
+  p.qbase = ws->max_rows;
   p.tok = tok;
   p.parent = parent;
   p.max_nodes = max_nodes;
@@ -1858,6 +1878,7 @@ extern "C" cudaError_t spec_launch_sample_drafts(int32_t batch, int32_t K, int32
   p.batch = batch;
   p.vocab = vocab;
   p.max_rows = ws->max_rows;
+  p.qbase = ws->max_rows;
   p.draft = draft_logits;
   p.K = K;
   p.c = (float)(1.4426950408889634 / (double)temperature);

@@ -64,12 +64,14 @@ class ChainRound:
                                 self.chain, self.S, self.chain_len, self.source, self.verify_len,
                                 self.row_off, self.point_mass, self.ws, stream)
 
-    def verify(self, temperature=0.0, seed=0, step=0, row_off=None, stream=None):
+    def verify(self, temperature=0.0, seed=0, step=0, row_off=None, stream=None, drafted=False):
+        """drafted: the draft rows' statistics come from this round's
+        spec_sample_drafts (spec_verify_chain_drafted)."""
         spec_verify_chain(self.logits, self.row_off if row_off is None else row_off, self.max_rows,
                           self.chain, self.verify_len, self.out_tokens, self.n_accepted, self.n_emitted,
                           self.ws, draft_logits=self.draft_logits,
                           point_mass=self.point_mass, temperature=temperature, seed=seed, step=step,
-                          stream=stream)
+                          stream=stream, drafted=drafted)
 
     def run(self, lam, budget, max_verify_len, policy="proposed", draft_greedy=True, temperature=0.0,
             seed=0, step=0, stream=None):

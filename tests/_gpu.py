@@ -58,7 +58,7 @@ def gpu_price(S, ws, est, d, c, d_len, g, g_len, n, a, m, lam, budget, mvl, poli
 
 
 def gpu_chain(S, ws, logits, row_off, chain, verify_len, pm=None, draft=None, T=0.0, seed=0, step=0,
-              logits_t=None, draft_t=None):
+              logits_t=None, draft_t=None, drafted=False):
     B, L = chain.shape
     i32 = dict(dtype=torch.int32, device=DEV)
     out = torch.full((B, L + 1), -7, **i32)
@@ -72,7 +72,7 @@ def gpu_chain(S, ws, logits, row_off, chain, verify_len, pm=None, draft=None, T=
     S.spec_verify_chain(lt, dev(row_off, torch.int32), max_rows, dev(chain, torch.int32),
                         dev(verify_len, torch.int32), out, na, ne, ws, draft_logits=dt,
                         point_mass=None if pm is None else dev(pm, torch.uint8), temperature=T, seed=seed,
-                        step=step, dbg_ratio=ratio, dbg_u=u, dbg_resid=resid)
+                        step=step, dbg_ratio=ratio, dbg_u=u, dbg_resid=resid, drafted=drafted)
     torch.cuda.synchronize()
     return dict(out=host(out), na=host(na), ne=host(ne), ratio=host(ratio), u=host(u), resid=host(resid))
 

@@ -167,6 +167,13 @@ def test_host_validation_rejects_bad_arguments_without_a_gpu(spec):
     assert chain(V=2048) == WSE
     assert chain(T=float("nan")) == INV
     assert chain(draft=P, K=0) == INV
+    # drafted verification: draft rows, point-mass flags and T > 0 required
+    def drafted(T=1.0, draft=P, pm=P, K=7):
+        return lib.spec_verify_chain_drafted(4, 1024, 1, P, P, 64, draft, K, P, 15, P, pm, T, 0, 0, P, P, P,
+                                             None, None, None, C.byref(w), None)
+    assert drafted(draft=None, K=0) == INV
+    assert drafted(pm=None) == INV
+    assert drafted(T=0.0) == INV
     # tree: too many nodes
     assert lib.spec_verify_tree(4, 1024, 1, P, P, 64, P, P, 300, P, P, P, C.byref(w), None) == UNS
     assert lib.spec_verify_tree(4, 1024, 1, P, None, 64, P, P, 16, P, P, P, C.byref(w), None) == INV
