@@ -263,6 +263,39 @@ static __device__ __forceinline__ void select_budget_cta(const SelectCtx& sc, in
   const int B = sc.batch, L = sc.L;
   const int nslots = B * L;
   const int tid = threadIdx.x, nt = blockDim.x;
+  // At most 32 requests: warp 0 counts each request's valid slots (lane r,
+  // request r).  A budget of zero or one that covers every valid slot decides
+  // every length at once (all valid slots, or none), and the warp writes the
+  // lengths and offsets itself; the block-wide selection runs otherwise.
+  if (B <= 32) {
+    __shared__ int32_t s_done;
+    if (tid < 32) {
+      int32_t cnt = 0;
+      if (tid < B) {
+#pragma unroll 4
+        for (int k = 0; k < L; ++k) cnt += __ldcg(sc.keys + tid * L + k) != 0u;
+      }
+      const int32_t n_valid = __reduce_add_sync(0xFFFFFFFFu, cnt);
+      const bool done = sc.budget == 0 || sc.budget >= n_valid;
+      if (done) {
+        const int32_t len = sc.budget == 0 ? 0 : cnt;  // lanes past B hold 0
+        int32_t incl = len;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int32_t t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+          if (tid >= o) incl += t;
+        }
+        if (tid < B) {
+          sc.verify_len[tid] = len;
+          sc.row_off[tid] = tid + incl - len;
+        }
+        if (tid == 31) sc.row_off[B] = B + incl;
+      }
+      if (tid == 0) s_done = done ? 1 : 0;
+    }
+    __syncthreads();
+    if (s_done) return;
+  }
   uint32_t* s_key = reinterpret_cast<uint32_t*>(scratch);          // [nslots]
   int32_t* s_hist = scratch + ((nslots + 3) & ~3);                  // [2][NB], 16-byte aligned
   uint32_t* s_cand = reinterpret_cast<uint32_t*>(s_hist + 2 * NB);  // [NCAND]
