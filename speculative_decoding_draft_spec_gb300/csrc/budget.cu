@@ -146,6 +146,115 @@ __global__ void __launch_bounds__(BU_THREADS) size_budget_kernel(BudgetParams p,
   }
 }
 
+// The same sizing with every slot in registers when the batch has at most
+// BU_REG_SLOTS slots: thread t holds slots t + 256 j (j < 8), each survival
+// with its fixed-point value (-1 marks a slot that may not be verified), all
+// loaded at once (no compaction), so a round is eight register terms per
+// thread, one warp reduction and thread 0's ratio between two barriers.
+#define BU_REG_SLOTS 2048
+__global__ void __launch_bounds__(BU_THREADS) size_budget_reg_kernel(BudgetParams p, uint32_t* status) {
+  constexpr int J = BU_REG_SLOTS / BU_THREADS;
+  __shared__ unsigned long long s_part[BU_THREADS / 32];
+  __shared__ int32_t s_cnt[BU_THREADS / 32];
+  __shared__ float s_thr;
+  __shared__ int32_t s_done;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int32_t nslots = p.batch * p.L;
+  float v[J];
+  uint64_t f[J];
+  bool bad = false;
+  {
+    // slot q = tid + 256 j: request q / L and position q % L, advanced without division
+    int32_t rr[J], kk[J];
+    int32_t r = tid / p.L, k = tid - r * p.L;
+    const int32_t dr = BU_THREADS / p.L, dk = BU_THREADS - dr * p.L;
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+      rr[j] = r;
+      kk[j] = k;
+      k += dk;
+      r += dr;
+      if (k >= p.L) {
+        k -= p.L;
+        ++r;
+      }
+    }
+    int32_t len[J];
+#pragma unroll
+    for (int j = 0; j < J; ++j) {  // every load issued before any is used
+      const int32_t q = tid + BU_THREADS * j;
+      len[j] = q < nslots ? __ldg(p.chain_len + rr[j]) : 0;
+      v[j] = q < nslots ? __ldg(p.S + q) : -1.0f;
+    }
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+      const int32_t q = tid + BU_THREADS * j;
+      float x = v[j];
+      if (q < nslots && kk[j] < min(len[j], p.mvl)) {
+        if (!(x >= 0.0f && x <= 1.0f)) {  // survivals are probabilities
+          bad = true;
+          x = x > 1.0f ? 1.0f : 0.0f;
+        }
+      } else {
+        x = -1.0f;
+      }
+      v[j] = x;
+      f[j] = x >= 0.0f ? fixed48(x) : 0ull;
+    }
+  }
+  if (__any_sync(0xFFFFFFFFu, bad) && lane == 0) set_status(status, SPEC_DEV_BAD_VALUE);
+  // Dinkelbach's iteration, as in size_budget_kernel
+  double lam = (double)p.batch / p.C0;  // G(0) (thread 0's copy is the one used)
+  int32_t b = 0;
+  if (tid == 0) {
+    s_thr = __double2float_rd(lam * p.p);
+    s_done = 0;
+  }
+  __syncthreads();
+  for (int it = 0; it < 64; ++it) {
+    const float thr = s_thr;
+    int32_t cnt = 0;
+    uint64_t sum = 0;
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+      const bool in = v[j] > thr;  // slots that may not be verified hold -1
+      cnt += in ? 1 : 0;
+      sum += in ? f[j] : 0ull;
+    }
+    cnt = __reduce_add_sync(0xFFFFFFFFu, cnt);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
+    if (lane == 0) {
+      s_part[warp] = sum;
+      s_cnt[warp] = cnt;
+    }
+    __syncthreads();
+    if (tid == 0) {
+      int32_t c = 0;
+      uint64_t sm = 0;
+#pragma unroll
+      for (int w = 0; w < BU_THREADS / 32; ++w) {
+        c += s_cnt[w];
+        sm += s_part[w];
+      }
+      const double lam_new = ((double)p.batch + (double)sm * 0x1p-48) / (p.C0 + p.p * (double)c);
+      if (c == b || !(lam_new > lam)) {
+        s_done = 1;  // the set stopped changing (or the ratio stopped rising)
+      } else {
+        b = c;
+        lam = lam_new;
+        s_thr = __double2float_rd(lam_new * p.p);
+      }
+    }
+    __syncthreads();
+    if (s_done) break;
+  }
+  if (tid == 0) {
+    *p.out_budget = b;
+    *p.out_lambda = (float)(lam * p.p);
+  }
+}
+
 }  // namespace spec
 
 extern "C" size_t spec_budget_smem_bytes(int32_t batch, int32_t L) {
@@ -167,6 +276,10 @@ extern "C" cudaError_t spec_launch_size_budget(int32_t batch, int32_t L, const f
   bp.p = p;
   bp.out_budget = out_budget;
   bp.out_lambda = out_lambda;
+  if ((int64_t)batch * L <= BU_REG_SLOTS) {  // every slot in registers
+    spec::size_budget_reg_kernel<<<1, BU_THREADS, 0, stream>>>(bp, status);
+    return cudaGetLastError();
+  }
   cudaError_t e = cudaFuncSetAttribute(spec::size_budget_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;

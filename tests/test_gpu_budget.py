@@ -58,7 +58,8 @@ def test_budget_parity_on_priced_workloads(S, name, C0, p):
     _check(S, pr.S, pr.chain_len, c["max_verify_len"], C0 * c["B"] / 8, p)
 
 
-@pytest.mark.parametrize("B,L,seed", [(1, 1, 0), (3, 15, 1), (100, 15, 2), (1024, 31, 3), (257, 7, 4)])
+@pytest.mark.parametrize("B,L,seed", [(1, 1, 0), (3, 15, 1), (100, 15, 2), (1024, 31, 3), (257, 7, 4), (128, 16, 5),
+                                        (129, 16, 6)])
 def test_budget_parity_random(S, B, L, seed):
     rng = np.random.default_rng(seed)
     Sv = np.cumprod(rng.uniform(0.3, 1.0, (B, L)), axis=1).astype(np.float32)
