@@ -305,7 +305,15 @@ static __device__ __forceinline__ void select_budget_cta(const SelectCtx& sc, in
   for (int i = tid; i < 2 * NB; i += nt) s_hist[i] = 0;
   for (int i = tid; i < NCAND; i += nt) s_cand[i] = 0u;  // the ranking reads whole groups of four
   if (tid == 0) bc[8] = 0;
-  // keys: batches of 8 slots per thread, every load issued before any is used
+  // Level 0 of the selection bins the survival value linearly (a valid key is
+  // the value's bits + 1, and value x 1024 is exact, so the bins keep the keys'
+  // order): keys close in value spread over many bins, and few share the
+  // chosen one.
+  auto vbin = [](uint32_t w) -> int { return min(NB - 1, (int)(__uint_as_float(w - 1u) * (float)NB)); };
+  // keys: batches of 8 slots per thread, every load issued before any is used;
+  // with at most 8 per thread they stay in registers (wk) for the candidates
+  const bool regs = nslots <= 8 * nt;
+  uint32_t wk[8];
   int32_t my_valid = 0;
   for (int q0 = 0; q0 < nslots; q0 += 8 * nt) {
     uint32_t w[8];
@@ -319,6 +327,7 @@ static __device__ __forceinline__ void select_budget_cta(const SelectCtx& sc, in
       const int q = q0 + tid + i * nt;
       if (q < nslots) s_key[q] = w[i];
       my_valid += w[i] != 0u;
+      wk[i] = w[i];
     }
   }
   const int32_t n_valid = cta_sum(my_valid, red, parity);  // (its barrier orders the stores above)
@@ -332,12 +341,9 @@ static __device__ __forceinline__ void select_budget_cta(const SelectCtx& sc, in
     theta = 0u;
     need = 0;
   } else {
-    // Level 0 bins the survival value linearly (a valid key is the value's
-    // bits + 1, and value x 1024 is exact, so the bins keep the keys' order):
-    // keys close in value spread over many bins, and few share the chosen one.
-    // Only when that bin still holds more than NCAND keys do the next levels
-    // fix the key's bits ten at a time among the bin's keys.
-    auto vbin = [](uint32_t w) -> int { return min(NB - 1, (int)(__uint_as_float(w - 1u) * (float)NB)); };
+    // Level 0: the value bins.  Only when the chosen bin still holds more than
+    // NCAND keys do the next levels fix the key's bits ten at a time among the
+    // bin's keys.
     int vb = -1;           // the chosen value bin
     uint32_t prefix = 0u;  // key bits at and above `hi` fixed so far (levels 1..3)
     int hi = 30;           // keys are below 2^30
@@ -408,10 +414,16 @@ static __device__ __forceinline__ void select_budget_cta(const SelectCtx& sc, in
     } else {
       // the chosen bin's keys, ranked directly: theta is the value v with
       // #(keys > v) < rem <= #(keys >= v)
+      if (regs) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          if (tid + i * nt < nslots && member(wk[i])) s_cand[atomicAdd(&bc[8], 1)] = wk[i];
+      } else {
 #pragma unroll 4
-      for (int q = tid; q < nslots; q += nt) {
-        const uint32_t w = s_key[q];
-        if (member(w)) s_cand[atomicAdd(&bc[8], 1)] = w;
+        for (int q = tid; q < nslots; q += nt) {
+          const uint32_t w = s_key[q];
+          if (member(w)) s_cand[atomicAdd(&bc[8], 1)] = w;
+        }
       }
       __syncthreads();
       int32_t* b = bc + 4 * 2;  // words 8..11: [8] count (done), [9] theta, [10] need

@@ -338,10 +338,13 @@ def test_chain_long_bs64_full_fp32_T07(S):
     ro = c["row_off_materialised"]
     logits = W.materialised_logits(c)
     ws = _ws(S, c["B"], int(ro[-1]), c["K"], c["V"])
-    g = gpu_chain(S, ws, logits, ro, lay.chain, lay.verify_len, lay.point_mass, None, 0.7)
-    o = O.verify_chain(logits, ro, lay.chain, lay.verify_len, lay.point_mass, None, 0.7, 0, 0)
-    st = compare_sampled(g, o, logits, ro, lay.chain, lay.verify_len, lay.point_mass, None, 0.7)
-    assert st["exact"] + st["band"] == c["B"]
+    lt = logits_dev(logits)
+    for step in range(4):  # four draw sets: accept tests, bonus and correction draws at full size
+        g = gpu_chain(S, ws, None, ro, lay.chain, lay.verify_len, lay.point_mass, None, 0.7, step=step,
+                      logits_t=lt)
+        o = O.verify_chain(logits, ro, lay.chain, lay.verify_len, lay.point_mass, None, 0.7, 0, step)
+        st = compare_sampled(g, o, logits, ro, lay.chain, lay.verify_len, lay.point_mass, None, 0.7)
+        assert st["exact"] + st["band"] == c["B"]
     assert ws.status() == 0
 
 
