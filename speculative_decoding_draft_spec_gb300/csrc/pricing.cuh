@@ -215,6 +215,12 @@ __device__ __forceinline__ void price_request_warp(const PriceCtx& cx, int r, in
 // ell_r = above_r + min(eq_r, max(0, need - E_r)) with E_r the ties of the
 // requests before r, and row_off[r] = r + sum_{r' < r} above_r' + min(need, E_r),
 // one block scan of the pair (above, eq).
+// The histogram and candidate passes over the keys are rolled loops: one CTA
+// runs this once per launch, on an SM whose instruction cache holds other
+// code by then (in a decode step the verification kernel runs between two
+// launches), so fewer instruction lines count for more there than iterations
+// in flight.  The ranking and the per-request counts keep four iterations in
+// flight: rolled, their dependent shared-memory reads add up.
 // Shared scratch: select_scratch_ints(batch, L) ints.
 __host__ __device__ inline int select_scratch_ints(int batch, int L) {
   return ((batch * L + 3) & ~3) + 2 * 1024 + 256 + 96;
@@ -354,7 +360,7 @@ static __device__ __forceinline__ void select_budget_cta(const SelectCtx& sc, in
     for (int level = 0; level < 4; ++level) {
       const int shift = hi - 10;
       int32_t* hist = s_hist + (level & 1) * NB;
-#pragma unroll 4
+#pragma unroll 1
       for (int q = tid; q < nslots; q += nt) {
         const uint32_t w = s_key[q];
         if (level == 0) {
@@ -419,7 +425,7 @@ static __device__ __forceinline__ void select_budget_cta(const SelectCtx& sc, in
         for (int i = 0; i < 8; ++i)
           if (tid + i * nt < nslots && member(wk[i])) s_cand[atomicAdd(&bc[8], 1)] = wk[i];
       } else {
-#pragma unroll 4
+#pragma unroll 1
         for (int q = tid; q < nslots; q += nt) {
           const uint32_t w = s_key[q];
           if (member(w)) s_cand[atomicAdd(&bc[8], 1)] = w;

@@ -183,6 +183,32 @@ def test_price_parity_random_stress(S):
         _assert_price_equal(gp, op)
 
 
+@pytest.mark.parametrize("kind", ["copies", "distinct", "copies_and_distinct"])
+@pytest.mark.parametrize("B", [128, 300])
+def test_price_crowded_value_bin(S, kind, B):
+    """More than 256 keys within one 1/1024 of survival value, where the budget's
+    threshold falls: copies of one key (confidences of exactly 1), distinct
+    keys (confidences just below 1), or both.  Batch 300 keeps the keys in
+    shared memory only, batch 128 also in registers."""
+    rng = np.random.default_rng(B + len(kind))
+    K, L = 7, 15
+    if kind == "copies":
+        c = np.ones((B, K), np.float32)
+    elif kind == "distinct":
+        c = (1.0 - rng.random((B, K)) * 1e-4).astype(np.float32)
+    else:
+        c = np.where(rng.random((B, K)) < 0.5, 1.0, 1.0 - rng.random((B, K)) * 1e-4).astype(np.float32)
+    cfg = dict(d=rng.integers(0, 50, (B, K)).astype(np.int32), c=c, d_len=np.full(B, K, np.int32), L=L,
+               coef=W.table5_coef())
+    ng = O.NgramOut(np.full((B, L), -1, np.int32), np.zeros(B, np.int32), np.zeros(B, np.int32),
+                    np.zeros(B, np.int32), np.zeros(B, np.int32), 0)
+    for budget in (1, 257, B * K // 2 + 1, B * K - 1):
+        g, o, ws = _price_both(S, cfg, ng, policy="model_only", greedy=True, budget=budget, lam=0.04, mvl=15)
+        _assert_price_equal(g, o)
+        assert int(o.verify_len.sum()) == budget
+        assert ws.status() == 0
+
+
 def test_price_flags_out_of_range_confidences(S):
     cfg = dict(d=np.zeros((2, 7), np.int32), c=np.array([[1.5] * 7, [-0.2] * 7], np.float32),
                d_len=np.full(2, 7, np.int32), L=15, coef=W.table5_coef())
