@@ -255,6 +255,10 @@ __global__ void __launch_bounds__(SPEC_CTA_THREADS, 1) ngram_kernel(NgramParams 
           v[u] = c < j1 ? *reinterpret_cast<const int4*>(wv + c) : make_int4(0, 0, 0, 0);
           prev[u] = (two_ok && c < j1 && c >= j0 && c >= 1) ? wv[c - 1] : 0;
         }
+        // the groups' match masks, packed four bits per group (bit 4 u + e:
+        // position c0 + u gstride + e), so that one copy of the extension code
+        // serves every group
+        uint32_t ones = 0u, twos = 0u;
 #pragma unroll
         for (int u = 0; u < NG_UNROLL; ++u) {
           const int32_t c = c0 + u * gstride;
@@ -266,21 +270,21 @@ __global__ void __launch_bounds__(SPEC_CTA_THREADS, 1) ngram_kernel(NgramParams 
               two_ok ? m & ((uint32_t)(prev[u] == s1 && c >= 1) | ((uint32_t)(v[u].x == s1) << 1) |
                             ((uint32_t)(v[u].y == s1) << 2) | ((uint32_t)(v[u].z == s1) << 3))
                      : 0u;
-          if (keep_ones && (m & ~m2)) {
-            // single matches (l = 1) enter the top two as (1, j): no extension
-            uint32_t m1 = m & ~m2;
-            while (m1) {
-              const int e = __ffs(m1) - 1;
-              m1 &= m1 - 1u;
-              top2_insert(b1, b2, (1ull << 32) | (uint32_t)(c + e));
-            }
+          ones |= (m & ~m2) << (4 * u);
+          twos |= m2 << (4 * u);
+        }
+        // single matches (l = 1) enter the top two as (1, j): no extension
+        if (keep_ones) {
+          while (ones) {
+            const int e = __ffs(ones) - 1;
+            ones &= ones - 1u;
+            top2_insert(b1, b2, (1ull << 32) | (uint32_t)(c0 + (e >> 2) * gstride + (e & 3)));
           }
-          uint32_t mx = m2;
-          while (mx) {
-            const int e = __ffs(mx) - 1;
-            mx &= mx - 1u;
-            extend(c + e);
-          }
+        }
+        while (twos) {
+          const int e = __ffs(twos) - 1;
+          twos &= twos - 1u;
+          extend(c0 + (e >> 2) * gstride + (e & 3));
         }
       }
     }
