@@ -50,6 +50,10 @@ struct NgramParams {
   PriceCtx cx;
   SelectCtx sc;
   uint32_t* arrive;  // request arrival counter (zero between calls)
+  // batches of at most SPEC_PACKED_ARRIVAL requests: request r adds (its valid
+  // slots + 1) << 5 r here instead (zero between calls), so the last arrival
+  // returns every request's count with the arrival itself
+  unsigned long long* arrive64;
   // the Eq. (1) table staged in the pricing CTA's shared memory: its offset in
   // 4-byte words (16-byte aligned), -1 when it is read from global memory
   int32_t tab_off;
@@ -381,6 +385,7 @@ __global__ void __launch_bounds__(SPEC_CTA_THREADS, 1) ngram_kernel(NgramParams 
       // price this request from on-chip values (warp 0), then arrive; the CTA
       // of the last request to arrive allocates the budget for the whole batch
       __shared__ int32_t s_last;
+      __shared__ int32_t s_cnt[SPEC_PACKED_ARRIVAL];  // every request's valid slots (packed arrival)
       if (tid < 32) {
         uint32_t st = 0;
         if (tid < p.L) s_ps.g[tid] = tid < len ? tok_at(jb + 1 + tid) : -1;
@@ -394,17 +399,33 @@ __global__ void __launch_bounds__(SPEC_CTA_THREADS, 1) ngram_kernel(NgramParams 
           }
         }
         __syncwarp();
-        price_request_warp(p.cx, r, tid, s_ps, len, n_out, a_out, m_out, s_dl, st, stab);
+        const int32_t clen = price_request_warp(p.cx, r, tid, s_ps, len, n_out, a_out, m_out, s_dl, st, stab);
         if (st) set_status(p.status, st);
-        __syncwarp();
+        // the request's valid slots: the keys written nonzero
+        const int32_t nv = __popc(__ballot_sync(0xFFFFFFFFu, tid < p.cx.L && tid < clen && tid < p.cx.mvl));
         if (tid == 0) {
-          const uint32_t old = atomic_add_acq_rel(p.arrive, 1u);
-          s_last = (old + 1u == (uint32_t)p.batch) ? 1 : 0;
-          if (s_last) *p.arrive = 0u;  // ready for the next call
+          if (p.batch <= SPEC_PACKED_ARRIVAL) {
+            const unsigned long long mine = (unsigned long long)(nv + 1) << (5 * r);
+            const unsigned long long now = atomic_add_acq_rel_u64(p.arrive64, mine) + mine;
+            int last = 1;
+            for (int q = 0; q < p.batch; ++q) {
+              const int32_t f = (int32_t)((now >> (5 * q)) & 31u);
+              last &= f != 0;
+              s_cnt[q] = f - 1;
+            }
+            s_last = last;
+            if (last) *p.arrive64 = 0ull;  // ready for the next call
+          } else {
+            const uint32_t old = atomic_add_acq_rel(p.arrive, 1u);
+            s_last = (old + 1u == (uint32_t)p.batch) ? 1 : 0;
+            if (s_last) *p.arrive = 0u;  // ready for the next call
+          }
         }
       }
       __syncthreads();
-      if (s_last) select_budget_cta(p.sc, smem_tok + p.win_cap + p.suf_cap);
+      if (s_last)
+        select_budget_cta(p.sc, smem_tok + p.win_cap + p.suf_cap,
+                          p.batch <= SPEC_PACKED_ARRIVAL ? s_cnt : nullptr);
     }
   }
   if (CLUSTER) cluster.sync();  // peers keep their shared memory until rank 0 has read it
@@ -555,6 +576,7 @@ extern "C" cudaError_t spec_launch_draft_price(
   p.sc.verify_len = verify_len;
   p.sc.row_off = row_off;
   p.arrive = status + 2;  // the third word of the workspace header
+  p.arrive64 = reinterpret_cast<unsigned long long*>(status + 4);  // header words 4 and 5
   int64_t C;
   size_t smem;
   if (!ngram_geometry(stride < 1 ? 1 : stride, cap, spec::select_scratch_ints(batch, L), &C, &p, &smem)) {

@@ -88,7 +88,7 @@ struct PriceStage {
 // round.
 // stab: a copy of the Eq. (1) table in this CTA's shared memory, or null to
 // read the table in global memory.
-__device__ __forceinline__ void price_request_warp(const PriceCtx& cx, int r, int lane, PriceStage& ps,
+__device__ __forceinline__ int32_t price_request_warp(const PriceCtx& cx, int r, int lane, PriceStage& ps,
                                                    int32_t gl, int32_t n, int32_t a, int32_t m, int32_t dl,
                                                    uint32_t& st, const float* stab) {
   const int32_t K = cx.K, L = cx.L;
@@ -197,6 +197,7 @@ __device__ __forceinline__ void price_request_warp(const PriceCtx& cx, int r, in
     cx.chain_len[r] = len;
     cx.source[r] = src;
   }
+  return len;
 }
 
 // ---------------------------------------------------------------------------
@@ -263,14 +264,15 @@ static __device__ __forceinline__ int32_t cta_incl_scan(int32_t v, int32_t* red,
   return incl + before;
 }
 
-static __device__ __forceinline__ void select_budget_cta(const SelectCtx& sc, int32_t* scratch) {
+static __device__ __forceinline__ void select_budget_cta(const SelectCtx& sc, int32_t* scratch,
+                                                         const int32_t* counts = nullptr) {
   constexpr int NB = 1024;   // histogram bins (10 key bits per level)
   constexpr int NCAND = 256; // keys ranked directly
   const int B = sc.batch, L = sc.L;
   const int nslots = B * L;
   const int tid = threadIdx.x, nt = blockDim.x;
   // At most 32 requests: warp 0 counts each request's valid slots (lane r,
-  // request r).  A budget of zero or one that covers every valid slot decides
+  // request r; from `counts` when the caller has them, else from the keys).  A budget of zero or one that covers every valid slot decides
   // every length at once (all valid slots, or none), and the warp writes the
   // lengths and offsets itself; the block-wide selection runs otherwise.
   if (B <= 32) {
@@ -278,8 +280,12 @@ static __device__ __forceinline__ void select_budget_cta(const SelectCtx& sc, in
     if (tid < 32) {
       int32_t cnt = 0;
       if (tid < B) {
+        if (counts) {
+          cnt = counts[tid];
+        } else {
 #pragma unroll 4
-        for (int k = 0; k < L; ++k) cnt += __ldcg(sc.keys + tid * L + k) != 0u;
+          for (int k = 0; k < L; ++k) cnt += __ldcg(sc.keys + tid * L + k) != 0u;
+        }
       }
       const int32_t n_valid = __reduce_add_sync(0xFFFFFFFFu, cnt);
       const bool done = sc.budget == 0 || sc.budget >= n_valid;
