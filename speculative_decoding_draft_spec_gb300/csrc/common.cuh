@@ -9,7 +9,6 @@
 #define SPEC_WARPS_PER_CTA 8
 #define SPEC_CTA_THREADS (32 * SPEC_WARPS_PER_CTA)
 #define SPEC_UNIT 2048  // vocabulary entries per work unit (one warp)
-#define SPEC_PACKED_ARRIVAL 12  // batches whose per-request counts ride in one 64-bit arrival word (5 bits each)
 
 // float2 entries between two rows of the workspace's chunk partials: one per
 // chunk of the finest chunking (2048 fp32 entries), then a spare entry (the
@@ -174,11 +173,6 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
 __device__ __forceinline__ uint32_t atomic_add_acq_rel(uint32_t* p, uint32_t v) {
   uint32_t old;
   asm volatile("atom.add.acq_rel.gpu.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
-  return old;
-}
-__device__ __forceinline__ unsigned long long atomic_add_acq_rel_u64(unsigned long long* p, unsigned long long v) {
-  unsigned long long old;
-  asm volatile("atom.add.acq_rel.gpu.u64 %0, [%1], %2;" : "=l"(old) : "l"(p), "l"(v) : "memory");
   return old;
 }
 

@@ -88,6 +88,14 @@ __device__ __forceinline__ void top2_insert(unsigned long long& b1, unsigned lon
 #define NG_SHORT 8  // tokens a thread extends a candidate by itself
 #define NG_QCAP 64  // queued long candidates per warp
 #define NG_UNROLL 4 // 16-byte groups per thread in flight in the candidate filter
+#define SPEC_PACKED_ARRIVAL 12  // batches whose per-request counts ride in one 64-bit arrival word (5 bits each)
+
+// device-scope 64-bit fetch-add with acquire-release ordering
+__device__ __forceinline__ unsigned long long atomic_add_acq_rel_u64(unsigned long long* p, unsigned long long v) {
+  unsigned long long old;
+  asm volatile("atom.add.acq_rel.gpu.u64 %0, [%1], %2;" : "=l"(old) : "l"(p), "l"(v) : "memory");
+  return old;
+}
 
 template <bool CLUSTER, bool PRICE>
 __global__ void __launch_bounds__(SPEC_CTA_THREADS, 1) ngram_kernel(NgramParams p) {
