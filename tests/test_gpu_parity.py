@@ -253,6 +253,27 @@ def test_fused_draft_and_price_on_workloads(S, name):
     assert np.array_equal(got2["row_off"], o.row_off)
 
 
+@pytest.mark.parametrize("B", [1, 11, 12, 13, 32, 33])
+def test_fused_draft_and_price_small_batch_paths(S, B):
+    """Batches around the bounds of the small-batch allocation paths: request
+    counts carried in the arrival (at most 12 requests), the one-warp path (at
+    most 32), the block-wide selection; budgets of zero, of every valid slot,
+    and of part of them.  Each call twice in a row (the arrival words return
+    to zero)."""
+    rng = np.random.default_rng(700 + B)
+    K, L, stride = 7, 15, 300
+    hist = rng.integers(0, 5, (B, stride)).astype(np.int32)
+    hist_len = rng.integers(2, stride + 1, B).astype(np.int32)
+    d = np.where(rng.random((B, K)) < 0.5, hist[:, :K], rng.integers(0, 5, (B, K))).astype(np.int32)
+    c = {"hist": hist, "hist_len": hist_len, "n_min": 1, "n_max": 4, "copy_cap": 256, "d": d,
+         "c": rng.choice([0.5, 0.9, 1.0, 0.3], (B, K)).astype(np.float32),
+         "d_len": rng.integers(0, K + 1, B).astype(np.int32), "L": L, "coef": W.table5_coef(n_full=4)}
+    for budget in (0, B * L, max(1, B * L // 3)):
+        for _ in range(2):
+            got, o, ws = _fused_vs_oracle(S, c, policy="proposed", greedy=True, budget=budget, lam=0.04, mvl=15)
+            assert ws.status() == 0
+
+
 def test_fused_draft_and_price_random_stress(S):
     rng = np.random.default_rng(41)
     for trial in range(30):
