@@ -478,6 +478,10 @@ spec_status spec_price_and_allocate_static(
  * Limits: L <= SPEC_MAX_L, 1 <= vocab <= SPEC_MAX_VOCAB, batch <= 2048,
  * (max_rows + batch K) x ceil(vocab / chunk) < 2^31 with chunk = 4096 (bf16)
  * or 2048 (fp32) entries; else SPEC_ERR_UNSUPPORTED.
+ * Launches: one kernel streams every row once and finalises each request;
+ * with draft distributions (T > 0), a second kernel makes the draws from
+ * max(0, p_i - q_i) of the requests that reject a drafted token (it reads
+ * the two rows again, from L2).
  * ------------------------------------------------------------------------ */
 spec_status spec_verify_chain(
     int32_t batch, int32_t vocab, spec_dtype dtype, const void* target_logits,
