@@ -1155,6 +1155,17 @@ struct Cursor {
   const char* row;
 };
 
+// a bulk copy whose lines are marked for early eviction from L2 (the rows are
+// read once; what the next kernels read stays resident)
+__device__ __forceinline__ void bulk_g2s_stream(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                                uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;\n" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
 template <int MODE>
 __device__ __forceinline__ void locate(const VerifyParams& p, const int32_t* s_pre, const int32_t* s_base,
                                        const int32_t* s_len, const uint32_t* s_qm, int item, size_t esz,
@@ -1336,6 +1347,8 @@ __global__ void __launch_bounds__(VR_THREADS, 1) verify_rows_kernel(VerifyParams
   // row only when it enters it and then advances its source pointer
   int is_item = first, is_u = (int)(lo - (uint32_t)first * nch);
   const char* is_src = nullptr;
+  uint64_t l2_first;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(l2_first));
   auto issue = [&](int s) {
     if (is_src == nullptr) {
       locate<MODE>(p, s_pre, s_base, s_len, s_qm, is_item, esz, ic);
@@ -1343,7 +1356,7 @@ __global__ void __launch_bounds__(VR_THREADS, 1) verify_rows_kernel(VerifyParams
     }
     const uint32_t bytes = (is_u + 1 < (int)nch) ? (uint32_t)VR_STAGE : (uint32_t)((p.vocab - is_u * CH) * esz);
     mbar_arrive_expect_tx(&bars[s], bytes);
-    bulk_g2s(wbuf + (size_t)s * VR_STAGE, is_src, bytes, &bars[s]);
+    bulk_g2s_stream(wbuf + (size_t)s * VR_STAGE, is_src, bytes, &bars[s], l2_first);
     is_src += VR_STAGE;
     if (++is_u == (int)nch) {
       is_u = 0;
