@@ -51,7 +51,7 @@ struct NgramParams {
   SelectCtx sc;
   uint32_t* arrive;  // request arrival counter (zero between calls)
   // batches of at most SPEC_PACKED_ARRIVAL requests: request r adds (its valid
-  // slots + 1) << 5 r here instead (zero between calls), so the last arrival
+  // slots + 1) << (SPEC_PACKED_BITS r) here instead (zero between calls), so the last arrival
   // returns every request's count with the arrival itself
   unsigned long long* arrive64;
   // the Eq. (1) table staged in the pricing CTA's shared memory: its offset in
@@ -88,7 +88,8 @@ __device__ __forceinline__ void top2_insert(unsigned long long& b1, unsigned lon
 #define NG_SHORT 8  // tokens a thread extends a candidate by itself
 #define NG_QCAP 64  // queued long candidates per warp
 #define NG_UNROLL 4 // 16-byte groups per thread in flight in the candidate filter
-#define SPEC_PACKED_ARRIVAL 12  // batches whose per-request counts ride in one 64-bit arrival word (5 bits each)
+#define SPEC_PACKED_ARRIVAL 10  // batches whose per-request counts ride in one 64-bit arrival word
+#define SPEC_PACKED_BITS 6      // bits per request: valid slots + 1 <= SPEC_MAX_L + 1 = 32 < 2^6
 
 // device-scope 64-bit fetch-add with acquire-release ordering
 __device__ __forceinline__ unsigned long long atomic_add_acq_rel_u64(unsigned long long* p, unsigned long long v) {
@@ -413,11 +414,11 @@ __global__ void __launch_bounds__(SPEC_CTA_THREADS, 1) ngram_kernel(NgramParams 
         const int32_t nv = __popc(__ballot_sync(0xFFFFFFFFu, tid < p.cx.L && tid < clen && tid < p.cx.mvl));
         if (tid == 0) {
           if (p.batch <= SPEC_PACKED_ARRIVAL) {
-            const unsigned long long mine = (unsigned long long)(nv + 1) << (5 * r);
+            const unsigned long long mine = (unsigned long long)(nv + 1) << (SPEC_PACKED_BITS * r);
             const unsigned long long now = atomic_add_acq_rel_u64(p.arrive64, mine) + mine;
             int last = 1;
             for (int q = 0; q < p.batch; ++q) {
-              const int32_t f = (int32_t)((now >> (5 * q)) & 31u);
+              const int32_t f = (int32_t)((now >> (SPEC_PACKED_BITS * q)) & ((1u << SPEC_PACKED_BITS) - 1u));
               last &= f != 0;
               s_cnt[q] = f - 1;
             }

@@ -253,15 +253,17 @@ def test_fused_draft_and_price_on_workloads(S, name):
     assert np.array_equal(got2["row_off"], o.row_off)
 
 
-@pytest.mark.parametrize("B", [1, 11, 12, 13, 32, 33])
-def test_fused_draft_and_price_small_batch_paths(S, B):
+@pytest.mark.parametrize("L", [15, 31])
+@pytest.mark.parametrize("B", [1, 9, 10, 11, 32, 33])
+def test_fused_draft_and_price_small_batch_paths(S, B, L):
     """Batches around the bounds of the small-batch allocation paths: request
-    counts carried in the arrival (at most 12 requests), the one-warp path (at
+    counts carried in the arrival (at most 10 requests), the one-warp path (at
     most 32), the block-wide selection; budgets of zero, of every valid slot,
-    and of part of them.  Each call twice in a row (the arrival words return
-    to zero)."""
-    rng = np.random.default_rng(700 + B)
-    K, L, stride = 7, 15, 300
+    and of part of them; chains of up to 15 and of up to 31 slots (a request's
+    count field must hold 31).  Each call twice in a row (the arrival words
+    return to zero)."""
+    rng = np.random.default_rng(700 + B + L)
+    K, stride = 7, 300
     hist = rng.integers(0, 5, (B, stride)).astype(np.int32)
     hist_len = rng.integers(2, stride + 1, B).astype(np.int32)
     d = np.where(rng.random((B, K)) < 0.5, hist[:, :K], rng.integers(0, 5, (B, K))).astype(np.int32)
@@ -270,8 +272,10 @@ def test_fused_draft_and_price_small_batch_paths(S, B):
          "d_len": rng.integers(0, K + 1, B).astype(np.int32), "L": L, "coef": W.table5_coef(n_full=4)}
     for budget in (0, B * L, max(1, B * L // 3)):
         for _ in range(2):
-            got, o, ws = _fused_vs_oracle(S, c, policy="proposed", greedy=True, budget=budget, lam=0.04, mvl=15)
+            got, o, ws = _fused_vs_oracle(S, c, policy="proposed", greedy=True, budget=budget, lam=0.04, mvl=L)
             assert ws.status() == 0
+    if L == 31:  # some request's chain fills all 31 slots
+        assert int(o.chain_len.max()) == 31
 
 
 def test_fused_draft_and_price_random_stress(S):
